@@ -1,0 +1,208 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the fused mixture-of-experts expert layer for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer (sources are named by page title and section):
+ *   out[t] = sum_{j<k} w[t,j] * FFN_{idx[t,j]}(x[t]) + FFN_shared(x[t])
+ * with
+ *   - fp32 router logits and softmax top-k with renormalised weights
+ *     ("Optimising Ling-2.6-1T on TPU with SGLang-JAX", s.1: 256 routed experts,
+ *     top-8 plus one shared expert; "Kimi K3 ... feasibility analysis", s.2.4:
+ *     moe_renormalize, routed_scaling_factor 1.0);
+ *   - dynamic per-token fp8 e4m3 activation quantisation before the scatter
+ *     (Ling write-up, s.5 "activation quantisation");
+ *   - scatter of token rows into expert-contiguous order, which on one GPU is a
+ *     local permutation (Ling write-up, s.1: scatter -> local expert FFN -> gather);
+ *   - SwiGLU experts h = silu(W1 x) * (W3 x), y = W2 h on fp8 per-output-channel
+ *     weights with the scale applied after the full-K sum (Ling write-up, s.5
+ *     "per-channel direct_scaled_dot": out[m,n] = (sum_k A W) * scale[n]);
+ *     MXFP4 (e2m1 + e8m0 per 32) for the LatentMoE case (Kimi K3 report, s.2.5);
+ *   - weighted top-k gather back to token order plus the shared expert (Ling
+ *     write-up, s.5 "in-kernel shared expert").
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_host are host pointers; every other tensor pointer is a
+ *     DEVICE pointer owned by the caller, C-contiguous (row-major), on the
+ *     current CUDA device.  bf16 tensors are passed as void* (IEEE bfloat16
+ *     bits), fp8 tensors as void* (OCP E4M3FN bytes).
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *     stream.  Every call is asynchronous on `stream` and returns once its
+ *     kernels are queued; no call synchronises except moe_get_last_error and
+ *     moe_profile_read.
+ *   - The library allocates no device memory on the call path: scratch comes
+ *     from the caller's workspace `ws` of `ws_bytes` bytes (moe_workspace_bytes),
+ *     256-byte aligned.  Outputs must not alias inputs.
+ *   - Return value: a moe_status.  Argument checks happen on the host before any
+ *     launch and return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *     MOE_ERR_WORKSPACE with nothing queued; a failed launch returns
+ *     MOE_ERR_CUDA.  Faults detected on the device (a pipeline wait that ran out
+ *     of time) set a per-device error word that moe_get_last_error returns.
+ *     Nothing aborts, throws or falls back to another implementation.
+ *   - Shapes: H, I, I_shared (and latent) must be multiples of 128; T >= 0
+ *     (T = 0 is a no-op); 1 <= top_k <= min(E, 32); E <= 4096.
+ */
+#ifndef MOE_GB300_MOE_H_
+#define MOE_GB300_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, top_k > E, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2, /* valid problem this build does not implement        */
+  MOE_ERR_WORKSPACE = 3,   /* ws NULL or ws_bytes < moe_workspace_bytes           */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed         */
+  MOE_ERR_TIMEOUT = 5      /* a device-side pipeline wait exceeded its limit      */
+} moe_status;
+
+typedef enum {
+  MOE_W_FP8_E4M3_PER_CHANNEL = 0, /* e4m3 bytes + fp32 scale per output channel   */
+  MOE_W_MXFP4_E2M1_E8M0_B32 = 1   /* packed e2m1 (low nibble = even k) + e8m0/32  */
+} moe_wfmt;
+
+#define MOE_F_ROUTER_BIAS 0x1u /* add router_bias[e] to every logit before top-k    */
+#define MOE_F_SHARED_BF16 0x2u /* shared expert weights are bf16 (no quantisation)   */
+
+typedef struct {
+  int32_t T;        /* tokens                                                      */
+  int32_t H;        /* hidden width                                                */
+  int32_t I;        /* routed expert intermediate width                            */
+  int32_t E;        /* routed experts                                              */
+  int32_t top_k;    /* experts per token                                           */
+  int32_t I_shared; /* shared expert intermediate width; 0 = no shared expert      */
+  int32_t latent;   /* LatentMoE width L (experts run on L instead of H); 0 = none */
+  int32_t wfmt;     /* moe_wfmt of the routed expert weights                       */
+  uint32_t flags;   /* MOE_F_*                                                     */
+} moe_problem;
+
+/* Stage indices for the profiling counters. */
+enum {
+  MOE_STAGE_ROUTER = 0,  /* S1 router logits                     */
+  MOE_STAGE_TOPK = 1,    /* S2 top-k + renormalise               */
+  MOE_STAGE_INDEX = 2,   /* S3 histogram, scan, ranks, tile list */
+  MOE_STAGE_SCATTER = 3, /* S4 per-token fp8 quant + row scatter */
+  MOE_STAGE_FFN1 = 4,    /* S5 grouped W1|W3 GEMM + SiLU*gate    */
+  MOE_STAGE_REQUANT = 5, /* S6a per-row fp8 requant of h         */
+  MOE_STAGE_FFN2 = 6,    /* S6 grouped W2 GEMM + routing weight  */
+  MOE_STAGE_COMBINE = 7, /* S7/S8 weighted gather + shared add   */
+  MOE_STAGE_COUNT = 8
+};
+
+/* Human-readable name of a moe_status (static storage). */
+const char* moe_status_string(int status);
+
+/* Bytes of device workspace that moe_forward, moe_permute and moe_expert_ffn
+ * need for problem `p` (0 if `p` is invalid).  Pure host computation. */
+size_t moe_workspace_bytes(const moe_problem* p);
+
+/* S1 -- router logits.  logits[t,e] = sum_h float(x[t,h]) * router_w[e,h]
+ * (+ bias[e] when MOE_F_ROUTER_BIAS), fp32, summed in one fixed order: 32
+ * partial sums (partial l takes h = l, l+32, ... ascending, fused multiply-add
+ * from +0), then p_l += p_{l+o} for o = 16, 8, 4, 2, 1, bias added last.  The
+ * order is fixed so that routing is reproducible bit for bit.
+ * (Ling write-up, s.6: routing metadata.)
+ *   x        [T, H] bf16           router_w [E, H] fp32
+ *   bias     [E] fp32, required iff MOE_F_ROUTER_BIAS, else ignored
+ *   logits   [T, E] fp32 (output) */
+int moe_router_logits(const moe_problem* p, const void* x, const float* router_w,
+                      const float* bias, float* logits, void* stream);
+
+/* S2 -- top-k.  For each token the top_k largest logits in descending order,
+ * equal logits ordered by lower expert index; weights are the softmax over the
+ * chosen logits, w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0), fp32.
+ * (Ling write-up, s.1 top-8 routing; Kimi K3 report, s.2.4 moe_renormalize.)
+ *   logits [T, E] fp32 -> topk_idx [T, top_k] int32, topk_w [T, top_k] fp32 */
+int moe_route(const moe_problem* p, const float* logits, int32_t* topk_idx, float* topk_w,
+              void* stream);
+
+/* S3 + S4 -- expert-contiguous permutation and per-token fp8 quantisation.
+ * counts[e] = #{(t,j): idx[t,j] = e}; offsets[e] = sum_{e'<e} counts[e'],
+ * offsets[E] = T*top_k; the row of (t,j) is offsets[e] + #{t' < t : e in
+ * idx[t']} (stable in token order), perm[t,j] = that row, src_row[row] = t.
+ * Each token is quantised once, s[t] = max_h |x[t,h]| / 448 in fp32 (1 if the
+ * row is all zero), q = e4m3(x / s) rounded to nearest even and saturated to
+ * +-448, and copied to each of its rows: xq_perm[row] = q[t], xscale_perm[row]
+ * = s[t].  (Ling write-up, s.5 activation quantisation before the scatter;
+ * s.6 per-expert offsets and scatter indices.)  With a latent problem, x is
+ * the latent input [T, latent].
+ *   topk_idx [T, top_k] int32 in [0, E)   x [T, H] bf16
+ *   counts [E], offsets [E+1], perm [T, top_k], src_row [T*top_k] int32 (out)
+ *   xq_perm [T*top_k, H] e4m3 (out), xscale_perm [T*top_k] fp32 (out)
+ *   ws / ws_bytes: workspace, at least moe_workspace_bytes(p)
+ * Indices outside [0, E) are reported as MOE_ERR_INVALID_ARG by
+ * moe_get_last_error and their rows are left unwritten. */
+int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, int32_t* counts,
+                int32_t* offsets, int32_t* perm, int32_t* src_row, void* xq_perm,
+                float* xscale_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* S5 + S6 -- grouped SwiGLU experts over expert-contiguous rows.  For rows r
+ * in [offsets[e], offsets[e+1]):
+ *   g[n] = (sum_k xq[r,k] W1_e[n,k]) * xscale[r] * s13_e[n]      (W1 = rows 0..I-1)
+ *   u[n] = (sum_k xq[r,k] W3_e[n,k]) * xscale[r] * s13_e[I+n]    (W3 = rows I..2I-1)
+ *   h[n] = bf16(silu(g[n]) * u[n]);  s_h = max_n |h[n]| / 448;  hq = e4m3(h / s_h)
+ *   y[r,m] = bf16(row_w[r] * (sum_n hq[n] W2_e[m,n]) * s_h * s2_e[m])
+ * (Ling write-up, s.5 per-channel direct_scaled_dot; FFN1/FFN2 of s.1.)
+ *   offsets   [E+1] int32 (device), offsets[E] = R rows
+ *   xq_perm   [R, K] e4m3, xscale_perm [R] fp32, row_w [R] fp32 or NULL (= 1)
+ *   fp8:   w13 [E, 2I, K] e4m3, w13_scale [E, 2I] fp32,
+ *          w2  [E, K, I] e4m3,  w2_scale  [E, K] fp32
+ *   y         [R, K] bf16 (out); K = H (or latent)
+ * R is read from p as T*top_k. */
+int moe_expert_ffn(const moe_problem* p, const int32_t* offsets, const void* xq_perm,
+                   const float* xscale_perm, const float* row_w, const void* w13,
+                   const void* w13_scale, const void* w2, const void* w2_scale, void* y,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* S7 (+ S8 add) -- weighted gather back to token order.
+ *   out[t,:] = bf16( sum_{j ascending} float(y_rows[perm[t,j],:]) + float(shared[t,:]) )
+ * in fp32.  The routing weight is already folded into y_rows (moe_expert_ffn).
+ * (Ling write-up, s.1 gather results; s.5 shared expert on every token.)
+ *   y_rows [T*top_k, H] bf16, perm [T, top_k] int32,
+ *   shared [T, H] bf16 or NULL, out [T, H] bf16 (out) */
+int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
+                  const void* shared, void* out, void* stream);
+
+/* The whole layer, S1..S8, queued on `stream` with no host round trip.
+ *   x [T, H] bf16; router_w [E, H] fp32; router_bias [E] fp32 (MOE_F_ROUTER_BIAS)
+ *   routed experts: see moe_expert_ffn (K = H, or latent for a LatentMoE problem)
+ *   shared expert (I_shared > 0): fp8 shared_w13 [2*I_shared, H] e4m3 +
+ *     shared_w13_scale [2*I_shared] fp32, shared_w2 [H, I_shared] e4m3 +
+ *     shared_w2_scale [H] fp32; with MOE_F_SHARED_BF16 the two weights are bf16
+ *     and the scales are ignored.  The shared expert takes weight 1 and the
+ *     same per-token fp8 activations as the routed experts.
+ *   latent (L > 0): latent_down [L, H] bf16, latent_up [H, L] bf16,
+ *     latent_gamma [L] bf16 (RMSNorm weight, eps 1e-6), Kimi K3 report s.2.4.
+ *   out [T, H] bf16 (output); ws / ws_bytes as for moe_permute. */
+int moe_forward(const moe_problem* p, const void* x, const float* router_w,
+                const float* router_bias, const void* w13, const void* w13_scale,
+                const void* w2, const void* w2_scale, const void* shared_w13,
+                const void* shared_w13_scale, const void* shared_w2,
+                const void* shared_w2_scale, const void* latent_down, const void* latent_up,
+                const void* latent_gamma, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the current device's error
+ * word (MOE_OK if no device-side fault was recorded; MOE_ERR_CUDA if the
+ * synchronisation itself failed). */
+int moe_get_last_error(void* stream);
+
+/* Number of kernels this library has launched in this process (all devices).
+ * Host-side counter, for accounting; never reset. */
+int64_t moe_launch_count(void);
+
+/* Per-stage device timing.  While enabled, every stage launch is bracketed by
+ * CUDA events recorded on the launching stream.  moe_profile_read waits for
+ * the recorded events, writes the summed milliseconds and launch counts per
+ * stage (MOE_STAGE_*, arrays of MOE_STAGE_COUNT) and clears the record.
+ * Returns MOE_OK, or MOE_ERR_CUDA. */
+int moe_profile_enable(int on);
+int moe_profile_read(double* stage_ms, int64_t* stage_launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_MOE_H_ */
