@@ -1,0 +1,372 @@
+"""Benchmark of the fused MoE expert layer on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config decode|prefill|skewed|toy]
+
+A step is one moe_forward over one batch (router logits -> top-k -> permute +
+fp8 quant -> grouped FFN1 -> requant -> grouped FFN2 -> gather + shared),
+inputs resident in HBM.  The default workload is the Ling-style decode batch
+(T=512, H=8192, I=2048, 256 experts top-8 + a shared expert, fp8 e4m3
+per-channel weights), whose ~12.9 GB of expert weights exceed L2 on every
+step, so no flush is needed.  ``value`` is algorithmic bytes per step (touched
+expert weights + scales, shared weights, router, x, out) / step time, summed
+over ranks; replicas run independent copies (the layer does not shard here).
+``--impl reference`` times the CPU oracle on a bounded token sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer µs; TFLOP/s (prefill) & weight GB/s (decode) vs GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode")
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="tokens per oracle step (default: one per host core)")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 0.0, "fallback"
+
+
+def workload_name(cfg):
+    kind = {"decode": "Ling-style decode", "prefill": "Ling-style prefill",
+            "skewed": "skewed-routing stress (Zipf 1.2 router bias)", "toy": "toy"}.get(cfg.name, cfg.name)
+    s = (f"{kind}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}"
+         + (f" + shared expert I_s={cfg.I_s}" if cfg.I_s else "")
+         + f", {cfg.wfmt} e4m3 per-output-channel weights, per-token fp8 activations")
+    return s
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def kernel_traffic(kernel: str, cfg_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{cfg_name}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_sha") != source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_expert_layer_02_gb300", "csrc")
+    for n in ("ffn_gemm.cu", "device.cuh", "internal.h"):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def cpu_baseline(cfg, inp_host, n_tokens: int, reps: int = 1):
+    import numpy as np
+
+    import oracle
+    threads = oracle.threads()
+    n = n_tokens or threads
+    toks = np.arange(min(n, cfg.T), dtype=np.int32)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.moe_forward(cfg.oracle_problem(), inp_host, tokens=toks, nthreads=threads)
+    dt = (time.perf_counter() - t0) / reps
+    return dt, len(toks), threads
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, cfg):
+    import torch
+
+    import moe_inputs as mi
+    from moe_expert_layer_02_gb300 import accounting as acc
+    ws, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = mi.make_inputs(cfg, device=dev)
+    host = mi.to_numpy(inp)
+    del inp
+    import numpy as np
+
+    import oracle
+    n = args.ref_tokens or oracle.threads()
+    toks = np.arange(min(n, cfg.T), dtype=np.int32)
+    for _ in range(args.warmup):
+        oracle.moe_forward(cfg.oracle_problem(), host, tokens=toks)
+    times = []
+    budget_s = 240.0  # keep the whole reference arm within a few minutes
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, _, idx, _ = oracle.moe_forward(cfg.oracle_problem(), host, tokens=toks)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    step = statistics.mean(times)
+    # per-step work of the sample: the same algorithmic bytes, scaled to the sample
+    touched = cfg.E if cfg.T * cfg.k >= 4 * cfg.E else len(np.unique(idx))
+    bytes_full = acc.layer_work(cfg, touched)["bytes"]
+    frac = len(toks) / cfg.T
+    value = bytes_full * frac / step / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "parallelism": "replicas",
+                   "sample": f"{len(toks)} of {cfg.T} tokens per step"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"first {len(toks)} of {cfg.T} tokens, whole layer per token "
+                                   f"(route, top-{cfg.k} experts, shared), bytes scaled by {frac:.4f}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, cfg):
+    import numpy as np
+    import torch
+
+    import moe_expert_layer_02_gb300 as m
+    import moe_inputs as mi
+    from moe_expert_layer_02_gb300 import accounting as acc
+    from moe_expert_layer_02_gb300 import build as mb
+
+    ws_n, rank, local = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    mb.build()
+    m.load_library()
+    dev = torch.device("cuda", local)
+    inp = mi.make_inputs(cfg, device=dev, seed=0)
+    flags = m.F_ROUTER_BIAS if cfg.zipf_bias else 0
+    p = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, flags=flags)
+    wsb = torch.empty(m.moe_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(x=None):
+        m.moe_forward(p, inp["x"] if x is None else x, inp["router_w"], inp["router_bias"],
+                      inp["w13"], inp["w13_scale"], inp["w2"], inp["w2_scale"], inp["sw13"],
+                      inp["sw13_scale"], inp["sw2"], inp["sw2_scale"], None, None, None, out, wsb)
+
+    # touched experts (for algorithmic bytes): routing through the library itself
+    logits = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
+    tidx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+    tw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+    m.moe_router_logits(p, inp["x"], inp["router_w"], inp["router_bias"], logits)
+    m.moe_route(p, logits, tidx, tw)
+    touched = int(torch.unique(tidx).numel())
+    work = acc.layer_work(cfg, touched)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    rc = m.moe_get_last_error()
+    if rc != 0:
+        raise SystemExit(f"device error word {rc} after warm-up")
+
+    clocks = ClockSampler(local)
+    time.sleep(0.2)
+    m.moe_profile_read()
+    m.moe_profile_enable(True)
+    n0 = m.moe_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    launches = m.moe_launch_count() - n0
+    m.moe_profile_enable(False)
+    stage_ms, stage_n = m.moe_profile_read()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = max_over_ranks(ms, ws_n)
+    rc = m.moe_get_last_error()
+    if rc != 0:
+        raise SystemExit(f"device error word {rc} after the timed region")
+
+    # end to end through the public call with host buffers
+    x_host = inp["x"].cpu().pin_memory()
+    out_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(args.steps // 2, 3)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws_n)
+
+    bytes_step = work["bytes"]
+    value = ws_n * bytes_step / (ms_max * 1e-3) / 1e9
+    e2e_value = ws_n * bytes_step / (e2e_ms * 1e-3) / 1e9
+    hbm, bf16, bf16_sus, src = peaks()
+    ffn1_ms = stage_ms["ffn1"] / max(stage_n["ffn1"], 1)
+    ffn2_ms = stage_ms["ffn2"] / max(stage_n["ffn2"], 1)
+    ffn1_bytes = acc.ffn1_launch_bytes(cfg, touched)
+    ffn1_gbs = ffn1_bytes / (ffn1_ms * 1e-3) / 1e9
+    traffic = kernel_traffic("ffn1", cfg.name)
+    fl = work["flops_fp8"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                   "top_k": cfg.k, "I_shared": cfg.I_s, "touched_experts": touched,
+                   "parallelism": "replicas" if ws_n > 1 else "single",
+                   "l2": "inputs larger than L2 (%.1f GB of weights per step), no flush" % (
+                       (work["bytes_weights_routed"] + work["bytes_weights_shared"]) / 1e9)},
+        "latency_us": ms_max * 1e3,
+        "tflops_fp8": fl / (ms_max * 1e-3) / 1e12,
+        "roofline": {"bound": "hbm", "kernel": "grouped_ffn_kernel<FFN1> (W1|W3 + SiLU*gate)",
+                     "achieved": ffn1_gbs, "peak": hbm, "unit": "GB/s", "frac": ffn1_gbs / hbm,
+                     "peak_source": f"hbm_gbs of {src}", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ffn1_bytes, "avg_launch_ms": ffn1_ms,
+                     "layer_frac": (bytes_step / (ms_max * 1e-3) / 1e9) / hbm},
+        "stages_ms": {k: v / max(stage_n[k], 1) for k, v in stage_ms.items()},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
+    }
+    if rank == 0 and ws_n == 1:
+        host = mi.to_numpy({k: v for k, v in inp.items()})
+        dt, n, cores = cpu_baseline(cfg, host, args.ref_tokens)
+        frac = n / cfg.T
+        line["cpu_baseline"] = {
+            "value": bytes_step * frac / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {cfg.T} tokens, whole layer per token, bytes scaled by {frac:.4f}",
+            "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    import moe_inputs as mi
+    cfg = mi.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

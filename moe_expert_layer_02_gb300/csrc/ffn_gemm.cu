@@ -1,0 +1,357 @@
+// ffn_gemm.cu -- S5/S6: grouped fp8 SwiGLU expert GEMMs on tcgen05.
+//
+// What is computed ("Optimising Ling-2.6-1T on TPU with SGLang-JAX", s.1 cost
+// model FFN1/FFN2 and s.5 "per-channel direct_scaled_dot"): for each routed
+// row r of expert e,
+//   FFN1  g[n] = (sum_k xq[r,k] W1_e[n,k]) * xs[r] * s13_e[n]
+//         u[n] = (sum_k xq[r,k] W3_e[n,k]) * xs[r] * s13_e[I+n]
+//         h[r,n] = bf16(silu(g) * u)
+//   FFN2  y[r,m] = bf16(row_w[r] * (sum_n hq[r,n] W2_e[m,n]) * hs[r] * s2_e[m])
+// e4m3 x e4m3 products are summed in fp32 by the tensor core over the full K;
+// the per-token and per-channel scales are applied after the reduction, which
+// is what makes one long-K contraction possible (the write-up contrasts this
+// with block-wise scales that force K into short pieces).
+//
+// How (GB300-specific; the TPU kernel of the write-up is prior art only):
+//   * Work list: items {group, row0, rows<=BN} over expert-contiguous rows
+//     (group E = the shared expert, whose rows follow the routed ones); a tile
+//     is (item, 128-wide output block).  One persistent CTA per SM walks tiles
+//     blockIdx.x, +gridDim.x, ...
+//   * Swap-AB: the MMA's M=128 runs over weight rows (output features) and N
+//     over the item's token rows (N = rows rounded up to 16, <= BN), so decode
+//     batches of ~16 rows per expert still issue full-height MMAs and every
+//     weight byte is streamed once.  D[feature, row] lives in tensor memory.
+//   * Warp roles: warp 0 = TMA producer (W tiles through a 3-D map
+//     [E][rows][K], activation rows through a 2-D map, 128-byte swizzle),
+//     warp 1 = MMA issuer (tcgen05.mma kind::f8f6f4, commit to mbarriers),
+//     warps 2-5 = epilogue (tcgen05.ld, scales, SiLU*gate or routing weight,
+//     bf16 stores).  Multi-stage smem ring + double-buffered accumulators
+//     (the write-up's "weight double-buffering" becomes this ring).
+//   * Every pipeline wait is bounded; on timeout the CTA records
+//     MOE_ERR_TIMEOUT, drains its own TMA loads and MMAs and frees its tensor
+//     memory before returning.
+#include <cudaTypedefs.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;     // output features per tile (MMA M)
+constexpr int BK = 128;     // K bytes per stage (= one 128-byte swizzle row)
+constexpr int UMMA_K = 32;  // K per tcgen05.mma for 8-bit operands
+constexpr int kThreads = 192;
+constexpr int kSmemBudget = 221 * 1024;
+
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+constexpr int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <bool FFN1, int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK;  // one weight box, 16 KB
+  static constexpr int NA = FFN1 ? 2 : 1;  // W1 and W3 boxes for FFN1
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+  static constexpr int STAGES = cmin(kSmemBudget / STAGE_BYTES, 12);
+  static constexpr int ACC_COLS = NA * BN;
+  static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_COLS = pow2_at_least(ACC_STAGES * ACC_COLS);
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + STAGES * 4;
+  static_assert(B_BYTES % 1024 == 0, "operand tiles must keep 1024-byte alignment");
+  static_assert(ACC_STAGES * ACC_COLS <= 512, "tensor memory holds 512 columns");
+  static_assert(STAGES >= 2, "need at least two pipeline stages");
+};
+
+__device__ __forceinline__ uint32_t f32_bits_to_bf16(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+template <bool FFN1, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_ffn_kernel(const __grid_constant__ CUtensorMap tm_w,
+                       const __grid_constant__ CUtensorMap tm_ws,
+                       const __grid_constant__ CUtensorMap tm_x, const GroupedFfnArgs a) {
+  using C = Cfg<FFN1, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + C::ACC_STAGES;
+  uint64_t* drain = tempty + C::ACC_STAGES;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint32_t* s_issued = s_tmem + 4;  // per stage: 0 = never, else phase + 1
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+      s_issued[s] = 0;
+    }
+    for (int s = 0; s < C::ACC_STAGES; ++s) {
+      mbar_init(smem_u32(&tfull[s]), 1);
+      mbar_init(smem_u32(&tempty[s]), 4);  // one arrive per epilogue warp
+    }
+    mbar_init(smem_u32(drain), 1);
+    *s_abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_ws);
+    tma_prefetch_desc(&tm_x);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(s_tmem), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  const int NB = FFN1 ? a.I / BM : a.K / BM;  // output blocks per item
+  const int KB = FFN1 ? a.K / BK : a.I / BK;  // K stages per tile
+  const int n_items = min(*a.n_items, a.max_items);
+  const int n_tiles = n_items * NB;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && !*s_abort; tile += gridDim.x) {
+        const int item = tile / NB, nb = tile - item * NB;
+        const int4 it = a.items[item];
+        const bool shared = it.x >= a.E;
+        const CUtensorMap* tw = shared ? &tm_ws : &tm_w;
+        const int gc = shared ? 0 : it.x;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_3d(st, tw, kb * BK, nb * BM, gc, fb);
+          if (FFN1) tma_load_3d(st + C::A_BYTES, tw, kb * BK, a.I + nb * BM, gc, fb);
+          tma_load_2d(st + C::NA * C::A_BYTES, &tm_x, kb * BK, it.y, fb);
+          s_issued[stage] = phase + 1u;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (*s_abort) {  // let our own copies land before the CTA can exit
+        for (int s = 0; s < C::STAGES; ++s)
+          if (s_issued[s]) mbar_wait_drain(smem_u32(&full[s]), s_issued[s] - 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, it_local = 0;
+      uint32_t phase = 0;
+      bool issued_any = false;
+      for (int tile = blockIdx.x; tile < n_tiles && !*s_abort; tile += gridDim.x, ++it_local) {
+        const int item = tile / NB;
+        const int rows = a.items[item].z;
+        const int n = min(BN, (rows + 15) & ~15);
+        const uint32_t idesc = idesc_e4m3_f32(BM, n);
+        const int acc = it_local % C::ACC_STAGES;
+        const uint32_t acc_phase = (uint32_t)(it_local / C::ACC_STAGES) & 1u;
+        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, a.err, s_abort)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem + acc * C::ACC_COLS;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, a.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + C::NA * C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(b0 + kk * UMMA_K);
+            const uint32_t accum = (kb | kk) ? 1u : 0u;
+            mma_f8f6f4(d0, smem_desc_sw128(a0 + kk * UMMA_K), bdesc, idesc, accum);
+            if (FFN1)
+              mma_f8f6f4(d0 + BN, smem_desc_sw128(a0 + C::A_BYTES + kk * UMMA_K), bdesc, idesc,
+                         accum);
+          }
+          issued_any = true;
+          mma_commit(smem_u32(&empty[stage]));  // frees the stage once these MMAs finish
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&tfull[acc]));  // accumulator ready for the epilogue
+      }
+      if (*s_abort && issued_any) {  // wait for our MMAs before tensor memory is freed
+        mma_commit(smem_u32(drain));
+        mbar_wait_drain(smem_u32(drain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+    int it_local = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it_local) {
+      const int item = tile / NB, nb = tile - item * NB;
+      const int4 it = a.items[item];
+      const bool shared = it.x >= a.E;
+      const int row0 = it.y, rows = it.z;
+      const int acc = it_local % C::ACC_STAGES;
+      const uint32_t acc_phase = (uint32_t)(it_local / C::ACC_STAGES) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(smem_u32(&tfull[acc]), acc_phase, a.err, s_abort) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * C::ACC_COLS;
+      const int f = nb * BM + q * 32 + lane;  // feature (FFN1) / output channel (FFN2)
+      if (FFN1) {
+        const float* sc = shared ? a.sw13_scale : a.w13_scale + (size_t)it.x * 2 * a.I;
+        const float sg = sc[f], su = sc[a.I + f];
+        uint16_t* hout = static_cast<uint16_t*>(a.h);
+        for (int c0 = 0; c0 < rows; c0 += 16) {
+          uint32_t vg[16], vu[16];
+          __syncwarp();
+          tmem_ld16(tbase + c0, vg);
+          tmem_ld16(tbase + BN + c0, vu);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = c0 + j;
+            const int row = row0 + r;
+            if (r < rows && (unsigned)row < (unsigned)a.rows_total) {
+              const float xs = a.xscale[row];
+              const float g = (__uint_as_float(vg[j]) * xs) * sg;
+              const float u = (__uint_as_float(vu[j]) * xs) * su;
+              const float hv = g / (1.0f + expf(-g)) * u;
+              hout[(size_t)row * a.I + f] = (uint16_t)f32_bits_to_bf16(hv);
+            }
+          }
+        }
+      } else {
+        const float* sc = shared ? a.sw2_scale : a.w2_scale + (size_t)it.x * a.K;
+        const float s2 = sc[f];
+        uint16_t* yout = static_cast<uint16_t*>(a.y);
+        for (int c0 = 0; c0 < rows; c0 += 16) {
+          uint32_t v[16];
+          __syncwarp();
+          tmem_ld16(tbase + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = c0 + j;
+            const int row = row0 + r;
+            if (r < rows && (unsigned)row < (unsigned)a.rows_total) {
+              const float rw = (!shared && a.row_w) ? a.row_w[row] : 1.0f;
+              const float yv = ((__uint_as_float(v[j]) * a.hs[row]) * s2) * rw;
+              yout[(size_t)row * a.K + f] = (uint16_t)f32_bits_to_bf16(yv);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Byte tensor map with a 128-byte-wide, 128-byte-swizzled box.  rank 3:
+// {inner K, rows, groups} with box {128, box_rows, 1} (weights, one group per
+// expert; a single group still uses rank 3 because the loads are 3-D);
+// rank 2: {inner K, rows} with box {128, box_rows} (activation rows).
+bool make_map(CUtensorMap* m, int rank, const void* base, uint64_t inner, uint64_t rows,
+              uint64_t groups, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc || !base) return false;
+  cuuint64_t dims[3] = {inner, rows, groups};
+  cuuint64_t strides[2] = {inner, inner * rows};
+  cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool FFN1, int BN>
+cudaError_t launch_impl(const GroupedFfnArgs& a, cudaStream_t s) {
+  using C = Cfg<FFN1, BN>;
+  const int K = FFN1 ? a.K : a.I;      // reduction width
+  const int Wrows = FFN1 ? 2 * a.I : a.K;
+  const void* w = FFN1 ? a.w13 : a.w2;
+  const void* ws = FFN1 ? a.sw13 : a.sw2;
+  const void* x = FFN1 ? a.xq : a.hq;
+  CUtensorMap tw, tws, tx;
+  if (!make_map(&tw, 3, w, K, Wrows, a.E, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tws, 3, ws ? ws : w, K, Wrows, 1, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tx, 2, x, K, a.rows_total, 1, BN)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(grouped_ffn_kernel<FFN1, BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  grouped_ffn_kernel<FFN1, BN><<<device_sm_count(), kThreads, C::SMEM, s>>>(tw, tws, tx, a);
+  return cudaGetLastError();
+}
+
+template <bool FFN1>
+cudaError_t launch_bn(const GroupedFfnArgs& a, cudaStream_t s) {
+  switch (a.BN) {
+    case 32: return launch_impl<FFN1, 32>(a, s);
+    case 64: return launch_impl<FFN1, 64>(a, s);
+    case 128: return launch_impl<FFN1, 128>(a, s);
+    case 256: return launch_impl<FFN1, 256>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ffn1(const GroupedFfnArgs& a, cudaStream_t s) { return launch_bn<true>(a, s); }
+cudaError_t launch_ffn2(const GroupedFfnArgs& a, cudaStream_t s) { return launch_bn<false>(a, s); }
+
+}  // namespace moe

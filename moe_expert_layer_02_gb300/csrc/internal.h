@@ -1,0 +1,87 @@
+// internal.h -- host-side launchers shared between the translation units of
+// libmoe.so.  Not part of the public C ABI (include/moe.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Tokens per warp chunk in the index kernels (one token per lane).
+constexpr int kChunk = 32;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+inline int num_chunks(int T) { return (T + kChunk - 1) / kChunk; }
+
+// ---------------------------------------------------------------- route.cu
+cudaError_t launch_router_logits(const void* x, const float* wr, const float* bias, float* logits,
+                                 int T, int H, int E, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int32_t* idx, float* w, int T, int E, int k,
+                        cudaStream_t s);
+
+// ---------------------------------------------------------------- permute.cu
+// cc[e * nch + c] = #tokens of chunk c that picked expert e.
+cudaError_t launch_count(const int32_t* idx, int32_t* cc, int T, int E, int k, int* err,
+                         cudaStream_t s);
+// cbase[e * nch + c] = rows of expert e in chunks < c; cnt, off (E+1); then the
+// tile work list: groups 0..E-1 are the routed experts (rows off[g]..off[g+1]),
+// group E (if shared_rows > 0) covers rows shared_row0 .. shared_row0+shared_rows.
+cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t* off, int T, int E,
+                        int k, int4* items, int32_t* n_items, int max_items, int BN,
+                        int shared_row0, int shared_rows, cudaStream_t s);
+cudaError_t launch_items_from_offsets(const int32_t* off, int E, int4* items, int32_t* n_items,
+                                      int max_items, int BN, cudaStream_t s);
+cudaError_t launch_rank(const int32_t* idx, const float* topk_w, const int32_t* off,
+                        const int32_t* cbase, int32_t* perm, int32_t* src, float* row_w, int T,
+                        int E, int k, cudaStream_t s);
+// Per-token fp8 quantisation of x, copied to each routed row perm[t, :] and
+// (when shared_row0 >= 0) to row shared_row0 + t.
+cudaError_t launch_quant_scatter(const void* x, const int32_t* perm, void* xq, float* xscale,
+                                 int T, int H, int k, int shared_row0, int* err, cudaStream_t s);
+// Per-row fp8 requantisation of h [rows, I] bf16.
+cudaError_t launch_requant(const void* h, void* hq, float* hs, int rows, int I, cudaStream_t s);
+// out[t] = bf16(sum_j y[perm[t,j]] + shared[t]); shared may be NULL.
+cudaError_t launch_combine(const void* y, const int32_t* perm, const void* shared, void* out,
+                           int T, int H, int k, int* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- ffn_gemm.cu
+struct GroupedFfnArgs {
+  // work list
+  const int4* items;      // {group, row0, rows, 0}
+  const int32_t* n_items;
+  int max_items;
+  int E;                  // group index E is the shared expert
+  int K;                  // expert input/output width (H or latent)
+  int I;                  // expert intermediate width (shared must match)
+  int rows_total;         // rows in the activation buffers
+  // operands
+  const void* xq;         // [rows_total, K] e4m3
+  const float* xscale;    // [rows_total]
+  const float* row_w;     // [rows_total] or NULL (=1)
+  const void* w13;        // [E, 2I, K] e4m3
+  const float* w13_scale; // [E, 2I]
+  const void* w2;         // [E, K, I] e4m3
+  const float* w2_scale;  // [E, K]
+  const void* sw13;       // [2I, K] e4m3 or NULL
+  const float* sw13_scale;
+  const void* sw2;        // [K, I] e4m3 or NULL
+  const float* sw2_scale;
+  // intermediates / outputs
+  void* h;                // [rows_total, I] bf16
+  void* hq;               // [rows_total, I] e4m3
+  float* hs;              // [rows_total]
+  void* y;                // [rows_total, K] bf16
+  int BN;                 // token rows per tile (32, 64, 128, 256)
+  int* err;
+};
+
+cudaError_t launch_ffn1(const GroupedFfnArgs& a, cudaStream_t s);
+cudaError_t launch_ffn2(const GroupedFfnArgs& a, cudaStream_t s);
+
+// Shared helpers (moe_api.cu)
+int device_sm_count();
+void count_launch();
+
+}  // namespace moe

@@ -1,0 +1,499 @@
+// moe_api.cu -- the extern "C" boundary of libmoe.so (declared in include/moe.h).
+//
+// Host-side argument checks, the workspace plan, the per-device error word,
+// the launch counter, optional per-stage CUDA-event timing, and the sequence of
+// stage launches S1..S8 on the caller's stream.  No device memory is
+// allocated here: all scratch comes from the caller's workspace.
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__device__ int g_error_word;  // per-device fault word, see moe_get_last_error
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int64_t> g_launches{0};
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int* err = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+DeviceInfo* device_info() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+  DeviceInfo& di = g_dev[d];
+  if (!di.ready) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!di.ready) {
+      if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+        return nullptr;
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+      di.err = static_cast<int*>(p);
+      di.ready = true;
+    }
+  }
+  return &di;
+}
+
+// ------------------------------------------------------------------ profiling
+struct ProfRec {
+  int stage;
+  cudaEvent_t a, b;
+};
+std::atomic<bool> g_prof_on{false};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct StageTimer {
+  int stage;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  StageTimer(int st, cudaStream_t str) : stage(st), s(str) {
+    if (g_prof_on.load(std::memory_order_relaxed)) {
+      std::lock_guard<std::mutex> lk(g_prof_mu);
+      a = take_event();
+      if (a) cudaEventRecord(a, s);
+    }
+  }
+  ~StageTimer() {
+    if (!a) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    cudaEvent_t b = take_event();
+    if (!b) return;
+    cudaEventRecord(b, s);
+    g_prof.push_back({stage, a, b});
+  }
+};
+
+// ------------------------------------------------------------------ plan
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Plan {
+  int T, H, I, E, k, K, R, RT, nch, BN, max_items;
+  bool shared;
+  size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
+      hq, hs, y, total;
+};
+
+int choose_bn(const moe_problem* p) {
+  const char* env = std::getenv("MOE_TILE_N");
+  if (env) {
+    int v = std::atoi(env);
+    if (v == 32 || v == 64 || v == 128 || v == 256) return v;
+  }
+  const double avg = (double)p->T * p->top_k / (p->E > 0 ? p->E : 1);
+  if (avg <= 24.0) return 32;
+  if (avg <= 48.0) return 64;
+  if (avg <= 96.0) return 128;
+  return 256;
+}
+
+Plan make_plan(const moe_problem* p) {
+  Plan q{};
+  q.T = p->T;
+  q.H = p->H;
+  q.I = p->I;
+  q.E = p->E;
+  q.k = p->top_k;
+  q.K = p->latent > 0 ? p->latent : p->H;
+  q.R = p->T * p->top_k;
+  q.shared = p->I_shared > 0;
+  q.RT = q.R + (q.shared ? p->T : 0);
+  q.nch = num_chunks(p->T);
+  q.BN = choose_bn(p);
+  q.max_items = (q.R + q.BN - 1) / q.BN + q.E + (q.shared ? (p->T + q.BN - 1) / q.BN + 1 : 0) + 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const size_t T = q.T, E = q.E, k = q.k, R = q.R, RT = q.RT;
+  q.logits = take(T * E * 4);
+  q.idx = take(T * k * 4);
+  q.tw = take(T * k * 4);
+  q.cc = take(E * q.nch * 4);
+  q.cbase = take(E * q.nch * 4);
+  q.cnt = take(E * 4);
+  q.off = take((E + 1) * 4);
+  q.perm = take(T * k * 4);
+  q.src = take(R * 4);
+  q.row_w = take(RT * 4);
+  q.xscale = take(RT * 4);
+  q.items = take((size_t)q.max_items * 16);
+  q.n_items = take(16);
+  q.xq = take(RT * (size_t)q.K);
+  q.h = take(RT * (size_t)q.I * 2);
+  q.hq = take(RT * (size_t)q.I);
+  q.hs = take(RT * 4);
+  q.y = take(RT * (size_t)q.K * 2);
+  q.total = o;
+  return q;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ------------------------------------------------------------------ checks
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_problem(const moe_problem* p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (p->top_k > p->E || p->top_k > kMaxTopK || p->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (p->H % 128 || p->I % 128 || p->I_shared < 0 || p->I_shared % 128 || p->latent < 0 ||
+      p->latent % 128)
+    return MOE_ERR_INVALID_ARG;
+  if (p->wfmt != MOE_W_FP8_E4M3_PER_CHANNEL && p->wfmt != MOE_W_MXFP4_E2M1_E8M0_B32)
+    return MOE_ERR_INVALID_ARG;
+  if ((int64_t)p->T * p->top_k > (1 << 30) || (int64_t)p->T * p->H > (int64_t)1 << 40)
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// Shapes this build runs on the GPU.
+int check_supported(const moe_problem* p) {
+  if (p->wfmt != MOE_W_FP8_E4M3_PER_CHANNEL || p->latent > 0) return MOE_ERR_UNSUPPORTED;
+  if (p->I_shared > 0 && ((p->flags & MOE_F_SHARED_BF16) || p->I_shared != p->I))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                 \
+  do {                                \
+    cudaError_t _e = (expr);          \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xscale,
+                        const float* row_w, const void* w13, const void* w13_scale,
+                        const void* w2, const void* w2_scale, const void* sw13,
+                        const void* sw13_scale, const void* sw2, const void* sw2_scale, void* y,
+                        int rows_total, int* err) {
+  GroupedFfnArgs a{};
+  a.items = at<int4>(ws, q.items);
+  a.n_items = at<int32_t>(ws, q.n_items);
+  a.max_items = q.max_items;
+  a.E = q.E;
+  a.K = q.K;
+  a.I = q.I;
+  a.rows_total = rows_total;
+  a.xq = xq;
+  a.xscale = xscale;
+  a.row_w = row_w;
+  a.w13 = w13;
+  a.w13_scale = static_cast<const float*>(w13_scale);
+  a.w2 = w2;
+  a.w2_scale = static_cast<const float*>(w2_scale);
+  a.sw13 = sw13;
+  a.sw13_scale = static_cast<const float*>(sw13_scale);
+  a.sw2 = sw2;
+  a.sw2_scale = static_cast<const float*>(sw2_scale);
+  a.h = at<void>(ws, q.h);
+  a.hq = at<void>(ws, q.hq);
+  a.hs = at<float>(ws, q.hs);
+  a.y = y;
+  a.BN = q.BN;
+  a.err = err;
+  return a;
+}
+
+int run_experts(const Plan& q, const GroupedFfnArgs& a, int rows_total, cudaStream_t s) {
+  {
+    StageTimer t(MOE_STAGE_FFN1, s);
+    MOE_TRY(launch_ffn1(a, s));
+  }
+  {
+    StageTimer t(MOE_STAGE_REQUANT, s);
+    MOE_TRY(launch_requant(a.h, a.hq, a.hs, rows_total, q.I, s));
+  }
+  {
+    StageTimer t(MOE_STAGE_FFN2, s);
+    MOE_TRY(launch_ffn2(a, s));
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  DeviceInfo* d = device_info();
+  return d ? d->sms : 1;
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+size_t moe_workspace_bytes(const moe_problem* p) {
+  if (check_problem(p) != MOE_OK) return 0;
+  return make_plan(p).total;
+}
+
+int moe_router_logits(const moe_problem* p, const void* x, const float* router_w,
+                      const float* bias, float* logits, void* stream) {
+  int st = check_problem(p);
+  if (st) return st;
+  if (!x || !router_w || !logits) return MOE_ERR_INVALID_ARG;
+  if ((p->flags & MOE_F_ROUTER_BIAS) && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(router_w, 16)) return MOE_ERR_INVALID_ARG;
+  if (p->T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StageTimer t(MOE_STAGE_ROUTER, s);
+  return cuda_status(launch_router_logits(x, router_w, (p->flags & MOE_F_ROUTER_BIAS) ? bias : nullptr,
+                                          logits, p->T, p->H, p->E, s));
+}
+
+int moe_route(const moe_problem* p, const float* logits, int32_t* topk_idx, float* topk_w,
+              void* stream) {
+  int st = check_problem(p);
+  if (st) return st;
+  if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (p->T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StageTimer t(MOE_STAGE_TOPK, s);
+  return cuda_status(launch_topk(logits, topk_idx, topk_w, p->T, p->E, p->top_k, s));
+}
+
+int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, int32_t* counts,
+                int32_t* offsets, int32_t* perm, int32_t* src_row, void* xq_perm,
+                float* xscale_perm, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_problem(p);
+  if (st) return st;
+  if (!topk_idx || !x || !counts || !offsets || !perm || !src_row || !xq_perm || !xscale_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xq_perm, 16)) return MOE_ERR_INVALID_ARG;
+  const Plan q = make_plan(p);
+  if (!ws || ws_bytes < q.total || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  if (p->T == 0) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MOE_TRY(cudaMemsetAsync(counts, 0, sizeof(int32_t) * p->E, s));
+    MOE_TRY(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (p->E + 1), s));
+    return MOE_OK;
+  }
+  const int K = q.K;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    StageTimer t(MOE_STAGE_INDEX, s);
+    MOE_TRY(launch_count(topk_idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
+    MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), counts, offsets, q.T, q.E,
+                        q.k, nullptr, nullptr, 0, q.BN, 0, 0, s));
+    MOE_TRY(launch_rank(topk_idx, nullptr, offsets, at<int32_t>(ws, q.cbase), perm, src_row,
+                        nullptr, q.T, q.E, q.k, s));
+  }
+  {
+    StageTimer t(MOE_STAGE_SCATTER, s);
+    MOE_TRY(launch_quant_scatter(x, perm, xq_perm, xscale_perm, q.T, K, q.k, -1, di->err, s));
+  }
+  return MOE_OK;
+}
+
+int moe_expert_ffn(const moe_problem* p, const int32_t* offsets, const void* xq_perm,
+                   const float* xscale_perm, const float* row_w, const void* w13,
+                   const void* w13_scale, const void* w2, const void* w2_scale, void* y,
+                   void* ws, size_t ws_bytes, void* stream) {
+  int st = check_problem(p);
+  if (st) return st;
+  if (!offsets || !xq_perm || !xscale_perm || !w13 || !w13_scale || !w2 || !w2_scale || !y)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(xq_perm, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y, 16))
+    return MOE_ERR_INVALID_ARG;
+  st = check_supported(p);
+  if (st) return st;
+  const Plan q = make_plan(p);
+  if (!ws || ws_bytes < q.total || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  if (p->T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    StageTimer t(MOE_STAGE_INDEX, s);
+    MOE_TRY(launch_items_from_offsets(offsets, q.E, at<int4>(ws, q.items),
+                                      at<int32_t>(ws, q.n_items), q.max_items, q.BN, s));
+  }
+  GroupedFfnArgs a = ffn_args(q, ws, xq_perm, xscale_perm, row_w, w13, w13_scale, w2, w2_scale,
+                              nullptr, nullptr, nullptr, nullptr, y, q.R, di->err);
+  return run_experts(q, a, q.R, s);
+}
+
+int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
+                  const void* shared, void* out, void* stream) {
+  int st = check_problem(p);
+  if (st) return st;
+  if (!y_rows || !perm || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y_rows, 16) || !aligned(out, 16) || (shared && !aligned(shared, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if (p->T == 0) return MOE_OK;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StageTimer t(MOE_STAGE_COMBINE, s);
+  return cuda_status(launch_combine(y_rows, perm, shared, out, p->T, p->H, p->top_k, di->err, s));
+}
+
+int moe_forward(const moe_problem* p, const void* x, const float* router_w,
+                const float* router_bias, const void* w13, const void* w13_scale,
+                const void* w2, const void* w2_scale, const void* shared_w13,
+                const void* shared_w13_scale, const void* shared_w2,
+                const void* shared_w2_scale, const void* latent_down, const void* latent_up,
+                const void* latent_gamma, void* out, void* ws, size_t ws_bytes, void* stream) {
+  (void)latent_down;
+  (void)latent_up;
+  (void)latent_gamma;
+  int st = check_problem(p);
+  if (st) return st;
+  if (!x || !router_w || !w13 || !w13_scale || !w2 || !w2_scale || !out) return MOE_ERR_INVALID_ARG;
+  if ((p->flags & MOE_F_ROUTER_BIAS) && !router_bias) return MOE_ERR_INVALID_ARG;
+  if (p->I_shared > 0 && (!shared_w13 || !shared_w2)) return MOE_ERR_INVALID_ARG;
+  if (p->I_shared > 0 && !(p->flags & MOE_F_SHARED_BF16) && (!shared_w13_scale || !shared_w2_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
+      !aligned(out, 16) || (shared_w13 && !aligned(shared_w13, 16)) ||
+      (shared_w2 && !aligned(shared_w2, 16)))
+    return MOE_ERR_INVALID_ARG;
+  st = check_supported(p);
+  if (st) return st;
+  const Plan q = make_plan(p);
+  if (!ws || ws_bytes < q.total || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  if (p->T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* logits = at<float>(ws, q.logits);
+  int32_t* idx = at<int32_t>(ws, q.idx);
+  float* tw = at<float>(ws, q.tw);
+  int32_t* off = at<int32_t>(ws, q.off);
+  int32_t* perm = at<int32_t>(ws, q.perm);
+  float* row_w = at<float>(ws, q.row_w);
+  float* xscale = at<float>(ws, q.xscale);
+  uint8_t* xq = at<uint8_t>(ws, q.xq);
+  uint16_t* y = at<uint16_t>(ws, q.y);
+  {
+    StageTimer t(MOE_STAGE_ROUTER, s);
+    MOE_TRY(launch_router_logits(x, router_w, (p->flags & MOE_F_ROUTER_BIAS) ? router_bias : nullptr,
+                                 logits, q.T, q.H, q.E, s));
+  }
+  {
+    StageTimer t(MOE_STAGE_TOPK, s);
+    MOE_TRY(launch_topk(logits, idx, tw, q.T, q.E, q.k, s));
+  }
+  {
+    StageTimer t(MOE_STAGE_INDEX, s);
+    MOE_TRY(launch_count(idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
+    MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), at<int32_t>(ws, q.cnt), off,
+                        q.T, q.E, q.k, at<int4>(ws, q.items), at<int32_t>(ws, q.n_items),
+                        q.max_items, q.BN, q.R, q.shared ? q.T : 0, s));
+    MOE_TRY(launch_rank(idx, tw, off, at<int32_t>(ws, q.cbase), perm, at<int32_t>(ws, q.src), row_w,
+                        q.T, q.E, q.k, s));
+  }
+  {
+    StageTimer t(MOE_STAGE_SCATTER, s);
+    MOE_TRY(launch_quant_scatter(x, perm, xq, xscale, q.T, q.H, q.k, q.shared ? q.R : -1, di->err, s));
+  }
+  GroupedFfnArgs a = ffn_args(q, ws, xq, xscale, row_w, w13, w13_scale, w2, w2_scale, shared_w13,
+                              shared_w13_scale, shared_w2, shared_w2_scale, y, q.RT, di->err);
+  st = run_experts(q, a, q.RT, s);
+  if (st) return st;
+  {
+    StageTimer t(MOE_STAGE_COMBINE, s);
+    MOE_TRY(launch_combine(y, perm, q.shared ? y + (size_t)q.R * q.H : nullptr, out, q.T, q.H, q.k,
+                           di->err, s));
+  }
+  return MOE_OK;
+}
+
+int moe_get_last_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, di->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (v != 0) {
+    int zero = 0;
+    if (cudaMemcpy(di->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return v;
+}
+
+int64_t moe_launch_count(void) { return g_launches.load(); }
+
+int moe_profile_enable(int on) {
+  g_prof_on.store(on != 0);
+  return MOE_OK;
+}
+
+int moe_profile_read(double* stage_ms, int64_t* stage_launches) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (int i = 0; i < MOE_STAGE_COUNT; ++i) {
+    if (stage_ms) stage_ms[i] = 0.0;
+    if (stage_launches) stage_launches[i] = 0;
+  }
+  int rc = MOE_OK;
+  for (const ProfRec& r : g_prof) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+      rc = MOE_ERR_CUDA;
+    if (r.stage >= 0 && r.stage < MOE_STAGE_COUNT) {
+      if (stage_ms) stage_ms[r.stage] += ms;
+      if (stage_launches) stage_launches[r.stage] += 1;
+    }
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  return rc;
+}
+
+}  // extern "C"

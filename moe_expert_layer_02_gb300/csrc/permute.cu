@@ -1,0 +1,404 @@
+// permute.cu -- routing metadata, scatter and gather kernels.
+//
+// S3  per-expert counts, offsets and a stable rank of every (token, slot) pair
+//     ("Optimising Ling-2.6-1T on TPU with SGLang-JAX", s.6: the metadata block
+//     holds the token->expert map, per-expert offsets/counts and the
+//     scatter/gather indices; it moves little data).
+// S4  dynamic per-token fp8 quantisation applied before the scatter (same
+//     write-up, s.5 "activation quantisation"), then 16-byte row copies into
+//     expert-contiguous order.  On one GPU the ICI scatter is this local copy.
+// S6a per-row fp8 requantisation of the bf16 intermediate.
+// S7  weighted gather back to token order plus the shared-expert rows
+//     (s.1 "gather results"; s.5 in-kernel shared expert).
+//
+// Determinism: counts are order-independent; the rank of a pair inside its
+// 32-token chunk comes from a per-warp bitmask table (popcount of the lanes
+// below), and chunk bases from a prefix scan, so every row index is fixed.
+#include "device.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 8;  // warps per block in the index kernels
+
+// Build, for the warp's 32-token chunk, bits[e] = mask of lanes whose token
+// picked expert e.  Returns false for the lane if its token is out of range.
+__device__ __forceinline__ void build_chunk_bits(const int32_t* __restrict__ idx, uint32_t* bits,
+                                                 int t, int T, int E, int k, int lane, int* err) {
+  for (int e = lane; e < E; e += 32) bits[e] = 0u;
+  __syncwarp();
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      int e = idx[(size_t)t * k + j];
+      if ((unsigned)e < (unsigned)E)
+        atomicOr(&bits[e], 1u << lane);
+      else
+        record_error(err, kErrInvalidArg);
+    }
+  }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    count_kernel(const int32_t* __restrict__ idx, int32_t* __restrict__ cc, int T, int E, int k,
+                 int nch, int* err) {
+  extern __shared__ uint32_t s_bits[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kWarps + warp;
+  if (c >= nch) return;  // whole warp leaves together
+  uint32_t* bits = s_bits + warp * E;
+  build_chunk_bits(idx, bits, c * kChunk + lane, T, E, k, lane, err);
+  for (int e = lane; e < E; e += 32) cc[(size_t)e * nch + c] = __popc(bits[e]);
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    rank_kernel(const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
+                const int32_t* __restrict__ off, const int32_t* __restrict__ cbase,
+                int32_t* __restrict__ perm, int32_t* __restrict__ src, float* __restrict__ row_w,
+                int T, int E, int k, int nch) {
+  extern __shared__ uint32_t s_bits[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kWarps + warp;
+  if (c >= nch) return;
+  uint32_t* bits = s_bits + warp * E;
+  const int t = c * kChunk + lane;
+  build_chunk_bits(idx, bits, t, T, E, k, lane, nullptr);
+  if (t >= T) return;
+  const uint32_t below = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    int e = idx[(size_t)t * k + j];
+    if ((unsigned)e >= (unsigned)E) continue;
+    int row = off[e] + cbase[(size_t)e * nch + c] + __popc(bits[e] & below);
+    perm[(size_t)t * k + j] = row;
+    src[row] = t;
+    if (row_w) row_w[row] = topk_w[(size_t)t * k + j];
+  }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+    int z = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
+    }
+    s_warp[lane] = z - w;  // exclusive warp base
+    if (lane == 31) s_warp[32] = z;
+  }
+  __syncthreads();
+  int res = s_warp[warp] + x - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return res;
+}
+
+// Tile work list over groups 0..E-1 (offsets) and, when shared_rows > 0, one
+// more group for the shared expert.  Items are {group, row0, rows, 0} with
+// rows <= BN, in group order.  Called by every thread of a 1024-thread block.
+__device__ void build_items(const int32_t* off, int E, int BN, int shared_row0, int shared_rows,
+                            int4* items, int32_t* n_items, int max_items, int* s_warp) {
+  const int G = E + (shared_rows > 0 ? 1 : 0);
+  int carry = 0;
+  for (int base = 0; base < G; base += blockDim.x) {
+    const int g = base + threadIdx.x;
+    int n = 0, start = 0, rows = 0;
+    if (g < G) {
+      if (g < E) {
+        start = off[g];
+        rows = off[g + 1] - start;
+      } else {
+        start = shared_row0;
+        rows = shared_rows;
+      }
+      n = (rows + BN - 1) / BN;
+    }
+    int total;
+    const int ex = block_exclusive_scan(n, s_warp, &total);
+    for (int i = 0; i < n; ++i) {
+      int id = carry + ex + i;
+      if (id < max_items) items[id] = make_int4(g, start + i * BN, min(BN, rows - i * BN), 0);
+    }
+    carry += total;
+  }
+  if (threadIdx.x == 0) *n_items = min(carry, max_items);
+}
+
+__global__ void __launch_bounds__(1024)
+    scan_kernel(const int32_t* __restrict__ cc, int32_t* __restrict__ cbase, int32_t* cnt,
+                int32_t* off, int E, int nch, int R, int4* items, int32_t* n_items, int max_items,
+                int BN, int shared_row0, int shared_rows) {
+  __shared__ int s_cnt[kMaxExperts + 1];
+  __shared__ int s_warp[33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += 32) {
+    int run = 0;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = (c < nch) ? cc[(size_t)e * nch + c] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (c < nch) cbase[(size_t)e * nch + c] = run + x - v;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) s_cnt[e] = run;
+  }
+  __syncthreads();
+  const int v = threadIdx.x < E ? s_cnt[threadIdx.x] : 0;
+  int total;
+  const int ex = block_exclusive_scan(v, s_warp, &total);
+  if (threadIdx.x < E) {
+    cnt[threadIdx.x] = v;
+    off[threadIdx.x] = ex;
+    s_cnt[threadIdx.x] = ex;
+  }
+  if (threadIdx.x == 0) {
+    off[E] = total;  // == R when every index was valid
+    s_cnt[E] = total;
+  }
+  __syncthreads();
+  if (items) build_items(s_cnt, E, BN, shared_row0, shared_rows, items, n_items, max_items, s_warp);
+}
+
+__global__ void __launch_bounds__(1024)
+    items_kernel(const int32_t* __restrict__ off, int E, int4* items, int32_t* n_items,
+                 int max_items, int BN) {
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_warp[33];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = off[e];
+  __syncthreads();
+  build_items(s_off, E, BN, 0, 0, items, n_items, max_items, s_warp);
+}
+
+// Block-wide max of non-negative floats (blockDim.x == 256).
+__device__ __forceinline__ float block_max256(float v, float* s_red) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float w = lane < 8 ? s_red[lane] : 0.0f;
+    w = warp_max(w);
+    if (lane == 0) s_red[8] = w;
+  }
+  __syncthreads();
+  float r = s_red[8];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+    f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+}
+
+// q = e4m3(v / s) for 8 values (fp32 IEEE division, round-to-nearest-even).
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lo |= (uint32_t)f32_to_e4m3(f[i] / s) << (8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) hi |= (uint32_t)f32_to_e4m3(f[4 + i] / s) << (8 * i);
+  return make_uint2(lo, hi);
+}
+
+__global__ void __launch_bounds__(256)
+    quant_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                         uint8_t* __restrict__ xq, float* __restrict__ xscale, int H, int k,
+                         int shared_row0, int R, int* err) {
+  __shared__ float s_red[9];
+  __shared__ int s_rows[kMaxTopK + 1];
+  const int t = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  const int nv = H / 8;
+  float amax = 0.0f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float f[8];
+    unpack_bf16x8(xr[v], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+  amax = block_max256(amax, s_red);
+  const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+  const int nrows = k + (shared_row0 >= 0 ? 1 : 0);
+  if (threadIdx.x < k) {
+    // rows come from the rank pass; anything outside [0, R) (possible only for
+    // invalid expert indices) is dropped rather than written
+    int row = perm[(size_t)t * k + threadIdx.x];
+    if ((unsigned)row >= (unsigned)R) {
+      record_error(err, kErrInvalidArg);
+      row = -1;
+    }
+    s_rows[threadIdx.x] = row;
+  }
+  if (threadIdx.x == k && shared_row0 >= 0) s_rows[k] = shared_row0 + t;
+  __syncthreads();
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float f[8];
+    unpack_bf16x8(xr[v], f);
+    const uint2 q = quant8(f, s);
+    for (int j = 0; j < nrows; ++j)
+      if (s_rows[j] >= 0) *reinterpret_cast<uint2*>(xq + (size_t)s_rows[j] * H + (size_t)v * 8) = q;
+  }
+  if (threadIdx.x < nrows && s_rows[threadIdx.x] >= 0) xscale[s_rows[threadIdx.x]] = s;
+}
+
+__global__ void __launch_bounds__(256)
+    requant_kernel(const uint16_t* __restrict__ h, uint8_t* __restrict__ hq, float* __restrict__ hs,
+                   int I) {
+  __shared__ float s_red[9];
+  const size_t r = blockIdx.x;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + r * I);
+  const int nv = I / 8;
+  float amax = 0.0f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float f[8];
+    unpack_bf16x8(hr[v], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+  amax = block_max256(amax, s_red);
+  const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float f[8];
+    unpack_bf16x8(hr[v], f);
+    *reinterpret_cast<uint2*>(hq + r * I + (size_t)v * 8) = quant8(f, s);
+  }
+  if (threadIdx.x == 0) hs[r] = s;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(a, b);  // a -> low half
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__global__ void __launch_bounds__(256)
+    combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ perm,
+                   const uint16_t* __restrict__ shared, uint16_t* __restrict__ out, int H, int k,
+                   int R, int* err) {
+  __shared__ int s_rows[kMaxTopK];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    int row = perm[(size_t)t * k + threadIdx.x];
+    if ((unsigned)row >= (unsigned)R) {  // invalid permutation entry: contributes nothing
+      record_error(err, kErrInvalidArg);
+      row = -1;
+    }
+    s_rows[threadIdx.x] = row;
+  }
+  __syncthreads();
+  const int nv = H / 8;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      if (s_rows[j] < 0) continue;
+      float f[8];
+      unpack_bf16x8(reinterpret_cast<const uint4*>(y + (size_t)s_rows[j] * H)[v], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+    }
+    if (shared) {
+      float f[8];
+      unpack_bf16x8(reinterpret_cast<const uint4*>(shared + (size_t)t * H)[v], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_count(const int32_t* idx, int32_t* cc, int T, int E, int k, int* err,
+                         cudaStream_t s) {
+  const int nch = num_chunks(T);
+  const int blocks = (nch + kWarps - 1) / kWarps;
+  const size_t smem = (size_t)kWarps * E * sizeof(uint32_t);
+  count_launch();
+  count_kernel<<<blocks, kWarps * 32, smem, s>>>(idx, cc, T, E, k, nch, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t* off, int T, int E,
+                        int k, int4* items, int32_t* n_items, int max_items, int BN,
+                        int shared_row0, int shared_rows, cudaStream_t s) {
+  count_launch();
+  scan_kernel<<<1, 1024, 0, s>>>(cc, cbase, cnt, off, E, num_chunks(T), T * k, items, n_items,
+                                 max_items, BN, shared_row0, shared_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_items_from_offsets(const int32_t* off, int E, int4* items, int32_t* n_items,
+                                      int max_items, int BN, cudaStream_t s) {
+  count_launch();
+  items_kernel<<<1, 1024, 0, s>>>(off, E, items, n_items, max_items, BN);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rank(const int32_t* idx, const float* topk_w, const int32_t* off,
+                        const int32_t* cbase, int32_t* perm, int32_t* src, float* row_w, int T,
+                        int E, int k, cudaStream_t s) {
+  const int nch = num_chunks(T);
+  const int blocks = (nch + kWarps - 1) / kWarps;
+  const size_t smem = (size_t)kWarps * E * sizeof(uint32_t);
+  count_launch();
+  rank_kernel<<<blocks, kWarps * 32, smem, s>>>(idx, topk_w, off, cbase, perm, src, row_w, T, E,
+                                                 k, nch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_scatter(const void* x, const int32_t* perm, void* xq, float* xscale,
+                                 int T, int H, int k, int shared_row0, int* err, cudaStream_t s) {
+  count_launch();
+  quant_scatter_kernel<<<T, 256, 0, s>>>(static_cast<const uint16_t*>(x), perm,
+                                         static_cast<uint8_t*>(xq), xscale, H, k, shared_row0,
+                                         T * k, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_requant(const void* h, void* hq, float* hs, int rows, int I, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  count_launch();
+  requant_kernel<<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(h), static_cast<uint8_t*>(hq),
+                                      hs, I);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* perm, const void* shared, void* out,
+                           int T, int H, int k, int* err, cudaStream_t s) {
+  count_launch();
+  combine_kernel<<<T, 256, 0, s>>>(static_cast<const uint16_t*>(y), perm,
+                                   static_cast<const uint16_t*>(shared),
+                                   static_cast<uint16_t*>(out), H, k, T * k, err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

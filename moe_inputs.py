@@ -118,13 +118,15 @@ def _bf16_randn(shape, fan_in, gen, device):
     return (torch.randn(shape, generator=gen, device=device) / math.sqrt(fan_in)).to(torch.bfloat16)
 
 
-def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0) -> dict:
+def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, expert_weights: dict | None = None) -> dict:
     """All layer inputs for ``cfg`` as torch tensors on ``device``.
 
     Keys: x (bf16 [T,H]), router_w (f32 [E,H]), router_bias (f32 [E] or None),
     w13 / w2 (uint8 bytes), w13_scale / w2_scale (f32 for fp8, uint8 e8m0 for
     mxfp4), sw13 / sw2 (+ scales for fp8; bf16 when shared_bf16), wd / wu / gamma
-    (latent case, bf16).
+    (latent case, bf16).  ``expert_weights`` (a previous result for the same
+    E, I, K, I_s, weight format and seed) is reused instead of regenerating the
+    expert, shared and latent weights, which depend only on those.
     """
     device = torch.device(device)
     g = torch.Generator().manual_seed(seed)
@@ -138,6 +140,12 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0) -> dict:
         p = rank.pow(-1.2)
         p = p / p.sum()
         out["router_bias"] = (2.0 * torch.log(p)).float().to(device)
+
+    if expert_weights is not None:
+        for key in ("w13", "w13_scale", "w2", "w2_scale", "sw13", "sw13_scale", "sw2",
+                    "sw2_scale", "wd", "wu", "gamma"):
+            out[key] = expert_weights[key]
+        return out
 
     if cfg.wfmt == "fp8":
         w13 = torch.empty(E, 2 * I, K, dtype=torch.uint8, device=device)

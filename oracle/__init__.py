@@ -89,6 +89,7 @@ def lib():
                                       P, P, P, P, ctypes.c_int]
         L.orc_expert_rows.argtypes = [i32, i64, i64, i64, P, P, P, P, P, P, P, P, P, P, P, P,
                                       ctypes.c_int]
+        L.orc_combine.argtypes = [i64, i64, ctypes.c_int, P, P, P, P]
         _lib = L
     return _lib
 
@@ -212,6 +213,18 @@ def expert_rows(wfmt, off, xq, xs, row_w, w13, w13_scale, w2, w2_scale, want_h=F
                           _p(w13_scale), _p(w2), _p(w2_scale), _p(y), _p(h), _p(hq), _p(hs),
                           nthreads)
     return (y, h, hq, hs) if want_h else y
+
+
+def combine(y_bf16_u16, perm, shared_bf16_u16=None):
+    """S7: out[t] = bf16(sum_j y[perm[t,j]] + shared[t]) (fp64 sum), uint16 bits."""
+    y = _c(y_bf16_u16, np.uint16)
+    perm = _c(perm, np.int32)
+    T, k = perm.shape
+    H = y.shape[1]
+    sh = None if shared_bf16_u16 is None else _c(shared_bf16_u16, np.uint16)
+    out = np.empty((T, H), dtype=np.uint16)
+    lib().orc_combine(T, H, k, _p(y), _p(perm), _p(sh), _p(out))
+    return out
 
 
 def moe_forward(prob: dict, w: dict, tokens=None, nthreads: int = 0):

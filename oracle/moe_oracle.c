@@ -328,11 +328,23 @@ void orc_quant_rows(int64_t T, int64_t H, const uint16_t* x, float* scale, uint8
  * width L), N its output width (same as K). */
 enum { ORC_FP8 = 0, ORC_MXFP4 = 1 };
 
+/* Decode tables filled once from the decoders above (lookup instead of a call
+ * per element; same values). */
+static double tab_e4m3[256], tab_e2m1[16], tab_e8m0[256];
+static pthread_once_t tab_once = PTHREAD_ONCE_INIT;
+static void fill_tables(void) {
+  for (int c = 0; c < 256; c++) {
+    tab_e4m3[c] = orc_e4m3_decode((uint8_t)c);
+    tab_e8m0[c] = orc_e8m0_decode((uint8_t)c);
+  }
+  for (int c = 0; c < 16; c++) tab_e2m1[c] = orc_e2m1_decode((uint8_t)c);
+}
+
 static double weight_at(int fmt, const uint8_t* wrow, const void* srow, int64_t k) {
-  if (fmt == ORC_FP8) return orc_e4m3_decode(wrow[k]);
+  if (fmt == ORC_FP8) return tab_e4m3[wrow[k]];
   uint8_t byte = wrow[k / 2];
   uint8_t nib = (k & 1) ? (byte >> 4) : (byte & 15);
-  return orc_e2m1_decode(nib) * orc_e8m0_decode(((const uint8_t*)srow)[k / 32]);
+  return tab_e2m1[nib] * tab_e8m0[((const uint8_t*)srow)[k / 32]];
 }
 
 /* y[n] = (sum_i hq_i W2[n,i]) * s_h * s2[n] (fp8 also applies the per-channel
@@ -348,7 +360,7 @@ static void expert_ffn(int fmt, int64_t K, int64_t I, const uint8_t* xq, float s
   uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
   uint8_t* hq = (uint8_t*)malloc((size_t)I);
   double* hd = (double*)malloc(sizeof(double) * (size_t)I);
-  for (int64_t k = 0; k < K; k++) xd[k] = orc_e4m3_decode(xq[k]);
+  for (int64_t k = 0; k < K; k++) xd[k] = tab_e4m3[xq[k]];
   for (int64_t n = 0; n < I; n++) {
     const uint8_t* wg = w13 + n * rowb13;
     const uint8_t* wu = w13 + (I + n) * rowb13;
@@ -374,7 +386,7 @@ static void expert_ffn(int fmt, int64_t K, int64_t I, const uint8_t* xq, float s
     hf[n] = bf16_to_float(hb[n]);
   }
   float s_h = quant_row(I, hf, hq);
-  for (int64_t i = 0; i < I; i++) hd[i] = orc_e4m3_decode(hq[i]);
+  for (int64_t i = 0; i < I; i++) hd[i] = tab_e4m3[hq[i]];
   for (int64_t n = 0; n < K; n++) {
     const uint8_t* wr = w2 + n * rowb2;
     const void* sr = (fmt == ORC_FP8) ? NULL : (const void*)((const uint8_t*)s2 + n * rows2);
@@ -564,6 +576,7 @@ static void token_forward(int64_t i, void* c) {
 void orc_moe_forward(const orc_problem* p, const orc_weights* w, const int32_t* tokens,
                      int64_t n_tokens, double* out_f64, uint16_t* out_bf16, int32_t* idx_out,
                      double* w_out, int nthreads) {
+  pthread_once(&tab_once, fill_tables);
   fwd_ctx c = {p, w, tokens, out_f64, out_bf16, idx_out, w_out};
   orc_parallel_for(n_tokens, nthreads, token_forward, &c);
 }
@@ -615,6 +628,22 @@ void orc_expert_rows(int32_t wfmt, int64_t K, int64_t I, int64_t E, const int32_
                      const uint8_t* xq, const float* xs, const float* row_w, const uint8_t* w13,
                      const void* w13_scale, const uint8_t* w2, const void* w2_scale, double* y,
                      uint16_t* h, uint8_t* hq, float* hs, int nthreads) {
+  pthread_once(&tab_once, fill_tables);
   rows_ctx c = {wfmt, K, I, E, off, xq, xs, row_w, w13, w13_scale, w2, w2_scale, y, h, hq, hs};
   orc_parallel_for(off[E], nthreads, rows_body, &c);
+}
+
+/* S7: weighted gather back to token order [LING s.1 "gather results"; s.5
+ * shared expert added on every token]: out[t] = bf16(sum_j y[perm[t,j]] +
+ * shared[t]) with the routing weights already inside the y rows; the sum is
+ * taken in fp64 over the given bf16 values, j ascending, shared last. */
+void orc_combine(int64_t T, int64_t H, int k, const uint16_t* y, const int32_t* perm,
+                 const uint16_t* shared, uint16_t* out) {
+  for (int64_t t = 0; t < T; t++)
+    for (int64_t h = 0; h < H; h++) {
+      double acc = 0.0;
+      for (int j = 0; j < k; j++) acc += orc_bf16_decode(y[(int64_t)perm[t * k + j] * H + h]);
+      if (shared) acc += orc_bf16_decode(shared[t * H + h]);
+      out[t * H + h] = orc_bf16_from_double(acc);
+    }
 }

@@ -1,0 +1,111 @@
+"""Shared helpers for the -m gpu parity tests: seeded inputs on the device, their
+host copies for the oracle, the C-ABI problem struct, and the output tolerance.
+
+Tolerance (fp32-accumulated output, stated for this layer): relative L2 error
+<= 1e-2 and max-abs error <= 5e-2 x RMS(reference).  Integer and byte outputs
+(routing indices, counts, offsets, permutation, fp8 codes) are compared
+bit for bit.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import moe_inputs as mi
+
+REL_L2 = 1e-2
+MAX_ABS_RMS = 5e-2
+
+
+@functools.lru_cache(maxsize=None)
+def lib():
+    from moe_expert_layer_02_gb300 import build
+    build.build()
+    import moe_expert_layer_02_gb300 as m
+    m.load_library()
+    return m
+
+
+_weights_cache: dict = {}
+
+
+def gpu_inputs(cfg: mi.MoEConfig, seed: int = 0) -> dict:
+    """Inputs on cuda:0; expert weights are shared between configs of equal shape."""
+    key = (cfg.E, cfg.I, cfg.K, cfg.I_s, cfg.wfmt, cfg.shared_bf16, cfg.H, cfg.L, seed)
+    reuse = _weights_cache.get(key)
+    inp = mi.make_inputs(cfg, device="cuda", seed=seed, expert_weights=reuse)
+    if reuse is None:
+        _weights_cache.clear()  # keep at most one large weight set resident
+        _weights_cache[key] = inp
+    return inp
+
+
+_host_cache: dict = {}
+
+
+def host(inp: dict, keys=None) -> dict:
+    """numpy copies for the oracle (weights cached by identity)."""
+    out = {}
+    for k, v in inp.items():
+        if keys is not None and k not in keys:
+            continue
+        if v is None:
+            out[k] = None
+            continue
+        ck = (k, v.data_ptr(), tuple(v.shape))
+        if k not in ("x", "router_w", "router_bias") and ck in _host_cache:
+            out[k] = _host_cache[ck]
+            continue
+        a = mi.to_numpy({k: v})[k]
+        if k not in ("x", "router_w", "router_bias"):
+            _host_cache[ck] = a
+        out[k] = a
+    return out
+
+
+def problem(cfg: mi.MoEConfig):
+    m = lib()
+    flags = m.F_ROUTER_BIAS if cfg.zipf_bias else 0
+    if cfg.shared_bf16:
+        flags |= m.F_SHARED_BF16
+    return m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, latent=cfg.L,
+                          wfmt=m.W_MXFP4 if cfg.wfmt == "mxfp4" else m.W_FP8, flags=flags)
+
+
+def workspace(p) -> torch.Tensor:
+    n = lib().moe_workspace_bytes(p)
+    assert n > 0
+    return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    rms = np.sqrt(np.mean(ref ** 2))
+    err = got - ref
+    rel = np.sqrt(np.sum(err ** 2)) / max(np.sqrt(np.sum(ref ** 2)), 1e-30)
+    mx = np.max(np.abs(err)) if err.size else 0.0
+    assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2}"
+    assert mx <= MAX_ABS_RMS * rms, f"{what}: max-abs error {mx:.3e} > {MAX_ABS_RMS} x RMS {rms:.3e}"
+    return rel, mx / max(rms, 1e-30)
+
+
+def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
+    """Token sample for full-size checks: first, last and random tokens."""
+    if T <= n:
+        return np.arange(T, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(T, n - 2, replace=False).tolist()) | {0, T - 1}
+    return np.array(sorted(pick), dtype=np.int32)

@@ -1,0 +1,109 @@
+"""GPU parity of the whole layer (moe_forward, S1..S8 in one call) against the
+oracle's per-token definition, in the launch configuration bench.py uses."""
+import numpy as np
+import pytest
+import torch
+
+import _gpu as G
+import moe_inputs as mi
+from test_gpu_stages import BIASED, E3, KE, MAXE, RAGGED, T1
+
+pytestmark = pytest.mark.gpu
+
+SHARED_SMALL = mi.MoEConfig("small_shared", T=96, H=256, I=128, E=6, k=3, I_s=128)
+SMALL = [mi.CONFIGS["toy"], SHARED_SMALL, RAGGED, MAXE, T1, KE, E3, BIASED.with_(I_s=128)]
+FULL = [mi.CONFIGS["decode"], mi.CONFIGS["prefill"], mi.CONFIGS["skewed"]]
+ids = lambda c: c.name
+
+
+def run_forward(cfg, inp, out=None, ws=None):
+    m = G.lib()
+    p = G.problem(cfg)
+    ws = G.workspace(p) if ws is None else ws
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda") if out is None else out
+    m.moe_forward(p, inp["x"], inp["router_w"], inp["router_bias"], inp["w13"], inp["w13_scale"],
+                  inp["w2"], inp["w2_scale"], inp["sw13"], inp["sw13_scale"], inp["sw2"],
+                  inp["sw2_scale"], inp["wd"], inp["wu"], inp["gamma"], out, ws)
+    return out
+
+
+def _check(orc, cfg, n_sample):
+    m = G.lib()
+    inp = G.gpu_inputs(cfg)
+    out = run_forward(cfg, inp)
+    assert m.moe_get_last_error() == 0
+    h = G.host(inp)
+    toks = G.sample_tokens(cfg.T, n_sample, seed=11)
+    ref_f, ref_b, _, _ = orc.moe_forward(cfg.oracle_problem(), h, tokens=toks)
+    got = G.bf16_values(G.bf16_bits(out))[toks]
+    return G.assert_close(got, ref_f, f"moe_forward {cfg.name}")
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=ids)
+def test_forward_small(orc, cfg):
+    _check(orc, cfg, n_sample=10 ** 9)
+
+
+@pytest.mark.parametrize("cfg", FULL, ids=ids)
+def test_forward_full_size_sampled(orc, cfg):
+    _check(orc, cfg, n_sample=24)
+
+
+def test_forward_deterministic_and_counted():
+    m = G.lib()
+    cfg = SHARED_SMALL
+    inp = G.gpu_inputs(cfg)
+    n0 = m.moe_launch_count()
+    a = G.bf16_bits(run_forward(cfg, inp))
+    n1 = m.moe_launch_count()
+    b = G.bf16_bits(run_forward(cfg, inp))
+    assert np.array_equal(a, b)
+    assert n1 - n0 == 10  # router, top-k, count, scan, rank, scatter, ffn1, requant, ffn2, combine
+
+
+def test_profile_counts_each_stage():
+    m = G.lib()
+    cfg = SHARED_SMALL
+    inp = G.gpu_inputs(cfg)
+    m.moe_profile_read()
+    m.moe_profile_enable(True)
+    try:
+        run_forward(cfg, inp)
+        run_forward(cfg, inp)
+        ms, n = m.moe_profile_read()
+    finally:
+        m.moe_profile_enable(False)
+    assert all(v == 2 for v in n.values()), n
+    assert all(v > 0 for v in ms.values()), ms
+
+
+def test_empty_batch_is_a_noop():
+    m = G.lib()
+    cfg = mi.CONFIGS["toy"].with_(T=0)
+    inp = G.gpu_inputs(mi.CONFIGS["toy"])
+    p = G.problem(cfg)
+    ws = G.workspace(p)
+    n0 = m.moe_launch_count()
+    out = torch.empty(0, cfg.H, dtype=torch.bfloat16, device="cuda")
+    m.moe_forward(p, inp["x"], inp["router_w"], None, inp["w13"], inp["w13_scale"], inp["w2"],
+                  inp["w2_scale"], None, None, None, None, None, None, None,
+                  torch.empty(16, dtype=torch.bfloat16, device="cuda"), ws)
+    assert m.moe_launch_count() == n0
+
+
+def test_all_tokens_to_one_expert(orc):
+    # a router whose bias sends every token to experts 5 (and 2 for k=2):
+    # one expert holds every row, the rest are empty
+    m = G.lib()
+    cfg = mi.MoEConfig("one_hot_route", T=200, H=256, I=128, E=8, k=2, zipf_bias=True)
+    inp = G.gpu_inputs(cfg)
+    bias = torch.full((cfg.E,), -100.0, device="cuda")
+    bias[5] = 100.0
+    bias[2] = 50.0
+    inp = dict(inp, router_bias=bias)
+    out = run_forward(cfg, inp)
+    assert m.moe_get_last_error() == 0
+    h = G.host(inp)
+    ref_f, _, idx, _ = orc.moe_forward(cfg.oracle_problem(), h)
+    assert np.all(idx[:, 0] == 5) and np.all(idx[:, 1] == 2)
+    G.assert_close(G.bf16_values(G.bf16_bits(out)), ref_f, "one-expert routing")

@@ -177,3 +177,22 @@ def test_zipf_bias_is_a_valid_log_distribution():
     p = torch.exp(b / 2)[r]
     ratio = p[0] / p[1]
     assert abs(float(ratio) - 2.0 ** 1.2) < 1e-3
+
+
+def test_combine_one_hot_rows(orc):
+    # y row r is the unit vector e_{r mod H} (bf16 1.0): out[t] counts, at each
+    # column, how many of the token's rows land there; plus a shared row of 0.5.
+    T, k, H = 9, 3, 16
+    rng = np.random.default_rng(8)
+    perm = np.stack([rng.permutation(T * k)[:k] for _ in range(T)]).astype(np.int32)
+    y = np.zeros((T * k, H), np.float32)
+    y[np.arange(T * k), np.arange(T * k) % H] = 1.0
+    sh = np.full((T, H), 0.5, np.float32)
+    out = orc.combine(_bf16_bits(y), perm, _bf16_bits(sh))
+    expect = np.full((T, H), 0.5)
+    for t in range(T):
+        for j in range(k):
+            expect[t, perm[t, j] % H] += 1.0
+    assert np.array_equal(_bf16_val(out), expect)
+    out2 = orc.combine(_bf16_bits(y), perm)
+    assert np.array_equal(_bf16_val(out2), expect - 0.5)
