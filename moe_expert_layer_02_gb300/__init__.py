@@ -71,7 +71,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_permute.argtypes = [PP, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_unpermute.argtypes = [PP, P, P, P, P, P]
-    L.moe_forward.argtypes = [PP] + [P] * 17 + [ctypes.c_size_t, P]
+    L.moe_forward.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P]
     L.moe_get_last_error.argtypes = [P]
     L.moe_launch_count.restype = ctypes.c_int64
     L.moe_profile_enable.argtypes = [ctypes.c_int]

@@ -58,16 +58,16 @@ def test_invalid_problems_rejected_on_host(m, bad):
     base.update(bad)
     p = m.make_problem(**base)
     lib = m.load_library()
-    assert lib.moe_forward(ctypes.byref(p), *([ctypes.c_void_p(256)] * 17), 1 << 30, None) == 1
+    assert lib.moe_forward(ctypes.byref(p), *([ctypes.c_void_p(256)] * 16), 1 << 30, None) == 1
     assert lib.moe_workspace_bytes(ctypes.byref(p)) == 0
 
 
 def test_null_and_workspace_checks(m):
     lib = m.load_library()
     p = m.make_problem(4, 256, 128, 8, 2)
-    args = [ctypes.c_void_p(256)] * 17
+    args = [ctypes.c_void_p(256)] * 16  # x .. ws
     assert lib.moe_forward(ctypes.byref(p), *([None] + args[1:]), 1 << 30, None) == 1
-    assert lib.moe_forward(ctypes.byref(p), *(args[:16] + [None]), 1 << 30, None) == 3
+    assert lib.moe_forward(ctypes.byref(p), *(args[:15] + [None]), 1 << 30, None) == 3
     assert lib.moe_forward(ctypes.byref(p), *args, 16, None) == 3
     # misaligned x
     bad = [ctypes.c_void_p(258)] + args[1:]
@@ -75,6 +75,18 @@ def test_null_and_workspace_checks(m):
     # the LatentMoE / MXFP4 problem is valid but not yet run by this build
     q = m.make_problem(4, 256, 128, 8, 2, latent=128, wfmt=m.W_MXFP4)
     assert lib.moe_forward(ctypes.byref(q), *args, 1 << 30, None) == 2
+
+
+def test_argument_counts_match_header(m):
+    # every binding declares exactly the parameters of its C prototype
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lib = m.load_library()
+    for name, params in re.findall(r"\b(moe_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", src):
+        n = 0 if params.strip() in ("", "void") else params.count(",") + 1
+        fn = getattr(lib, name)
+        if fn.argtypes is not None:
+            assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
 
 
 def test_binding_names_match_c_names(m):
