@@ -57,6 +57,7 @@ def peaks():
 
 def workload_name(cfg):
     kind = {"decode": "Ling-style decode", "prefill": "Ling-style prefill",
+            "decode_e32": "Ling-style decode, 32 experts (profiling case)",
             "skewed": "skewed-routing stress (Zipf 1.2 router bias)", "toy": "toy"}.get(cfg.name, cfg.name)
     s = (f"{kind}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}"
          + (f" + shared expert I_s={cfg.I_s}" if cfg.I_s else "")

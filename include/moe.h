@@ -39,7 +39,7 @@
  *     of time) set a per-device error word that moe_get_last_error returns.
  *     Nothing aborts, throws or falls back to another implementation.
  *   - Shapes: H, I, I_shared (and latent) must be multiples of 128; T >= 0
- *     (T = 0 is a no-op); 1 <= top_k <= min(E, 32); E <= 4096.
+ *     (T = 0 is a no-op); 1 <= top_k <= min(E, 32); E <= 1024.
  */
 #ifndef MOE_GB300_MOE_H_
 #define MOE_GB300_MOE_H_

@@ -77,6 +77,9 @@ CONFIGS = {
     "latent": MoEConfig("latent", T=4096, H=7168, I=3072, E=896, k=16, I_s=6144, L=3584,
                         wfmt="mxfp4", shared_bf16=True),
     "skewed": MoEConfig("skewed", T=8192, H=8192, I=2048, E=256, k=8, I_s=2048, zipf_bias=True),
+    # profiling stand-in for "decode": same expert shapes and ~16 rows per
+    # expert, 32 experts (1.6 GB of weights: above L2, small enough to capture)
+    "decode_e32": MoEConfig("decode_e32", T=64, H=8192, I=2048, E=32, k=8, I_s=2048),
 }
 
 
