@@ -140,6 +140,26 @@ int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, in
                 int32_t* offsets, int32_t* perm, int32_t* src_row, void* xq_perm,
                 float* xscale_perm, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_permute without a workspace.  The pages have no counterpart for this
+ * entry point: it exists for callers that cannot allocate device memory --
+ * hosts that plan every byte up front and hand a plugin only its input and
+ * output buffers, or latency-critical loops where cudaMalloc is not allowed
+ * because it may synchronise the device.  Same arguments, results and errors
+ * as moe_permute minus `ws`/`ws_bytes`: its scratch (two int32 tables of
+ * E * ceil(T/32) entries) lives in a fixed 4 MiB array inside libmoe.so
+ * (2^19 entries per table), which every GPU that loads the library holds
+ * until the process exits.  Problems with E * ceil(T/32) > 2^19 return
+ * MOE_ERR_WORKSPACE.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library routine.  All calls on a device share the
+ * array and it keeps the last call's contents; every entry a call reads is
+ * written earlier in the same call, but calls whose kernels overlap on the
+ * GPU (other streams or threads) race on it and must be serialised. */
+int moe_permute_static(const moe_problem* p, const int32_t* topk_idx, const void* x,
+                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* src_row,
+                       void* xq_perm, float* xscale_perm, void* stream);
+
 /* S5 + S6 -- grouped SwiGLU experts over expert-contiguous rows.  For rows r
  * in [offsets[e], offsets[e+1]):
  *   g[n] = (sum_k xq[r,k] W1_e[n,k]) * xscale[r] * s13_e[n]      (W1 = rows 0..I-1)

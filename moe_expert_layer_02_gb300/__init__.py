@@ -13,7 +13,8 @@ import os
 
 __all__ = [
     "MoEError", "MoEProblem", "make_problem", "load_library", "moe_workspace_bytes",
-    "moe_router_logits", "moe_route", "moe_permute", "moe_expert_ffn", "moe_unpermute",
+    "moe_router_logits", "moe_route", "moe_permute", "moe_permute_static", "moe_expert_ffn",
+    "moe_unpermute",
     "moe_forward", "moe_get_last_error", "moe_launch_count", "moe_profile_enable",
     "moe_profile_read", "STAGES", "W_FP8", "W_MXFP4", "F_ROUTER_BIAS", "F_SHARED_BF16",
 ]
@@ -49,7 +50,7 @@ def make_problem(T, H, I, E, top_k, I_shared=0, latent=0, wfmt=W_FP8, flags=0) -
 
 _lib = None
 _EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_router_logits", "moe_route",
-            "moe_permute", "moe_expert_ffn", "moe_unpermute", "moe_forward",
+            "moe_permute", "moe_permute_static", "moe_expert_ffn", "moe_unpermute", "moe_forward",
             "moe_get_last_error", "moe_launch_count", "moe_profile_enable", "moe_profile_read")
 
 
@@ -69,6 +70,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_router_logits.argtypes = [PP, P, P, P, P, P]
     L.moe_route.argtypes = [PP, P, P, P, P]
     L.moe_permute.argtypes = [PP, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    L.moe_permute_static.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_unpermute.argtypes = [PP, P, P, P, P, P]
     L.moe_forward.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P]
@@ -120,6 +122,18 @@ def moe_permute(p, topk_idx, x, counts, offsets, perm, src_row, xq_perm, xscale_
                                       _ptr(offsets), _ptr(perm), _ptr(src_row), _ptr(xq_perm),
                                       _ptr(xscale_perm), _ptr(ws), ws.numel() * ws.element_size(),
                                       _stream(stream)), "moe_permute")
+
+
+def moe_permute_static(p, topk_idx, x, counts, offsets, perm, src_row, xq_perm, xscale_perm,
+                       stream=None):
+    """moe_permute for callers that cannot allocate: no workspace argument; the
+    scratch is a fixed array inside the library (limit E * ceil(T/32) <= 2^19,
+    else MoEError MOE_ERR_WORKSPACE).  Calls that overlap on the GPU race on
+    that array; the first call on a device should precede any stream capture."""
+    _check(load_library().moe_permute_static(ctypes.byref(p), _ptr(topk_idx), _ptr(x),
+                                             _ptr(counts), _ptr(offsets), _ptr(perm),
+                                             _ptr(src_row), _ptr(xq_perm), _ptr(xscale_perm),
+                                             _stream(stream)), "moe_permute_static")
 
 
 def moe_expert_ffn(p, offsets, xq_perm, xscale_perm, row_w, w13, w13_scale, w2, w2_scale, y, ws,

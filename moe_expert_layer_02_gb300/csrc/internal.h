@@ -83,5 +83,6 @@ cudaError_t launch_ffn2(const GroupedFfnArgs& a, cudaStream_t s);
 // Shared helpers (moe_api.cu)
 int device_sm_count();
 void count_launch();
+int* device_error_word();  // device address of the current device's error word
 
 }  // namespace moe

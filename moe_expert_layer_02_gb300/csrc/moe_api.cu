@@ -254,6 +254,11 @@ int device_sm_count() {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+int* device_error_word() {
+  DeviceInfo* d = device_info();
+  return d ? d->err : nullptr;
+}
+
 }  // namespace moe
 
 using namespace moe;
