@@ -17,7 +17,7 @@ inline int num_chunks(int T) { return (T + kChunk - 1) / kChunk; }
 
 // ---------------------------------------------------------------- route.cu
 cudaError_t launch_router_logits(const void* x, const float* wr, const float* bias, float* logits,
-                                 int T, int H, int E, cudaStream_t s);
+                                 int T, int H, int E, int* err, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int32_t* idx, float* w, int T, int E, int k,
                         cudaStream_t s);
 
@@ -79,6 +79,11 @@ struct GroupedFfnArgs {
 
 cudaError_t launch_ffn1(const GroupedFfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn2(const GroupedFfnArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- ffn_gemm_2cta.cu
+// Same contract on pairs of SMs (256-row tiles); needs BN == 256, K % 256 == 0.
+cudaError_t launch_ffn1_pair(const GroupedFfnArgs& a, cudaStream_t s);
+cudaError_t launch_ffn2_pair(const GroupedFfnArgs& a, cudaStream_t s);
 
 // Shared helpers (moe_api.cu)
 int device_sm_count();

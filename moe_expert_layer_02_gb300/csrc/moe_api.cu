@@ -229,10 +229,19 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
   return a;
 }
 
+// Large batches (256-row tiles) run the grouped GEMMs on SM pairs; MOE_GEMM=1cta
+// forces the single-SM kernels.
+bool use_pair_gemm(const Plan& q) {
+  const char* env = std::getenv("MOE_GEMM");
+  if (env && std::strcmp(env, "1cta") == 0) return false;
+  return q.BN == 256 && q.K % 256 == 0;
+}
+
 int run_experts(const Plan& q, const GroupedFfnArgs& a, int rows_total, cudaStream_t s) {
+  const bool pair = use_pair_gemm(q);
   {
     StageTimer t(MOE_STAGE_FFN1, s);
-    MOE_TRY(launch_ffn1(a, s));
+    MOE_TRY(pair ? launch_ffn1_pair(a, s) : launch_ffn1(a, s));
   }
   {
     StageTimer t(MOE_STAGE_REQUANT, s);
@@ -240,7 +249,7 @@ int run_experts(const Plan& q, const GroupedFfnArgs& a, int rows_total, cudaStre
   }
   {
     StageTimer t(MOE_STAGE_FFN2, s);
-    MOE_TRY(launch_ffn2(a, s));
+    MOE_TRY(pair ? launch_ffn2_pair(a, s) : launch_ffn2(a, s));
   }
   return MOE_OK;
 }
@@ -290,10 +299,12 @@ int moe_router_logits(const moe_problem* p, const void* x, const float* router_w
   if ((p->flags & MOE_F_ROUTER_BIAS) && !bias) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(router_w, 16)) return MOE_ERR_INVALID_ARG;
   if (p->T == 0) return MOE_OK;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StageTimer t(MOE_STAGE_ROUTER, s);
   return cuda_status(launch_router_logits(x, router_w, (p->flags & MOE_F_ROUTER_BIAS) ? bias : nullptr,
-                                          logits, p->T, p->H, p->E, s));
+                                          logits, p->T, p->H, p->E, di->err, s));
 }
 
 int moe_route(const moe_problem* p, const float* logits, int32_t* topk_idx, float* topk_w,
@@ -425,7 +436,7 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   {
     StageTimer t(MOE_STAGE_ROUTER, s);
     MOE_TRY(launch_router_logits(x, router_w, (p->flags & MOE_F_ROUTER_BIAS) ? router_bias : nullptr,
-                                 logits, q.T, q.H, q.E, s));
+                                 logits, q.T, q.H, q.E, di->err, s));
   }
   {
     StageTimer t(MOE_STAGE_TOPK, s);

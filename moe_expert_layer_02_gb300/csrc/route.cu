@@ -13,6 +13,8 @@
 // index, so equal logits go to the lower index), then w_j = exp(l_j - l_0) /
 // sum exp(l_j' - l_0): the softmax over the chosen k (Ling write-up, s.1 top-8;
 // "Kimi K3 ... feasibility analysis", s.2.4, moe_renormalize, scaling 1.0).
+#include <cudaTypedefs.h>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -20,76 +22,144 @@ namespace moe {
 
 namespace {
 
-constexpr int RT_TOK = 32;  // tokens per block
-constexpr int RT_EXP = 16;  // experts per block
-constexpr int RT_HK = 128;  // h per staged chunk
-constexpr int RT_TW = 8;    // tokens per warp
-constexpr int RT_EW = 8;    // experts per warp
+// ---------------------------------------------------------------- S1 router
+// Block = 8 compute warps (4 token groups x 2 expert groups) + 1 TMA producer
+// warp.  Warp tile TW tokens x EW experts; lane l owns h = l (mod 32) of every
+// chunk, so each logit is one fma chain over h ascending, as the canonical
+// order requires.  Chunks of RT_HK h-values stream through a RT_STAGES-deep
+// shared-memory ring filled by 2-D TMA loads (x tile bf16, router tile fp32;
+// out-of-range rows read as zero).  Pairs of experts share one packed
+// fma.rn.f32x2 (two independent fp32 fused multiply-adds, same rounding).
+constexpr int RT_HK = 128;
+constexpr int RT_STAGES = 4;
+constexpr int RT_WT = 4, RT_WE = 2;  // warp grid
+constexpr int RT_THREADS = (RT_WT * RT_WE + 1) * 32;
 
-__global__ void __launch_bounds__(256)
-    router_logits_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
-                         const float* __restrict__ bias, float* __restrict__ logits, int T, int H,
-                         int E) {
-  __shared__ float xs[RT_TOK][RT_HK];
-  __shared__ float ws[RT_EXP][RT_HK];
+template <int TW, int EW>
+struct RouterCfg {
+  static constexpr int BT = RT_WT * TW;             // tokens per block
+  static constexpr int BE = RT_WE * EW;             // experts per block
+  static constexpr int X_BYTES = BT * RT_HK * 2;    // bf16 tile
+  static constexpr int W_BYTES = BE * RT_HK * 4;    // fp32 tile
+  static constexpr int STAGE = X_BYTES + W_BYTES;
+  static constexpr int SMEM = 128 + RT_STAGES * STAGE + 2 * RT_STAGES * 8 + 16;
+};
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+template <int TW, int EW>
+__global__ void __launch_bounds__(RT_THREADS, 1)
+    router_logits_kernel(const __grid_constant__ CUtensorMap tm_x,
+                         const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ bias,
+                         float* __restrict__ logits, int T, int H, int E, int* err) {
+  using C = RouterCfg<TW, EW>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RT_STAGES * C::STAGE);
+  uint64_t* empty = full + RT_STAGES;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + RT_STAGES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tg = warp & 3, eg = warp >> 2;
-  const int t0 = blockIdx.x * RT_TOK, e0 = blockIdx.y * RT_EXP;
-  float acc[RT_TW][RT_EW];
-#pragma unroll
-  for (int i = 0; i < RT_TW; ++i)
-#pragma unroll
-    for (int j = 0; j < RT_EW; ++j) acc[i][j] = 0.0f;
+  const int t0 = blockIdx.x * C::BT, e0 = blockIdx.y * C::BE;
+  const int nchunk = H / RT_HK;
 
-  for (int h0 = 0; h0 < H; h0 += RT_HK) {
-    // x tile: 32 tokens x 128 h, 8 bf16 per thread-iteration
-    for (int i = threadIdx.x; i < RT_TOK * (RT_HK / 8); i += blockDim.x) {
-      const int r = i / (RT_HK / 8), c = (i % (RT_HK / 8)) * 8;
-      const int t = t0 + r;
-      uint4 u = make_uint4(0, 0, 0, 0);
-      if (t < T) u = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h0 + c);
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xs[r][c + 2 * q] = bf16_bits_to_f32(w4[q] & 0xFFFFu);
-        xs[r][c + 2 * q + 1] = bf16_bits_to_f32(w4[q] >> 16);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RT_STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), RT_WT * RT_WE);
+    }
+    *s_abort = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  if (warp == RT_WT * RT_WE) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_w);
+      for (int c = 0; c < nchunk; ++c) {
+        const int s = c % RT_STAGES;
+        const uint32_t ph = (uint32_t)(c / RT_STAGES) & 1u;
+        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, err, s_abort)) break;
+        const uint32_t st = smem_u32(smem + s * C::STAGE);
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, C::STAGE);
+        tma_load_2d(st, &tm_x, c * RT_HK, t0, fb);
+        tma_load_2d(st + C::X_BYTES, &tm_w, c * RT_HK, e0, fb);
       }
+      // drain: every issued chunk lands before the block may exit
+      for (int c = max(0, nchunk - RT_STAGES); c < nchunk; ++c)
+        mbar_wait_drain(smem_u32(&full[c % RT_STAGES]), (uint32_t)(c / RT_STAGES) & 1u);
     }
-    for (int i = threadIdx.x; i < RT_EXP * (RT_HK / 4); i += blockDim.x) {
-      const int r = i / (RT_HK / 4), c = (i % (RT_HK / 4)) * 4;
-      const int e = e0 + r;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < E) v = *reinterpret_cast<const float4*>(wr + (size_t)e * H + h0 + c);
-      ws[r][c] = v.x;
-      ws[r][c + 1] = v.y;
-      ws[r][c + 2] = v.z;
-      ws[r][c + 3] = v.w;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int s = 0; s < RT_HK / 32; ++s) {
-      float xv[RT_TW], wv[RT_EW];
-#pragma unroll
-      for (int i = 0; i < RT_TW; ++i) xv[i] = xs[tg * RT_TW + i][s * 32 + lane];
-#pragma unroll
-      for (int j = 0; j < RT_EW; ++j) wv[j] = ws[eg * RT_EW + j][s * 32 + lane];
-#pragma unroll
-      for (int i = 0; i < RT_TW; ++i)
-#pragma unroll
-        for (int j = 0; j < RT_EW; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
-    }
-    __syncthreads();
+    return;
   }
 
+  // ------------------------------------------------------------ compute warps
+  const int tg = warp % RT_WT, eg = warp / RT_WT;
+  uint64_t acc[TW][EW / 2];
 #pragma unroll
-  for (int i = 0; i < RT_TW; ++i) {
+  for (int i = 0; i < TW; ++i)
 #pragma unroll
-    for (int j = 0; j < RT_EW; ++j) {
-      float v = acc[i][j];
+    for (int j = 0; j < EW / 2; ++j) acc[i][j] = 0;  // +0.0f, +0.0f
+  bool ok = true;
+  for (int c = 0; c < nchunk; ++c) {
+    const int s = c % RT_STAGES;
+    const uint32_t ph = (uint32_t)(c / RT_STAGES) & 1u;
+    int got = 1;
+    if (lane == 0) got = mbar_wait(smem_u32(&full[s]), ph, err, s_abort) ? 1 : 0;
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (!got) {
+      ok = false;
+      break;
+    }
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + s * C::STAGE) + tg * TW * RT_HK;
+    const float* ws = reinterpret_cast<const float*>(smem + s * C::STAGE + C::X_BYTES) +
+                      eg * EW * RT_HK;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v = v + __shfl_down_sync(0xffffffffu, v, o);
-      const int t = t0 + tg * RT_TW + i, e = e0 + eg * RT_EW + j;
-      if (lane == 0 && t < T && e < E) logits[(size_t)t * E + e] = bias ? v + bias[e] : v;
+    for (int q = 0; q < RT_HK / 32; ++q) {
+      const int h = q * 32 + lane;
+      uint64_t wv[EW / 2];
+#pragma unroll
+      for (int j = 0; j < EW / 2; ++j)
+        wv[j] = pack2(ws[(2 * j) * RT_HK + h], ws[(2 * j + 1) * RT_HK + h]);
+#pragma unroll
+      for (int i = 0; i < TW; ++i) {
+        const float xv = bf16_bits_to_f32(xs[i * RT_HK + h]);
+        const uint64_t xx = pack2(xv, xv);
+#pragma unroll
+        for (int j = 0; j < EW / 2; ++j) fma2(acc[i][j], xx, wv[j]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+  }
+  if (!ok) return;
+
+#pragma unroll
+  for (int i = 0; i < TW; ++i) {
+#pragma unroll
+    for (int j = 0; j < EW / 2; ++j) {
+      float v[2];
+      unpack2(acc[i][j], v[0], v[1]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float r = v[u];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r = r + __shfl_down_sync(0xffffffffu, r, o);
+        const int t = t0 + tg * TW + i, e = e0 + eg * EW + 2 * j + u;
+        if (lane == 0 && t < T && e < E) logits[(size_t)t * E + e] = bias ? r + bias[e] : r;
+      }
     }
   }
 }
@@ -142,13 +212,56 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_router_logits(const void* x, const float* wr, const float* bias, float* logits,
-                                 int T, int H, int E, cudaStream_t s) {
-  dim3 grid((T + RT_TOK - 1) / RT_TOK, (E + RT_EXP - 1) / RT_EXP);
+namespace {
+
+bool router_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int H,
+                int rows, int box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)H * esize};
+  cuuint32_t box[2] = {(cuuint32_t)RT_HK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int TW, int EW>
+cudaError_t launch_router_impl(const void* x, const float* wr, const float* bias, float* logits,
+                               int T, int H, int E, int* err, cudaStream_t s) {
+  using C = RouterCfg<TW, EW>;
+  CUtensorMap tx, tw;
+  if (!router_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, C::BT) ||
+      !router_map(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wr, H, E, C::BE))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<TW, EW>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((T + C::BT - 1) / C::BT, (E + C::BE - 1) / C::BE);
   count_launch();
-  router_logits_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), wr, bias, logits, T,
-                                            H, E);
+  router_logits_kernel<TW, EW><<<grid, RT_THREADS, C::SMEM, s>>>(tx, tw, bias, logits, T, H, E, err);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const void* x, const float* wr, const float* bias, float* logits,
+                                 int T, int H, int E, int* err, cudaStream_t s) {
+  // large tiles (8 tokens x 16 experts per warp) when they still give every SM
+  // at least two blocks, else small ones
+  const long big_blocks = (long)((T + 31) / 32) * ((E + 31) / 32);
+  if (big_blocks >= 2L * device_sm_count())
+    return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
+  return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
 }
 
 cudaError_t launch_topk(const float* logits, int32_t* idx, float* w, int T, int E, int k,

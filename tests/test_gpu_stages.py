@@ -16,6 +16,8 @@ T1 = mi.MoEConfig("t1", T=1, H=256, I=128, E=8, k=2, I_s=128)
 KE = mi.MoEConfig("k_eq_e", T=33, H=256, I=128, E=8, k=8, I_s=128)
 E3 = mi.MoEConfig("e3", T=50, H=128, I=256, E=3, k=1)
 BIASED = mi.MoEConfig("biased", T=300, H=256, I=128, E=64, k=6, zipf_bias=True)
+# skewed routing at small size: experts from hundreds of rows down to none
+SKEW_SMALL = mi.MoEConfig("skew_small", T=640, H=512, I=256, E=16, k=4, zipf_bias=True)
 SMALL = [mi.CONFIGS["toy"], RAGGED, MAXE, T1, KE, E3, BIASED]
 FULL = [mi.CONFIGS["decode"], mi.CONFIGS["skewed"], mi.CONFIGS["prefill"]]
 ids = lambda c: c.name
@@ -130,9 +132,14 @@ def _expert_problem(orc, cfg, h):
     return off, q[src], s[src], row_w
 
 
-@pytest.mark.parametrize("bn", [32, 64, 128, 256])
-@pytest.mark.parametrize("cfg", [mi.CONFIGS["toy"], RAGGED, KE, E3], ids=ids)
+@pytest.mark.parametrize("bn", [32, 64, 128, 256, "256-1cta"])
+@pytest.mark.parametrize("cfg", [mi.CONFIGS["toy"], RAGGED, KE, E3, SKEW_SMALL], ids=ids)
 def test_expert_ffn_all_tiles(orc, cfg, bn, monkeypatch):
+    # 256-row tiles run on SM pairs when H % 256 == 0; "256-1cta" forces the
+    # single-SM kernel for the same tiles
+    if bn == "256-1cta":
+        monkeypatch.setenv("MOE_GEMM", "1cta")
+        bn = 256
     monkeypatch.setenv("MOE_TILE_N", str(bn))
     _check_expert_ffn(orc, cfg, rows_sample=None)
 
