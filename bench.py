@@ -59,10 +59,14 @@ def workload_name(cfg):
     kind = {"decode": "Ling-style decode", "prefill": "Ling-style prefill",
             "decode_e32": "Ling-style decode, 32 experts (profiling case)",
             "prefill_e32": "Ling-style prefill, 32 experts (profiling case)",
+            "latent": "Kimi-K3-style LatentMoE",
             "skewed": "skewed-routing stress (Zipf 1.2 router bias)", "toy": "toy"}.get(cfg.name, cfg.name)
     s = (f"{kind}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}"
          + (f" + shared expert I_s={cfg.I_s}" if cfg.I_s else "")
-         + f", {cfg.wfmt} e4m3 per-output-channel weights, per-token fp8 activations")
+         + (f", latent L={cfg.L} (bf16 down/up, RMSNorm)" if cfg.L else "")
+         + (", MXFP4 e2m1 + e8m0/32 expert weights" if cfg.wfmt == "mxfp4"
+            else ", fp8 e4m3 per-output-channel weights")
+         + ", per-token fp8 activations")
     return s
 
 
@@ -245,8 +249,9 @@ def run_ours(args, cfg):
     m.load_library()
     dev = torch.device("cuda", local)
     inp = mi.make_inputs(cfg, device=dev, seed=0)
-    flags = m.F_ROUTER_BIAS if cfg.zipf_bias else 0
-    p = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, flags=flags)
+    flags = (m.F_ROUTER_BIAS if cfg.zipf_bias else 0) | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
+    p = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, latent=cfg.L,
+                       wfmt=m.W_MXFP4 if cfg.wfmt == "mxfp4" else m.W_FP8, flags=flags)
     wsb = torch.empty(m.moe_workspace_bytes(p), dtype=torch.uint8, device=dev)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
@@ -254,7 +259,8 @@ def run_ours(args, cfg):
     def step(x=None):
         m.moe_forward(p, inp["x"] if x is None else x, inp["router_w"], inp["router_bias"],
                       inp["w13"], inp["w13_scale"], inp["w2"], inp["w2_scale"], inp["sw13"],
-                      inp["sw13_scale"], inp["sw2"], inp["sw2_scale"], None, None, None, out, wsb)
+                      inp["sw13_scale"], inp["sw2"], inp["sw2_scale"], inp["wd"], inp["wu"],
+                      inp["gamma"], out, wsb)
 
     # touched experts (for algorithmic bytes): routing through the library itself
     logits = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)

@@ -90,7 +90,11 @@ enum {
   MOE_STAGE_REQUANT = 5, /* S6a per-row fp8 requant of h         */
   MOE_STAGE_FFN2 = 6,    /* S6 grouped W2 GEMM + routing weight  */
   MOE_STAGE_COMBINE = 7, /* S7/S8 weighted gather + shared add   */
-  MOE_STAGE_COUNT = 8
+                         /*   (LatentMoE: gather + RMSNorm)     */
+  MOE_STAGE_LATENT_DOWN = 8, /* S9 z = x Wd^T                   */
+  MOE_STAGE_SHARED = 9,      /* S8 bf16 shared expert gate/up   */
+  MOE_STAGE_LATENT_UP = 10,  /* S9 yn Wu^T + shared down        */
+  MOE_STAGE_COUNT = 11
 };
 
 /* Human-readable name of a moe_status (static storage). */

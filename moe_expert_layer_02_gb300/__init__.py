@@ -26,7 +26,8 @@ W_FP8 = 0
 W_MXFP4 = 1
 F_ROUTER_BIAS = 0x1
 F_SHARED_BF16 = 0x2
-STAGES = ("router", "topk", "index", "scatter", "ffn1", "requant", "ffn2", "combine")
+STAGES = ("router", "topk", "index", "scatter", "ffn1", "requant", "ffn2", "combine",
+          "latent_down", "shared", "latent_up")
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT"}
 

@@ -85,12 +85,19 @@ def layer_work(cfg, touched_experts: int) -> dict:
     }
 
 
+def _matrix_bytes(rows: int, cols: int, wfmt: str) -> float:
+    """Bytes of one weight matrix with its scales (fp8: fp32 per row; mxfp4:
+    4-bit elements + one e8m0 byte per 32)."""
+    if wfmt == "fp8":
+        return rows * cols + 4 * rows
+    return rows * cols / 2 + rows * cols / 32
+
+
 def ffn1_launch_bytes(cfg, touched_experts: int) -> float:
     """Algorithmic bytes of one grouped FFN1 launch: touched W1|W3 (+ scales),
     shared W1|W3, and the quantised rows it reads / the bf16 h it writes."""
     K, I = cfg.K, cfg.I
-    per = 2 * I * K + 4 * 2 * I
-    b = touched_experts * per
+    b = touched_experts * _matrix_bytes(2 * I, K, cfg.wfmt)
     rows = cfg.T * cfg.k
     if cfg.I_s and not cfg.shared_bf16:
         b += 2 * cfg.I_s * K + 4 * 2 * cfg.I_s
@@ -103,7 +110,7 @@ def ffn1_launch_bytes(cfg, touched_experts: int) -> float:
 
 def ffn2_launch_bytes(cfg, touched_experts: int) -> float:
     K, I = cfg.K, cfg.I
-    b = touched_experts * (K * I + 4 * K)
+    b = touched_experts * _matrix_bytes(K, I, cfg.wfmt)
     rows = cfg.T * cfg.k
     rows_s = cfg.T if (cfg.I_s and not cfg.shared_bf16) else 0
     if rows_s:

@@ -1,29 +1,35 @@
-// ffn_gemm_2cta.cu -- S5/S6 for large batches: the grouped fp8 expert GEMMs
-// on pairs of SMs (tcgen05 cta_group::2).
+// ffn_gemm_2cta.cu -- GEMMs on pairs of SMs (tcgen05 cta_group::2).
 //
-// Same arithmetic as ffn_gemm.cu ("Optimising Ling-2.6-1T on TPU with
-// SGLang-JAX", s.5 per-channel direct_scaled_dot; FFN1/FFN2 of the s.1 cost
-// model), different shape, chosen when experts hold hundreds of rows
-// (prefill): a cluster of two CTAs computes a 256-row x 256-column tile with
-// one MMA stream.  Each CTA stages half of the token rows (A, 128 x 128 B per
-// K step) and half of the weight rows (B, 128 x 128 B), so every SM moves 32 KB
-// per 4.2 M multiply-adds instead of 48-64 KB for a single-SM tile of the same
-// depth; the tile's accumulator (128 rows x 256 fp32 columns per CTA) is
-// double-buffered in tensor memory.
+// One pipeline, used for
+//   * S5/S6 of large batches: the grouped fp8 expert GEMMs (same arithmetic as
+//     ffn_gemm.cu: "Optimising Ling-2.6-1T on TPU with SGLang-JAX", s.5
+//     per-channel direct_scaled_dot; FFN1/FFN2 of the s.1 cost model), when
+//     experts hold hundreds of rows (prefill);
+//   * S9 of the LatentMoE block ("Kimi K3 ... feasibility analysis", s.2.4):
+//     the bf16 dense GEMMs z = x Wd^T, the shared expert's gate/up with the
+//     SwiGLU epilogue, and out = yn Wu^T + h_s W2s^T as one accumulation over
+//     two K segments (up_proj and the shared expert's down projection).
 //
-//   FFN1: columns 0..127 = g (W1 rows f0..f0+127, staged by CTA 0),
-//         columns 128..255 = u (W3 rows I+f0.., staged by CTA 1), so each
-//         epilogue thread holds g and u of one token row and writes 128
-//         contiguous bf16 of h.
-//   FFN2: columns = 256 output channels (W2 rows c0.., 128 per CTA).
+// A cluster of two CTAs computes a 256-row x 256-column tile with one MMA
+// stream.  Each CTA stages half of the activation rows (A, 128 rows x 128 B
+// per K step) and half of the weight rows (B, 128 rows x 128 B), so every SM
+// moves 32 KB per K step for 4.2 M (fp8) or 2.1 M (bf16) multiply-adds; the
+// tile's accumulator (128 rows x 256 fp32 columns per CTA) is double-buffered
+// in tensor memory.
+//
+// Epilogues (thread = one activation row, 16 columns per tcgen05.ld):
+//   SWIGLU: columns 0..127 = g (weight rows f0.., staged by CTA 0), columns
+//           128..255 = u (rows I+f0.., staged by CTA 1); h = bf16(silu(g) u),
+//           with the fp8 per-row and per-channel scales when the operands are fp8.
+//   DOWN:   y = bf16(((acc * hs[row]) * s[c]) * row_w[row])   (fp8 FFN2)
+//   STORE:  out = bf16(acc)                                   (bf16 dense)
 //
 // Roles per CTA (192 threads): warp 0 TMA producer, warp 1 MMA issuer (even
 // CTA only; the odd CTA's warp 1 only joins the tensor-memory allocation),
-// warps 2-5 epilogue (thread = token row, 16 columns per tcgen05.ld).  Both
-// CTAs' TMA loads complete on the even CTA's `full` barrier; the even CTA's
-// commits arrive on both CTAs' `empty` / `tfull` barriers; both epilogues
-// release an accumulator on the even CTA's `tempty` barrier.  All waits are
-// bounded as in ffn_gemm.cu.
+// warps 2-5 epilogue.  Both CTAs' TMA loads complete on the even CTA's `full`
+// barrier; the even CTA's commits arrive on both CTAs' `empty` / `tfull`
+// barriers; both epilogues release an accumulator on the even CTA's `tempty`
+// barrier.  All waits are bounded as in ffn_gemm.cu.
 #include <cudaTypedefs.h>
 
 #include "device.cuh"
@@ -33,10 +39,10 @@ namespace moe {
 
 namespace {
 
-constexpr int P_ROWS = 128;   // token rows per CTA (M = 256 per pair)
+constexpr int P_ROWS = 128;   // activation rows per CTA (M = 256 per pair)
 constexpr int P_N = 256;      // output columns per tile
 constexpr int P_BK = 128;     // K bytes per stage
-constexpr int P_UMMA_K = 32;  // K per tcgen05.mma for 8-bit operands
+constexpr int P_UMMA_B = 32;  // K bytes per tcgen05.mma (32 fp8 or 16 bf16)
 constexpr int P_THREADS = 192;
 constexpr int P_A_BYTES = P_ROWS * P_BK;       // 16 KB
 constexpr int P_B_BYTES = (P_N / 2) * P_BK;    // 16 KB (this CTA's half of N)
@@ -47,16 +53,72 @@ constexpr int P_TMEM_COLS = 512;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 2 * P_ACC_STAGES + 1;
 constexpr int P_SMEM = 1024 + P_STAGES * P_STAGE + P_NUM_BARS * 8 + 16 + P_STAGES * 4;
 
+enum { KIND_FP8 = 0, KIND_BF16 = 1 };
+enum { EPI_SWIGLU = 0, EPI_DOWN = 1, EPI_STORE = 2 };
+
+// One launch: the tiles, the K segments and the epilogue's operands.
+struct PairGemm {
+  const int4* items;      // grouped work list {group, row0, rows, 0}; nullptr = dense
+  const int32_t* n_items;
+  int max_items;
+  int dense_rows;         // dense: rows of A, tiled in 256-row items
+  int E;                  // grouped: group E reads the shared-expert weight map
+  int nb;                 // output blocks per item
+  int kb1, kb2;           // K stages from (x, w) and from (x2, w2)
+  int I;                  // SWIGLU: first row of the up-projection block
+  int rows_total;         // rows of A (and of the output)
+  const float* xscale;    // fp8 SWIGLU: per-row activation scale
+  const float* w_scale;   // fp8: per-channel scale of group 0 (stride scale_stride)
+  const float* ws_scale;  // fp8: per-channel scale of the shared expert
+  int scale_stride;
+  const float* hs;        // DOWN: per-row scale of h
+  const float* row_w;     // DOWN: routing weight per row (nullptr = 1)
+  void* out;              // bf16 output, row stride ldo elements
+  int ldo;
+  int* err;
+};
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 p = __floats2bfloat162_rn(a, b);  // a -> low half
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
-template <bool FFN1>
+__device__ __forceinline__ int4 tile_item(const PairGemm& g, int item) {
+  if (g.items) return g.items[item];
+  const int row0 = item * 2 * P_ROWS;
+  return make_int4(0, row0, min(2 * P_ROWS, g.dense_rows - row0), 0);
+}
+
+template <int KIND>
+__device__ __forceinline__ uint32_t pair_idesc() {
+  // f32 accumulate, K-major A and B, M = 256 (pair), N = 256
+  const uint32_t fmt = KIND == KIND_FP8 ? 0u : 1u;  // e4m3 (kind::f8f6f4) / bf16 (kind::f16)
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(P_N >> 3) << 17) |
+         ((uint32_t)((2 * P_ROWS) >> 4) << 24);
+}
+
+template <int KIND>
+__device__ __forceinline__ void pair_mma(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t acc) {
+  if (KIND == KIND_FP8) {
+    mma_f8f6f4_pair(d, adesc, bdesc, idesc, acc);
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+  }
+}
+
+template <int KIND, int EPI>
 __global__ void __launch_bounds__(P_THREADS, 1)
-    grouped_ffn_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
-                            const __grid_constant__ CUtensorMap tm_ws,
-                            const __grid_constant__ CUtensorMap tm_x, const GroupedFfnArgs a) {
+    pair_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
+                     const __grid_constant__ CUtensorMap tm_ws,
+                     const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_w2,
+                     const __grid_constant__ CUtensorMap tm_x2, const PairGemm g) {
+  constexpr int EL = KIND == KIND_FP8 ? P_BK : P_BK / 2;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -92,6 +154,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_ws);
     tma_prefetch_desc(&tm_x);
+    if (g.kb2) {
+      tma_prefetch_desc(&tm_w2);
+      tma_prefetch_desc(&tm_x2);
+    }
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(s_tmem), P_TMEM_COLS);
   tc_fence_before();
@@ -100,9 +166,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  const int NB = FFN1 ? a.I / 128 : a.K / P_N;  // output blocks per item
-  const int KB = FFN1 ? a.K / P_BK : a.I / P_BK;
-  const int n_items = min(*a.n_items, a.max_items);
+  const int NB = g.nb;
+  const int KB = g.kb1 + g.kb2;
+  const int n_items = g.items ? min(*g.n_items, g.max_items)
+                              : (g.dense_rows + 2 * P_ROWS - 1) / (2 * P_ROWS);
   const int n_tiles = n_items * NB;
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
 
@@ -113,22 +180,29 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       uint32_t phase = 0;
       for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters) {
         const int item = tile / NB, nb = tile - item * NB;
-        const int4 it = a.items[item];
-        const bool shared = it.x >= a.E;
+        const int4 it = tile_item(g, item);
+        const bool shared = g.items && it.x >= g.E;
         const CUtensorMap* tw = shared ? &tm_ws : &tm_w;
         const int gc = shared ? 0 : it.x;
-        const int wrow = FFN1 ? (rank == 0 ? nb * 128 : a.I + nb * 128) : nb * P_N + 128 * (int)rank;
+        const int wrow = EPI == EPI_SWIGLU ? (rank == 0 ? nb * 128 : g.I + nb * 128)
+                                           : nb * P_N + 128 * (int)rank;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort)) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, g.err, s_abort)) {
             ok = false;
             break;
           }
           const uint32_t st = smem_u32(smem + stage * P_STAGE);
           const uint32_t fb_leader = mapa_shared(smem_u32(&full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * P_STAGE);
-          tma_load_2d_pair(st, &tm_x, kb * P_BK, it.y + 128 * (int)rank, fb_leader);
-          tma_load_3d_pair(st + P_A_BYTES, tw, kb * P_BK, wrow, gc, fb_leader);
+          if (kb < g.kb1) {
+            tma_load_2d_pair(st, &tm_x, kb * EL, it.y + 128 * (int)rank, fb_leader);
+            tma_load_3d_pair(st + P_A_BYTES, tw, kb * EL, wrow, gc, fb_leader);
+          } else {
+            const int k2 = (kb - g.kb1) * EL;
+            tma_load_2d_pair(st, &tm_x2, k2, it.y + 128 * (int)rank, fb_leader);
+            tma_load_3d_pair(st + P_A_BYTES, &tm_w2, k2, wrow, 0, fb_leader);
+          }
           s_issued[stage] = phase + 1u;
           if (++stage == P_STAGES) {
             stage = 0;
@@ -148,16 +222,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int stage = 0, it_local = 0;
       uint32_t phase = 0;
       bool issued_any = false;
-      const uint32_t idesc = idesc_e4m3_f32(2 * P_ROWS, P_N);
+      const uint32_t idesc = pair_idesc<KIND>();
       for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters, ++it_local) {
         const int acc = it_local % P_ACC_STAGES;
         const uint32_t acc_phase = (uint32_t)(it_local / P_ACC_STAGES) & 1u;
-        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, a.err, s_abort)) break;
+        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, g.err, s_abort)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * P_N;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(&full[stage]), phase, a.err, s_abort)) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, g.err, s_abort)) {
             ok = false;
             break;
           }
@@ -165,9 +239,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           const uint32_t a0 = smem_u32(smem + stage * P_STAGE);
           const uint32_t b0 = a0 + P_A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < P_BK / P_UMMA_K; ++kk)
-            mma_f8f6f4_pair(d, smem_desc_sw128(a0 + kk * P_UMMA_K),
-                            smem_desc_sw128(b0 + kk * P_UMMA_K), idesc, (kb | kk) ? 1u : 0u);
+          for (int kk = 0; kk < P_BK / P_UMMA_B; ++kk)
+            pair_mma<KIND>(d, smem_desc_sw128(a0 + kk * P_UMMA_B),
+                           smem_desc_sw128(b0 + kk * P_UMMA_B), idesc, (kb | kk) ? 1u : 0u);
           issued_any = true;
           mma_commit_pair(smem_u32(&empty[stage]), 0x3);
           if (++stage == P_STAGES) {
@@ -191,24 +265,26 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     int it_local = 0;
     for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++it_local) {
       const int item = tile / NB, nb = tile - item * NB;
-      const int4 it = a.items[item];
-      const bool shared = it.x >= a.E;
+      const int4 it = tile_item(g, item);
+      const bool shared = g.items && it.x >= g.E;
       const int acc = it_local % P_ACC_STAGES;
       const uint32_t acc_phase = (uint32_t)(it_local / P_ACC_STAGES) & 1u;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(smem_u32(&tfull[acc]), acc_phase, a.err, s_abort) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(smem_u32(&tfull[acc]), acc_phase, g.err, s_abort) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
       const int r = lrow + 128 * (int)rank;
       const int row = it.y + r;
-      const bool valid = r < it.z && (unsigned)row < (unsigned)a.rows_total;
+      const bool valid = r < it.z && (unsigned)row < (unsigned)g.rows_total;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * P_N;
-      if (FFN1) {
-        const float* sc = shared ? a.sw13_scale : a.w13_scale + (size_t)it.x * 2 * a.I;
+      uint16_t* orow = static_cast<uint16_t*>(g.out) + (size_t)(valid ? row : 0) * g.ldo;
+      if (EPI == EPI_SWIGLU) {
         const int f0 = nb * 128;
-        const float xs = valid ? a.xscale[row] : 0.0f;
-        uint16_t* hrow = static_cast<uint16_t*>(a.h) + (size_t)(valid ? row : 0) * a.I + f0;
+        const float* sc = KIND == KIND_FP8
+                              ? (shared ? g.ws_scale : g.w_scale + (size_t)it.x * g.scale_stride)
+                              : nullptr;
+        const float xs = KIND == KIND_FP8 ? (valid ? g.xscale[row] : 0.0f) : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 16) {
           uint32_t vg[16], vu[16];
@@ -222,25 +298,28 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             float hv[2];
 #pragma unroll
             for (int u2 = 0; u2 < 2; ++u2) {
-              const float sg = __ldg(sc + f0 + c + j + u2), su = __ldg(sc + a.I + f0 + c + j + u2);
-              const float g = (__uint_as_float(vg[j + u2]) * xs) * sg;
-              const float u = (__uint_as_float(vu[j + u2]) * xs) * su;
-              hv[u2] = g / (1.0f + expf(-g)) * u;
+              float gg = __uint_as_float(vg[j + u2]), uu = __uint_as_float(vu[j + u2]);
+              if (KIND == KIND_FP8) {
+                gg = (gg * xs) * __ldg(sc + f0 + c + j + u2);
+                uu = (uu * xs) * __ldg(sc + g.I + f0 + c + j + u2);
+              }
+              hv[u2] = gg / (1.0f + expf(-gg)) * uu;
             }
             packed[j / 2] = pack_bf16x2(hv[0], hv[1]);
           }
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(hrow + c);
+            uint4* dst = reinterpret_cast<uint4*>(orow + f0 + c);
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
           }
         }
       } else {
-        const float* sc = shared ? a.sw2_scale : a.w2_scale + (size_t)it.x * a.K;
         const int c0 = nb * P_N;
-        const float hs = valid ? a.hs[row] : 0.0f;
-        const float rw = (valid && !shared && a.row_w) ? a.row_w[row] : 1.0f;
-        uint16_t* yrow = static_cast<uint16_t*>(a.y) + (size_t)(valid ? row : 0) * a.K + c0;
+        const float* sc =
+            EPI == EPI_DOWN ? (shared ? g.ws_scale : g.w_scale + (size_t)it.x * g.scale_stride)
+                            : nullptr;
+        const float hs = EPI == EPI_DOWN ? (valid ? g.hs[row] : 0.0f) : 1.0f;
+        const float rw = (EPI == EPI_DOWN && valid && !shared && g.row_w) ? g.row_w[row] : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < P_N; c += 16) {
           uint32_t v[16];
@@ -250,12 +329,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           uint32_t packed[8];
 #pragma unroll
           for (int j = 0; j < 16; j += 2) {
-            const float y0 = ((__uint_as_float(v[j]) * hs) * __ldg(sc + c0 + c + j)) * rw;
-            const float y1 = ((__uint_as_float(v[j + 1]) * hs) * __ldg(sc + c0 + c + j + 1)) * rw;
+            float y0 = __uint_as_float(v[j]), y1 = __uint_as_float(v[j + 1]);
+            if (EPI == EPI_DOWN) {
+              y0 = ((y0 * hs) * __ldg(sc + c0 + c + j)) * rw;
+              y1 = ((y1 * hs) * __ldg(sc + c0 + c + j + 1)) * rw;
+            }
             packed[j / 2] = pack_bf16x2(y0, y1);
           }
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0 + c);
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
           }
@@ -290,31 +372,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-bool pair_map(CUtensorMap* m, int rank, const void* base, uint64_t inner, uint64_t rows,
-              uint64_t groups) {
+// Map over a row-major [groups][rows][inner] tensor of 1-byte (fp8) or
+// 2-byte (bf16) elements; box = 128 bytes x 128 rows, 128-byte swizzle.
+bool pair_map(CUtensorMap* m, int kind, int rank, const void* base, uint64_t inner,
+              uint64_t rows, uint64_t groups) {
   auto enc = encoder();
   if (!enc || !base) return false;
+  const int es = kind == KIND_FP8 ? 1 : 2;
   cuuint64_t dims[3] = {inner, rows, groups};
-  cuuint64_t strides[2] = {inner, inner * rows};
-  cuuint32_t box[3] = {(cuuint32_t)P_BK, 128, 1};
+  cuuint64_t strides[2] = {inner * es, inner * rows * es};
+  cuuint32_t box[3] = {(cuuint32_t)(P_BK / es), (cuuint32_t)P_ROWS, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, kind == KIND_FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FFN1>
-cudaError_t launch_pair(const GroupedFfnArgs& a, cudaStream_t s) {
-  const int K = FFN1 ? a.K : a.I;
-  const int Wrows = FFN1 ? 2 * a.I : a.K;
-  const void* w = FFN1 ? a.w13 : a.w2;
-  const void* ws = FFN1 ? a.sw13 : a.sw2;
-  const void* x = FFN1 ? a.xq : a.hq;
-  CUtensorMap tw, tws, tx;
-  if (!pair_map(&tw, 3, w, K, Wrows, a.E) || !pair_map(&tws, 3, ws ? ws : w, K, Wrows, 1) ||
-      !pair_map(&tx, 2, x, K, a.rows_total, 1))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(grouped_ffn_pair_kernel<FFN1>,
+template <int KIND, int EPI>
+cudaError_t launch_pair_gemm(const CUtensorMap& tw, const CUtensorMap& tws, const CUtensorMap& tx,
+                             const CUtensorMap& tw2, const CUtensorMap& tx2, const PairGemm& g,
+                             cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<KIND, EPI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -330,14 +409,84 @@ cudaError_t launch_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launch();
-  e = cudaLaunchKernelEx(&cfg, grouped_ffn_pair_kernel<FFN1>, tw, tws, tx, a);
+  e = cudaLaunchKernelEx(&cfg, pair_gemm_kernel<KIND, EPI>, tw, tws, tx, tw2, tx2, g);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
+template <bool FFN1>
+cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
+  const int K = FFN1 ? a.K : a.I;
+  const int Wrows = FFN1 ? 2 * a.I : a.K;
+  const void* w = FFN1 ? a.w13 : a.w2;
+  const void* ws = FFN1 ? a.sw13 : a.sw2;
+  const void* x = FFN1 ? a.xq : a.hq;
+  CUtensorMap tw, tws, tx;
+  if (!pair_map(&tw, KIND_FP8, 3, w, K, Wrows, a.E) ||
+      !pair_map(&tws, KIND_FP8, 3, ws ? ws : w, K, Wrows, 1) ||
+      !pair_map(&tx, KIND_FP8, 2, x, K, a.rows_total, 1))
+    return cudaErrorInvalidValue;
+  PairGemm g{};
+  g.items = a.items;
+  g.n_items = a.n_items;
+  g.max_items = a.max_items;
+  g.E = a.E;
+  g.nb = FFN1 ? a.I / 128 : a.K / P_N;
+  g.kb1 = K / P_BK;
+  g.kb2 = 0;
+  g.I = a.I;
+  g.rows_total = a.rows_total;
+  g.xscale = a.xscale;
+  g.w_scale = FFN1 ? a.w13_scale : a.w2_scale;
+  g.ws_scale = FFN1 ? a.sw13_scale : a.sw2_scale;
+  g.scale_stride = FFN1 ? 2 * a.I : a.K;
+  g.hs = a.hs;
+  g.row_w = a.row_w;
+  g.out = FFN1 ? a.h : a.y;
+  g.ldo = FFN1 ? a.I : a.K;
+  g.err = a.err;
+  if (FFN1) return launch_pair_gemm<KIND_FP8, EPI_SWIGLU>(tw, tws, tx, tw, tx, g, s);
+  return launch_pair_gemm<KIND_FP8, EPI_DOWN>(tw, tws, tx, tw, tx, g, s);
+}
+
 }  // namespace
 
-cudaError_t launch_ffn1_pair(const GroupedFfnArgs& a, cudaStream_t s) { return launch_pair<true>(a, s); }
-cudaError_t launch_ffn2_pair(const GroupedFfnArgs& a, cudaStream_t s) { return launch_pair<false>(a, s); }
+cudaError_t launch_ffn1_pair(const GroupedFfnArgs& a, cudaStream_t s) {
+  return launch_grouped_pair<true>(a, s);
+}
+cudaError_t launch_ffn2_pair(const GroupedFfnArgs& a, cudaStream_t s) {
+  return launch_grouped_pair<false>(a, s);
+}
+
+cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s) {
+  // A rows [rows, K1] (+ A2 [rows, K2]); B rows [N, K1] (+ B2 [N, K2]); bf16.
+  if (d.K1 % 64 || d.K2 % 64 || (d.swiglu ? d.N % 128 : d.N % P_N)) return cudaErrorInvalidValue;
+  CUtensorMap tw, tx, tw2, tx2;
+  const int wrows = d.swiglu ? 2 * d.N : d.N;
+  if (!pair_map(&tw, KIND_BF16, 3, d.w, d.K1, wrows, 1) ||
+      !pair_map(&tx, KIND_BF16, 2, d.x, d.K1, d.rows, 1))
+    return cudaErrorInvalidValue;
+  if (d.K2) {
+    if (!pair_map(&tw2, KIND_BF16, 3, d.w2, d.K2, d.N, 1) ||
+        !pair_map(&tx2, KIND_BF16, 2, d.x2, d.K2, d.rows, 1))
+      return cudaErrorInvalidValue;
+  } else {
+    tw2 = tw;
+    tx2 = tx;
+  }
+  PairGemm g{};
+  g.items = nullptr;
+  g.dense_rows = d.rows;
+  g.nb = d.swiglu ? d.N / 128 : d.N / P_N;
+  g.kb1 = d.K1 / 64;
+  g.kb2 = d.K2 / 64;
+  g.I = d.N;
+  g.rows_total = d.rows;
+  g.out = d.out;
+  g.ldo = d.N;
+  g.err = d.err;
+  if (d.swiglu) return launch_pair_gemm<KIND_BF16, EPI_SWIGLU>(tw, tw, tx, tw2, tx2, g, s);
+  return launch_pair_gemm<KIND_BF16, EPI_STORE>(tw, tw, tx, tw2, tx2, g, s);
+}
 
 }  // namespace moe

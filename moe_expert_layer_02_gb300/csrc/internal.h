@@ -45,6 +45,9 @@ cudaError_t launch_requant(const void* h, void* hq, float* hs, int rows, int I, 
 // out[t] = bf16(sum_j y[perm[t,j]] + shared[t]); shared may be NULL.
 cudaError_t launch_combine(const void* y, const int32_t* perm, const void* shared, void* out,
                            int T, int H, int k, int* err, cudaStream_t s);
+// yn[t] = bf16(RMSNorm(sum_j y[perm[t,j]]) * gamma), width L, eps given.
+cudaError_t launch_combine_rmsnorm(const void* y, const int32_t* perm, const void* gamma, void* yn,
+                                   int T, int L, int k, float eps, int* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- ffn_gemm.cu
 struct GroupedFfnArgs {
@@ -84,6 +87,29 @@ cudaError_t launch_ffn2(const GroupedFfnArgs& a, cudaStream_t s);
 // Same contract on pairs of SMs (256-row tiles); needs BN == 256, K % 256 == 0.
 cudaError_t launch_ffn1_pair(const GroupedFfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn2_pair(const GroupedFfnArgs& a, cudaStream_t s);
+
+// Dense bf16 GEMM on SM pairs: out[rows, N] = bf16(x w^T (+ x2 w2^T)), or with
+// swiglu: w holds 2N rows (gate rows then up rows) and out = bf16(silu(g) u).
+// K1, K2 multiples of 64; N a multiple of 256 (128 with swiglu).
+struct DenseGemmArgs {
+  const void* x;   // [rows, K1] bf16
+  const void* w;   // [N or 2N, K1] bf16
+  int K1;
+  const void* x2;  // [rows, K2] bf16 (K2 = 0: none)
+  const void* w2;  // [N, K2] bf16
+  int K2;
+  int rows, N;
+  bool swiglu;
+  void* out;       // [rows, N] bf16
+  int* err;
+};
+cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s);
+
+// ---------------------------------------------------------------- ffn_gemm_mx.cu
+// MXFP4 routed experts (w13/w2 packed e2m1, w13_scale/w2_scale e8m0 bytes);
+// BN in {32, 64, 96}; no shared-expert group.
+cudaError_t launch_ffn1_mx(const GroupedFfnArgs& a, cudaStream_t s);
+cudaError_t launch_ffn2_mx(const GroupedFfnArgs& a, cudaStream_t s);
 
 // Shared helpers (moe_api.cu)
 int device_sm_count();

@@ -96,10 +96,12 @@ struct StageTimer {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Plan {
-  int T, H, I, E, k, K, R, RT, nch, BN, max_items;
-  bool shared;
+  int T, H, I, E, k, K, R, RT, nch, BN, max_items, Is, L;
+  bool shared;      // fp8 shared expert fused into the grouped GEMMs (rows R..R+T)
+  bool shared_bf16; // bf16 shared expert as dense GEMMs (LatentMoE)
+  bool mx;          // MXFP4 routed experts
   size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
-      hq, hs, y, total;
+      hq, hs, y, z, yn, hsh, total;
 };
 
 int choose_bn(const moe_problem* p) {
@@ -109,6 +111,13 @@ int choose_bn(const moe_problem* p) {
     if (v == 32 || v == 64 || v == 128 || v == 256) return v;
   }
   const double avg = (double)p->T * p->top_k / (p->E > 0 ? p->E : 1);
+  if (p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32) {  // block-scaled kernel tiles: 32, 64, 96 rows
+    if (env) {
+      int v = std::atoi(env);
+      if (v == 32 || v == 64 || v == 96) return v;
+    }
+    return avg <= 24.0 ? 32 : avg <= 48.0 ? 64 : 96;
+  }
   if (avg <= 24.0) return 32;
   if (avg <= 48.0) return 64;
   if (avg <= 96.0) return 128;
@@ -124,11 +133,16 @@ Plan make_plan(const moe_problem* p) {
   q.k = p->top_k;
   q.K = p->latent > 0 ? p->latent : p->H;
   q.R = p->T * p->top_k;
-  q.shared = p->I_shared > 0;
+  q.Is = p->I_shared;
+  q.L = p->latent;
+  q.shared_bf16 = p->I_shared > 0 && (p->flags & MOE_F_SHARED_BF16);
+  q.shared = p->I_shared > 0 && !q.shared_bf16;
+  q.mx = p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32;
   q.RT = q.R + (q.shared ? p->T : 0);
   q.nch = num_chunks(p->T);
   q.BN = choose_bn(p);
-  q.max_items = (q.R + q.BN - 1) / q.BN + q.E + (q.shared ? (p->T + q.BN - 1) / q.BN + 1 : 0) + 1;
+  q.max_items = (q.R + q.BN - 1) / q.BN + q.E +
+                (p->I_shared > 0 ? (p->T + q.BN - 1) / q.BN + 1 : 0) + 1;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -154,6 +168,9 @@ Plan make_plan(const moe_problem* p) {
   q.hq = take(RT * (size_t)q.I);
   q.hs = take(RT * 4);
   q.y = take(RT * (size_t)q.K * 2);
+  q.z = take(q.L ? T * (size_t)q.L * 2 : 0);
+  q.yn = take(q.L ? T * (size_t)q.L * 2 : 0);
+  q.hsh = take(q.shared_bf16 ? T * (size_t)q.Is * 2 : 0);
   q.total = o;
   return q;
 }
@@ -180,11 +197,22 @@ int check_problem(const moe_problem* p) {
   return MOE_OK;
 }
 
-// Shapes this build runs on the GPU.
+// Shapes this build runs on the GPU: fp8 experts with an optional fp8 shared
+// expert (I_shared == I, fused into the grouped GEMMs), or the LatentMoE block
+// (latent > 0, optional bf16 shared expert) with fp8 or MXFP4 experts, or
+// MXFP4 experts on their own.
 int check_supported(const moe_problem* p) {
-  if (p->wfmt != MOE_W_FP8_E4M3_PER_CHANNEL || p->latent > 0) return MOE_ERR_UNSUPPORTED;
-  if (p->I_shared > 0 && ((p->flags & MOE_F_SHARED_BF16) || p->I_shared != p->I))
-    return MOE_ERR_UNSUPPORTED;
+  const bool mx = p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32;
+  const bool sb = p->I_shared > 0 && (p->flags & MOE_F_SHARED_BF16);
+  const bool s8 = p->I_shared > 0 && !sb;
+  if (p->latent > 0) {
+    if (s8) return MOE_ERR_UNSUPPORTED;
+    if (p->H % 256 || p->latent % 256) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (sb) return MOE_ERR_UNSUPPORTED;
+    if (mx && s8) return MOE_ERR_UNSUPPORTED;
+  }
+  if (s8 && p->I_shared != p->I) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -238,10 +266,10 @@ bool use_pair_gemm(const Plan& q) {
 }
 
 int run_experts(const Plan& q, const GroupedFfnArgs& a, int rows_total, cudaStream_t s) {
-  const bool pair = use_pair_gemm(q);
+  const bool pair = !q.mx && use_pair_gemm(q);
   {
     StageTimer t(MOE_STAGE_FFN1, s);
-    MOE_TRY(pair ? launch_ffn1_pair(a, s) : launch_ffn1(a, s));
+    MOE_TRY(q.mx ? launch_ffn1_mx(a, s) : pair ? launch_ffn1_pair(a, s) : launch_ffn1(a, s));
   }
   {
     StageTimer t(MOE_STAGE_REQUANT, s);
@@ -249,7 +277,7 @@ int run_experts(const Plan& q, const GroupedFfnArgs& a, int rows_total, cudaStre
   }
   {
     StageTimer t(MOE_STAGE_FFN2, s);
-    MOE_TRY(pair ? launch_ffn2_pair(a, s) : launch_ffn2(a, s));
+    MOE_TRY(q.mx ? launch_ffn2_mx(a, s) : pair ? launch_ffn2_pair(a, s) : launch_ffn2(a, s));
   }
   return MOE_OK;
 }
@@ -361,7 +389,7 @@ int moe_expert_ffn(const moe_problem* p, const int32_t* offsets, const void* xq_
   if (st) return st;
   if (!offsets || !xq_perm || !xscale_perm || !w13 || !w13_scale || !w2 || !w2_scale || !y)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned(xq_perm, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y, 16))
+  if (!aligned(xq_perm, 16) || !aligned(w13, 32) || !aligned(w2, 32) || !aligned(y, 16))
     return MOE_ERR_INVALID_ARG;
   st = check_supported(p);
   if (st) return st;
@@ -402,9 +430,6 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
                 const void* shared_w13_scale, const void* shared_w2,
                 const void* shared_w2_scale, const void* latent_down, const void* latent_up,
                 const void* latent_gamma, void* out, void* ws, size_t ws_bytes, void* stream) {
-  (void)latent_down;
-  (void)latent_up;
-  (void)latent_gamma;
   int st = check_problem(p);
   if (st) return st;
   if (!x || !router_w || !w13 || !w13_scale || !w2 || !w2_scale || !out) return MOE_ERR_INVALID_ARG;
@@ -412,9 +437,11 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   if (p->I_shared > 0 && (!shared_w13 || !shared_w2)) return MOE_ERR_INVALID_ARG;
   if (p->I_shared > 0 && !(p->flags & MOE_F_SHARED_BF16) && (!shared_w13_scale || !shared_w2_scale))
     return MOE_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
+  if (p->latent > 0 && (!latent_down || !latent_up || !latent_gamma)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(w13, 32) || !aligned(w2, 32) ||
       !aligned(out, 16) || (shared_w13 && !aligned(shared_w13, 16)) ||
-      (shared_w2 && !aligned(shared_w2, 16)))
+      (shared_w2 && !aligned(shared_w2, 16)) || (latent_down && !aligned(latent_down, 16)) ||
+      (latent_up && !aligned(latent_up, 16)) || (latent_gamma && !aligned(latent_gamma, 16)))
     return MOE_ERR_INVALID_ARG;
   st = check_supported(p);
   if (st) return st;
@@ -442,6 +469,21 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
     StageTimer t(MOE_STAGE_TOPK, s);
     MOE_TRY(launch_topk(logits, idx, tw, q.T, q.E, q.k, s));
   }
+  // LatentMoE: the experts run on z = bf16(x Wd^T) ("Kimi K3 ...", s.2.4)
+  const void* xin = x;
+  if (q.L) {
+    StageTimer t(MOE_STAGE_LATENT_DOWN, s);
+    DenseGemmArgs d{};
+    d.x = x;
+    d.w = latent_down;
+    d.K1 = q.H;
+    d.rows = q.T;
+    d.N = q.L;
+    d.out = at<void>(ws, q.z);
+    d.err = di->err;
+    MOE_TRY(launch_dense_bf16(d, s));
+    xin = at<void>(ws, q.z);
+  }
   {
     StageTimer t(MOE_STAGE_INDEX, s);
     MOE_TRY(launch_count(idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
@@ -453,16 +495,55 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   }
   {
     StageTimer t(MOE_STAGE_SCATTER, s);
-    MOE_TRY(launch_quant_scatter(x, perm, xq, xscale, q.T, q.H, q.k, q.shared ? q.R : -1, di->err, s));
+    MOE_TRY(launch_quant_scatter(xin, perm, xq, xscale, q.T, q.K, q.k, q.shared ? q.R : -1,
+                                 di->err, s));
   }
   GroupedFfnArgs a = ffn_args(q, ws, xq, xscale, row_w, w13, w13_scale, w2, w2_scale, shared_w13,
                               shared_w13_scale, shared_w2, shared_w2_scale, y, q.RT, di->err);
   st = run_experts(q, a, q.RT, s);
   if (st) return st;
-  {
+  if (!q.L) {
     StageTimer t(MOE_STAGE_COMBINE, s);
     MOE_TRY(launch_combine(y, perm, q.shared ? y + (size_t)q.R * q.H : nullptr, out, q.T, q.H, q.k,
                            di->err, s));
+    return MOE_OK;
+  }
+  // LatentMoE tail: RMSNorm of the routed combine, bf16 shared expert on the
+  // raw hidden, and out = bf16(yn Wu^T + h_s W2s^T) in one accumulation.
+  {
+    StageTimer t(MOE_STAGE_COMBINE, s);
+    MOE_TRY(launch_combine_rmsnorm(y, perm, latent_gamma, at<void>(ws, q.yn), q.T, q.L, q.k, 1e-6f,
+                                   di->err, s));
+  }
+  if (q.shared_bf16) {
+    StageTimer t(MOE_STAGE_SHARED, s);
+    DenseGemmArgs d{};
+    d.x = x;
+    d.w = shared_w13;
+    d.K1 = q.H;
+    d.rows = q.T;
+    d.N = q.Is;
+    d.swiglu = true;
+    d.out = at<void>(ws, q.hsh);
+    d.err = di->err;
+    MOE_TRY(launch_dense_bf16(d, s));
+  }
+  {
+    StageTimer t(MOE_STAGE_LATENT_UP, s);
+    DenseGemmArgs d{};
+    d.x = at<void>(ws, q.yn);
+    d.w = latent_up;
+    d.K1 = q.L;
+    if (q.shared_bf16) {
+      d.x2 = at<void>(ws, q.hsh);
+      d.w2 = shared_w2;
+      d.K2 = q.Is;
+    }
+    d.rows = q.T;
+    d.N = q.H;
+    d.out = out;
+    d.err = di->err;
+    MOE_TRY(launch_dense_bf16(d, s));
   }
   return MOE_OK;
 }

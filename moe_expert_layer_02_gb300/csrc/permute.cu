@@ -335,7 +335,95 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// LatentMoE: the routed combine feeds RMSNorm on the latent ("Kimi K3 ...
+// feasibility analysis", s.2.4: routed experts -> routed_expert_norm ->
+// up_proj).  acc = sum_j y[perm[t,j]] in fp32 (j ascending), then
+// yn = bf16(acc / sqrt(mean(acc^2) + eps) * gamma).
+__global__ void __launch_bounds__(256)
+    combine_rmsnorm_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ perm,
+                           const uint16_t* __restrict__ gamma, uint16_t* __restrict__ yn, int L,
+                           int k, int R, float eps, int* err) {
+  extern __shared__ float s_acc[];  // [L]
+  __shared__ int s_rows[kMaxTopK];
+  __shared__ float s_red[9];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    int row = perm[(size_t)t * k + threadIdx.x];
+    if ((unsigned)row >= (unsigned)R) {
+      record_error(err, kErrInvalidArg);
+      row = -1;
+    }
+    s_rows[threadIdx.x] = row;
+  }
+  __syncthreads();
+  const int nv = L / 8;
+  float sq = 0.0f;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      if (s_rows[j] < 0) continue;
+      float f[8];
+      unpack_bf16x8(reinterpret_cast<const uint4*>(y + (size_t)s_rows[j] * L)[v], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s_acc[v * 8 + i] = acc[i];
+      sq += acc[i] * acc[i];
+    }
+  }
+  // block sum of squares (non-negative: reuse the max helper's layout with adds)
+  sq = [&] {
+    float x = sq;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) s_red[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      float w = lane < 8 ? s_red[lane] : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+      if (lane == 0) s_red[8] = w;
+    }
+    __syncthreads();
+    return s_red[8];
+  }();
+  const float scale = 1.0f / sqrtf(sq / (float)L + eps);
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    float g[8];
+    unpack_bf16x8(reinterpret_cast<const uint4*>(gamma)[v], g);
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = s_acc[v * 8 + i] * scale * g[i];
+    uint4 u;
+    u.x = pack_bf16x2(o[0], o[1]);
+    u.y = pack_bf16x2(o[2], o[3]);
+    u.z = pack_bf16x2(o[4], o[5]);
+    u.w = pack_bf16x2(o[6], o[7]);
+    reinterpret_cast<uint4*>(yn + (size_t)t * L)[v] = u;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_rmsnorm(const void* y, const int32_t* perm, const void* gamma, void* yn,
+                                   int T, int L, int k, float eps, int* err, cudaStream_t s) {
+  const size_t smem = (size_t)L * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(combine_rmsnorm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  count_launch();
+  combine_rmsnorm_kernel<<<T, 256, smem, s>>>(static_cast<const uint16_t*>(y), perm,
+                                              static_cast<const uint16_t*>(gamma),
+                                              static_cast<uint16_t*>(yn), L, k, T * k, eps, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_count(const int32_t* idx, int32_t* cc, int T, int E, int k, int* err,
                          cudaStream_t s) {

@@ -73,8 +73,10 @@ def test_profile_counts_each_stage():
         ms, n = m.moe_profile_read()
     finally:
         m.moe_profile_enable(False)
-    assert all(v == 2 for v in n.values()), n
-    assert all(v > 0 for v in ms.values()), ms
+    base = ("router", "topk", "index", "scatter", "ffn1", "requant", "ffn2", "combine")
+    assert all(n[k] == 2 for k in base), n
+    assert all(ms[k] > 0 for k in base), ms
+    assert all(n[k] == 0 for k in n if k not in base)  # LatentMoE stages idle
 
 
 def test_empty_batch_is_a_noop():
