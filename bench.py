@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode")
+    ap.add_argument("--no-pack", action="store_true",
+                    help="time row-major expert weights instead of the packed tile order")
     ap.add_argument("--ref-tokens", type=int, default=0,
                     help="tokens per oracle step (default: one per host core)")
     return ap.parse_args()
@@ -60,6 +62,7 @@ def workload_name(cfg):
             "decode_e32": "Ling-style decode, 32 experts (profiling case)",
             "prefill_e32": "Ling-style prefill, 32 experts (profiling case)",
             "latent": "Kimi-K3-style LatentMoE",
+            "latent_e64": "Kimi-K3-style LatentMoE, 64 experts (profiling case)",
             "skewed": "skewed-routing stress (Zipf 1.2 router bias)", "toy": "toy"}.get(cfg.name, cfg.name)
     s = (f"{kind}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}"
          + (f" + shared expert I_s={cfg.I_s}" if cfg.I_s else "")
@@ -250,8 +253,27 @@ def run_ours(args, cfg):
     dev = torch.device("cuda", local)
     inp = mi.make_inputs(cfg, device=dev, seed=0)
     flags = (m.F_ROUTER_BIAS if cfg.zipf_bias else 0) | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
+    wfmt = m.W_MXFP4 if cfg.wfmt == "mxfp4" else m.W_FP8
+    pack = not args.no_pack and cfg.wfmt == "fp8"  # MXFP4 weights stay row-major
+    if pack:
+        # one-time load-time weight preparation (untimed): tile-major expert weights
+        pp = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+        w13p, w2p = torch.empty_like(inp["w13"]), torch.empty_like(inp["w2"])
+        m.moe_pack_weights(pp, inp["w13"], inp["w2"], None, None, w13p, w2p)
+        packed = dict(w13=w13p, w2=w2p)
+        if cfg.I_s and not cfg.shared_bf16:
+            ps = m.make_problem(cfg.T, cfg.H, cfg.I_s, 1, 1)
+            s13, s2 = torch.empty_like(inp["sw13"]), torch.empty_like(inp["sw2"])
+            m.moe_pack_weights(ps, inp["sw13"], inp["sw2"], None, None, s13, s2)
+            packed.update(sw13=s13, sw2=s2)
+        torch.cuda.synchronize()
+        host_inp = inp  # the oracle reads the original layout
+        inp = dict(inp, **packed)
+        flags |= m.F_PACKED_WEIGHTS
+    else:
+        host_inp = inp
     p = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, latent=cfg.L,
-                       wfmt=m.W_MXFP4 if cfg.wfmt == "mxfp4" else m.W_FP8, flags=flags)
+                       wfmt=wfmt, flags=flags)
     wsb = torch.empty(m.moe_workspace_bytes(p), dtype=torch.uint8, device=dev)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
@@ -355,6 +377,7 @@ def run_ours(args, cfg):
         "config": {"workload": workload_name(cfg), "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
                    "top_k": cfg.k, "I_shared": cfg.I_s, "touched_experts": touched,
                    "parallelism": "replicas" if ws_n > 1 else "single",
+                   "weights": "tile-major (moe_pack_weights, untimed)" if pack else "row-major",
                    "l2": "inputs larger than L2 (%.1f GB of weights per step), no flush" % (
                        (work["bytes_weights_routed"] + work["bytes_weights_shared"]) / 1e9)},
         "latency_us": ms_max * 1e3,
@@ -367,7 +390,7 @@ def run_ours(args, cfg):
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
     }
     if rank == 0 and ws_n == 1:
-        host = mi.to_numpy({k: v for k, v in inp.items()})
+        host = mi.to_numpy({k: v for k, v in host_inp.items()})
         dt, n, cores = cpu_baseline(cfg, host, args.ref_tokens)
         frac = n / cfg.T
         line["cpu_baseline"] = {

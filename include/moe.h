@@ -67,6 +67,8 @@ typedef enum {
 
 #define MOE_F_ROUTER_BIAS 0x1u /* add router_bias[e] to every logit before top-k    */
 #define MOE_F_SHARED_BF16 0x2u /* shared expert weights are bf16 (no quantisation)   */
+#define MOE_F_PACKED_WEIGHTS 0x4u /* fp8 routed (and shared) expert weights are in
+                                     moe_pack_weights' tile order; MXFP4: unsupported */
 
 typedef struct {
   int32_t T;        /* tokens                                                      */
@@ -163,6 +165,23 @@ int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, in
 int moe_permute_static(const moe_problem* p, const int32_t* topk_idx, const void* x,
                        int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* src_row,
                        void* xq_perm, float* xscale_perm, void* stream);
+
+/* One-time weight preparation (the "process weights after loading" step of a
+ * serving stack, Kimi K3 report s.12.2): copies fp8 routed expert weights into
+ * tile-major order, [E][rows/128][K/128][128 rows][128 bytes], so that every
+ * 128 x 128 tile a grouped-GEMM stage reads is one contiguous 16 KB block
+ * instead of 128 strided rows.  Bytes are only permuted; the per-channel scales
+ * are unchanged.  Pass the results with MOE_F_PACKED_WEIGHTS.  An fp8 shared
+ * expert is packed by calling this with E = 1 and I = I_shared on its two
+ * matrices.
+ *   w13 [E, 2I, K] / w2 [E, K, I] fp8 bytes, 16-byte aligned (K = H)
+ *   w13_scale, w2_scale, w13_scale_packed, w2_scale_packed: unused (reserved)
+ *   outputs: device buffers of the same sizes, not aliasing the inputs
+ * Asynchronous on `stream`; MOE_ERR_UNSUPPORTED for MXFP4 (its weights stay
+ * row-major), MOE_ERR_INVALID_ARG for bad shapes or pointers. */
+int moe_pack_weights(const moe_problem* p, const void* w13, const void* w2, const void* w13_scale,
+                     const void* w2_scale, void* w13_packed, void* w2_packed,
+                     void* w13_scale_packed, void* w2_scale_packed, void* stream);
 
 /* S5 + S6 -- grouped SwiGLU experts over expert-contiguous rows.  For rows r
  * in [offsets[e], offsets[e+1]):

@@ -16,7 +16,8 @@ __all__ = [
     "moe_router_logits", "moe_route", "moe_permute", "moe_permute_static", "moe_expert_ffn",
     "moe_unpermute",
     "moe_forward", "moe_get_last_error", "moe_launch_count", "moe_profile_enable",
-    "moe_profile_read", "STAGES", "W_FP8", "W_MXFP4", "F_ROUTER_BIAS", "F_SHARED_BF16",
+    "moe_profile_read", "moe_pack_weights", "STAGES", "W_FP8", "W_MXFP4", "F_ROUTER_BIAS",
+    "F_SHARED_BF16", "F_PACKED_WEIGHTS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -26,6 +27,7 @@ W_FP8 = 0
 W_MXFP4 = 1
 F_ROUTER_BIAS = 0x1
 F_SHARED_BF16 = 0x2
+F_PACKED_WEIGHTS = 0x4
 STAGES = ("router", "topk", "index", "scatter", "ffn1", "requant", "ffn2", "combine",
           "latent_down", "shared", "latent_up")
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -52,7 +54,8 @@ def make_problem(T, H, I, E, top_k, I_shared=0, latent=0, wfmt=W_FP8, flags=0) -
 _lib = None
 _EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_router_logits", "moe_route",
             "moe_permute", "moe_permute_static", "moe_expert_ffn", "moe_unpermute", "moe_forward",
-            "moe_get_last_error", "moe_launch_count", "moe_profile_enable", "moe_profile_read")
+            "moe_get_last_error", "moe_launch_count", "moe_profile_enable", "moe_profile_read",
+            "moe_pack_weights")
 
 
 def load_library(path: str = LIB_PATH):
@@ -72,6 +75,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_route.argtypes = [PP, P, P, P, P]
     L.moe_permute.argtypes = [PP, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_permute_static.argtypes = [PP, P, P, P, P, P, P, P, P, P]
+    L.moe_pack_weights.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_unpermute.argtypes = [PP, P, P, P, P, P]
     L.moe_forward.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P]
@@ -144,6 +148,14 @@ def moe_expert_ffn(p, offsets, xq_perm, xscale_perm, row_w, w13, w13_scale, w2, 
                                          _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(y),
                                          _ptr(ws), ws.numel() * ws.element_size(),
                                          _stream(stream)), "moe_expert_ffn")
+
+
+def moe_pack_weights(p, w13, w2, w13_scale, w2_scale, w13_packed, w2_packed,
+                     w13_scale_packed=None, w2_scale_packed=None, stream=None):
+    _check(load_library().moe_pack_weights(ctypes.byref(p), _ptr(w13), _ptr(w2), _ptr(w13_scale),
+                                           _ptr(w2_scale), _ptr(w13_packed), _ptr(w2_packed),
+                                           _ptr(w13_scale_packed), _ptr(w2_scale_packed),
+                                           _stream(stream)), "moe_pack_weights")
 
 
 def moe_unpermute(p, y_rows, perm, shared, out, stream=None):

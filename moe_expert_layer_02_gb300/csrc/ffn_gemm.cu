@@ -145,8 +145,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_3d(st, tw, kb * BK, nb * BM, gc, fb);
-          if (FFN1) tma_load_3d(st + C::A_BYTES, tw, kb * BK, a.I + nb * BM, gc, fb);
+          if (a.packed) {  // tile-major weights: tile (row block, k block) is contiguous
+            tma_load_3d(st, tw, 0, BM * (nb * KB + kb), gc, fb);
+            if (FFN1) tma_load_3d(st + C::A_BYTES, tw, 0, BM * ((a.I / BM + nb) * KB + kb), gc, fb);
+          } else {
+            tma_load_3d(st, tw, kb * BK, nb * BM, gc, fb);
+            if (FFN1) tma_load_3d(st + C::A_BYTES, tw, kb * BK, a.I + nb * BM, gc, fb);
+          }
           tma_load_2d(st + C::NA * C::A_BYTES, &tm_x, kb * BK, it.y, fb);
           s_issued[stage] = phase + 1u;
           if (++stage == C::STAGES) {
@@ -327,8 +332,11 @@ cudaError_t launch_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   const void* ws = FFN1 ? a.sw13 : a.sw2;
   const void* x = FFN1 ? a.xq : a.hq;
   CUtensorMap tw, tws, tx;
-  if (!make_map(&tw, 3, w, K, Wrows, a.E, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tws, 3, ws ? ws : w, K, Wrows, 1, BM)) return cudaErrorInvalidValue;
+  // tile-major weights are [group][tiles * 128 rows][128 bytes]
+  const uint64_t winner = a.packed ? BK : K;
+  const uint64_t wrows = a.packed ? (uint64_t)Wrows * (K / BK) : Wrows;
+  if (!make_map(&tw, 3, w, winner, wrows, a.E, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tws, 3, ws ? ws : w, winner, wrows, 1, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tx, 2, x, K, a.rows_total, 1, BN)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(grouped_ffn_kernel<FFN1, BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

@@ -66,6 +66,7 @@ struct PairGemm {
   int nb;                 // output blocks per item
   int kb1, kb2;           // K stages from (x, w) and from (x2, w2)
   int I;                  // SWIGLU: first row of the up-projection block
+  int packed;             // first-segment weights in tile-major order (pack.cu)
   int rows_total;         // rows of A (and of the output)
   const float* xscale;    // fp8 SWIGLU: per-row activation scale
   const float* w_scale;   // fp8: per-channel scale of group 0 (stride scale_stride)
@@ -197,7 +198,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * P_STAGE);
           if (kb < g.kb1) {
             tma_load_2d_pair(st, &tm_x, kb * EL, it.y + 128 * (int)rank, fb_leader);
-            tma_load_3d_pair(st + P_A_BYTES, tw, kb * EL, wrow, gc, fb_leader);
+            if (g.packed)  // tile-major weights: (row block, k block) is contiguous
+              tma_load_3d_pair(st + P_A_BYTES, tw, 0, 128 * ((wrow / 128) * g.kb1 + kb), gc,
+                               fb_leader);
+            else
+              tma_load_3d_pair(st + P_A_BYTES, tw, kb * EL, wrow, gc, fb_leader);
           } else {
             const int k2 = (kb - g.kb1) * EL;
             tma_load_2d_pair(st, &tm_x2, k2, it.y + 128 * (int)rank, fb_leader);
@@ -422,8 +427,10 @@ cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   const void* ws = FFN1 ? a.sw13 : a.sw2;
   const void* x = FFN1 ? a.xq : a.hq;
   CUtensorMap tw, tws, tx;
-  if (!pair_map(&tw, KIND_FP8, 3, w, K, Wrows, a.E) ||
-      !pair_map(&tws, KIND_FP8, 3, ws ? ws : w, K, Wrows, 1) ||
+  const uint64_t winner = a.packed ? P_BK : K;
+  const uint64_t wrows = a.packed ? (uint64_t)Wrows * (K / P_BK) : Wrows;
+  if (!pair_map(&tw, KIND_FP8, 3, w, winner, wrows, a.E) ||
+      !pair_map(&tws, KIND_FP8, 3, ws ? ws : w, winner, wrows, 1) ||
       !pair_map(&tx, KIND_FP8, 2, x, K, a.rows_total, 1))
     return cudaErrorInvalidValue;
   PairGemm g{};
@@ -435,6 +442,7 @@ cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   g.kb1 = K / P_BK;
   g.kb2 = 0;
   g.I = a.I;
+  g.packed = a.packed;
   g.rows_total = a.rows_total;
   g.xscale = a.xscale;
   g.w_scale = FFN1 ? a.w13_scale : a.w2_scale;

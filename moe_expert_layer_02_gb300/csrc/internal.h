@@ -77,6 +77,7 @@ struct GroupedFfnArgs {
   float* hs;              // [rows_total]
   void* y;                // [rows_total, K] bf16
   int BN;                 // token rows per tile (32, 64, 128, 256)
+  int packed;             // fp8 weights in tile-major order (pack.cu)
   int* err;
 };
 

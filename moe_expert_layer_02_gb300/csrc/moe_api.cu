@@ -100,6 +100,7 @@ struct Plan {
   bool shared;      // fp8 shared expert fused into the grouped GEMMs (rows R..R+T)
   bool shared_bf16; // bf16 shared expert as dense GEMMs (LatentMoE)
   bool mx;          // MXFP4 routed experts
+  int packed;       // expert weights in tile-major order (moe_pack_weights)
   size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
       hq, hs, y, z, yn, hsh, total;
 };
@@ -138,6 +139,7 @@ Plan make_plan(const moe_problem* p) {
   q.shared_bf16 = p->I_shared > 0 && (p->flags & MOE_F_SHARED_BF16);
   q.shared = p->I_shared > 0 && !q.shared_bf16;
   q.mx = p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32;
+  q.packed = (p->flags & MOE_F_PACKED_WEIGHTS) ? 1 : 0;
   q.RT = q.R + (q.shared ? p->T : 0);
   q.nch = num_chunks(p->T);
   q.BN = choose_bn(p);
@@ -213,6 +215,7 @@ int check_supported(const moe_problem* p) {
     if (mx && s8) return MOE_ERR_UNSUPPORTED;
   }
   if (s8 && p->I_shared != p->I) return MOE_ERR_UNSUPPORTED;
+  if (mx && (p->flags & MOE_F_PACKED_WEIGHTS)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -253,6 +256,7 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
   a.hs = at<float>(ws, q.hs);
   a.y = y;
   a.BN = q.BN;
+  a.packed = q.packed;
   a.err = err;
   return a;
 }

@@ -57,8 +57,10 @@ __device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
+// Small warp tiles fit two blocks per SM (more warps to hide shared-memory and
+// FMA latency); large ones need one block's worth of registers.
 template <int TW, int EW>
-__global__ void __launch_bounds__(RT_THREADS, 1)
+__global__ void __launch_bounds__(RT_THREADS, (TW * EW <= 64) ? 2 : 1)
     router_logits_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ bias,
                          float* __restrict__ logits, int T, int H, int E, int* err) {

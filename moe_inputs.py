@@ -80,6 +80,9 @@ CONFIGS = {
     # profiling stand-in for "decode": same expert shapes and ~16 rows per
     # expert, 32 experts (1.6 GB of weights: above L2, small enough to capture)
     "decode_e32": MoEConfig("decode_e32", T=64, H=8192, I=2048, E=32, k=8, I_s=2048),
+    # profiling stand-in for "latent": ~72 rows per expert, 64 experts
+    "latent_e64": MoEConfig("latent_e64", T=288, H=7168, I=3072, E=64, k=16, I_s=6144, L=3584,
+                            wfmt="mxfp4", shared_bf16=True),
     # profiling stand-in for "prefill": ~512 rows per expert, 32 experts
     "prefill_e32": MoEConfig("prefill_e32", T=2048, H=8192, I=2048, E=32, k=8, I_s=2048),
 }

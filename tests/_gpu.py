@@ -65,9 +65,28 @@ def host(inp: dict, keys=None) -> dict:
     return out
 
 
-def problem(cfg: mi.MoEConfig):
+def pack(cfg: mi.MoEConfig, inp: dict) -> dict:
+    """The same inputs with fp8 expert weights in moe_pack_weights' tile order."""
+    m = lib()
+    out = dict(inp)
+    p = problem(cfg)
+    w13p, w2p = torch.empty_like(inp["w13"]), torch.empty_like(inp["w2"])
+    m.moe_pack_weights(p, inp["w13"], inp["w2"], None, None, w13p, w2p)
+    out.update(w13=w13p, w2=w2p)
+    if cfg.I_s and not cfg.shared_bf16:
+        ps = m.make_problem(cfg.T, cfg.H, cfg.I_s, 1, 1)
+        s13, s2 = torch.empty_like(inp["sw13"]), torch.empty_like(inp["sw2"])
+        m.moe_pack_weights(ps, inp["sw13"], inp["sw2"], None, None, s13, s2)
+        out.update(sw13=s13, sw2=s2)
+    torch.cuda.synchronize()
+    return out
+
+
+def problem(cfg: mi.MoEConfig, packed: bool = False):
     m = lib()
     flags = m.F_ROUTER_BIAS if cfg.zipf_bias else 0
+    if packed:
+        flags |= m.F_PACKED_WEIGHTS
     if cfg.shared_bf16:
         flags |= m.F_SHARED_BF16
     return m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, latent=cfg.L,

@@ -72,9 +72,27 @@ def test_null_and_workspace_checks(m):
     # misaligned x
     bad = [ctypes.c_void_p(258)] + args[1:]
     assert lib.moe_forward(ctypes.byref(p), *bad, 1 << 30, None) == 1
-    # the LatentMoE / MXFP4 problem is valid but not yet run by this build
+    # a latent width that is not a multiple of 256 is valid but not implemented
     q = m.make_problem(4, 256, 128, 8, 2, latent=128, wfmt=m.W_MXFP4)
     assert lib.moe_forward(ctypes.byref(q), *args, 1 << 30, None) == 2
+    # MXFP4 weights have no tile-major form
+    q = m.make_problem(4, 256, 128, 8, 2, latent=256, wfmt=m.W_MXFP4,
+                       flags=m.F_PACKED_WEIGHTS | m.F_SHARED_BF16)
+    assert lib.moe_forward(ctypes.byref(q), *args, 1 << 30, None) == 2
+
+
+def test_pack_weights_checks(m):
+    lib = m.load_library()
+    a, b, c, d = (ctypes.c_void_p(v) for v in (256, 512, 768, 1024))
+    p = m.make_problem(4, 256, 128, 8, 2)
+    assert lib.moe_pack_weights(ctypes.byref(p), a, b, None, None, a, d, None, None, None) == 1
+    assert lib.moe_pack_weights(ctypes.byref(p), a, None, None, None, c, d, None, None, None) == 1
+    assert lib.moe_pack_weights(ctypes.byref(p), ctypes.c_void_p(260), b, None, None, c, d,
+                                None, None, None) == 1
+    assert lib.moe_pack_weights(ctypes.byref(m.make_problem(4, 256, 100, 8, 2)), a, b, None,
+                                None, c, d, None, None, None) == 1
+    q = m.make_problem(4, 256, 128, 8, 2, wfmt=m.W_MXFP4)
+    assert lib.moe_pack_weights(ctypes.byref(q), a, b, a, b, c, d, c, d, None) == 2
 
 
 def test_argument_counts_match_header(m):

@@ -16,9 +16,9 @@ FULL = [mi.CONFIGS["decode"], mi.CONFIGS["prefill"], mi.CONFIGS["skewed"]]
 ids = lambda c: c.name
 
 
-def run_forward(cfg, inp, out=None, ws=None):
+def run_forward(cfg, inp, out=None, ws=None, packed=False):
     m = G.lib()
-    p = G.problem(cfg)
+    p = G.problem(cfg, packed=packed)
     ws = G.workspace(p) if ws is None else ws
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda") if out is None else out
     m.moe_forward(p, inp["x"], inp["router_w"], inp["router_bias"], inp["w13"], inp["w13_scale"],
@@ -42,6 +42,39 @@ def _check(orc, cfg, n_sample):
 @pytest.mark.parametrize("cfg", SMALL, ids=ids)
 def test_forward_small(orc, cfg):
     _check(orc, cfg, n_sample=10 ** 9)
+
+
+def test_pack_is_a_tile_permutation():
+    # packed[e, rb, kb, r, :] == w[e, rb*128 + r, kb*128 : kb*128 + 128]
+    cfg = SHARED_SMALL.with_(I=256, H=384)
+    inp = G.gpu_inputs(cfg)
+    pk = G.pack(cfg, inp)
+    for key, R, C in (("w13", 2 * cfg.I, cfg.H), ("w2", cfg.H, cfg.I)):
+        w, p = inp[key], pk[key]
+        tiles = p.view(cfg.E, R // 128, C // 128, 128, 128)
+        back = tiles.permute(0, 1, 3, 2, 4).reshape(cfg.E, R, C)
+        assert torch.equal(back, w), key
+
+
+@pytest.mark.parametrize("cfg", [SHARED_SMALL, RAGGED, KE], ids=ids)
+def test_forward_packed_weights_small(orc, cfg):
+    m = G.lib()
+    inp = G.gpu_inputs(cfg)
+    out = run_forward(cfg, G.pack(cfg, inp), packed=True)
+    assert m.moe_get_last_error() == 0
+    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), G.host(inp))
+    G.assert_close(G.bf16_values(G.bf16_bits(out)), ref, f"packed {cfg.name}")
+
+
+@pytest.mark.parametrize("cfg", FULL, ids=ids)
+def test_forward_packed_weights_full_size(orc, cfg):
+    m = G.lib()
+    inp = G.gpu_inputs(cfg)
+    out = run_forward(cfg, G.pack(cfg, inp), packed=True)
+    assert m.moe_get_last_error() == 0
+    toks = G.sample_tokens(cfg.T, 16, seed=21)
+    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), G.host(inp), tokens=toks)
+    G.assert_close(G.bf16_values(G.bf16_bits(out))[toks], ref, f"packed {cfg.name}")
 
 
 @pytest.mark.parametrize("cfg", FULL, ids=ids)

@@ -53,9 +53,9 @@ def test_mxfp4_expert_ffn(orc, cfg, bn, monkeypatch):
     G.assert_close(G.bf16_values(G.bf16_bits(y)), ref, f"mxfp4 expert_ffn {cfg.name}")
 
 
-def _forward(cfg, inp):
+def _forward(cfg, inp, packed=False):
     m = G.lib()
-    p = G.problem(cfg)
+    p = G.problem(cfg, packed=packed)
     ws = G.workspace(p)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
     m.moe_forward(p, inp["x"], inp["router_w"], inp["router_bias"], inp["w13"], inp["w13_scale"],
