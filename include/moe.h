@@ -194,6 +194,12 @@ int moe_pack_weights(const moe_problem* p, const void* w13, const void* w2, cons
  *   xq_perm   [R, K] e4m3, xscale_perm [R] fp32, row_w [R] fp32 or NULL (= 1)
  *   fp8:   w13 [E, 2I, K] e4m3, w13_scale [E, 2I] fp32,
  *          w2  [E, K, I] e4m3,  w2_scale  [E, K] fp32
+ *   MXFP4 (Kimi K3 report, s.2.5): w13 [E, 2I, K/2] and w2 [E, K, I/2] bytes
+ *          holding two e2m1 values each (low nibble = even k), w13_scale
+ *          [E, 2I, K/32] and w2_scale [E, K, I/32] e8m0 bytes (one per 32
+ *          consecutive k, 4-byte aligned); the block scale multiplies inside the
+ *          K-sum, so the per-channel factors s13/s2 above are 1; K must be a
+ *          multiple of 256.
  *   y         [R, K] bf16 (out); K = H (or latent)
  * R is read from p as T*top_k. */
 int moe_expert_ffn(const moe_problem* p, const int32_t* offsets, const void* xq_perm,
@@ -220,7 +226,11 @@ int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
  *     same per-token fp8 activations as the routed experts.
  *   latent (L > 0): latent_down [L, H] bf16, latent_up [H, L] bf16,
  *     latent_gamma [L] bf16 (RMSNorm weight, eps 1e-6), Kimi K3 report s.2.4.
- *   out [T, H] bf16 (output); ws / ws_bytes as for moe_permute. */
+ *   out [T, H] bf16 (output); ws / ws_bytes as for moe_permute.
+ * Combinations this build runs (others return MOE_ERR_UNSUPPORTED): without
+ * latent, an fp8 shared expert with I_shared = I or none; with latent, a bf16
+ * shared expert or none and H, L multiples of 256; MXFP4 experts with K (H or
+ * L) a multiple of 256, no fp8 shared expert and row-major weights. */
 int moe_forward(const moe_problem* p, const void* x, const float* router_w,
                 const float* router_bias, const void* w13, const void* w13_scale,
                 const void* w2, const void* w2_scale, const void* shared_w13,
@@ -232,6 +242,20 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
  * word (MOE_OK if no device-side fault was recorded; MOE_ERR_CUDA if the
  * synchronisation itself failed). */
 int moe_get_last_error(void* stream);
+
+/* Self-test of the device watchdog (no counterpart in the pages: it checks this
+ * library's failure handling).  Launches one CTA shaped like the grouped GEMMs
+ * (one warp holding 32 tensor-memory columns, four warps in pipeline waits)
+ * whose mbarriers nothing arrives on.  Each wait gives up after the kernels'
+ * wait limit (2 s), the first to expire records MOE_ERR_TIMEOUT in the error
+ * word and raises the CTA's abort flag, the others stop on the flag, tensor
+ * memory is freed and the kernel returns; the context stays usable.
+ *   role_status [4] int32 device (out, nullable): 1 if warp w's wait completed,
+ *     0 if it gave up (always 0 here)
+ * Asynchronous on `stream`: read the result with moe_get_last_error, which then
+ * returns MOE_ERR_TIMEOUT.  Returns MOE_OK, or MOE_ERR_CUDA if the launch
+ * failed. */
+int moe_watchdog_selftest(int32_t* role_status, void* stream);
 
 /* Number of kernels this library has launched in this process (all devices).
  * Host-side counter, for accounting; never reset. */

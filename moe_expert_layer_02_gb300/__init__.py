@@ -16,8 +16,8 @@ __all__ = [
     "moe_router_logits", "moe_route", "moe_permute", "moe_permute_static", "moe_expert_ffn",
     "moe_unpermute",
     "moe_forward", "moe_get_last_error", "moe_launch_count", "moe_profile_enable",
-    "moe_profile_read", "moe_pack_weights", "STAGES", "W_FP8", "W_MXFP4", "F_ROUTER_BIAS",
-    "F_SHARED_BF16", "F_PACKED_WEIGHTS",
+    "moe_profile_read", "moe_pack_weights", "moe_watchdog_selftest", "STAGES", "W_FP8",
+    "W_MXFP4", "F_ROUTER_BIAS", "F_SHARED_BF16", "F_PACKED_WEIGHTS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -55,7 +55,7 @@ _lib = None
 _EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_router_logits", "moe_route",
             "moe_permute", "moe_permute_static", "moe_expert_ffn", "moe_unpermute", "moe_forward",
             "moe_get_last_error", "moe_launch_count", "moe_profile_enable", "moe_profile_read",
-            "moe_pack_weights")
+            "moe_pack_weights", "moe_watchdog_selftest")
 
 
 def load_library(path: str = LIB_PATH):
@@ -76,6 +76,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_permute.argtypes = [PP, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_permute_static.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.moe_pack_weights.argtypes = [PP, P, P, P, P, P, P, P, P, P]
+    L.moe_watchdog_selftest.argtypes = [P, P]
     L.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_unpermute.argtypes = [PP, P, P, P, P, P]
     L.moe_forward.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P]
@@ -175,6 +176,11 @@ def moe_forward(p, x, router_w, router_bias, w13, w13_scale, w2, w2_scale, share
 
 def moe_get_last_error(stream=None) -> int:
     return int(load_library().moe_get_last_error(_stream(stream)))
+
+
+def moe_watchdog_selftest(role_status=None, stream=None):
+    _check(load_library().moe_watchdog_selftest(_ptr(role_status), _stream(stream)),
+           "moe_watchdog_selftest")
 
 
 def moe_launch_count() -> int:

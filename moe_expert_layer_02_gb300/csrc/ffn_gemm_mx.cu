@@ -13,20 +13,29 @@
 // expanded in software.
 //
 // Structure as ffn_gemm.cu (persistent, one CTA per SM, swap-AB: M = 128
-// weight rows, N = the item's token rows rounded up to 16), plus four
-// scale-writer warps:
-//   warp 0      TMA producer: weights through a 16U4_ALIGN16B map (each 16
-//               packed e2m1 land in 16 bytes of shared memory, the operand
-//               layout kind::f8f6f4 reads; the transaction is counted in packed
-//               bytes), activation rows through a byte map; 128-byte swizzle.
-//   warp 1      MMA issuer: 4 MMAs of K=32 per 128-element stage, scale byte
-//               k selected by the descriptor's scale-factor ids.
+// weight rows, N = the item's token rows rounded up to 16):
+//   warp 0      producer.  Lane 0 waits for a free stage and issues the TMA
+//               loads: weights through a 16U4_ALIGN16B map (each 16 packed e2m1
+//               land in 16 bytes of shared memory, the operand layout
+//               kind::f8f6f4 reads; the transaction is counted in packed bytes)
+//               and activation rows through a byte map, 128-byte swizzle.  All
+//               32 lanes copy the stage's e8m0 weight scales with 4-byte
+//               cp.async straight into the layout tcgen05.cp reads (lane l,
+//               32-bit column c = the four k-block scales of row 32c + l), and
+//               each lane's copies arrive on the stage's full barrier when they
+//               land (cp.async.mbarrier.arrive.noinc), so no warp ever waits on
+//               a scale load.
+//   Each stage carries two 128-row weight blocks that share the activation
+//   tile: W1 and W3 rows of one output block (FFN1), or two adjacent W2 output
+//   blocks (FFN2), so every stage streams 16 KB of packed weights.
+//   warp 1      MMA issuer: per stage, a proxy fence (the scales were written
+//               through the generic proxy), tcgen05.cp of each weight block's
+//               scales into its tensor-memory slot (32x128b replicated to the
+//               four lane quarters), then 4 MMAs of K=32 per block, the scale
+//               byte picked by the descriptor's scale-factor id.  tcgen05.cp and
+//               tcgen05.mma from one thread execute in issue order.  The
+//               activation scales are a constant 2^0, copied once.
 //   warps 2-5   epilogue.
-//   warps 6-9   scale writers: for each stage, the e8m0 scales of the stage's
-//               weight rows go to tensor memory with tcgen05.st (row r of the
-//               128-row block at lane r mod 32 of every lane quarter, column
-//               r / 32, byte = k-block within the stage); the activation
-//               scales are a constant 2^0.
 #include <cudaTypedefs.h>
 
 #include "device.cuh"
@@ -40,14 +49,15 @@ constexpr int MX_BM = 128;         // weight rows per tile
 constexpr int MX_BK = 128;         // K elements per stage
 constexpr int MX_A_SMEM = MX_BM * MX_BK;          // 16 KB unpacked in shared memory
 constexpr int MX_A_TX = MX_BM * MX_BK / 2;        // 8 KB packed from global memory
-constexpr int MX_THREADS = 320;
+constexpr int MX_THREADS = 192;
+constexpr int MX_SF_SLOT = 512;  // one weight block's scales for one stage: 32 lanes x 16 B
 constexpr int MX_SMEM_BUDGET = 220 * 1024;
 
 constexpr int mx_min(int a, int b) { return a < b ? a : b; }
 
 template <bool FFN1, int BN>
 struct MxCfg {
-  static constexpr int NA = FFN1 ? 2 : 1;
+  static constexpr int NA = 2;  // 128-row weight blocks per stage: W1|W3 (FFN1), two W2 blocks (FFN2)
   static constexpr int B_BYTES = BN * MX_BK;
   static constexpr int STAGE_SMEM = NA * MX_A_SMEM + B_BYTES;
   static constexpr int STAGE_TX = NA * MX_A_TX + B_BYTES;
@@ -58,10 +68,12 @@ struct MxCfg {
   static constexpr int SFA_COL = SFB_COL + 8;                // NA x 4 columns per stage
   static constexpr int TMEM_USED = SFA_COL + STAGES * NA * 4;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_STAGES + 1;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_SMEM + NUM_BARS * 8 + 16 + STAGES * 4;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
+  static constexpr int SF_BYTES = STAGES * NA * MX_SF_SLOT + MX_SF_SLOT;  // + the 2^0 block
+  static constexpr int SMEM = 1024 + STAGES * STAGE_SMEM + SF_BYTES + NUM_BARS * 8 + 16 + STAGES * 4;
   static_assert(TMEM_USED <= TMEM_COLS, "tensor memory budget");
   static_assert(B_BYTES % 1024 == 0, "operand tiles keep 1024-byte alignment");
+  static_assert(SMEM <= 232448, "dynamic shared memory per block");
 };
 
 // kind::mxf8f6f4 block-scaled instruction descriptor: A = e2m1 (5), B = e4m3
@@ -82,14 +94,39 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t adesc, uint64_t bdes
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
-               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
-               : "memory");
+// 4-byte asynchronous global -> shared copy (both addresses 4-byte aligned).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+// The mbarrier receives one arrival (counted in its expected count) once every
+// cp.async this thread issued before has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Generic-proxy shared-memory writes become visible to later async-proxy reads
+// (tcgen05.cp) of this thread.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte scale block, no swizzle: 8-row
+// core matrices of 128 contiguous bytes, 128 bytes apart (both offset fields).
+__device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) |
+         ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
+}
+
+// Copy a 32-row x 128-bit block from shared memory to tensor memory columns
+// [taddr, taddr + 4) of all four lane quarters (row l -> lane l of each quarter).
+__device__ __forceinline__ void tmem_cp_32x128_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t f32_to_bf16_bits(float v) {
@@ -105,11 +142,11 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_SMEM);
-  uint64_t* full = bars;                    // TMA data landed
-  uint64_t* sfull = bars + C::STAGES;       // scales in tensor memory
-  uint64_t* empty = bars + 2 * C::STAGES;   // MMAs done with the stage
-  uint64_t* tfull = bars + 3 * C::STAGES;
+  uint8_t* sf = smem + C::STAGES * C::STAGE_SMEM;  // [STAGES][NA][512 B], then the 2^0 block
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf + C::SF_BYTES);
+  uint64_t* full = bars;                    // weights, activations and scales landed
+  uint64_t* empty = bars + C::STAGES;       // MMAs done with the stage
+  uint64_t* tfull = bars + 2 * C::STAGES;
   uint64_t* tempty = tfull + C::ACC_STAGES;
   uint64_t* drain = tempty + C::ACC_STAGES;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
@@ -117,10 +154,15 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   uint32_t* s_issued = s_tmem + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {
+    // activation scale block: every byte e8m0 127 = 2^0
+    uint32_t* one = reinterpret_cast<uint32_t*>(sf + C::STAGES * C::NA * MX_SF_SLOT);
+    for (int i = threadIdx.x; i < MX_SF_SLOT / 4; i += blockDim.x) one[i] = 0x7F7F7F7Fu;
+    fence_proxy_async_smem();
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&sfull[s]), 4);
+      mbar_init(smem_u32(&full[s]), 1 + 32);  // TMA expect_tx + one cp.async arrival per lane
       mbar_init(smem_u32(&empty[s]), 1);
       s_issued[s] = 0;
     }
@@ -142,44 +184,69 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  const int NB = FFN1 ? a.I / MX_BM : a.K / MX_BM;
+  const int NB = FFN1 ? a.I / MX_BM : a.K / (2 * MX_BM);  // tiles per item
   const int Kel = FFN1 ? a.K : a.I;  // reduction width in elements
   const int KB = Kel / MX_BK;
   const int n_items = min(*a.n_items, a.max_items);
   const int n_tiles = n_items * NB;
+  // first weight row of block blk (0, 1) of tile column nb
+  auto block_row = [&](int blk, int nb) {
+    return FFN1 ? blk * a.I + nb * MX_BM : (2 * nb + blk) * MX_BM;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && !*s_abort; tile += gridDim.x) {
-        const int item = tile / NB, nb = tile - item * NB;
-        const int4 it = a.items[item];
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort)) {
-            ok = false;
-            break;
-          }
+    // e8m0 scales [E][rows][K/32] (passed through the fp32 scale fields)
+    const uint8_t* scales = reinterpret_cast<const uint8_t*>(FFN1 ? a.w13_scale : a.w2_scale);
+    const int wrows = FFN1 ? 2 * a.I : a.K;  // weight rows per expert
+    const int sbytes = Kel / 32;             // scale bytes per weight row
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      // the whole warp takes the abort decision lane 0 reads (shuffles below need all lanes)
+      if (__shfl_sync(0xffffffffu, lane == 0 ? *s_abort : 0, 0)) break;
+      const int item = tile / NB, nb = tile - item * NB;
+      const int4 it = a.items[item];
+      const uint8_t* sb = scales + (size_t)it.x * wrows * sbytes;
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        int got = 1;
+        if (lane == 0) got = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[stage]);
+        const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT) + lane * 16;
+#pragma unroll
+        for (int blk = 0; blk < C::NA; ++blk) {
+          const uint8_t* src = sb + (size_t)(block_row(blk, nb) + lane) * sbytes + kb * 4;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            cp_async4(sfs + blk * MX_SF_SLOT + c * 4, src + (size_t)(32 * c) * sbytes);
+        }
+        cp_async_arrive_noinc(fb);
+        if (lane == 0) {
           const uint32_t st = smem_u32(smem + stage * C::STAGE_SMEM);
-          const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(fb, C::STAGE_TX);
-          tma_load_3d(st, &tm_w, kb * MX_BK, nb * MX_BM, it.x, fb);
-          if (FFN1) tma_load_3d(st + MX_A_SMEM, &tm_w, kb * MX_BK, a.I + nb * MX_BM, it.x, fb);
+          tma_load_3d(st, &tm_w, kb * MX_BK, block_row(0, nb), it.x, fb);
+          tma_load_3d(st + MX_A_SMEM, &tm_w, kb * MX_BK, block_row(1, nb), it.x, fb);
           tma_load_2d(st + C::NA * MX_A_SMEM, &tm_x, kb * MX_BK, it.y, fb);
           s_issued[stage] = phase + 1u;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (!ok) break;
+        __syncwarp();
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (*s_abort) {
-        for (int s = 0; s < C::STAGES; ++s)
-          if (s_issued[s]) mbar_wait_drain(smem_u32(&full[s]), s_issued[s] - 1u);
-      }
+      if (!ok) break;
+    }
+    cp_async_wait_all();  // no copy into this CTA's shared memory outlives it
+    if (lane == 0 && *s_abort) {
+      for (int s = 0; s < C::STAGES; ++s)
+        if (s_issued[s]) mbar_wait_drain(smem_u32(&full[s]), s_issued[s] - 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -187,6 +254,12 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       int stage = 0, it_local = 0;
       uint32_t phase = 0;
       bool issued_any = false;
+      const uint32_t sfb = tmem + C::SFB_COL;
+      {
+        const uint64_t one = sf_desc(smem_u32(sf + C::STAGES * C::NA * MX_SF_SLOT));
+        tmem_cp_32x128_x4(sfb, one);
+        tmem_cp_32x128_x4(sfb + 4, one);
+      }
       for (int tile = blockIdx.x; tile < n_tiles && !*s_abort; tile += gridDim.x, ++it_local) {
         const int item = tile / NB;
         const int rows = a.items[item].z;
@@ -198,25 +271,27 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         const uint32_t d0 = tmem + acc * C::ACC_COLS;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(&full[stage]), phase, a.err, s_abort) ||
-              !mbar_wait(smem_u32(&sfull[stage]), phase, a.err, s_abort)) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, a.err, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          fence_proxy_async_smem();
           const uint32_t a0 = smem_u32(smem + stage * C::STAGE_SMEM);
           const uint32_t b0 = a0 + C::NA * MX_A_SMEM;
           const uint32_t sfa = tmem + C::SFA_COL + stage * C::NA * 4;
-          const uint32_t sfb = tmem + C::SFB_COL;
+          const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT);
+#pragma unroll
+          for (int blk = 0; blk < C::NA; ++blk)
+            tmem_cp_32x128_x4(sfa + blk * 4, sf_desc(sfs + blk * MX_SF_SLOT));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t idesc = idesc_mx(MX_BM, n, kk);
             const uint64_t bdesc = smem_desc_sw128(b0 + kk * 32);
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             mma_mx(d0, smem_desc_sw128(a0 + kk * 32), bdesc, idesc, sfa, sfb, accum);
-            if (FFN1)
-              mma_mx(d0 + BN, smem_desc_sw128(a0 + MX_A_SMEM + kk * 32), bdesc, idesc, sfa + 4, sfb,
-                     accum);
+            mma_mx(d0 + BN, smem_desc_sw128(a0 + MX_A_SMEM + kk * 32), bdesc, idesc, sfa + 4, sfb,
+                   accum);
           }
           issued_any = true;
           mma_commit(smem_u32(&empty[stage]));
@@ -231,55 +306,6 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       if (*s_abort && issued_any) {
         mma_commit(smem_u32(drain));
         mbar_wait_drain(smem_u32(drain), 0);
-      }
-    }
-  } else if (warp >= 6) {
-    // ------------------------------------------------------------ scale writers
-    const int q = warp & 3;
-    const uint32_t lq = (uint32_t)(q * 32) << 16;
-    {
-      const uint32_t one[4] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu};
-      tmem_st4(tmem + lq + C::SFB_COL, one);
-      tmem_st4(tmem + lq + C::SFB_COL + 4, one);
-    }
-    // e8m0 scales [E][rows][K/32] (passed through the fp32 scale fields)
-    const uint8_t* scales = reinterpret_cast<const uint8_t*>(FFN1 ? a.w13_scale : a.w2_scale);
-    const int wrows = FFN1 ? 2 * a.I : a.K;  // weight rows per expert
-    const int sbytes = Kel / 32;             // scale bytes per weight row
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const int item = tile / NB, nb = tile - item * NB;
-      const int4 it = a.items[item];
-      const uint8_t* sb = scales + (size_t)it.x * wrows * sbytes;
-      for (int kb = 0; kb < KB; ++kb) {
-        int got = 1;
-        if (lane == 0) got = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort) ? 1 : 0;
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int blk = 0; blk < C::NA; ++blk) {
-          const int r0 = (blk == 0 ? 0 : a.I) + nb * MX_BM;
-          uint32_t v[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            v[c] = __ldg(reinterpret_cast<const uint32_t*>(sb + (size_t)(r0 + lane + 32 * c) * sbytes +
-                                                           kb * 4));
-          tmem_st4(tmem + lq + C::SFA_COL + stage * C::NA * 4 + blk * 4, v);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sfull[stage]));
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
       }
     }
   } else {
@@ -298,7 +324,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * C::ACC_COLS;
-      const int f = nb * MX_BM + q * 32 + lane;
+      const int f = nb * MX_BM + q * 32 + lane;            // FFN1: h column
+      const int f2 = 2 * nb * MX_BM + q * 32 + lane;       // FFN2: y column of block 0
       if (FFN1) {
         uint16_t* hout = static_cast<uint16_t*>(a.h);
         for (int c0 = 0; c0 < rows; c0 += 16) {
@@ -322,9 +349,10 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       } else {
         uint16_t* yout = static_cast<uint16_t*>(a.y);
         for (int c0 = 0; c0 < rows; c0 += 16) {
-          uint32_t v[16];
+          uint32_t v0[16], v1[16];
           __syncwarp();
-          tmem_ld16(tbase + c0, v);
+          tmem_ld16(tbase + c0, v0);
+          tmem_ld16(tbase + BN + c0, v1);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -332,8 +360,10 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             const int row = row0 + r;
             if (r < rows && (unsigned)row < (unsigned)a.rows_total) {
               const float rw = a.row_w ? a.row_w[row] : 1.0f;
-              yout[(size_t)row * a.K + f] =
-                  (uint16_t)f32_to_bf16_bits((__uint_as_float(v[j]) * a.hs[row]) * rw);
+              const float hs = a.hs[row];
+              uint16_t* yr = yout + (size_t)row * a.K + f2;
+              yr[0] = (uint16_t)f32_to_bf16_bits((__uint_as_float(v0[j]) * hs) * rw);
+              yr[MX_BM] = (uint16_t)f32_to_bf16_bits((__uint_as_float(v1[j]) * hs) * rw);
             }
           }
         }
@@ -375,6 +405,9 @@ cudaError_t launch_mx_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   const int Wrows = FFN1 ? 2 * a.I : a.K;
   const void* w = FFN1 ? a.w13 : a.w2;
   const void* x = FFN1 ? a.xq : a.hq;
+  const void* sc = FFN1 ? a.w13_scale : a.w2_scale;
+  if (reinterpret_cast<uintptr_t>(sc) % 4) return cudaErrorInvalidValue;  // 4-byte cp.async
+  if (!FFN1 && a.K % (2 * MX_BM)) return cudaErrorInvalidValue;           // two W2 blocks per tile
   CUtensorMap tw, tx;
   {
     // packed e2m1 weights [E][rows][Kel/2 bytes], unpacked to 16 bytes per 16 values

@@ -216,6 +216,7 @@ int check_supported(const moe_problem* p) {
   }
   if (s8 && p->I_shared != p->I) return MOE_ERR_UNSUPPORTED;
   if (mx && (p->flags & MOE_F_PACKED_WEIGHTS)) return MOE_ERR_UNSUPPORTED;
+  if (mx && (p->latent > 0 ? p->latent : p->H) % 256) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -393,7 +394,8 @@ int moe_expert_ffn(const moe_problem* p, const int32_t* offsets, const void* xq_
   if (st) return st;
   if (!offsets || !xq_perm || !xscale_perm || !w13 || !w13_scale || !w2 || !w2_scale || !y)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned(xq_perm, 16) || !aligned(w13, 32) || !aligned(w2, 32) || !aligned(y, 16))
+  if (!aligned(xq_perm, 16) || !aligned(w13, 32) || !aligned(w2, 32) || !aligned(y, 16) ||
+      !aligned(w13_scale, 4) || !aligned(w2_scale, 4))
     return MOE_ERR_INVALID_ARG;
   st = check_supported(p);
   if (st) return st;
@@ -445,7 +447,8 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(w13, 32) || !aligned(w2, 32) ||
       !aligned(out, 16) || (shared_w13 && !aligned(shared_w13, 16)) ||
       (shared_w2 && !aligned(shared_w2, 16)) || (latent_down && !aligned(latent_down, 16)) ||
-      (latent_up && !aligned(latent_up, 16)) || (latent_gamma && !aligned(latent_gamma, 16)))
+      (latent_up && !aligned(latent_up, 16)) || (latent_gamma && !aligned(latent_gamma, 16)) ||
+      !aligned(w13_scale, 4) || !aligned(w2_scale, 4))
     return MOE_ERR_INVALID_ARG;
   st = check_supported(p);
   if (st) return st;

@@ -75,6 +75,9 @@ def test_null_and_workspace_checks(m):
     # a latent width that is not a multiple of 256 is valid but not implemented
     q = m.make_problem(4, 256, 128, 8, 2, latent=128, wfmt=m.W_MXFP4)
     assert lib.moe_forward(ctypes.byref(q), *args, 1 << 30, None) == 2
+    # MXFP4 experts need K (here H) to be a multiple of 256
+    q = m.make_problem(4, 384, 128, 8, 2, wfmt=m.W_MXFP4)
+    assert lib.moe_forward(ctypes.byref(q), *args, 1 << 30, None) == 2
     # MXFP4 weights have no tile-major form
     q = m.make_problem(4, 256, 128, 8, 2, latent=256, wfmt=m.W_MXFP4,
                        flags=m.F_PACKED_WEIGHTS | m.F_SHARED_BF16)
