@@ -254,13 +254,19 @@ def run_ours(args, cfg):
     inp = mi.make_inputs(cfg, device=dev, seed=0)
     flags = (m.F_ROUTER_BIAS if cfg.zipf_bias else 0) | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
     wfmt = m.W_MXFP4 if cfg.wfmt == "mxfp4" else m.W_FP8
-    pack = not args.no_pack and cfg.wfmt == "fp8"  # MXFP4 weights stay row-major
+    pack = not args.no_pack
     if pack:
         # one-time load-time weight preparation (untimed): tile-major expert weights
-        pp = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+        pp = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, latent=cfg.L, wfmt=wfmt)
         w13p, w2p = torch.empty_like(inp["w13"]), torch.empty_like(inp["w2"])
-        m.moe_pack_weights(pp, inp["w13"], inp["w2"], None, None, w13p, w2p)
         packed = dict(w13=w13p, w2=w2p)
+        if cfg.wfmt == "mxfp4":  # e8m0 scales regrouped into per-stage tensor-memory images
+            s13p, s2p = torch.empty_like(inp["w13_scale"]), torch.empty_like(inp["w2_scale"])
+            m.moe_pack_weights(pp, inp["w13"], inp["w2"], inp["w13_scale"], inp["w2_scale"], w13p,
+                               w2p, s13p, s2p)
+            packed.update(w13_scale=s13p, w2_scale=s2p)
+        else:
+            m.moe_pack_weights(pp, inp["w13"], inp["w2"], None, None, w13p, w2p)
         if cfg.I_s and not cfg.shared_bf16:
             ps = m.make_problem(cfg.T, cfg.H, cfg.I_s, 1, 1)
             s13, s2 = torch.empty_like(inp["sw13"]), torch.empty_like(inp["sw2"])

@@ -67,8 +67,8 @@ typedef enum {
 
 #define MOE_F_ROUTER_BIAS 0x1u /* add router_bias[e] to every logit before top-k    */
 #define MOE_F_SHARED_BF16 0x2u /* shared expert weights are bf16 (no quantisation)   */
-#define MOE_F_PACKED_WEIGHTS 0x4u /* fp8 routed (and shared) expert weights are in
-                                     moe_pack_weights' tile order; MXFP4: unsupported */
+#define MOE_F_PACKED_WEIGHTS 0x4u /* routed (and fp8 shared) expert weights are in
+                                     moe_pack_weights' tile order                  */
 
 typedef struct {
   int32_t T;        /* tokens                                                      */
@@ -167,18 +167,27 @@ int moe_permute_static(const moe_problem* p, const int32_t* topk_idx, const void
                        void* xq_perm, float* xscale_perm, void* stream);
 
 /* One-time weight preparation (the "process weights after loading" step of a
- * serving stack, Kimi K3 report s.12.2): copies fp8 routed expert weights into
- * tile-major order, [E][rows/128][K/128][128 rows][128 bytes], so that every
- * 128 x 128 tile a grouped-GEMM stage reads is one contiguous 16 KB block
- * instead of 128 strided rows.  Bytes are only permuted; the per-channel scales
- * are unchanged.  Pass the results with MOE_F_PACKED_WEIGHTS.  An fp8 shared
- * expert is packed by calling this with E = 1 and I = I_shared on its two
- * matrices.
- *   w13 [E, 2I, K] / w2 [E, K, I] fp8 bytes, 16-byte aligned (K = H)
- *   w13_scale, w2_scale, w13_scale_packed, w2_scale_packed: unused (reserved)
+ * serving stack, Kimi K3 report s.12.2): copies routed expert weights (and
+ * MXFP4 scales) into the order the grouped GEMMs stream them.  Bytes are only
+ * permuted.  Pass the results with MOE_F_PACKED_WEIGHTS.
+ *   fp8: tile-major [E][rows/128][K/128][128 rows][128 bytes], so every 128 x
+ *     128 tile a stage reads is one contiguous 16 KB block instead of 128
+ *     strided rows; per-channel scales are unchanged (scale arguments unused).
+ *     An fp8 shared expert is packed by calling this with E = 1 and I =
+ *     I_shared on its two matrices.
+ *   MXFP4 (K = H or latent a multiple of 256): a stage reads two 128-row
+ *     blocks, W1 and W3 block p (rows p*128 and I + p*128) of w13, or W2 blocks
+ *     2p and 2p+1 of w2.  Weights become [E][P][K/128][2][128 rows][64 bytes]
+ *     and scales [E][P][K/128][2][32][4] 32-bit words, word (l, c) of block
+ *     b holding the four e8m0 bytes of k-stage kb of that block's row 32c + l
+ *     (the image tcgen05.cp copies into tensor memory): one 256-row copy and
+ *     one 1 KB copy per stage.
+ *   w13 [E, 2I, K] / w2 [E, K, I]: fp8 bytes, or MXFP4 bytes of two e2m1 each
+ *     ([E, 2I, K/2] / [E, K, I/2]), 16-byte aligned (K = H, or latent)
+ *   w13_scale [E, 2I, K/32], w2_scale [E, K, I/32] e8m0 and their packed
+ *     outputs of the same sizes: MXFP4 only (16-byte aligned), else ignored
  *   outputs: device buffers of the same sizes, not aliasing the inputs
- * Asynchronous on `stream`; MOE_ERR_UNSUPPORTED for MXFP4 (its weights stay
- * row-major), MOE_ERR_INVALID_ARG for bad shapes or pointers. */
+ * Asynchronous on `stream`; MOE_ERR_INVALID_ARG for bad shapes or pointers. */
 int moe_pack_weights(const moe_problem* p, const void* w13, const void* w2, const void* w13_scale,
                      const void* w2_scale, void* w13_packed, void* w2_packed,
                      void* w13_scale_packed, void* w2_scale_packed, void* stream);
@@ -230,7 +239,7 @@ int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
  * Combinations this build runs (others return MOE_ERR_UNSUPPORTED): without
  * latent, an fp8 shared expert with I_shared = I or none; with latent, a bf16
  * shared expert or none and H, L multiples of 256; MXFP4 experts with K (H or
- * L) a multiple of 256, no fp8 shared expert and row-major weights. */
+ * L) a multiple of 256 and no fp8 shared expert. */
 int moe_forward(const moe_problem* p, const void* x, const float* router_w,
                 const float* router_bias, const void* w13, const void* w13_scale,
                 const void* w2, const void* w2_scale, const void* shared_w13,

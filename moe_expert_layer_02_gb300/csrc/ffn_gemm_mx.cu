@@ -18,18 +18,24 @@
 //               loads: weights through a 16U4_ALIGN16B map (each 16 packed e2m1
 //               land in 16 bytes of shared memory, the operand layout
 //               kind::f8f6f4 reads; the transaction is counted in packed bytes)
-//               and activation rows through a byte map, 128-byte swizzle.  All
-//               32 lanes copy the stage's e8m0 weight scales with 4-byte
-//               cp.async straight into the layout tcgen05.cp reads (lane l,
-//               32-bit column c = the four k-block scales of row 32c + l), and
-//               each lane's copies arrive on the stage's full barrier when they
-//               land (cp.async.mbarrier.arrive.noinc), so no warp ever waits on
-//               a scale load.
+//               and activation rows through a byte map, 128-byte swizzle.
+//               The stage's e8m0 weight scales go to shared memory in the image
+//               tcgen05.cp reads (lane l, 32-bit column c = the four k-block
+//               scales of row 32c + l): with scales from moe_pack_weights that
+//               image is one contiguous 512-byte block per weight block, fetched
+//               by lane 0 with one bulk copy counted on the stage's transaction
+//               bytes; with row-major scales all 32 lanes fetch it with 4-byte
+//               cp.async whose completion arrives on the stage's full barrier
+//               (cp.async.mbarrier.arrive.noinc).  No warp waits on a scale load.
 //   Each stage carries two 128-row weight blocks that share the activation
 //   tile: W1 and W3 rows of one output block (FFN1), or two adjacent W2 output
 //   blocks (FFN2), so every stage streams 16 KB of packed weights.
-//   warp 1      MMA issuer: per stage, a proxy fence (the scales were written
-//               through the generic proxy), tcgen05.cp of each weight block's
+//   With moe_pack_weights' order the two blocks of a stage are one 256-row
+//   TMA box and their scales one 1 KB bulk copy: a stage costs the producer
+//   three copies, which keeps its issue rate off the critical path.  Each next
+//   tile's scales are prefetched into L2 a tile ahead.
+//   warp 1      MMA issuer: per stage, a proxy fence (row-major scales are
+//               written through the generic proxy), tcgen05.cp of each weight block's
 //               scales into its tensor-memory slot (32x128b replicated to the
 //               four lane quarters), then 4 MMAs of K=32 per block, the scale
 //               byte picked by the descriptor's scale-factor id.  tcgen05.cp and
@@ -162,7 +168,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1 + 32);  // TMA expect_tx + one cp.async arrival per lane
+      // TMA expect_tx (+ one cp.async arrival per producer lane for row-major scales)
+      mbar_init(smem_u32(&full[s]), a.packed ? 1 : 1 + 32);
       mbar_init(smem_u32(&empty[s]), 1);
       s_issued[s] = 0;
     }
@@ -200,6 +207,12 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     const uint8_t* scales = reinterpret_cast<const uint8_t*>(FFN1 ? a.w13_scale : a.w2_scale);
     const int wrows = FFN1 ? 2 * a.I : a.K;  // weight rows per expert
     const int sbytes = Kel / 32;             // scale bytes per weight row
+    const bool sf_pf_ok = (reinterpret_cast<uintptr_t>(scales) & 15) == 0;  // bulk prefetch alignment
+    // packed (moe_pack_weights): weights [E][NB][KB][2 blocks][128 rows][64 B] and
+    // scales [E][NB][KB][2 blocks][512 B], so a stage is one 256-row box + 1 KB
+    auto sf_packed = [&](int e, int nb, int kb) {
+      return scales + (((size_t)e * NB + nb) * KB + kb) * (C::NA * MX_SF_SLOT);
+    };
     int stage = 0;
     uint32_t phase = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
@@ -208,6 +221,23 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       const int item = tile / NB, nb = tile - item * NB;
       const int4 it = a.items[item];
       const uint8_t* sb = scales + (size_t)it.x * wrows * sbytes;
+      // L2 lookahead: the next tile's item, and its scale rows (one contiguous
+      // 128 x K/32-byte range per weight block) fetched a whole tile early
+      const int ntile = tile + gridDim.x;
+      const bool has_next = ntile < n_tiles;
+      const int nnb = has_next ? ntile % NB : 0;
+      const int4 itn = has_next ? a.items[ntile / NB] : it;
+      if (lane == 0 && has_next && sf_pf_ok) {
+#pragma unroll
+        for (int blk = 0; blk < C::NA; ++blk) {
+          if (a.packed) {
+            if (blk == 0)
+              prefetch_l2(sf_packed(itn.x, nnb, 0), (uint32_t)(KB * C::NA * MX_SF_SLOT));
+          } else
+            prefetch_l2(scales + ((size_t)itn.x * wrows + block_row(blk, nnb)) * sbytes,
+                        (uint32_t)(MX_BM * sbytes));
+        }
+      }
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
         int got = 1;
@@ -218,20 +248,28 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
           break;
         }
         const uint32_t fb = smem_u32(&full[stage]);
-        const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT) + lane * 16;
+        const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT);
+        if (!a.packed) {
+          // row-major scales: lane l copies rows 32c + l of each block (4 bytes each)
 #pragma unroll
-        for (int blk = 0; blk < C::NA; ++blk) {
-          const uint8_t* src = sb + (size_t)(block_row(blk, nb) + lane) * sbytes + kb * 4;
+          for (int blk = 0; blk < C::NA; ++blk) {
+            const uint8_t* src = sb + (size_t)(block_row(blk, nb) + lane) * sbytes + kb * 4;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            cp_async4(sfs + blk * MX_SF_SLOT + c * 4, src + (size_t)(32 * c) * sbytes);
+            for (int c = 0; c < 4; ++c)
+              cp_async4(sfs + lane * 16 + blk * MX_SF_SLOT + c * 4, src + (size_t)(32 * c) * sbytes);
+          }
+          cp_async_arrive_noinc(fb);
         }
-        cp_async_arrive_noinc(fb);
         if (lane == 0) {
           const uint32_t st = smem_u32(smem + stage * C::STAGE_SMEM);
-          mbar_arrive_expect_tx(fb, C::STAGE_TX);
-          tma_load_3d(st, &tm_w, kb * MX_BK, block_row(0, nb), it.x, fb);
-          tma_load_3d(st + MX_A_SMEM, &tm_w, kb * MX_BK, block_row(1, nb), it.x, fb);
+          mbar_arrive_expect_tx(fb, C::STAGE_TX + (a.packed ? C::NA * MX_SF_SLOT : 0));
+          if (a.packed) {
+            bulk_load(sfs, sf_packed(it.x, nb, kb), C::NA * MX_SF_SLOT, fb);
+            tma_load_3d(st, &tm_w, 0, C::NA * MX_BM * (nb * KB + kb), it.x, fb);  // both blocks
+          } else {
+            tma_load_3d(st, &tm_w, kb * MX_BK, block_row(0, nb), it.x, fb);
+            tma_load_3d(st + MX_A_SMEM, &tm_w, kb * MX_BK, block_row(1, nb), it.x, fb);
+          }
           tma_load_2d(st + C::NA * MX_A_SMEM, &tm_x, kb * MX_BK, it.y, fb);
           s_issued[stage] = phase + 1u;
         }
@@ -406,14 +444,19 @@ cudaError_t launch_mx_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   const void* w = FFN1 ? a.w13 : a.w2;
   const void* x = FFN1 ? a.xq : a.hq;
   const void* sc = FFN1 ? a.w13_scale : a.w2_scale;
-  if (reinterpret_cast<uintptr_t>(sc) % 4) return cudaErrorInvalidValue;  // 4-byte cp.async
+  // 4-byte cp.async (row-major scales) or 16-byte bulk copies (packed scales)
+  if (reinterpret_cast<uintptr_t>(sc) % (a.packed ? 16 : 4)) return cudaErrorInvalidValue;
   if (!FFN1 && a.K % (2 * MX_BM)) return cudaErrorInvalidValue;           // two W2 blocks per tile
   CUtensorMap tw, tx;
   {
-    // packed e2m1 weights [E][rows][Kel/2 bytes], unpacked to 16 bytes per 16 values
-    cuuint64_t dims[3] = {(cuuint64_t)Kel, (cuuint64_t)Wrows, (cuuint64_t)a.E};
-    cuuint64_t strides[2] = {(cuuint64_t)Kel / 2, (cuuint64_t)Kel / 2 * Wrows};
-    cuuint32_t box[3] = {MX_BK, MX_BM, 1};
+    // packed e2m1 weights [E][rows][Kel/2 bytes], unpacked to 16 bytes per 16 values;
+    // moe_pack_weights' order is [E][rows/256 * Kel/128 * 256 rows][64 bytes], read as
+    // one box of both blocks of a stage
+    const cuuint64_t inner = a.packed ? MX_BK : Kel;
+    const cuuint64_t wr = a.packed ? (cuuint64_t)Wrows * (Kel / MX_BK) : Wrows;
+    cuuint64_t dims[3] = {inner, wr, (cuuint64_t)a.E};
+    cuuint64_t strides[2] = {inner / 2, inner / 2 * wr};
+    cuuint32_t box[3] = {MX_BK, (cuuint32_t)(a.packed ? 2 * MX_BM : MX_BM), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(w), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -215,7 +215,6 @@ int check_supported(const moe_problem* p) {
     if (mx && s8) return MOE_ERR_UNSUPPORTED;
   }
   if (s8 && p->I_shared != p->I) return MOE_ERR_UNSUPPORTED;
-  if (mx && (p->flags & MOE_F_PACKED_WEIGHTS)) return MOE_ERR_UNSUPPORTED;
   if (mx && (p->latent > 0 ? p->latent : p->H) % 256) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }

@@ -66,12 +66,18 @@ def host(inp: dict, keys=None) -> dict:
 
 
 def pack(cfg: mi.MoEConfig, inp: dict) -> dict:
-    """The same inputs with fp8 expert weights in moe_pack_weights' tile order."""
+    """The same inputs with expert weights in moe_pack_weights' tile order."""
     m = lib()
     out = dict(inp)
     p = problem(cfg)
     w13p, w2p = torch.empty_like(inp["w13"]), torch.empty_like(inp["w2"])
-    m.moe_pack_weights(p, inp["w13"], inp["w2"], None, None, w13p, w2p)
+    if cfg.wfmt == "mxfp4":
+        s13p, s2p = torch.empty_like(inp["w13_scale"]), torch.empty_like(inp["w2_scale"])
+        m.moe_pack_weights(p, inp["w13"], inp["w2"], inp["w13_scale"], inp["w2_scale"], w13p, w2p,
+                           s13p, s2p)
+        out.update(w13_scale=s13p, w2_scale=s2p)
+    else:
+        m.moe_pack_weights(p, inp["w13"], inp["w2"], None, None, w13p, w2p)
     out.update(w13=w13p, w2=w2p)
     if cfg.I_s and not cfg.shared_bf16:
         ps = m.make_problem(cfg.T, cfg.H, cfg.I_s, 1, 1)

@@ -73,17 +73,52 @@ def test_latent_and_mxfp4_forward_small(orc, cfg):
     G.assert_close(G.bf16_values(G.bf16_bits(out)), ref, f"moe_forward {cfg.name}")
 
 
-def _latent_full(orc):
+def _block_rows(key, cfg, p, b):
+    # the 128 weight rows of block b of stage pair p: W1|W3 block p (w13), W2 block 2p+b (w2)
+    start = (b * cfg.I + p * 128) if key.startswith("w13") else (2 * p + b) * 128
+    return torch.arange(start, start + 128)
+
+
+def test_mxfp4_pack_is_a_permutation():
+    # weights: packed[e, p, kb, b, r, :] == w[e, row(p, b) + r, 64kb : 64kb + 64]  (128 e2m1)
+    # scales:  packed[e, p, kb, b, l, c, :] == s[e, row(p, b) + 32c + l, 4kb : 4kb + 4]
+    cfg = MX_PLAIN.with_(I=512)
+    inp = G.gpu_inputs(cfg)
+    pk = G.pack(cfg, inp)
+    for key, R, C in (("w13", 2 * cfg.I, cfg.H), ("w2", cfg.H, cfg.I)):
+        w, t = inp[key].view(cfg.E, R, C // 2), pk[key].reshape(cfg.E, R // 256, C // 128, 2, 128, 64)
+        sk = key + "_scale"
+        s = inp[sk].view(cfg.E, R, C // 32)
+        img = pk[sk].reshape(cfg.E, R // 256, C // 128, 2, 32, 4, 4)  # e, p, kb, b, l, c, byte
+        for p in range(R // 256):
+            for b in range(2):
+                rows = _block_rows(key, cfg, p, b)
+                got_w = t[:, p, :, b].permute(0, 2, 1, 3).reshape(cfg.E, 128, C // 2)
+                assert torch.equal(got_w, w[:, rows]), (key, p, b)
+                got_s = img[:, p, :, b].permute(0, 3, 2, 1, 4).reshape(cfg.E, 128, C // 32)
+                assert torch.equal(got_s, s[:, rows]), (sk, p, b)
+
+
+@pytest.mark.parametrize("cfg", [LAT_SMALL, MX_PLAIN], ids=ids)
+def test_mxfp4_packed_forward_small(orc, cfg):
+    inp = G.gpu_inputs(cfg)
+    out = _forward(cfg, G.pack(cfg, inp), packed=True)
+    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), G.host(inp))
+    G.assert_close(G.bf16_values(G.bf16_bits(out)), ref, f"packed {cfg.name}")
+
+
+def _latent_full(orc, packed=False):
     cfg = mi.CONFIGS["latent"]
     inp = G.gpu_inputs(cfg)
-    out = _forward(cfg, inp)
+    out = _forward(cfg, G.pack(cfg, inp) if packed else inp, packed=packed)
     toks = G.sample_tokens(cfg.T, 24, seed=5)
     ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), G.host(inp), tokens=toks)
     return G.bf16_values(G.bf16_bits(out))[toks], ref
 
 
-def test_latent_full_size_sampled_rel_l2(orc):
-    got, ref = _latent_full(orc)
+@pytest.mark.parametrize("packed", [False, True], ids=["row-major", "packed"])
+def test_latent_full_size_sampled_rel_l2(orc, packed):
+    got, ref = _latent_full(orc, packed)
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     assert rel <= G.REL_L2, rel
 
