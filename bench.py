@@ -371,7 +371,9 @@ def run_ours(args, cfg):
         roof = {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": ach / fp8_peak,
                 "peak_source": f"2 x bf16_tflops_sustained of {src} (fp8 = 2 x bf16 nominal ratio)"}
-    roof.update({"kernel": "grouped_ffn_kernel<FFN1> (W1|W3 + SiLU*gate)", "traffic": traffic,
+    plan = m.moe_describe(p)
+    ffn1_kernel = plan.split()[0].split("=", 1)[1]
+    roof.update({"kernel": f"{ffn1_kernel} (W1|W3 + SiLU*gate)", "traffic": traffic,
                  "algorithmic_bytes_per_launch": ffn1_bytes, "flops_per_launch": ffn1_flops,
                  "avg_launch_ms": ffn1_ms,
                  "layer_hbm_frac": (bytes_step / (ms_max * 1e-3) / 1e9) / hbm,
@@ -384,6 +386,7 @@ def run_ours(args, cfg):
                    "top_k": cfg.k, "I_shared": cfg.I_s, "touched_experts": touched,
                    "parallelism": "replicas" if ws_n > 1 else "single",
                    "weights": "tile-major (moe_pack_weights, untimed)" if pack else "row-major",
+                   "plan": plan,
                    "l2": "inputs larger than L2 (%.1f GB of weights per step), no flush" % (
                        (work["bytes_weights_routed"] + work["bytes_weights_shared"]) / 1e9)},
         "latency_us": ms_max * 1e3,

@@ -102,6 +102,13 @@ enum {
 /* Human-readable name of a moe_status (static storage). */
 const char* moe_status_string(int status);
 
+/* Host-only: a one-line description of how moe_forward runs problem `p` (the
+ * grouped-GEMM kernels, token-tile rows, weight format, workspace bytes),
+ * written NUL-terminated into buf[len].  MOE_ERR_INVALID_ARG if `p` is invalid
+ * or buf too short, MOE_ERR_UNSUPPORTED for a combination this build does not
+ * run.  For logs and benchmarks; the text format may change. */
+int moe_describe(const moe_problem* p, char* buf, size_t len);
+
 /* Bytes of device workspace that moe_forward, moe_permute and moe_expert_ffn
  * need for problem `p` (0 if `p` is invalid).  Pure host computation. */
 size_t moe_workspace_bytes(const moe_problem* p);

@@ -16,7 +16,8 @@ __all__ = [
     "moe_router_logits", "moe_route", "moe_permute", "moe_permute_static", "moe_expert_ffn",
     "moe_unpermute",
     "moe_forward", "moe_get_last_error", "moe_launch_count", "moe_profile_enable",
-    "moe_profile_read", "moe_pack_weights", "moe_watchdog_selftest", "STAGES", "W_FP8",
+    "moe_profile_read", "moe_pack_weights", "moe_watchdog_selftest", "moe_describe", "STAGES",
+    "W_FP8",
     "W_MXFP4", "F_ROUTER_BIAS", "F_SHARED_BF16", "F_PACKED_WEIGHTS",
 ]
 
@@ -55,7 +56,7 @@ _lib = None
 _EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_router_logits", "moe_route",
             "moe_permute", "moe_permute_static", "moe_expert_ffn", "moe_unpermute", "moe_forward",
             "moe_get_last_error", "moe_launch_count", "moe_profile_enable", "moe_profile_read",
-            "moe_pack_weights", "moe_watchdog_selftest")
+            "moe_pack_weights", "moe_watchdog_selftest", "moe_describe")
 
 
 def load_library(path: str = LIB_PATH):
@@ -77,6 +78,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_permute_static.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.moe_pack_weights.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.moe_watchdog_selftest.argtypes = [P, P]
+    L.moe_describe.argtypes = [PP, ctypes.c_char_p, ctypes.c_size_t]
     L.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_unpermute.argtypes = [PP, P, P, P, P, P]
     L.moe_forward.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P]
@@ -181,6 +183,12 @@ def moe_get_last_error(stream=None) -> int:
 def moe_watchdog_selftest(role_status=None, stream=None):
     _check(load_library().moe_watchdog_selftest(_ptr(role_status), _stream(stream)),
            "moe_watchdog_selftest")
+
+
+def moe_describe(p) -> str:
+    buf = ctypes.create_string_buffer(512)
+    _check(load_library().moe_describe(ctypes.byref(p), buf, len(buf)), "moe_describe")
+    return buf.value.decode()
 
 
 def moe_launch_count() -> int:

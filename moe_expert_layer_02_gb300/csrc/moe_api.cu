@@ -318,6 +318,25 @@ const char* moe_status_string(int status) {
   }
 }
 
+int moe_describe(const moe_problem* p, char* buf, size_t len) {
+  if (!buf || len == 0) return MOE_ERR_INVALID_ARG;
+  buf[0] = 0;
+  int st = check_problem(p);
+  if (st) return st;
+  st = check_supported(p);
+  if (st) return st;
+  const Plan q = make_plan(p);
+  const bool pair = !q.mx && use_pair_gemm(q);
+  const char* g = q.mx ? "grouped_mx_kernel" : pair ? "pair_gemm_kernel" : "grouped_ffn_kernel";
+  const int n = std::snprintf(
+      buf, len,
+      "ffn1=%s<FFN1,BN=%d> ffn2=%s<FFN2,BN=%d> tile_rows=%d weights=%s%s%s max_items=%d "
+      "workspace=%zu",
+      g, q.BN, g, q.BN, q.BN, q.mx ? "mxfp4" : "fp8", q.packed ? ",packed" : "",
+      q.L > 0 ? " latent=bf16-pair-gemms" : "", q.max_items, q.total);
+  return (n < 0 || (size_t)n >= len) ? MOE_ERR_INVALID_ARG : MOE_OK;
+}
+
 size_t moe_workspace_bytes(const moe_problem* p) {
   if (check_problem(p) != MOE_OK) return 0;
   return make_plan(p).total;

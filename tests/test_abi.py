@@ -110,3 +110,17 @@ def test_binding_names_match_c_names(m):
     for n in declared_functions():
         if n != "moe_status_string":
             assert hasattr(m, n), n
+
+
+def test_describe_names_the_kernels(m):
+    p = m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048)
+    assert m.moe_describe(p).startswith("ffn1=grouped_ffn_kernel<FFN1,BN=32>")
+    q = m.make_problem(16384, 8192, 2048, 256, 8, I_shared=2048)
+    assert "pair_gemm_kernel<FFN1,BN=256>" in m.moe_describe(q)
+    x = m.make_problem(4096, 7168, 3072, 896, 16, I_shared=6144, latent=3584, wfmt=m.W_MXFP4,
+                       flags=m.F_SHARED_BF16)
+    assert "grouped_mx_kernel<FFN1,BN=96>" in m.moe_describe(x)
+    lib = m.load_library()
+    buf = ctypes.create_string_buffer(8)
+    assert lib.moe_describe(ctypes.byref(p), buf, 8) == 1  # too short
+    assert lib.moe_describe(ctypes.byref(m.make_problem(4, 100, 128, 8, 2)), buf, 8) == 1
