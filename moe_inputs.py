@@ -53,6 +53,9 @@ class MoEConfig:
     shared_bf16: bool = False
     zipf_bias: bool = False
     rms_eps: float = 1e-6
+    routing: str = "softmax"  # "softmax" top-k | "sigmoid" (noaux_tc, selection bias)
+    act: str = "swiglu"       # "swiglu" | "situ" (beta = 4)
+    sel_bias: bool = False    # noaux_tc selection bias ~ N(0, 0.05^2) per expert
 
     @property
     def K(self) -> int:   # expert input/output width
@@ -67,7 +70,8 @@ class MoEConfig:
 
     def oracle_problem(self) -> dict:
         return dict(T=self.T, H=self.H, I=self.I, E=self.E, k=self.k, I_s=self.I_s, L=self.L,
-                    wfmt=self.wfmt, shared_bf16=self.shared_bf16, rms_eps=self.rms_eps)
+                    wfmt=self.wfmt, shared_bf16=self.shared_bf16, rms_eps=self.rms_eps,
+                    routing=self.routing, act=self.act)
 
 
 CONFIGS = {
@@ -77,6 +81,11 @@ CONFIGS = {
     "latent": MoEConfig("latent", T=4096, H=7168, I=3072, E=896, k=16, I_s=6144, L=3584,
                         wfmt="mxfp4", shared_bf16=True),
     "skewed": MoEConfig("skewed", T=8192, H=8192, I=2048, E=256, k=8, I_s=2048, zipf_bias=True),
+    # the LatentMoE workload with Kimi K3's own routing and activation (noaux_tc
+    # sigmoid routing with a selection bias, SiTU experts)
+    "latent_k3": MoEConfig("latent_k3", T=4096, H=7168, I=3072, E=896, k=16, I_s=6144, L=3584,
+                           wfmt="mxfp4", shared_bf16=True, routing="sigmoid", act="situ",
+                           sel_bias=True),
     # profiling stand-in for "decode": same expert shapes and ~16 rows per
     # expert, 32 experts (1.6 GB of weights: above L2, small enough to capture)
     "decode_e32": MoEConfig("decode_e32", T=64, H=8192, I=2048, E=32, k=8, I_s=2048),
@@ -148,6 +157,8 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, expert_weights: dic
         p = rank.pow(-1.2)
         p = p / p.sum()
         out["router_bias"] = (2.0 * torch.log(p)).float().to(device)
+    if cfg.sel_bias:
+        out["router_bias"] = (0.05 * torch.randn(E, generator=g)).float().to(device)
 
     if expert_weights is not None:
         for key in ("w13", "w13_scale", "w2", "w2_scale", "sw13", "sw13_scale", "sw2",

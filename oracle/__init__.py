@@ -31,6 +31,8 @@ _lib = None
 
 FP8 = 0
 MXFP4 = 1
+SWIGLU = 0
+SITU = 1
 
 
 def build(force: bool = False) -> str:
@@ -51,7 +53,7 @@ class Problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
                 ("E", ctypes.c_int64), ("k", ctypes.c_int64), ("I_s", ctypes.c_int64),
                 ("L", ctypes.c_int64), ("wfmt", ctypes.c_int32), ("shared_bf16", ctypes.c_int32),
-                ("rms_eps", ctypes.c_double)]
+                ("rms_eps", ctypes.c_double), ("routing", ctypes.c_int32), ("act", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -83,11 +85,16 @@ def lib():
         L.orc_default_threads.restype = ctypes.c_int
         L.orc_router_logits.argtypes = [i64, i64, i64, P, P, P, P, ctypes.c_int]
         L.orc_topk.argtypes = [i64, i64, ctypes.c_int, P, P, P]
+        L.orc_topk_sigmoid.argtypes = [i64, i64, ctypes.c_int, P, P, P, P]
+        L.orc_exp_canon.restype = ctypes.c_float
+        L.orc_exp_canon.argtypes = [ctypes.c_float]
+        L.orc_sigmoid_canon.restype = ctypes.c_float
+        L.orc_sigmoid_canon.argtypes = [ctypes.c_float]
         L.orc_permute.argtypes = [i64, i64, ctypes.c_int, P, P, P, P, P]
         L.orc_quant_rows.argtypes = [i64, i64, P, P, P]
         L.orc_moe_forward.argtypes = [ctypes.POINTER(Problem), ctypes.POINTER(Weights), P, i64,
                                       P, P, P, P, ctypes.c_int]
-        L.orc_expert_rows.argtypes = [i32, i64, i64, i64, P, P, P, P, P, P, P, P, P, P, P, P,
+        L.orc_expert_rows.argtypes = [i32, i32, i64, i64, i64, P, P, P, P, P, P, P, P, P, P, P, P,
                                       ctypes.c_int]
         L.orc_combine.argtypes = [i64, i64, ctypes.c_int, P, P, P, P]
         _lib = L
@@ -159,14 +166,37 @@ def router_logits(x_bf16_u16, router_w, bias=None, nthreads: int = 0) -> np.ndar
     return out
 
 
-def topk(logits, k: int):
-    """S2: (idx int32 [T, k], weights float64 [T, k])."""
+def topk(logits, k: int, routing: str = "softmax", bias=None):
+    """S2: (idx int32 [T, k], weights float64 [T, k]).
+
+    routing "softmax": the k largest logits, softmax over them (a bias, if any,
+    is already inside the logits).  "sigmoid" (noaux_tc): the k largest
+    sigmoid(logit) + bias, weights = the chosen sigmoid scores renormalised."""
     lg = _c(logits, np.float32)
     T, E = lg.shape
     idx = np.empty((T, k), dtype=np.int32)
     w = np.empty((T, k), dtype=np.float64)
-    lib().orc_topk(T, E, k, _p(lg), _p(idx), _p(w))
+    if routing == "sigmoid":
+        b = None if bias is None else _c(bias, np.float32)
+        lib().orc_topk_sigmoid(T, E, k, _p(lg), _p(b), _p(idx), _p(w))
+    else:
+        assert bias is None
+        lib().orc_topk(T, E, k, _p(lg), _p(idx), _p(w))
     return idx, w
+
+
+def exp_canon(a) -> np.ndarray:
+    """The canonical fp32 exp(a), a <= 0, used by sigmoid routing's selection."""
+    f = lib().orc_exp_canon
+    return np.array([f(float(v)) for v in np.asarray(a, dtype=np.float32).ravel()],
+                    dtype=np.float32).reshape(np.shape(a))
+
+
+def sigmoid_canon(l) -> np.ndarray:
+    """The canonical fp32 sigmoid used by sigmoid routing's selection."""
+    f = lib().orc_sigmoid_canon
+    return np.array([f(float(v)) for v in np.asarray(l, dtype=np.float32).ravel()],
+                    dtype=np.float32).reshape(np.shape(l))
 
 
 def permute(idx, E: int):
@@ -192,8 +222,9 @@ def quant_rows(x_bf16_u16):
 
 
 def expert_rows(wfmt, off, xq, xs, row_w, w13, w13_scale, w2, w2_scale, want_h=False,
-                nthreads: int = 0):
-    """y[r] = row_w[r] * FFN_{e(r)}(xq[r]) for expert-contiguous rows (fp64)."""
+                nthreads: int = 0, act: int = 0):
+    """y[r] = row_w[r] * FFN_{e(r)}(xq[r]) for expert-contiguous rows (fp64);
+    act = SWIGLU (0) or SITU (1)."""
     off = _c(off, np.int32)
     xq = _c(xq, np.uint8)
     R, K = xq.shape
@@ -209,7 +240,7 @@ def expert_rows(wfmt, off, xq, xs, row_w, w13, w13_scale, w2, w2_scale, want_h=F
     h = np.empty((R, I), dtype=np.uint16) if want_h else None
     hq = np.empty((R, I), dtype=np.uint8) if want_h else None
     hs = np.empty(R, dtype=np.float32) if want_h else None
-    lib().orc_expert_rows(wfmt, K, I, E, _p(off), _p(xq), _p(xs), _p(row_w), _p(w13),
+    lib().orc_expert_rows(wfmt, act, K, I, E, _p(off), _p(xq), _p(xs), _p(row_w), _p(w13),
                           _p(w13_scale), _p(w2), _p(w2_scale), _p(y), _p(h), _p(hq), _p(hs),
                           nthreads)
     return (y, h, hq, hs) if want_h else y
@@ -230,7 +261,8 @@ def combine(y_bf16_u16, perm, shared_bf16_u16=None):
 def moe_forward(prob: dict, w: dict, tokens=None, nthreads: int = 0):
     """The whole layer for the listed tokens.
 
-    ``prob``: T, H, I, E, k, I_s, L, wfmt ('fp8'|'mxfp4'), shared_bf16, rms_eps.
+    ``prob``: T, H, I, E, k, I_s, L, wfmt ('fp8'|'mxfp4'), shared_bf16, rms_eps,
+    routing ('softmax'|'sigmoid'), act ('swiglu'|'situ').
     ``w``: numpy arrays keyed like the C struct (bf16 as uint16, fp8/fp4 as uint8).
     Returns (out_f64 [n, H], out_bf16_u16 [n, H], idx [n, k], weights [n, k]).
     """
@@ -238,7 +270,9 @@ def moe_forward(prob: dict, w: dict, tokens=None, nthreads: int = 0):
                 I_s=prob.get("I_s", 0), L=prob.get("L", 0),
                 wfmt=MXFP4 if prob.get("wfmt", "fp8") == "mxfp4" else FP8,
                 shared_bf16=int(bool(prob.get("shared_bf16", False))),
-                rms_eps=float(prob.get("rms_eps", 1e-6)))
+                rms_eps=float(prob.get("rms_eps", 1e-6)),
+                routing=1 if prob.get("routing", "softmax") == "sigmoid" else 0,
+                act=SITU if prob.get("act", "swiglu") == "situ" else SWIGLU)
     keep = {}
 
     def ptr(name, dtype=None):

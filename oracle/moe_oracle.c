@@ -35,7 +35,12 @@
  *     k chosen logits (== softmax over all E, top-k, renormalise);
  *   - per-token scale s = amax/448 in fp32 (s = 1 when amax == 0); codes are
  *     e4m3(RNE, saturating) of the fp32 quotient x/s;
- *   - activation is SwiGLU, h = bf16(silu(g) * u);
+ *   - activation is SwiGLU, h = bf16(silu(g) * u); with act = SiTU it is
+ *     h = bf16(beta * tanh(g / beta) * sigmoid(g) * u), beta = 4 [K3 s.2.6];
+ *   - sigmoid routing (K3's noaux_tc, s.2.4, ungrouped, scaling factor 1):
+ *     score s_e = sigmoid(logit_e), experts chosen by s_e + bias_e (the bias
+ *     steers selection only), weights s_j / sum_j' s_j'.  The selection takes
+ *     sigmoid in one canonical fp32 sequence (below) so that it is exact;
  *   - h is requantised per routed row to fp8 the same way as x;
  *   - the shared expert has no gate (weight 1);
  *   - LatentMoE: router on the hidden x, z = bf16(x Wd^T) quantised per token,
@@ -267,6 +272,74 @@ void orc_topk(int64_t T, int64_t E, int k, const float* logits, int32_t* idx, do
   for (int64_t t = 0; t < T; t++) topk_row(E, k, logits + t * E, idx + t * k, w + t * k);
 }
 
+/* Canonical fp32 exp(a) for a <= 0, written from the mathematics so that two
+ * implementations following it agree bit for bit: Cody-Waite range reduction
+ * a = n ln2 + r (n = rint(a log2 e), ln2 split into a 24-bit-exact head and a
+ * tail, both products through fmaf), e^r by its Taylor series to r^7/7!
+ * (Horner, fmaf; |r| <= 0.35 so the truncation is below 2^-26), then an exact
+ * scaling by 2^n (n >= -125, so the result stays a normal number).  Inputs
+ * at or below -86 (results below ~4.5e-38) give 0. */
+float orc_exp_canon(float a) {
+  if (!(a > -86.0f)) return 0.0f;
+  if (a > 0.0f) a = 0.0f;
+  const float log2e = 1.44269504f, ln2_hi = 0.693145751953125f, ln2_lo = 1.42860677e-6f;
+  float n = rintf(a * log2e);
+  float r = fmaf(-n, ln2_hi, a);
+  r = fmaf(-n, ln2_lo, r);
+  float q = 1.0f / 5040.0f;
+  q = fmaf(q, r, 1.0f / 720.0f);
+  q = fmaf(q, r, 1.0f / 120.0f);
+  q = fmaf(q, r, 1.0f / 24.0f);
+  q = fmaf(q, r, 1.0f / 6.0f);
+  q = fmaf(q, r, 0.5f);
+  q = fmaf(q, r, 1.0f);
+  q = fmaf(q, r, 1.0f);
+  union { uint32_t u; float f; } two = {(uint32_t)((int)n + 127) << 23};
+  return q * two.f;
+}
+
+/* sigmoid(l) = 1 / (1 + e^-l) for l >= 0, e^l / (1 + e^l) for l < 0, with
+ * u = orc_exp_canon(-|l|) and IEEE fp32 add and divide. */
+float orc_sigmoid_canon(float l) {
+  float u = orc_exp_canon(l >= 0.0f ? -l : l);
+  return l >= 0.0f ? 1.0f / (1.0f + u) : u / (1.0f + u);
+}
+
+/* noaux_tc top-k: keys s_e + bias_e (fp32), k largest in descending order, ties
+ * to the lower index; weights are the chosen (unbiased) scores renormalised.
+ * [K3 s.2.4: noaux_tc + sigmoid, moe_renormalize, routed_scaling_factor 1] */
+static void topk_sigmoid_row(int64_t E, int k, const float* l, const float* bias, int32_t* idx,
+                             double* w) {
+  float* key = (float*)malloc(sizeof(float) * (size_t)E);
+  float* sc = (float*)malloc(sizeof(float) * (size_t)E);
+  for (int64_t e = 0; e < E; e++) {
+    sc[e] = orc_sigmoid_canon(l[e]);
+    key[e] = bias ? sc[e] + bias[e] : sc[e];
+  }
+  for (int j = 0; j < k; j++) {
+    int64_t best = -1;
+    for (int64_t e = 0; e < E; e++) {
+      int taken = 0;
+      for (int jj = 0; jj < j; jj++)
+        if (idx[jj] == e) taken = 1;
+      if (taken) continue;
+      if (best < 0 || key[e] > key[best]) best = e;
+    }
+    idx[j] = (int32_t)best;
+  }
+  double z = 0.0;
+  for (int j = 0; j < k; j++) z += (double)sc[idx[j]];
+  for (int j = 0; j < k; j++) w[j] = (double)sc[idx[j]] / z;
+  free(key);
+  free(sc);
+}
+
+void orc_topk_sigmoid(int64_t T, int64_t E, int k, const float* logits, const float* bias,
+                      int32_t* idx, double* w) {
+  for (int64_t t = 0; t < T; t++)
+    topk_sigmoid_row(E, k, logits + t * E, bias, idx + t * k, w + t * k);
+}
+
 /* ------------------------------------------------------------------------- */
 /* S3/S4: stable counting sort of (token, slot) pairs by expert                */
 /* ------------------------------------------------------------------------- */
@@ -347,10 +420,19 @@ static double weight_at(int fmt, const uint8_t* wrow, const void* srow, int64_t 
   return tab_e2m1[nib] * tab_e8m0[((const uint8_t*)srow)[k / 32]];
 }
 
+enum { ORC_SWIGLU = 0, ORC_SITU = 1 };
+
+/* Gated activation times the up projection: SwiGLU silu(g) * u, or SiTU
+ * beta * tanh(g / beta) * sigmoid(g) * u with beta = 4 [K3 s.2.6]. */
+static double gated(int act, double g, double u) {
+  if (act == ORC_SITU) return 4.0 * tanh(g / 4.0) / (1.0 + exp(-g)) * u;
+  return g / (1.0 + exp(-g)) * u;
+}
+
 /* y[n] = (sum_i hq_i W2[n,i]) * s_h * s2[n] (fp8 also applies the per-channel
- * scale after the full-K sum, [LING s.5 direct_scaled_dot]); h = bf16(silu(g)*u)
+ * scale after the full-K sum, [LING s.5 direct_scaled_dot]); h = bf16(act(g, u))
  * with g = (sum_k xq_k W1[n,k]) * s_x * s1[n], u likewise with W3. */
-static void expert_ffn(int fmt, int64_t K, int64_t I, const uint8_t* xq, float sx,
+static void expert_ffn(int fmt, int act, int64_t K, int64_t I, const uint8_t* xq, float sx,
                        const uint8_t* w13, const void* s13, const uint8_t* w2, const void* s2,
                        double* y, uint16_t* h_out, float* sh_out, uint8_t* hq_out) {
   int64_t rowb13 = (fmt == ORC_FP8) ? K : K / 2, rows13 = (fmt == ORC_FP8) ? 1 : K / 32;
@@ -381,8 +463,7 @@ static void expert_ffn(int fmt, int64_t K, int64_t I, const uint8_t* xq, float s
       g *= (double)((const float*)s13)[n];
       u *= (double)((const float*)s13)[I + n];
     }
-    double hv = g / (1.0 + exp(-g)) * u;
-    hb[n] = orc_bf16_from_double(hv);
+    hb[n] = orc_bf16_from_double(gated(act, g, u));
     hf[n] = bf16_to_float(hb[n]);
   }
   float s_h = quant_row(I, hf, hq);
@@ -407,8 +488,8 @@ static void expert_ffn(int fmt, int64_t K, int64_t I, const uint8_t* xq, float s
 }
 
 /* Shared expert with bf16 weights and bf16 activations (LatentMoE: shared
- * experts stay BF16 [K3 s.2.5]): sh = W2s * bf16(silu(W1s x) * (W3s x)). */
-static void shared_ffn_bf16(int64_t H, int64_t Is, const uint16_t* xrow, const uint16_t* w13,
+ * experts stay BF16 [K3 s.2.5]): sh = W2s * bf16(act(W1s x, W3s x)). */
+static void shared_ffn_bf16(int act, int64_t H, int64_t Is, const uint16_t* xrow, const uint16_t* w13,
                             const uint16_t* w2, double* y) {
   double* xd = (double*)malloc(sizeof(double) * (size_t)H);
   double* hd = (double*)malloc(sizeof(double) * (size_t)Is);
@@ -419,7 +500,7 @@ static void shared_ffn_bf16(int64_t H, int64_t Is, const uint16_t* xrow, const u
       g += xd[k] * orc_bf16_decode(w13[n * H + k]);
       u += xd[k] * orc_bf16_decode(w13[(Is + n) * H + k]);
     }
-    hd[n] = orc_bf16_decode(orc_bf16_from_double(g / (1.0 + exp(-g)) * u));
+    hd[n] = orc_bf16_decode(orc_bf16_from_double(gated(act, g, u)));
   }
   for (int64_t m = 0; m < H; m++) {
     double acc = 0.0;
@@ -438,6 +519,8 @@ typedef struct {
   int32_t wfmt;                  /* ORC_FP8 or ORC_MXFP4 (routed experts)       */
   int32_t shared_bf16;           /* shared expert weights are bf16 (else fp8)   */
   double rms_eps;
+  int32_t routing;               /* 0 softmax top-k, 1 sigmoid (noaux_tc)        */
+  int32_t act;                   /* ORC_SWIGLU or ORC_SITU                       */
 } orc_problem;
 
 typedef struct {
@@ -483,8 +566,13 @@ static void token_forward(int64_t i, void* c) {
   double* y = (double*)malloc(sizeof(double) * (size_t)(K > H ? K : H));
   double* res = (double*)calloc((size_t)H, sizeof(double));
 
-  router_row(H, E, xrow, w->router_w, w->router_bias, logits);
-  topk_row(E, k, logits, idx, wt);
+  if (p->routing == 1) { /* the bias steers selection only */
+    router_row(H, E, xrow, w->router_w, NULL, logits);
+    topk_sigmoid_row(E, k, logits, w->router_bias, idx, wt);
+  } else {
+    router_row(H, E, xrow, w->router_w, w->router_bias, logits);
+    topk_row(E, k, logits, idx, wt);
+  }
 
   float sx;
   if (p->L > 0) {
@@ -515,7 +603,7 @@ static void token_forward(int64_t i, void* c) {
       s13 = (const uint8_t*)w->w13_scale + e * 2 * I * rows13;
       s2 = (const uint8_t*)w->w2_scale + e * K * rows2;
     }
-    expert_ffn(p->wfmt, K, I, xq, sx, w13, s13, w2, s2, y, NULL, NULL, NULL);
+    expert_ffn(p->wfmt, p->act, K, I, xq, sx, w13, s13, w2, s2, y, NULL, NULL, NULL);
     for (int64_t n = 0; n < K; n++) acc[n] += wt[j] * y[n]; /* j ascending */
   }
 
@@ -540,7 +628,8 @@ static void token_forward(int64_t i, void* c) {
   if (p->I_s > 0) {
     /* shared expert, weight 1 [LING s.5 in-kernel shared expert] */
     if (p->shared_bf16) {
-      shared_ffn_bf16(H, p->I_s, xrow, (const uint16_t*)w->sw13, (const uint16_t*)w->sw2, y);
+      shared_ffn_bf16(p->act, H, p->I_s, xrow, (const uint16_t*)w->sw13, (const uint16_t*)w->sw2,
+                      y);
     } else {
       uint8_t* xqh = xq;
       float sxh = sx;
@@ -550,7 +639,7 @@ static void token_forward(int64_t i, void* c) {
         sxh = quant_row_bf16(H, xrow, tmp);
         xqh = tmp;
       }
-      expert_ffn(ORC_FP8, H, p->I_s, xqh, sxh, (const uint8_t*)w->sw13, w->sw13_scale,
+      expert_ffn(ORC_FP8, p->act, H, p->I_s, xqh, sxh, (const uint8_t*)w->sw13, w->sw13_scale,
                  (const uint8_t*)w->sw2, w->sw2_scale, y, NULL, NULL, NULL);
       free(tmp);
     }
@@ -586,7 +675,7 @@ void orc_moe_forward(const orc_problem* p, const orc_weights* w, const int32_t* 
 /* rows (counts per expert), y[r] = row_w[r] * FFN_{e(r)}(xq[r]).               */
 /* ------------------------------------------------------------------------- */
 typedef struct {
-  int32_t wfmt;
+  int32_t wfmt, act;
   int64_t K, I, E;
   const int32_t* off;    /* [E+1] */
   const uint8_t* xq;     /* [R, K] */
@@ -618,18 +707,18 @@ static void rows_body(int64_t r, void* c) {
     s2 = (const uint8_t*)q->w2_scale + e * K * rows2;
   }
   double* y = q->y + r * K;
-  expert_ffn(q->wfmt, K, I, q->xq + r * K, q->xs[r], q->w13 + e * 2 * I * rowb13, s13,
+  expert_ffn(q->wfmt, q->act, K, I, q->xq + r * K, q->xs[r], q->w13 + e * 2 * I * rowb13, s13,
              q->w2 + e * K * rowb2, s2, y, q->h ? q->h + r * I : NULL, q->hs ? q->hs + r : NULL,
              q->hq ? q->hq + r * I : NULL);
   for (int64_t n = 0; n < K; n++) y[n] *= (double)q->row_w[r];
 }
 
-void orc_expert_rows(int32_t wfmt, int64_t K, int64_t I, int64_t E, const int32_t* off,
+void orc_expert_rows(int32_t wfmt, int32_t act, int64_t K, int64_t I, int64_t E, const int32_t* off,
                      const uint8_t* xq, const float* xs, const float* row_w, const uint8_t* w13,
                      const void* w13_scale, const uint8_t* w2, const void* w2_scale, double* y,
                      uint16_t* h, uint8_t* hq, float* hs, int nthreads) {
   pthread_once(&tab_once, fill_tables);
-  rows_ctx c = {wfmt, K, I, E, off, xq, xs, row_w, w13, w13_scale, w2, w2_scale, y, h, hq, hs};
+  rows_ctx c = {wfmt, act, K, I, E, off, xq, xs, row_w, w13, w13_scale, w2, w2_scale, y, h, hq, hs};
   orc_parallel_for(off[E], nthreads, rows_body, &c);
 }
 

@@ -74,12 +74,24 @@ def mxfp4_weight(packed, scales):
     return vals * np.repeat(sc, 32, axis=-1)
 
 
-def swiglu_rows(xq, sx, W13, W2, I):
+def sigm(v):
+    return 1.0 / (1.0 + np.exp(-v))
+
+
+def gated(g, u, act="swiglu"):
+    """silu(g) u, or SiTU 4 tanh(g/4) sigmoid(g) u written through the identity
+    tanh(v) = 2 sigmoid(2v) - 1 (a different route to the same value)."""
+    if act == "situ":
+        return 4.0 * (2.0 * sigm(g / 2.0) - 1.0) * sigm(g) * u
+    return g / (1.0 + np.exp(-g)) * u
+
+
+def swiglu_rows(xq, sx, W13, W2, I, act="swiglu"):
     """Rows xq [n, K] (decoded, fp64), sx [n]; W13 [2I, K] and W2 [K, I] fp64."""
     acc = xq @ W13.T
     g = acc[:, :I] * sx[:, None]
     u = acc[:, I:] * sx[:, None]
-    h = bf16_round(g / (1.0 + np.exp(-g)) * u)
+    h = bf16_round(gated(g, u, act))
     s_h, hq = quant_fp8(h.astype(np.float32))
     return (hq @ W2.T) * s_h[:, None].astype(np.float64)
 
@@ -101,7 +113,7 @@ def numpy_layer(cfg, w, idx, wt):
         else:
             W13 = mxfp4_weight(w["w13"][e], w["w13_scale"][e])
             W2 = mxfp4_weight(w["w2"][e], w["w2_scale"][e])
-        y = swiglu_rows(xq, sx.astype(np.float64), W13, W2, I)
+        y = swiglu_rows(xq, sx.astype(np.float64), W13, W2, I, cfg.act)
         coef = np.where(idx == e, wt, 0.0).sum(1)
         acc += coef[:, None] * y
     if cfg.L:
@@ -115,12 +127,12 @@ def numpy_layer(cfg, w, idx, wt):
             W13s = bf16_vals(w["sw13"])
             g = x @ W13s[: cfg.I_s].T
             u = x @ W13s[cfg.I_s:].T
-            hs = bf16_round(g / (1 + np.exp(-g)) * u)
+            hs = bf16_round(gated(g, u, cfg.act))
             res = res + hs @ bf16_vals(w["sw2"]).T
         else:
             sxs, xqs = quant_fp8(x.astype(np.float32))
             res = res + swiglu_rows(xqs, sxs.astype(np.float64), fp8_weight(w["sw13"], w["sw13_scale"]),
-                                    fp8_weight(w["sw2"], w["sw2_scale"]), cfg.I_s)
+                                    fp8_weight(w["sw2"], w["sw2_scale"]), cfg.I_s, cfg.act)
     return res
 
 
@@ -134,6 +146,10 @@ SMALL = [
     mi.CONFIGS["toy"],
     mi.MoEConfig("small_shared", T=24, H=256, I=128, E=6, k=3, I_s=128),
     mi.MoEConfig("small_bias", T=16, H=128, I=256, E=5, k=2, I_s=128, zipf_bias=True),
+    # Kimi K3 routing and activation: noaux_tc sigmoid routing with a selection
+    # bias, SiTU experts (fp8 shared expert here, bf16 in the latent case below)
+    mi.MoEConfig("small_k3", T=20, H=256, I=128, E=8, k=3, I_s=128, routing="sigmoid",
+                 act="situ", sel_bias=True),
 ]
 
 
@@ -146,8 +162,12 @@ def test_forward_matches_numpy_formulation(orc, cfg):
     mism = np.mean(ob != bf16_bits(ref))
     assert mism <= 1e-3
     # routing agrees with the separately pinned stages
-    lg = orc.router_logits(w["x"], w["router_w"], w["router_bias"])
-    idx2, wt2 = orc.topk(lg, cfg.k)
+    if cfg.routing == "sigmoid":  # the bias steers selection only
+        lg = orc.router_logits(w["x"], w["router_w"])
+        idx2, wt2 = orc.topk(lg, cfg.k, "sigmoid", w["router_bias"])
+    else:
+        lg = orc.router_logits(w["x"], w["router_w"], w["router_bias"])
+        idx2, wt2 = orc.topk(lg, cfg.k)
     assert np.array_equal(idx, idx2) and np.allclose(wt, wt2, rtol=0, atol=0)
 
 
@@ -198,9 +218,12 @@ def test_single_expert_one_hot_closed_form(orc):
     assert np.abs(of[0]).max() > 0.1
 
 
-def test_latent_mxfp4_matches_numpy(orc):
+@pytest.mark.parametrize("k3", [False, True], ids=["softmax-swiglu", "sigmoid-situ"])
+def test_latent_mxfp4_matches_numpy(orc, k3):
     cfg = mi.MoEConfig("latent_small", T=6, H=256, I=128, E=4, k=2, I_s=128, L=128,
                        wfmt="mxfp4", shared_bf16=True)
+    if k3:
+        cfg = cfg.with_(routing="sigmoid", act="situ", sel_bias=True)
     w = mi.to_numpy(mi.make_inputs(cfg, seed=3))
     of, ob, idx, wt = orc.moe_forward(cfg.oracle_problem(), w)
     ref = numpy_layer(cfg, w, idx, wt)
@@ -241,3 +264,39 @@ def test_expert_rows_matches_forward_pieces(orc):
     of, _, _, _ = orc.moe_forward(cfg.oracle_problem(), w)
     comb = (y[perm] * wt[:, :, None]).sum(1)
     assert _close(comb, of)
+
+
+def test_situ_one_hot_closed_form(orc):
+    # E = 1, k = 1, x = e_i: g = 448 s_x W1[:, i], u likewise; SiTU's h =
+    # bf16(4 tanh(g/4) sigmoid(g) u) checked value by value with math.tanh, and
+    # its two limits: h -> 4u for large g (tanh, sigmoid -> 1) and h -> g u / 2
+    # for small g (4 tanh(g/4) -> g, sigmoid -> 1/2).
+    H, I, i = 64, 128, 7
+    rng = np.random.default_rng(1)
+    vals = np.array([0.03125, 0.0625, 0.5, 1.0, 8.0, 16.0, -0.0625, -8.0])
+    W1 = np.zeros((I, H)); W3 = np.zeros((I, H)); W2 = np.eye(H, I)
+    W1[:, i] = rng.choice(vals, I)
+    W3[:, i] = rng.choice(vals, I)
+    enc = lambda M: torch.from_numpy(M.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    x = np.zeros((1, H), np.float32); x[0, i] = 1.0
+    w = dict(x=bf16_bits(x), router_w=np.ones((1, H), np.float32), router_bias=None,
+             w13=enc(np.concatenate([W1, W3]))[None], w13_scale=np.ones((1, 2 * I), np.float32),
+             w2=enc(W2)[None], w2_scale=np.ones((1, H), np.float32),
+             sw13=None, sw13_scale=None, sw2=None, sw2_scale=None, wd=None, wu=None, gamma=None)
+    prob = dict(T=1, H=H, I=I, E=1, k=1, I_s=0, L=0, wfmt="fp8", routing="sigmoid", act="situ")
+    cnt, off, perm, src = orc.permute(np.zeros((1, 1), np.int32), 1)
+    s, q = orc.quant_rows(w["x"])
+    y, h, hq, hs = orc.expert_rows(orc.FP8, off, q, s, np.ones(1, np.float32), w["w13"],
+                                   w["w13_scale"], w["w2"], w["w2_scale"], want_h=True,
+                                   act=orc.SITU)
+    g = 448.0 * W1[:, i] * float(np.float32(1.0) / np.float32(448.0))
+    u = 448.0 * W3[:, i] * float(np.float32(1.0) / np.float32(448.0))
+    expect = [4.0 * math.tanh(gg / 4.0) / (1.0 + math.exp(-gg)) * uu for gg, uu in zip(g, u)]
+    assert np.array_equal(h[0], bf16_bits(np.array(expect)))
+    big = np.abs(g) >= 16
+    assert np.allclose(bf16_vals(h[0])[big & (g > 0)], 4.0 * u[big & (g > 0)], rtol=2e-2)
+    small = np.abs(g) <= 0.0625
+    assert np.allclose(bf16_vals(h[0])[small], g[small] * u[small] / 2.0, rtol=5e-2)
+    # the layer uses the same activation
+    of, _, _, _ = orc.moe_forward(prob, w)
+    assert np.allclose(of[0], y[0], rtol=0, atol=0)

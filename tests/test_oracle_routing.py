@@ -196,3 +196,72 @@ def test_combine_one_hot_rows(orc):
     assert np.array_equal(_bf16_val(out), expect)
     out2 = orc.combine(_bf16_bits(y), perm)
     assert np.array_equal(_bf16_val(out2), expect - 0.5)
+
+
+# ----------------------------------------------------------------------------- sigmoid (noaux_tc)
+def _ulps(a, ref):
+    a = np.asarray(a, np.float64)
+    spacing = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    return np.abs(a - ref) / spacing
+
+
+def test_exp_canon_accuracy(orc):
+    # the canonical fp32 exp against the mathematics (fp64 exp) on (-86, 0]
+    a = np.concatenate([np.linspace(-85.99, 0.0, 40001), -np.logspace(-8, 1.9, 2001),
+                        [0.0, -1e-30, -0.5, -1.0, -np.log(2.0)]]).astype(np.float32)
+    got = orc.exp_canon(a)
+    ref = np.exp(a.astype(np.float64))
+    assert _ulps(got, ref).max() <= 2.0
+    assert orc.exp_canon(np.float32(0.0)) == 1.0
+    assert np.all(np.diff(got[:40001]) >= 0)  # monotone on the increasing grid
+    assert orc.exp_canon(np.float32(-86.0)) == 0.0 and orc.exp_canon(np.float32(-200.0)) == 0.0
+
+
+def test_sigmoid_canon_accuracy_and_symmetry(orc):
+    l = np.concatenate([np.linspace(-30, 30, 20001), [0.0, 1e-6, -1e-6, 85.0, -85.0]]).astype(np.float32)
+    got = orc.sigmoid_canon(l).astype(np.float64)
+    ref = 1.0 / (1.0 + np.exp(-l.astype(np.float64)))
+    assert _ulps(got, ref).max() <= 3.0
+    assert orc.sigmoid_canon(np.float32(0.0)) == 0.5
+    pair = orc.sigmoid_canon(l).astype(np.float64) + orc.sigmoid_canon(-l).astype(np.float64)
+    assert np.abs(pair - 1.0).max() <= 2 ** -22
+
+
+def test_topk_sigmoid_without_bias_follows_the_logits(orc):
+    # sigmoid is increasing, so with no bias the selection is the softmax one
+    # (the pinned routine above), away from fp32 saturation of the sigmoid
+    rng = np.random.default_rng(3)
+    lg = rng.uniform(-2, 2, (300, 48)).astype(np.float32)
+    i1, w1 = orc.topk(lg, 6, "sigmoid")
+    i2, _ = orc.topk(lg, 6)
+    assert np.array_equal(i1, i2)
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(lg, i1, 1).astype(np.float64)))
+    assert np.allclose(w1, s / s.sum(1, keepdims=True), rtol=1e-6)
+
+
+def test_topk_sigmoid_with_bias_brute_force(orc):
+    # keys = score + bias in fp32; selection by a library sort (descending key,
+    # then ascending index); weights are the unbiased scores renormalised
+    rng = np.random.default_rng(4)
+    T, E, k = 200, 40, 5
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    b = (0.05 * rng.standard_normal(E)).astype(np.float32)
+    idx, w = orc.topk(lg, k, "sigmoid", b)
+    sc = orc.sigmoid_canon(lg)
+    key = (sc + b[None, :]).astype(np.float32)
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -key[t].astype(np.float64)))
+        assert list(idx[t]) == list(order[:k])
+        chosen = sc[t, idx[t]].astype(np.float64)
+        assert np.allclose(w[t], chosen / chosen.sum(), rtol=0, atol=1e-15)
+    # the bias changes some selections (it is not ignored)
+    i0, _ = orc.topk(lg, k, "sigmoid")
+    assert not np.array_equal(i0, idx)
+
+
+def test_topk_sigmoid_ties_pick_lower_index(orc):
+    lg = np.zeros((1, 6), np.float32)
+    b = np.array([0.0, 0.1, 0.0, 0.1, 0.0, 0.0], np.float32)
+    idx, w = orc.topk(lg, 4, "sigmoid", b)
+    assert list(idx[0]) == [1, 3, 0, 2]
+    assert np.allclose(w[0], 0.25)
