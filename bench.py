@@ -63,13 +63,16 @@ def workload_name(cfg):
             "prefill_e32": "Ling-style prefill, 32 experts (profiling case)",
             "latent": "Kimi-K3-style LatentMoE",
             "latent_e64": "Kimi-K3-style LatentMoE, 64 experts (profiling case)",
+            "latent_k3": "Kimi-K3-style LatentMoE with K3 routing and activation",
             "skewed": "skewed-routing stress (Zipf 1.2 router bias)", "toy": "toy"}.get(cfg.name, cfg.name)
     s = (f"{kind}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}"
          + (f" + shared expert I_s={cfg.I_s}" if cfg.I_s else "")
          + (f", latent L={cfg.L} (bf16 down/up, RMSNorm)" if cfg.L else "")
          + (", MXFP4 e2m1 + e8m0/32 expert weights" if cfg.wfmt == "mxfp4"
             else ", fp8 e4m3 per-output-channel weights")
-         + ", per-token fp8 activations")
+         + ", per-token fp8 activations"
+         + (", noaux_tc sigmoid routing with selection bias" if cfg.routing == "sigmoid" else "")
+         + (", SiTU experts" if cfg.act == "situ" else ""))
     return s
 
 
@@ -252,7 +255,10 @@ def run_ours(args, cfg):
     m.load_library()
     dev = torch.device("cuda", local)
     inp = mi.make_inputs(cfg, device=dev, seed=0)
-    flags = (m.F_ROUTER_BIAS if cfg.zipf_bias else 0) | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
+    flags = ((m.F_ROUTER_BIAS if (cfg.zipf_bias or cfg.sel_bias) else 0)
+             | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
+             | (m.F_SIGMOID_ROUTING if cfg.routing == "sigmoid" else 0)
+             | (m.F_SITU if cfg.act == "situ" else 0))
     wfmt = m.W_MXFP4 if cfg.wfmt == "mxfp4" else m.W_FP8
     pack = not args.no_pack
     if pack:
@@ -295,7 +301,7 @@ def run_ours(args, cfg):
     tidx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
     tw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
     m.moe_router_logits(p, inp["x"], inp["router_w"], inp["router_bias"], logits)
-    m.moe_route(p, logits, tidx, tw)
+    m.moe_route(p, logits, inp["router_bias"], tidx, tw)
     touched = int(torch.unique(tidx).numel())
     work = acc.layer_work(cfg, touched)
 

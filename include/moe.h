@@ -69,6 +69,11 @@ typedef enum {
 #define MOE_F_SHARED_BF16 0x2u /* shared expert weights are bf16 (no quantisation)   */
 #define MOE_F_PACKED_WEIGHTS 0x4u /* routed (and fp8 shared) expert weights are in
                                      moe_pack_weights' tile order                  */
+#define MOE_F_SIGMOID_ROUTING 0x8u /* noaux_tc routing: scores sigmoid(logit), the
+                                      router bias steers selection only, weights =
+                                      chosen scores renormalised (K3 report s.2.4) */
+#define MOE_F_SITU 0x10u /* SiTU experts: h = 4 tanh(g/4) sigmoid(g) u instead of
+                            SwiGLU's silu(g) u (K3 report s.2.6)                 */
 
 typedef struct {
   int32_t T;        /* tokens                                                      */
@@ -114,7 +119,8 @@ int moe_describe(const moe_problem* p, char* buf, size_t len);
 size_t moe_workspace_bytes(const moe_problem* p);
 
 /* S1 -- router logits.  logits[t,e] = sum_h float(x[t,h]) * router_w[e,h]
- * (+ bias[e] when MOE_F_ROUTER_BIAS), fp32, summed in one fixed order: 32
+ * (+ bias[e] when MOE_F_ROUTER_BIAS without MOE_F_SIGMOID_ROUTING; with sigmoid
+ * routing the bias belongs to moe_route), fp32, summed in one fixed order: 32
  * partial sums (partial l takes h = l, l+32, ... ascending, fused multiply-add
  * from +0), then p_l += p_{l+o} for o = 16, 8, 4, 2, 1, bias added last.  The
  * order is fixed so that routing is reproducible bit for bit.
@@ -129,9 +135,16 @@ int moe_router_logits(const moe_problem* p, const void* x, const float* router_w
  * equal logits ordered by lower expert index; weights are the softmax over the
  * chosen logits, w_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0), fp32.
  * (Ling write-up, s.1 top-8 routing; Kimi K3 report, s.2.4 moe_renormalize.)
- *   logits [T, E] fp32 -> topk_idx [T, top_k] int32, topk_w [T, top_k] fp32 */
-int moe_route(const moe_problem* p, const float* logits, int32_t* topk_idx, float* topk_w,
-              void* stream);
+ * With MOE_F_SIGMOID_ROUTING (K3 report s.2.4, noaux_tc + sigmoid, ungrouped,
+ * scaling factor 1): scores s_e = sigmoid(l_e), the top_k largest keys s_e +
+ * bias[e] are chosen (ties to the lower index; bias only with
+ * MOE_F_ROUTER_BIAS), and w_j = s_j / sum_j' s_j'.  For the selection sigmoid
+ * is one fixed fp32 sequence (Cody-Waite reduction, Taylor series to degree 7
+ * through fma, IEEE add and divide) so that it is reproducible bit for bit.
+ *   logits [T, E] fp32; bias [E] fp32 (sigmoid routing with MOE_F_ROUTER_BIAS,
+ *   else ignored) -> topk_idx [T, top_k] int32, topk_w [T, top_k] fp32 */
+int moe_route(const moe_problem* p, const float* logits, const float* bias, int32_t* topk_idx,
+              float* topk_w, void* stream);
 
 /* S3 + S4 -- expert-contiguous permutation and per-token fp8 quantisation.
  * counts[e] = #{(t,j): idx[t,j] = e}; offsets[e] = sum_{e'<e} counts[e'],
@@ -233,7 +246,10 @@ int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
                   const void* shared, void* out, void* stream);
 
 /* The whole layer, S1..S8, queued on `stream` with no host round trip.
- *   x [T, H] bf16; router_w [E, H] fp32; router_bias [E] fp32 (MOE_F_ROUTER_BIAS)
+ *   x [T, H] bf16; router_w [E, H] fp32; router_bias [E] fp32 (MOE_F_ROUTER_BIAS:
+ *   added to the logits, or with MOE_F_SIGMOID_ROUTING to the scores for
+ *   selection only); MOE_F_SITU switches every expert (routed and shared) to
+ *   SiTU
  *   routed experts: see moe_expert_ffn (K = H, or latent for a LatentMoE problem)
  *   shared expert (I_shared > 0): fp8 shared_w13 [2*I_shared, H] e4m3 +
  *     shared_w13_scale [2*I_shared] fp32, shared_w2 [H, I_shared] e4m3 +

@@ -18,7 +18,7 @@ __all__ = [
     "moe_forward", "moe_get_last_error", "moe_launch_count", "moe_profile_enable",
     "moe_profile_read", "moe_pack_weights", "moe_watchdog_selftest", "moe_describe", "STAGES",
     "W_FP8",
-    "W_MXFP4", "F_ROUTER_BIAS", "F_SHARED_BF16", "F_PACKED_WEIGHTS",
+    "W_MXFP4", "F_ROUTER_BIAS", "F_SHARED_BF16", "F_PACKED_WEIGHTS", "F_SIGMOID_ROUTING", "F_SITU",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,6 +29,8 @@ W_MXFP4 = 1
 F_ROUTER_BIAS = 0x1
 F_SHARED_BF16 = 0x2
 F_PACKED_WEIGHTS = 0x4
+F_SIGMOID_ROUTING = 0x8
+F_SITU = 0x10
 STAGES = ("router", "topk", "index", "scatter", "ffn1", "requant", "ffn2", "combine",
           "latent_down", "shared", "latent_up")
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -73,7 +75,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_workspace_bytes.restype = ctypes.c_size_t
     L.moe_workspace_bytes.argtypes = [PP]
     L.moe_router_logits.argtypes = [PP, P, P, P, P, P]
-    L.moe_route.argtypes = [PP, P, P, P, P]
+    L.moe_route.argtypes = [PP, P, P, P, P, P]
     L.moe_permute.argtypes = [PP, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_permute_static.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.moe_pack_weights.argtypes = [PP, P, P, P, P, P, P, P, P, P]
@@ -119,9 +121,9 @@ def moe_router_logits(p, x, router_w, bias, logits, stream=None):
                                             _ptr(logits), _stream(stream)), "moe_router_logits")
 
 
-def moe_route(p, logits, topk_idx, topk_w, stream=None):
-    _check(load_library().moe_route(ctypes.byref(p), _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
-                                    _stream(stream)), "moe_route")
+def moe_route(p, logits, bias, topk_idx, topk_w, stream=None):
+    _check(load_library().moe_route(ctypes.byref(p), _ptr(logits), _ptr(bias), _ptr(topk_idx),
+                                    _ptr(topk_w), _stream(stream)), "moe_route")
 
 
 def moe_permute(p, topk_idx, x, counts, offsets, perm, src_row, xq_perm, xscale_perm, ws,

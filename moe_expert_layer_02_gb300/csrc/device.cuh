@@ -136,6 +136,15 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// ------------------------------------------------------------------ activation
+// Gated activation times the up projection (FFN1 epilogues): act 0 = SwiGLU,
+// silu(g) u; act 1 = SiTU, beta tanh(g / beta) sigmoid(g) u with beta = 4
+// ("Kimi K3 ... feasibility analysis", s.2.6).
+__device__ __forceinline__ float gated_act(int act, float g, float u) {
+  const float d = 1.0f + expf(-g);
+  return act ? (4.0f * tanhf(0.25f * g)) / d * u : g / d * u;
+}
+
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

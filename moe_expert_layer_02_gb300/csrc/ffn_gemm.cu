@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float xs = a.xscale[row];
               const float g = (__uint_as_float(vg[j]) * xs) * sg;
               const float u = (__uint_as_float(vu[j]) * xs) * su;
-              const float hv = g / (1.0f + expf(-g)) * u;
+              const float hv = gated_act(a.act, g, u);
               hout[(size_t)row * a.I + f] = (uint16_t)f32_bits_to_bf16(hv);
             }
           }

@@ -67,6 +67,7 @@ struct PairGemm {
   int kb1, kb2;           // K stages from (x, w) and from (x2, w2)
   int I;                  // SWIGLU: first row of the up-projection block
   int packed;             // first-segment weights in tile-major order (pack.cu)
+  int act;                // SwiGLU epilogue: 0 SwiGLU, 1 SiTU
   int rows_total;         // rows of A (and of the output)
   const float* xscale;    // fp8 SWIGLU: per-row activation scale
   const float* w_scale;   // fp8: per-channel scale of group 0 (stride scale_stride)
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                 gg = (gg * xs) * __ldg(sc + f0 + c + j + u2);
                 uu = (uu * xs) * __ldg(sc + g.I + f0 + c + j + u2);
               }
-              hv[u2] = gg / (1.0f + expf(-gg)) * uu;
+              hv[u2] = gated_act(g.act, gg, uu);
             }
             packed[j / 2] = pack_bf16x2(hv[0], hv[1]);
           }
@@ -443,6 +444,7 @@ cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   g.kb2 = 0;
   g.I = a.I;
   g.packed = a.packed;
+  g.act = a.act;
   g.rows_total = a.rows_total;
   g.xscale = a.xscale;
   g.w_scale = FFN1 ? a.w13_scale : a.w2_scale;
@@ -490,6 +492,7 @@ cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s) {
   g.kb2 = d.K2 / 64;
   g.I = d.N;
   g.rows_total = d.rows;
+  g.act = d.act;
   g.out = d.out;
   g.ldo = d.N;
   g.err = d.err;

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
               const float xs = a.xscale[row];
               const float g = __uint_as_float(vg[j]) * xs;
               const float u = __uint_as_float(vu[j]) * xs;
-              hout[(size_t)row * a.I + f] = (uint16_t)f32_to_bf16_bits(g / (1.0f + expf(-g)) * u);
+              hout[(size_t)row * a.I + f] = (uint16_t)f32_to_bf16_bits(gated_act(a.act, g, u));
             }
           }
         }

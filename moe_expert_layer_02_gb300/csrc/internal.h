@@ -18,8 +18,10 @@ inline int num_chunks(int T) { return (T + kChunk - 1) / kChunk; }
 // ---------------------------------------------------------------- route.cu
 cudaError_t launch_router_logits(const void* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, int* err, cudaStream_t s);
-cudaError_t launch_topk(const float* logits, int32_t* idx, float* w, int T, int E, int k,
-                        cudaStream_t s);
+// sigmoid = 0: softmax over the top-k logits; 1: noaux_tc, keys sigmoid(l) +
+// sel_bias (nullable), weights the chosen sigmoid scores renormalised
+cudaError_t launch_topk(const float* logits, const float* sel_bias, int sigmoid, int32_t* idx,
+                        float* w, int T, int E, int k, cudaStream_t s);
 
 // ---------------------------------------------------------------- permute.cu
 // cc[e * nch + c] = #tokens of chunk c that picked expert e.
@@ -78,6 +80,7 @@ struct GroupedFfnArgs {
   void* y;                // [rows_total, K] bf16
   int BN;                 // token rows per tile (32, 64, 128, 256)
   int packed;             // fp8 weights in tile-major order (pack.cu)
+  int act;                // FFN1 activation: 0 SwiGLU, 1 SiTU (gated_act)
   int* err;
 };
 
@@ -101,6 +104,7 @@ struct DenseGemmArgs {
   int K2;
   int rows, N;
   bool swiglu;
+  int act;                // with swiglu: 0 SwiGLU, 1 SiTU (gated_act)
   void* out;       // [rows, N] bf16
   int* err;
 };

@@ -101,6 +101,7 @@ struct Plan {
   bool shared_bf16; // bf16 shared expert as dense GEMMs (LatentMoE)
   bool mx;          // MXFP4 routed experts
   int packed;       // expert weights in tile-major order (moe_pack_weights)
+  int act;          // FFN1 activation: 0 SwiGLU, 1 SiTU
   size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
       hq, hs, y, z, yn, hsh, total;
 };
@@ -140,6 +141,7 @@ Plan make_plan(const moe_problem* p) {
   q.shared = p->I_shared > 0 && !q.shared_bf16;
   q.mx = p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32;
   q.packed = (p->flags & MOE_F_PACKED_WEIGHTS) ? 1 : 0;
+  q.act = (p->flags & MOE_F_SITU) ? 1 : 0;
   q.RT = q.R + (q.shared ? p->T : 0);
   q.nch = num_chunks(p->T);
   q.BN = choose_bn(p);
@@ -221,6 +223,16 @@ int check_supported(const moe_problem* p) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// The router bias: with softmax routing it is added to the logits; with
+// sigmoid (noaux_tc) routing it is added to the scores for selection only.
+bool sigmoid_routing(const moe_problem* p) { return (p->flags & MOE_F_SIGMOID_ROUTING) != 0; }
+const float* logit_bias(const moe_problem* p, const float* b) {
+  return ((p->flags & MOE_F_ROUTER_BIAS) && !sigmoid_routing(p)) ? b : nullptr;
+}
+const float* selection_bias(const moe_problem* p, const float* b) {
+  return ((p->flags & MOE_F_ROUTER_BIAS) && sigmoid_routing(p)) ? b : nullptr;
+}
+
 #define MOE_TRY(expr)                 \
   do {                                \
     cudaError_t _e = (expr);          \
@@ -257,6 +269,7 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
   a.y = y;
   a.BN = q.BN;
   a.packed = q.packed;
+  a.act = q.act;
   a.err = err;
   return a;
 }
@@ -354,19 +367,21 @@ int moe_router_logits(const moe_problem* p, const void* x, const float* router_w
   if (!di) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StageTimer t(MOE_STAGE_ROUTER, s);
-  return cuda_status(launch_router_logits(x, router_w, (p->flags & MOE_F_ROUTER_BIAS) ? bias : nullptr,
-                                          logits, p->T, p->H, p->E, di->err, s));
+  return cuda_status(launch_router_logits(x, router_w, logit_bias(p, bias), logits, p->T, p->H,
+                                          p->E, di->err, s));
 }
 
-int moe_route(const moe_problem* p, const float* logits, int32_t* topk_idx, float* topk_w,
-              void* stream) {
+int moe_route(const moe_problem* p, const float* logits, const float* bias, int32_t* topk_idx,
+              float* topk_w, void* stream) {
   int st = check_problem(p);
   if (st) return st;
   if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (sigmoid_routing(p) && (p->flags & MOE_F_ROUTER_BIAS) && !bias) return MOE_ERR_INVALID_ARG;
   if (p->T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   StageTimer t(MOE_STAGE_TOPK, s);
-  return cuda_status(launch_topk(logits, topk_idx, topk_w, p->T, p->E, p->top_k, s));
+  return cuda_status(launch_topk(logits, selection_bias(p, bias), sigmoid_routing(p) ? 1 : 0,
+                                 topk_idx, topk_w, p->T, p->E, p->top_k, s));
 }
 
 int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, int32_t* counts,
@@ -487,12 +502,13 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   uint16_t* y = at<uint16_t>(ws, q.y);
   {
     StageTimer t(MOE_STAGE_ROUTER, s);
-    MOE_TRY(launch_router_logits(x, router_w, (p->flags & MOE_F_ROUTER_BIAS) ? router_bias : nullptr,
-                                 logits, q.T, q.H, q.E, di->err, s));
+    MOE_TRY(launch_router_logits(x, router_w, logit_bias(p, router_bias), logits, q.T, q.H, q.E,
+                                 di->err, s));
   }
   {
     StageTimer t(MOE_STAGE_TOPK, s);
-    MOE_TRY(launch_topk(logits, idx, tw, q.T, q.E, q.k, s));
+    MOE_TRY(launch_topk(logits, selection_bias(p, router_bias), sigmoid_routing(p) ? 1 : 0, idx, tw,
+                        q.T, q.E, q.k, s));
   }
   // LatentMoE: the experts run on z = bf16(x Wd^T) ("Kimi K3 ...", s.2.4)
   const void* xin = x;
@@ -549,6 +565,7 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
     d.rows = q.T;
     d.N = q.Is;
     d.swiglu = true;
+    d.act = q.act;
     d.out = at<void>(ws, q.hsh);
     d.err = di->err;
     MOE_TRY(launch_dense_bf16(d, s));

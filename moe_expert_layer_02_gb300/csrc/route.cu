@@ -13,6 +13,9 @@
 // index, so equal logits go to the lower index), then w_j = exp(l_j - l_0) /
 // sum exp(l_j' - l_0): the softmax over the chosen k (Ling write-up, s.1 top-8;
 // "Kimi K3 ... feasibility analysis", s.2.4, moe_renormalize, scaling 1.0).
+// Sigmoid routing (K3 s.2.4, noaux_tc + sigmoid, ungrouped): the keys are
+// s_e + bias_e with s_e = sigmoid(logit_e) in a canonical fp32 sequence, the
+// bias steering selection only; w_j = s_j / sum_j' s_j'.
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
@@ -172,10 +175,41 @@ __global__ void __launch_bounds__(RT_THREADS, (TW * EW <= 64) ? 2 : 1)
   }
 }
 
+// exp(a) for a <= 0 in one fixed fp32 sequence: Cody-Waite reduction a = n ln2
+// + r with n = rint(a log2 e) and ln2 split into a head exact in 15 bits plus a
+// tail, e^r by its Taylor series through r^7/7! in Horner form (|r| <= 0.35,
+// truncation < 2^-26), then an exact multiply by 2^n (n >= -125).  a <= -86
+// gives 0.  Every step is an IEEE-rounded fp32 operation, so the result is the
+// same on any machine that follows the sequence.
+__device__ __forceinline__ float exp_fixed(float a) {
+  if (!(a > -86.0f)) return 0.0f;
+  if (a > 0.0f) a = 0.0f;
+  const float n = rintf(__fmul_rn(a, 1.44269504f));
+  float r = fmaf(-n, 0.693145751953125f, a);
+  r = fmaf(-n, 1.42860677e-6f, r);
+  float q = 1.0f / 5040.0f;
+  q = fmaf(q, r, 1.0f / 720.0f);
+  q = fmaf(q, r, 1.0f / 120.0f);
+  q = fmaf(q, r, 1.0f / 24.0f);
+  q = fmaf(q, r, 1.0f / 6.0f);
+  q = fmaf(q, r, 0.5f);
+  q = fmaf(q, r, 1.0f);
+  q = fmaf(q, r, 1.0f);
+  return __fmul_rn(q, __int_as_float(((int)n + 127) << 23));
+}
+
+// sigmoid(l): 1 / (1 + e^-l) for l >= 0, e^l / (1 + e^l) below, IEEE add/divide.
+__device__ __forceinline__ float sigmoid_fixed(float l) {
+  const float u = exp_fixed(l >= 0.0f ? -l : l);
+  const float d = __fadd_rn(1.0f, u);
+  return l >= 0.0f ? __fdiv_rn(1.0f, d) : __fdiv_rn(u, d);
+}
+
 template <int VPL>
 __global__ void __launch_bounds__(256)
-    topk_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ w,
-                int T, int E, int k) {
+    topk_kernel(const float* __restrict__ logits, const float* __restrict__ sel_bias,
+                int32_t* __restrict__ idx, float* __restrict__ w, int T, int E, int k,
+                int sigmoid) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -184,7 +218,15 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = i * 32 + lane;
-    key[i] = (e < E) ? ((uint64_t)float_order_key(row[e]) << 32) | (uint64_t)(0xFFFFFFFFu - e) : 0;
+    float v = 0.0f;
+    if (e < E) {
+      v = row[e];
+      if (sigmoid) {
+        v = sigmoid_fixed(v);
+        if (sel_bias) v = __fadd_rn(v, sel_bias[e]);
+      }
+    }
+    key[i] = (e < E) ? ((uint64_t)float_order_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - e) : 0;
   }
   float my_logit = 0.0f;  // lane j keeps the j-th chosen logit
   int my_idx = 0;
@@ -209,7 +251,8 @@ __global__ void __launch_bounds__(256)
       my_idx = e;
     }
   }
-  const float ex = lane < k ? expf(my_logit - l0) : 0.0f;
+  const float ex =
+      lane >= k ? 0.0f : sigmoid ? sigmoid_fixed(my_logit) : expf(my_logit - l0);
   float sum = 0.0f;
   for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);  // j ascending
   if (lane < k) {
@@ -278,23 +321,23 @@ cudaError_t launch_router_logits(const void* x, const float* wr, const float* bi
   return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
 }
 
-cudaError_t launch_topk(const float* logits, int32_t* idx, float* w, int T, int E, int k,
-                        cudaStream_t s) {
+cudaError_t launch_topk(const float* logits, const float* sel_bias, int sigmoid, int32_t* idx,
+                        float* w, int T, int E, int k, cudaStream_t s) {
   const int blocks = (T * 32 + 255) / 256;
   count_launch();
   const int vpl = (E + 31) / 32;
   if (vpl <= 1)
-    topk_kernel<1><<<blocks, 256, 0, s>>>(logits, idx, w, T, E, k);
+    topk_kernel<1><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
   else if (vpl <= 2)
-    topk_kernel<2><<<blocks, 256, 0, s>>>(logits, idx, w, T, E, k);
+    topk_kernel<2><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
   else if (vpl <= 4)
-    topk_kernel<4><<<blocks, 256, 0, s>>>(logits, idx, w, T, E, k);
+    topk_kernel<4><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
   else if (vpl <= 8)
-    topk_kernel<8><<<blocks, 256, 0, s>>>(logits, idx, w, T, E, k);
+    topk_kernel<8><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
   else if (vpl <= 16)
-    topk_kernel<16><<<blocks, 256, 0, s>>>(logits, idx, w, T, E, k);
+    topk_kernel<16><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
   else
-    topk_kernel<32><<<blocks, 256, 0, s>>>(logits, idx, w, T, E, k);
+    topk_kernel<32><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
   return cudaGetLastError();
 }
 

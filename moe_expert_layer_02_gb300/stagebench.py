@@ -46,7 +46,7 @@ def main(argv=None):
         idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
         wt = torch.empty(T, k, device="cuda")
         p = make_problem(T, 128, 128, E, k)
-        call = lambda: moe_route(p, logits, idx, wt)  # noqa: E731
+        call = lambda: moe_route(p, logits, None, idx, wt)  # noqa: E731
         work, unit = 4.0 * T * E, "GB/s"
     for _ in range(a.warmup):
         call()

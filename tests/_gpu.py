@@ -90,7 +90,11 @@ def pack(cfg: mi.MoEConfig, inp: dict) -> dict:
 
 def problem(cfg: mi.MoEConfig, packed: bool = False):
     m = lib()
-    flags = m.F_ROUTER_BIAS if cfg.zipf_bias else 0
+    flags = m.F_ROUTER_BIAS if (cfg.zipf_bias or cfg.sel_bias) else 0
+    if cfg.routing == "sigmoid":
+        flags |= m.F_SIGMOID_ROUTING
+    if cfg.act == "situ":
+        flags |= m.F_SITU
     if packed:
         flags |= m.F_PACKED_WEIGHTS
     if cfg.shared_bf16:

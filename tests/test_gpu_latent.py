@@ -36,7 +36,8 @@ def _latent_rows(orc, cfg, seed=9):
 
 
 @pytest.mark.parametrize("bn", [32, 64, 96])
-@pytest.mark.parametrize("cfg", [MX_PLAIN, LAT_SMALL], ids=ids)
+@pytest.mark.parametrize("cfg", [MX_PLAIN, LAT_SMALL, MX_PLAIN.with_(name="mx_situ", act="situ")],
+                         ids=ids)
 def test_mxfp4_expert_ffn(orc, cfg, bn, monkeypatch):
     monkeypatch.setenv("MOE_TILE_N", str(bn))
     m = G.lib()
@@ -49,7 +50,7 @@ def test_mxfp4_expert_ffn(orc, cfg, bn, monkeypatch):
                      inp["w13_scale"], inp["w2"], inp["w2_scale"], y, ws)
     assert m.moe_get_last_error() == 0
     ref = orc.expert_rows(orc.MXFP4, off, xq, xs, row_w, h["w13"], h["w13_scale"], h["w2"],
-                          h["w2_scale"])
+                          h["w2_scale"], act=orc.SITU if cfg.act == "situ" else orc.SWIGLU)
     G.assert_close(G.bf16_values(G.bf16_bits(y)), ref, f"mxfp4 expert_ffn {cfg.name}")
 
 

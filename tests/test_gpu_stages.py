@@ -53,7 +53,7 @@ def test_topk_bit_exact(orc, cfg):
     p = G.problem(cfg)
     gi = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device="cuda")
     gw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device="cuda")
-    m.moe_route(p, torch.from_numpy(lg).cuda(), gi, gw)
+    m.moe_route(p, torch.from_numpy(lg).cuda(), None, gi, gw)
     assert np.array_equal(gi.cpu().numpy(), idx)
     assert np.allclose(gw.cpu().numpy(), w, rtol=1e-6, atol=1e-7)
 
@@ -70,7 +70,7 @@ def test_topk_ties_lower_index(orc):
     p = m.make_problem(T, 128, 128, E, k)
     gi = torch.empty(T, k, dtype=torch.int32, device="cuda")
     gw = torch.empty(T, k, dtype=torch.float32, device="cuda")
-    m.moe_route(p, torch.from_numpy(lg).cuda(), gi, gw)
+    m.moe_route(p, torch.from_numpy(lg).cuda(), None, gi, gw)
     assert np.array_equal(gi.cpu().numpy(), idx)
     assert list(idx[0]) == [0, 1, 2, 3, 4]
     assert np.allclose(gw.cpu().numpy(), w, rtol=1e-6, atol=1e-7)
@@ -149,7 +149,7 @@ def test_expert_ffn_full_size(orc, cfg):
     _check_expert_ffn(orc, cfg, rows_sample=48)
 
 
-def _check_expert_ffn(orc, cfg, rows_sample):
+def _check_expert_ffn(orc, cfg, rows_sample, act=0):
     m = G.lib()
     inp = G.gpu_inputs(cfg)
     h = G.host(inp)
@@ -169,7 +169,7 @@ def _check_expert_ffn(orc, cfg, rows_sample):
     e_of = np.searchsorted(off, rows, side="right") - 1
     off_sub = np.concatenate([[0], np.cumsum(np.bincount(e_of, minlength=cfg.E))]).astype(np.int32)
     ref = orc.expert_rows(orc.FP8, off_sub, xq[rows], xs[rows], row_w[rows], h["w13"],
-                          h["w13_scale"], h["w2"], h["w2_scale"])
+                          h["w13_scale"], h["w2"], h["w2_scale"], act=act)
     G.assert_close(got[rows], ref, f"expert_ffn {cfg.name}")
 
 
