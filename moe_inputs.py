@@ -49,7 +49,7 @@ class MoEConfig:
     k: int
     I_s: int = 0          # shared-expert intermediate width; 0 = none
     L: int = 0            # latent width; 0 = no latent projection
-    wfmt: str = "fp8"     # routed expert weights: "fp8" | "mxfp4"
+    wfmt: str = "fp8"     # routed expert weights: "fp8" | "mxfp4" | "fp8_block" (128 x 128)
     shared_bf16: bool = False
     zipf_bias: bool = False
     rms_eps: float = 1e-6
@@ -105,6 +105,25 @@ def quantize_fp8_rows(w: torch.Tensor):
     scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
     q = (w / scale[:, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
     return q.view(torch.uint8), scale.float()
+
+
+def quantize_fp8_blocks(w: torch.Tensor):
+    """Block-wise fp8 e4m3 over 128 x 128 blocks: scale [R/128, C/128] = amax/448
+    of the block (1 if zero), bytes via torch's cast of w / scale."""
+    w = w.float()
+    R, C = w.shape
+    b = w.view(R // 128, 128, C // 128, 128)
+    amax = b.abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (b / scale[:, None, :, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(R, C)
+    return q.view(torch.uint8), scale.float()
+
+
+def _block_gain(R: int, C: int, gen, device):
+    """A seeded gain 2^u, u ~ U(-2, 2), per 128 x 128 block, so that block scales
+    differ (up to 16x) as they do in trained weights."""
+    u = torch.rand(R // 128, C // 128, generator=gen, device=device) * 4.0 - 2.0
+    return torch.pow(2.0, u).repeat_interleave(128, 0).repeat_interleave(128, 1)
 
 
 _E2M1_MIDS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
@@ -174,17 +193,27 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, expert_weights: dic
         w13s = torch.empty(E, 2 * I, dtype=torch.float32, device=device)
         w2 = torch.empty(E, K, I, dtype=torch.uint8, device=device)
         w2s = torch.empty(E, K, dtype=torch.float32, device=device)
+    elif cfg.wfmt == "fp8_block":
+        w13 = torch.empty(E, 2 * I, K, dtype=torch.uint8, device=device)
+        w13s = torch.empty(E, 2 * I // 128, K // 128, dtype=torch.float32, device=device)
+        w2 = torch.empty(E, K, I, dtype=torch.uint8, device=device)
+        w2s = torch.empty(E, K // 128, I // 128, dtype=torch.float32, device=device)
     else:
         w13 = torch.empty(E, 2 * I, K // 2, dtype=torch.uint8, device=device)
         w13s = torch.empty(E, 2 * I, K // 32, dtype=torch.uint8, device=device)
         w2 = torch.empty(E, K, I // 2, dtype=torch.uint8, device=device)
         w2s = torch.empty(E, K, I // 32, dtype=torch.uint8, device=device)
-    quant = quantize_fp8_rows if cfg.wfmt == "fp8" else quantize_mxfp4_rows
+    quant = {"fp8": quantize_fp8_rows, "mxfp4": quantize_mxfp4_rows,
+             "fp8_block": quantize_fp8_blocks}[cfg.wfmt]
+    blocks = cfg.wfmt == "fp8_block"
     for e in range(E):
         ge = torch.Generator(device=device).manual_seed((seed << 20) + e)
         a = torch.randn(2 * I, K, generator=ge, device=device) / math.sqrt(K)
-        w13[e], w13s[e] = quant(a)
         b = torch.randn(K, I, generator=ge, device=device) / math.sqrt(I)
+        if blocks:
+            a = a * _block_gain(2 * I, K, ge, device)
+            b = b * _block_gain(K, I, ge, device)
+        w13[e], w13s[e] = quant(a)
         w2[e], w2s[e] = quant(b)
         del a, b
     out.update(w13=w13, w13_scale=w13s, w2=w2, w2_scale=w2s)
@@ -196,10 +225,17 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, expert_weights: dic
             out["sw13"] = _bf16_randn((2 * cfg.I_s, H), H, gs, device)
             out["sw2"] = _bf16_randn((H, cfg.I_s), cfg.I_s, gs, device)
         else:
+            # an fp8 shared expert takes the routed experts' fp8 format
             a = torch.randn(2 * cfg.I_s, H, generator=gs, device=device) / math.sqrt(H)
-            out["sw13"], out["sw13_scale"] = quantize_fp8_rows(a)
             b = torch.randn(H, cfg.I_s, generator=gs, device=device) / math.sqrt(cfg.I_s)
-            out["sw2"], out["sw2_scale"] = quantize_fp8_rows(b)
+            if cfg.wfmt == "fp8_block":
+                a = a * _block_gain(2 * cfg.I_s, H, gs, device)
+                b = b * _block_gain(H, cfg.I_s, gs, device)
+                out["sw13"], out["sw13_scale"] = quantize_fp8_blocks(a)
+                out["sw2"], out["sw2_scale"] = quantize_fp8_blocks(b)
+            else:
+                out["sw13"], out["sw13_scale"] = quantize_fp8_rows(a)
+                out["sw2"], out["sw2_scale"] = quantize_fp8_rows(b)
 
     out.update(wd=None, wu=None, gamma=None)
     if cfg.L:

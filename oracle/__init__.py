@@ -31,6 +31,7 @@ _lib = None
 
 FP8 = 0
 MXFP4 = 1
+FP8_BLOCK = 2
 SWIGLU = 0
 SITU = 1
 
@@ -268,7 +269,7 @@ def moe_forward(prob: dict, w: dict, tokens=None, nthreads: int = 0):
     """
     P = Problem(T=prob["T"], H=prob["H"], I=prob["I"], E=prob["E"], k=prob["k"],
                 I_s=prob.get("I_s", 0), L=prob.get("L", 0),
-                wfmt=MXFP4 if prob.get("wfmt", "fp8") == "mxfp4" else FP8,
+                wfmt={"fp8": FP8, "mxfp4": MXFP4, "fp8_block": FP8_BLOCK}[prob.get("wfmt", "fp8")],
                 shared_bf16=int(bool(prob.get("shared_bf16", False))),
                 rms_eps=float(prob.get("rms_eps", 1e-6)),
                 routing=1 if prob.get("routing", "softmax") == "sigmoid" else 0,

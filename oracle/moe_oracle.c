@@ -399,7 +399,11 @@ void orc_quant_rows(int64_t T, int64_t H, const uint16_t* x, float* scale, uint8
  * MXFP4: w13 [2I, K/2] packed e2m1 (low nibble = even k), s13 [2I, K/32] e8m0;
  * w2 [N, I/2], s2 [N, I/32].  K is the expert input width (H, or the latent
  * width L), N its output width (same as K). */
-enum { ORC_FP8 = 0, ORC_MXFP4 = 1 };
+enum { ORC_FP8 = 0, ORC_MXFP4 = 1, ORC_FP8_BLOCK = 2 };
+/* FP8_BLOCK (block-wise fp8, weight_block_size [128, 128], K3 report s.3.7):
+ * w13 [2I, K] / w2 [N, I] e4m3 bytes as FP8, with one fp32 scale per 128 x 128
+ * block, s13 [2I/128, K/128] and s2 [N/128, I/128]; a weight is
+ * e4m3(q[n,k]) * s[n/128, k/128] and is applied inside the K-sum. */
 
 /* Decode tables filled once from the decoders above (lookup instead of a call
  * per element; same values). */
@@ -413,8 +417,11 @@ static void fill_tables(void) {
   for (int c = 0; c < 16; c++) tab_e2m1[c] = orc_e2m1_decode((uint8_t)c);
 }
 
+/* One weight value; srow is the row's scale row (MXFP4: e8m0 per 32 k;
+ * FP8_BLOCK: fp32 per 128 k of the row's 128-row block; FP8: unused). */
 static double weight_at(int fmt, const uint8_t* wrow, const void* srow, int64_t k) {
   if (fmt == ORC_FP8) return tab_e4m3[wrow[k]];
+  if (fmt == ORC_FP8_BLOCK) return tab_e4m3[wrow[k]] * (double)((const float*)srow)[k / 128];
   uint8_t byte = wrow[k / 2];
   uint8_t nib = (k & 1) ? (byte >> 4) : (byte & 15);
   return tab_e2m1[nib] * tab_e8m0[((const uint8_t*)srow)[k / 32]];
@@ -435,8 +442,8 @@ static double gated(int act, double g, double u) {
 static void expert_ffn(int fmt, int act, int64_t K, int64_t I, const uint8_t* xq, float sx,
                        const uint8_t* w13, const void* s13, const uint8_t* w2, const void* s2,
                        double* y, uint16_t* h_out, float* sh_out, uint8_t* hq_out) {
-  int64_t rowb13 = (fmt == ORC_FP8) ? K : K / 2, rows13 = (fmt == ORC_FP8) ? 1 : K / 32;
-  int64_t rowb2 = (fmt == ORC_FP8) ? I : I / 2, rows2 = (fmt == ORC_FP8) ? 1 : I / 32;
+  int64_t rowb13 = (fmt == ORC_MXFP4) ? K / 2 : K, rows13 = (fmt == ORC_MXFP4) ? K / 32 : 0;
+  int64_t rowb2 = (fmt == ORC_MXFP4) ? I / 2 : I, rows2 = (fmt == ORC_MXFP4) ? I / 32 : 0;
   double* xd = (double*)malloc(sizeof(double) * (size_t)K);
   float* hf = (float*)malloc(sizeof(float) * (size_t)I);
   uint16_t* hb = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
@@ -450,6 +457,9 @@ static void expert_ffn(int fmt, int act, int64_t K, int64_t I, const uint8_t* xq
     double ag = 0.0, au = 0.0;
     if (fmt == ORC_FP8) {
       sg = su = NULL;
+    } else if (fmt == ORC_FP8_BLOCK) {
+      sg = (const float*)s13 + (n / 128) * (K / 128);
+      su = (const float*)s13 + ((I + n) / 128) * (K / 128);
     } else {
       sg = (const uint8_t*)s13 + n * rows13;
       su = (const uint8_t*)s13 + (I + n) * rows13;
@@ -470,7 +480,9 @@ static void expert_ffn(int fmt, int act, int64_t K, int64_t I, const uint8_t* xq
   for (int64_t i = 0; i < I; i++) hd[i] = tab_e4m3[hq[i]];
   for (int64_t n = 0; n < K; n++) {
     const uint8_t* wr = w2 + n * rowb2;
-    const void* sr = (fmt == ORC_FP8) ? NULL : (const void*)((const uint8_t*)s2 + n * rows2);
+    const void* sr = (fmt == ORC_FP8)         ? NULL
+                     : (fmt == ORC_FP8_BLOCK) ? (const void*)((const float*)s2 + (n / 128) * (I / 128))
+                                              : (const void*)((const uint8_t*)s2 + n * rows2);
     double acc = 0.0;
     for (int64_t i = 0; i < I; i++) acc += hd[i] * weight_at(fmt, wr, sr, i);
     double v = acc * (double)s_h;
@@ -516,7 +528,7 @@ static void shared_ffn_bf16(int act, int64_t H, int64_t Is, const uint16_t* xrow
 /* ------------------------------------------------------------------------- */
 typedef struct {
   int64_t T, H, I, E, k, I_s, L; /* I_s = 0: no shared expert; L = 0: no latent */
-  int32_t wfmt;                  /* ORC_FP8 or ORC_MXFP4 (routed experts)       */
+  int32_t wfmt;                  /* ORC_FP8, ORC_MXFP4 or ORC_FP8_BLOCK (routed)  */
   int32_t shared_bf16;           /* shared expert weights are bf16 (else fp8)   */
   double rms_eps;
   int32_t routing;               /* 0 softmax top-k, 1 sigmoid (noaux_tc)        */
@@ -549,6 +561,26 @@ typedef struct {
   int32_t* idx_out;  /* [n, k] may be NULL */
   double* w_out;     /* [n, k] may be NULL */
 } fwd_ctx;
+
+/* Expert e's weights and scales within the [E, ...] arrays of format fmt. */
+static void expert_slice(int fmt, int64_t K, int64_t I, int64_t e, const uint8_t* w13,
+                         const void* s13, const uint8_t* w2, const void* s2,
+                         const uint8_t** w13e, const void** s13e, const uint8_t** w2e,
+                         const void** s2e) {
+  int64_t rb13 = (fmt == ORC_MXFP4) ? K / 2 : K, rb2 = (fmt == ORC_MXFP4) ? I / 2 : I;
+  *w13e = w13 + e * 2 * I * rb13;
+  *w2e = w2 + e * K * rb2;
+  if (fmt == ORC_FP8) {
+    *s13e = (const float*)s13 + e * 2 * I;
+    *s2e = (const float*)s2 + e * K;
+  } else if (fmt == ORC_FP8_BLOCK) {
+    *s13e = (const float*)s13 + e * (2 * I / 128) * (K / 128);
+    *s2e = (const float*)s2 + e * (K / 128) * (I / 128);
+  } else {
+    *s13e = (const uint8_t*)s13 + e * 2 * I * (K / 32);
+    *s2e = (const uint8_t*)s2 + e * K * (I / 32);
+  }
+}
 
 static void token_forward(int64_t i, void* c) {
   fwd_ctx* f = (fwd_ctx*)c;
@@ -589,20 +621,11 @@ static void token_forward(int64_t i, void* c) {
     sx = quant_row_bf16(H, xrow, xq);
   }
 
-  int64_t rowb13 = (p->wfmt == ORC_FP8) ? K : K / 2, rows13 = (p->wfmt == ORC_FP8) ? 1 : K / 32;
-  int64_t rowb2 = (p->wfmt == ORC_FP8) ? I : I / 2, rows2 = (p->wfmt == ORC_FP8) ? 1 : I / 32;
   for (int j = 0; j < k; j++) {
-    int64_t e = idx[j];
-    const uint8_t* w13 = w->w13 + e * 2 * I * rowb13;
-    const uint8_t* w2 = w->w2 + e * K * rowb2;
+    const uint8_t *w13, *w2;
     const void *s13, *s2;
-    if (p->wfmt == ORC_FP8) {
-      s13 = (const float*)w->w13_scale + e * 2 * I;
-      s2 = (const float*)w->w2_scale + e * K;
-    } else {
-      s13 = (const uint8_t*)w->w13_scale + e * 2 * I * rows13;
-      s2 = (const uint8_t*)w->w2_scale + e * K * rows2;
-    }
+    expert_slice(p->wfmt, K, I, idx[j], w->w13, w->w13_scale, w->w2, w->w2_scale, &w13, &s13,
+                 &w2, &s2);
     expert_ffn(p->wfmt, p->act, K, I, xq, sx, w13, s13, w2, s2, y, NULL, NULL, NULL);
     for (int64_t n = 0; n < K; n++) acc[n] += wt[j] * y[n]; /* j ascending */
   }
@@ -639,7 +662,9 @@ static void token_forward(int64_t i, void* c) {
         sxh = quant_row_bf16(H, xrow, tmp);
         xqh = tmp;
       }
-      expert_ffn(ORC_FP8, p->act, H, p->I_s, xqh, sxh, (const uint8_t*)w->sw13, w->sw13_scale,
+      /* an fp8 shared expert has the routed experts' fp8 format */
+      expert_ffn(p->wfmt == ORC_FP8_BLOCK ? ORC_FP8_BLOCK : ORC_FP8, p->act, H, p->I_s, xqh, sxh,
+                 (const uint8_t*)w->sw13, w->sw13_scale,
                  (const uint8_t*)w->sw2, w->sw2_scale, y, NULL, NULL, NULL);
       free(tmp);
     }
@@ -696,19 +721,11 @@ static void rows_body(int64_t r, void* c) {
   int64_t e = 0;
   while (e < q->E && q->off[e + 1] <= r) e++;
   int64_t K = q->K, I = q->I;
-  int64_t rowb13 = (q->wfmt == ORC_FP8) ? K : K / 2, rows13 = (q->wfmt == ORC_FP8) ? 1 : K / 32;
-  int64_t rowb2 = (q->wfmt == ORC_FP8) ? I : I / 2, rows2 = (q->wfmt == ORC_FP8) ? 1 : I / 32;
+  const uint8_t *w13, *w2;
   const void *s13, *s2;
-  if (q->wfmt == ORC_FP8) {
-    s13 = (const float*)q->w13_scale + e * 2 * I;
-    s2 = (const float*)q->w2_scale + e * K;
-  } else {
-    s13 = (const uint8_t*)q->w13_scale + e * 2 * I * rows13;
-    s2 = (const uint8_t*)q->w2_scale + e * K * rows2;
-  }
+  expert_slice(q->wfmt, K, I, e, q->w13, q->w13_scale, q->w2, q->w2_scale, &w13, &s13, &w2, &s2);
   double* y = q->y + r * K;
-  expert_ffn(q->wfmt, q->act, K, I, q->xq + r * K, q->xs[r], q->w13 + e * 2 * I * rowb13, s13,
-             q->w2 + e * K * rowb2, s2, y, q->h ? q->h + r * I : NULL, q->hs ? q->hs + r : NULL,
+  expert_ffn(q->wfmt, q->act, K, I, q->xq + r * K, q->xs[r], w13, s13, w2, s2, y, q->h ? q->h + r * I : NULL, q->hs ? q->hs + r : NULL,
              q->hq ? q->hq + r * I : NULL);
   for (int64_t n = 0; n < K; n++) y[n] *= (double)q->row_w[r];
 }

@@ -66,6 +66,12 @@ def fp8_weight(w_bytes, scale):
     return e4m3_values(w_bytes) * np.asarray(scale, np.float64)[..., None]
 
 
+def fp8_block_weight(w_bytes, scale):
+    """e4m3 values times the fp32 scale of their 128 x 128 block."""
+    full = np.repeat(np.repeat(np.asarray(scale, np.float64), 128, -2), 128, -1)
+    return e4m3_values(w_bytes) * full
+
+
 def mxfp4_weight(packed, scales):
     lo, hi = packed & 15, packed >> 4
     nib = np.stack([lo, hi], axis=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
@@ -110,6 +116,9 @@ def numpy_layer(cfg, w, idx, wt):
         if cfg.wfmt == "fp8":
             W13 = fp8_weight(w["w13"][e], w["w13_scale"][e])
             W2 = fp8_weight(w["w2"][e], w["w2_scale"][e])
+        elif cfg.wfmt == "fp8_block":
+            W13 = fp8_block_weight(w["w13"][e], w["w13_scale"][e])
+            W2 = fp8_block_weight(w["w2"][e], w["w2_scale"][e])
         else:
             W13 = mxfp4_weight(w["w13"][e], w["w13_scale"][e])
             W2 = mxfp4_weight(w["w2"][e], w["w2_scale"][e])
@@ -131,8 +140,9 @@ def numpy_layer(cfg, w, idx, wt):
             res = res + hs @ bf16_vals(w["sw2"]).T
         else:
             sxs, xqs = quant_fp8(x.astype(np.float32))
-            res = res + swiglu_rows(xqs, sxs.astype(np.float64), fp8_weight(w["sw13"], w["sw13_scale"]),
-                                    fp8_weight(w["sw2"], w["sw2_scale"]), cfg.I_s, cfg.act)
+            deq = fp8_block_weight if cfg.wfmt == "fp8_block" else fp8_weight
+            res = res + swiglu_rows(xqs, sxs.astype(np.float64), deq(w["sw13"], w["sw13_scale"]),
+                                    deq(w["sw2"], w["sw2_scale"]), cfg.I_s, cfg.act)
     return res
 
 
@@ -150,6 +160,9 @@ SMALL = [
     # bias, SiTU experts (fp8 shared expert here, bf16 in the latent case below)
     mi.MoEConfig("small_k3", T=20, H=256, I=128, E=8, k=3, I_s=128, routing="sigmoid",
                  act="situ", sel_bias=True),
+    # block-wise fp8 (128 x 128 weight blocks, scales of differing size); a
+    # non-square block grid so that a transposed scale index cannot pass
+    mi.MoEConfig("small_block", T=24, H=256, I=384, E=6, k=3, I_s=128, wfmt="fp8_block"),
 ]
 
 
@@ -300,3 +313,20 @@ def test_situ_one_hot_closed_form(orc):
     # the layer uses the same activation
     of, _, _, _ = orc.moe_forward(prob, w)
     assert np.allclose(of[0], y[0], rtol=0, atol=0)
+
+
+def test_fp8_block_with_uniform_row_scales_is_per_channel(orc):
+    # when every block of a 128-row block row has one scale c, the block-wise
+    # weight equals the per-channel weight with scale c on each of those rows
+    cfg = mi.MoEConfig("blk_uni", T=12, H=256, I=256, E=3, k=2, I_s=128, wfmt="fp8_block")
+    w = mi.to_numpy(mi.make_inputs(cfg, seed=6))
+    for key in ("w13_scale", "w2_scale", "sw13_scale", "sw2_scale"):
+        sc = w[key]
+        w[key] = np.repeat(sc[..., :1], sc.shape[-1], axis=-1).astype(np.float32)
+    of_b, _, idx_b, _ = orc.moe_forward(cfg.oracle_problem(), w)
+    wc = dict(w)
+    for key in ("w13_scale", "w2_scale", "sw13_scale", "sw2_scale"):
+        wc[key] = np.repeat(w[key][..., 0], 128, axis=-1).astype(np.float32)
+    of_c, _, idx_c, _ = orc.moe_forward(cfg.with_(wfmt="fp8").oracle_problem(), wc)
+    assert np.array_equal(idx_b, idx_c)
+    assert _close(of_b, of_c, rtol=1e-12)
