@@ -68,8 +68,9 @@ def workload_name(cfg):
     s = (f"{kind}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}"
          + (f" + shared expert I_s={cfg.I_s}" if cfg.I_s else "")
          + (f", latent L={cfg.L} (bf16 down/up, RMSNorm)" if cfg.L else "")
-         + (", MXFP4 e2m1 + e8m0/32 expert weights" if cfg.wfmt == "mxfp4"
-            else ", fp8 e4m3 per-output-channel weights")
+         + {"mxfp4": ", MXFP4 e2m1 + e8m0/32 expert weights",
+            "fp8_block": ", block-wise fp8 e4m3 weights (fp32 scale per 128x128 block)"}.get(
+             cfg.wfmt, ", fp8 e4m3 per-output-channel weights")
          + ", per-token fp8 activations"
          + (", noaux_tc sigmoid routing with selection bias" if cfg.routing == "sigmoid" else "")
          + (", SiTU experts" if cfg.act == "situ" else ""))
@@ -259,7 +260,7 @@ def run_ours(args, cfg):
              | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
              | (m.F_SIGMOID_ROUTING if cfg.routing == "sigmoid" else 0)
              | (m.F_SITU if cfg.act == "situ" else 0))
-    wfmt = m.W_MXFP4 if cfg.wfmt == "mxfp4" else m.W_FP8
+    wfmt = {"fp8": m.W_FP8, "mxfp4": m.W_MXFP4, "fp8_block": m.W_FP8_BLOCK}[cfg.wfmt]
     pack = not args.no_pack
     if pack:
         # one-time load-time weight preparation (untimed): tile-major expert weights

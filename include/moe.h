@@ -62,7 +62,8 @@ typedef enum {
 
 typedef enum {
   MOE_W_FP8_E4M3_PER_CHANNEL = 0, /* e4m3 bytes + fp32 scale per output channel   */
-  MOE_W_MXFP4_E2M1_E8M0_B32 = 1   /* packed e2m1 (low nibble = even k) + e8m0/32  */
+  MOE_W_MXFP4_E2M1_E8M0_B32 = 1,  /* packed e2m1 (low nibble = even k) + e8m0/32  */
+  MOE_W_FP8_E4M3_BLOCK128 = 2     /* e4m3 bytes + fp32 scale per 128 x 128 block  */
 } moe_wfmt;
 
 #define MOE_F_ROUTER_BIAS 0x1u /* add router_bias[e] to every logit before top-k    */
@@ -229,6 +230,13 @@ int moe_pack_weights(const moe_problem* p, const void* w13, const void* w2, cons
  *          consecutive k, 4-byte aligned); the block scale multiplies inside the
  *          K-sum, so the per-channel factors s13/s2 above are 1; K must be a
  *          multiple of 256.
+ *   block-wise fp8 (K3 report s.3.7, weight_block_size [128, 128]): w13, w2 as
+ *          fp8, w13_scale [E, 2I/128, K/128] and w2_scale [E, K/128, I/128]
+ *          fp32, one per 128 x 128 weight block; the block scale multiplies
+ *          each 128-wide slice of the K-sum (g = xs * sum_kb s13[n/128, kb] *
+ *          sum_{k in kb} xq W1, likewise u and y), so s13/s2 above become these
+ *          block scales; K, I <= 16384.  An fp8 shared expert uses the same
+ *          format ([2*I_shared/128, H/128] and [H/128, I_shared/128] scales).
  *   y         [R, K] bf16 (out); K = H (or latent)
  * R is read from p as T*top_k. */
 int moe_expert_ffn(const moe_problem* p, const int32_t* offsets, const void* xq_perm,

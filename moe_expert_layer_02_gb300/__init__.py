@@ -18,7 +18,8 @@ __all__ = [
     "moe_forward", "moe_get_last_error", "moe_launch_count", "moe_profile_enable",
     "moe_profile_read", "moe_pack_weights", "moe_watchdog_selftest", "moe_describe", "STAGES",
     "W_FP8",
-    "W_MXFP4", "F_ROUTER_BIAS", "F_SHARED_BF16", "F_PACKED_WEIGHTS", "F_SIGMOID_ROUTING", "F_SITU",
+    "W_MXFP4", "W_FP8_BLOCK", "F_ROUTER_BIAS", "F_SHARED_BF16", "F_PACKED_WEIGHTS",
+    "F_SIGMOID_ROUTING", "F_SITU",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -26,6 +27,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmoe.so")
 
 W_FP8 = 0
 W_MXFP4 = 1
+W_FP8_BLOCK = 2
 F_ROUTER_BIAS = 0x1
 F_SHARED_BF16 = 0x2
 F_PACKED_WEIGHTS = 0x4

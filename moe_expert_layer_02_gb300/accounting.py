@@ -36,13 +36,15 @@ def expert_weight_bytes(K: int, I: int, wfmt: str = "fp8", with_scales: bool = T
     n = 3 * K * I
     if wfmt == "fp8":
         return n + (4 * (2 * I + K) if with_scales else 0)
+    if wfmt == "fp8_block":  # one fp32 scale per 128 x 128 block
+        return n + (4 * 3 * (K // 128) * (I // 128) if with_scales else 0)
     if wfmt == "mxfp4":
         return n / 2 + (n / 32 if with_scales else 0)
     raise ValueError(wfmt)
 
 
 def bits_per_element(wfmt: str) -> float:
-    return {"fp8": 8.0, "mxfp4": 4.0 + 8.0 / 32.0}[wfmt]
+    return {"fp8": 8.0, "mxfp4": 4.0 + 8.0 / 32.0, "fp8_block": 8.0 + 32.0 / (128 * 128)}[wfmt]
 
 
 def router_flops(T: int, H: int, E: int) -> int:
@@ -69,7 +71,8 @@ def layer_work(cfg, touched_experts: int) -> dict:
     if cfg.I_s:
         w_shared = 3 * H * cfg.I_s * (2 if cfg.shared_bf16 else 1)
         if not cfg.shared_bf16:
-            w_shared += 4 * (2 * cfg.I_s + H)
+            w_shared += (4 * 3 * (H // 128) * (cfg.I_s // 128) if cfg.wfmt == "fp8_block"
+                         else 4 * (2 * cfg.I_s + H))
     else:
         w_shared = 0
     w_latent = 2 * (2 * H * cfg.L) + 2 * cfg.L if cfg.L else 0
@@ -86,10 +89,12 @@ def layer_work(cfg, touched_experts: int) -> dict:
 
 
 def _matrix_bytes(rows: int, cols: int, wfmt: str) -> float:
-    """Bytes of one weight matrix with its scales (fp8: fp32 per row; mxfp4:
-    4-bit elements + one e8m0 byte per 32)."""
+    """Bytes of one weight matrix with its scales (fp8: fp32 per row; fp8_block:
+    fp32 per 128 x 128 block; mxfp4: 4-bit elements + one e8m0 byte per 32)."""
     if wfmt == "fp8":
         return rows * cols + 4 * rows
+    if wfmt == "fp8_block":
+        return rows * cols + 4 * (rows // 128) * (cols // 128)
     return rows * cols / 2 + rows * cols / 32
 
 
@@ -100,7 +105,7 @@ def ffn1_launch_bytes(cfg, touched_experts: int) -> float:
     b = touched_experts * _matrix_bytes(2 * I, K, cfg.wfmt)
     rows = cfg.T * cfg.k
     if cfg.I_s and not cfg.shared_bf16:
-        b += 2 * cfg.I_s * K + 4 * 2 * cfg.I_s
+        b += _matrix_bytes(2 * cfg.I_s, K, "fp8_block" if cfg.wfmt == "fp8_block" else "fp8")
         rows_s = cfg.T
     else:
         rows_s = 0
@@ -114,6 +119,6 @@ def ffn2_launch_bytes(cfg, touched_experts: int) -> float:
     rows = cfg.T * cfg.k
     rows_s = cfg.T if (cfg.I_s and not cfg.shared_bf16) else 0
     if rows_s:
-        b += K * cfg.I_s + 4 * K
+        b += _matrix_bytes(K, cfg.I_s, "fp8_block" if cfg.wfmt == "fp8_block" else "fp8")
     b += rows * I + rows_s * cfg.I_s + (rows + rows_s) * K * 2
     return b

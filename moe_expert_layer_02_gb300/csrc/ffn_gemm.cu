@@ -27,6 +27,15 @@
 //     warps 2-5 = epilogue (tcgen05.ld, scales, SiLU*gate or routing weight,
 //     bf16 stores).  Multi-stage smem ring + double-buffered accumulators
 //     (the write-up's "weight double-buffering" becomes this ring).
+//   * Block-wise fp8 weights (one fp32 scale per 128 x 128 block, the format
+//     tpu-inference requires, "Kimi K3 ... feasibility analysis" s.3.7): the
+//     scale changes every 128 K, so the K-sum cannot run in one accumulator.
+//     With BLK the MMAs write each stage's partial sum into one of four (FFN1)
+//     or eight (FFN2) tensor-memory buffers (restarted per stage), and the
+//     epilogue warps add
+//     s[nb][kb] * partial into fp32 registers, stage by stage, before applying
+//     the per-token scale and the activation at the end of the tile (tiles of
+//     at most 64 token rows, the registers' limit).
 //   * Every pipeline wait is bounded; on timeout the CTA records
 //     MOE_ERR_TIMEOUT, drains its own TMA loads and MMAs and frees its tensor
 //     memory before returning.
@@ -52,7 +61,7 @@ constexpr int pow2_at_least(int v) {
   return p;
 }
 
-template <bool FFN1, int BN>
+template <bool FFN1, int BN, bool BLK>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK;  // one weight box, 16 KB
   static constexpr int NA = FFN1 ? 2 : 1;  // W1 and W3 boxes for FFN1
@@ -60,12 +69,19 @@ struct Cfg {
   static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
   static constexpr int STAGES = cmin(kSmemBudget / STAGE_BYTES, 12);
   static constexpr int ACC_COLS = NA * BN;
-  static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
-  static constexpr int TMEM_COLS = pow2_at_least(ACC_STAGES * ACC_COLS);
+  // accumulators per tile, or (BLK) per-stage partial-sum buffers, so the MMAs
+  // can run that many stages ahead of the warps that scale and add them: four
+  // for FFN1's 32 KB stages, eight for FFN2's 16 KB ones (measured best)
+  static constexpr int ACC_STAGES = BLK ? (FFN1 ? 4 : cmin(8, 512 / ACC_COLS))
+                                        : (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int ACC_BUFS = ACC_STAGES;
+  static constexpr int MAX_KB = 128;  // BLK: scale rows held in registers (K <= 16384)
+  static_assert(!BLK || BN <= 64, "block-wise tiles keep their sums in registers");
+  static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + STAGES * 4;
   static_assert(B_BYTES % 1024 == 0, "operand tiles must keep 1024-byte alignment");
-  static_assert(ACC_STAGES * ACC_COLS <= 512, "tensor memory holds 512 columns");
+  static_assert(ACC_BUFS * ACC_COLS <= 512, "tensor memory holds 512 columns");
   static_assert(STAGES >= 2, "need at least two pipeline stages");
 };
 
@@ -74,12 +90,123 @@ __device__ __forceinline__ uint32_t f32_bits_to_bf16(float v) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
-template <bool FFN1, int BN>
+// Block-wise epilogue helpers.  Scale rows [.. / 128][KB] of a tile: W1 and W3
+// block rows nb and I/128 + nb (FFN1), W2 block row nb (FFN2); lane l holds
+// entries l, l+32, l+64, l+96 (KB <= 128).
+constexpr int kHeld = 4;
+
+template <bool FFN1>
+__device__ __forceinline__ void load_block_scales(const GroupedFfnArgs& a, int item, int nb,
+                                                  int KB, int lane, float (&held)[FFN1 ? 2 : 1][kHeld]) {
+  constexpr int NA = FFN1 ? 2 : 1;
+  const int4 it = a.items[item];
+  const bool shared = it.x >= a.E;
+  const int wrow_blocks = FFN1 ? 2 * a.I / BM : a.K / BM;
+  const float* sbase = FFN1 ? (shared ? a.sw13_scale : a.w13_scale + (size_t)it.x * wrow_blocks * KB)
+                            : (shared ? a.sw2_scale : a.w2_scale + (size_t)it.x * wrow_blocks * KB);
+#pragma unroll
+  for (int b = 0; b < NA; ++b) {
+    const float* srow = sbase + (size_t)(b == 0 ? nb : a.I / BM + nb) * KB;
+#pragma unroll
+    for (int i = 0; i < kHeld; ++i) {
+      const int kb = i * 32 + lane;
+      held[b][i] = kb < KB ? __ldg(srow + kb) : 0.0f;
+    }
+  }
+}
+
+// Stage by stage, acc += s[kb] * partial; at the end of the tile the per-token
+// scale, activation / routing weight and bf16 store.  The next tile's scale
+// rows are loaded into held_next while this tile runs, and lane l loads the
+// per-row scalars of rows l and l + 32 once, for the final pass to shuffle.
+template <bool FFN1, int BN, int ACC_COLS, int PBUF>
+__device__ __forceinline__ bool block_epilogue(const GroupedFfnArgs& a, uint32_t tmem, int q,
+                                               int lane, int item, int nb, int KB,
+                                               const float (&held)[FFN1 ? 2 : 1][kHeld],
+                                               int next_item, int next_nb,
+                                               float (&held_next)[FFN1 ? 2 : 1][kHeld],
+                                               uint64_t* tfull, uint64_t* tempty,
+                                               volatile int* s_abort, int& pcount) {
+  constexpr int NA = FFN1 ? 2 : 1;
+  constexpr int RL = (BN + 31) / 32;  // rows per lane for the per-row scalars
+  const int4 it = a.items[item];
+  const bool shared = it.x >= a.E;
+  const int row0 = it.y, rows = it.z;
+  float rs[RL], rw[RL];  // xs (FFN1) or hs (FFN2), and the routing weight (FFN2)
+#pragma unroll
+  for (int i = 0; i < RL; ++i) {
+    const int r = i * 32 + lane, row = row0 + r;
+    const bool ok = r < rows && (unsigned)row < (unsigned)a.rows_total;
+    rs[i] = ok ? (FFN1 ? a.xscale[row] : a.hs[row]) : 0.0f;
+    rw[i] = (ok && !FFN1 && !shared && a.row_w) ? a.row_w[row] : 1.0f;
+  }
+  if (next_item >= 0) load_block_scales<FFN1>(a, next_item, next_nb, KB, lane, held_next);
+  float acc[NA][BN];
+#pragma unroll
+  for (int b = 0; b < NA; ++b)
+#pragma unroll
+    for (int j = 0; j < BN; ++j) acc[b][j] = 0.0f;
+  for (int kb = 0; kb < KB; ++kb, ++pcount) {
+    const int pb = pcount % PBUF;
+    const uint32_t ph = (uint32_t)(pcount / PBUF) & 1u;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(smem_u32(&tfull[pb]), ph, a.err, s_abort) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) return false;
+    tc_fence_after();
+    float sk[NA];
+#pragma unroll
+    for (int b = 0; b < NA; ++b) {
+      float v = held[b][0];
+#pragma unroll
+      for (int i = 1; i < kHeld; ++i) v = (kb >> 5) == i ? held[b][i] : v;
+      sk[b] = __shfl_sync(0xffffffffu, v, kb & 31);
+    }
+    const uint32_t pbase = tmem + ((uint32_t)(q * 32) << 16) + pb * ACC_COLS;
+#pragma unroll
+    for (int c = 0; c < BN / 16; ++c) {
+      if (c * 16 < rows) {  // warp-uniform
+        uint32_t v[NA][16];
+        __syncwarp();
+#pragma unroll
+        for (int b = 0; b < NA; ++b) tmem_ld16(pbase + b * BN + c * 16, v[b]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int b = 0; b < NA; ++b)
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            acc[b][c * 16 + j] = fmaf(sk[b], __uint_as_float(v[b][j]), acc[b][c * 16 + j]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&tempty[pb]));
+  }
+  const int f = nb * BM + q * 32 + lane;  // feature (FFN1) / output channel (FFN2)
+#pragma unroll
+  for (int j = 0; j < BN; ++j) {
+    const float sj = __shfl_sync(0xffffffffu, rs[j / 32], j % 32);
+    const float wj = __shfl_sync(0xffffffffu, rw[j / 32], j % 32);
+    const int row = row0 + j;
+    if (j < rows && (unsigned)row < (unsigned)a.rows_total) {
+      if (FFN1) {
+        const float hv = gated_act(a.act, acc[0][j] * sj, acc[NA - 1][j] * sj);
+        static_cast<uint16_t*>(a.h)[(size_t)row * a.I + f] = (uint16_t)f32_bits_to_bf16(hv);
+      } else {
+        static_cast<uint16_t*>(a.y)[(size_t)row * a.K + f] =
+            (uint16_t)f32_bits_to_bf16((acc[0][j] * sj) * wj);
+      }
+    }
+  }
+  return true;
+}
+
+template <bool FFN1, int BN, bool BLK>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_ffn_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_ws,
                        const __grid_constant__ CUtensorMap tm_x, const GroupedFfnArgs a) {
-  using C = Cfg<FFN1, BN>;
+  using C = Cfg<FFN1, BN, BLK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -168,7 +295,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && BLK) {
+      // one partial sum per stage, into buffer pcount % ACC_STAGES
+      int stage = 0, pcount = 0;
+      uint32_t phase = 0;
+      bool issued_any = false, ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok && !*s_abort; tile += gridDim.x) {
+        const int rows = a.items[tile / NB].z;
+        const uint32_t idesc = idesc_e4m3_f32(BM, min(BN, (rows + 15) & ~15));
+        for (int kb = 0; kb < KB; ++kb, ++pcount) {
+          const int pb = pcount % C::ACC_STAGES;
+          if (!mbar_wait(smem_u32(&tempty[pb]), ((uint32_t)(pcount / C::ACC_STAGES) & 1u) ^ 1u,
+                         a.err, s_abort) ||
+              !mbar_wait(smem_u32(&full[stage]), phase, a.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d0 = tmem + pb * C::ACC_COLS;
+          const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + C::NA * C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(b0 + kk * UMMA_K);
+            const uint32_t accum = kk ? 1u : 0u;
+            mma_f8f6f4(d0, smem_desc_sw128(a0 + kk * UMMA_K), bdesc, idesc, accum);
+            if (FFN1)
+              mma_f8f6f4(d0 + BN, smem_desc_sw128(a0 + C::A_BYTES + kk * UMMA_K), bdesc, idesc,
+                         accum);
+          }
+          issued_any = true;
+          mma_commit(smem_u32(&empty[stage]));
+          mma_commit(smem_u32(&tfull[pb]));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*s_abort && issued_any) {
+        mma_commit(smem_u32(drain));
+        mbar_wait_drain(smem_u32(drain), 0);
+      }
+    } else if (lane == 0) {
       int stage = 0, it_local = 0;
       uint32_t phase = 0;
       bool issued_any = false;
@@ -219,7 +388,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quarter this warp may access
     int it_local = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it_local) {
+    if (BLK) {
+      int pcount = 0;
+      float h0[C::NA][kHeld], h1[C::NA][kHeld];  // scale rows, this tile's and the next's
+      if (blockIdx.x < n_tiles)
+        load_block_scales<FFN1>(a, blockIdx.x / NB, blockIdx.x % NB, KB, lane, h0);
+      // tiles in pairs so that the two scale buffers swap roles without indexing
+      for (int tile = blockIdx.x; tile < n_tiles;) {
+        int nt = tile + gridDim.x;
+        if (!block_epilogue<FFN1, BN, C::ACC_COLS, C::ACC_STAGES>(
+                a, tmem, q, lane, tile / NB, tile % NB, KB, h0, nt < n_tiles ? nt / NB : -1,
+                nt % NB, h1, tfull, tempty, s_abort, pcount))
+          break;
+        tile = nt;
+        if (tile >= n_tiles) break;
+        nt = tile + gridDim.x;
+        if (!block_epilogue<FFN1, BN, C::ACC_COLS, C::ACC_STAGES>(
+                a, tmem, q, lane, tile / NB, tile % NB, KB, h1, nt < n_tiles ? nt / NB : -1,
+                nt % NB, h0, tfull, tempty, s_abort, pcount))
+          break;
+        tile = nt;
+      }
+    }
+    for (int tile = blockIdx.x; !BLK && tile < n_tiles; tile += gridDim.x, ++it_local) {
       const int item = tile / NB, nb = tile - item * NB;
       const int4 it = a.items[item];
       const bool shared = it.x >= a.E;
@@ -323,9 +514,9 @@ bool make_map(CUtensorMap* m, int rank, const void* base, uint64_t inner, uint64
   return r == CUDA_SUCCESS;
 }
 
-template <bool FFN1, int BN>
+template <bool FFN1, int BN, bool BLK>
 cudaError_t launch_impl(const GroupedFfnArgs& a, cudaStream_t s) {
-  using C = Cfg<FFN1, BN>;
+  using C = Cfg<FFN1, BN, BLK>;
   const int K = FFN1 ? a.K : a.I;      // reduction width
   const int Wrows = FFN1 ? 2 * a.I : a.K;
   const void* w = FFN1 ? a.w13 : a.w2;
@@ -338,21 +529,29 @@ cudaError_t launch_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   if (!make_map(&tw, 3, w, winner, wrows, a.E, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tws, 3, ws ? ws : w, winner, wrows, 1, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tx, 2, x, K, a.rows_total, 1, BN)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(grouped_ffn_kernel<FFN1, BN>,
+  if (BLK && (K / BK > C::MAX_KB || (FFN1 ? a.I : a.K) % BM)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(grouped_ffn_kernel<FFN1, BN, BLK>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   count_launch();
-  grouped_ffn_kernel<FFN1, BN><<<device_sm_count(), kThreads, C::SMEM, s>>>(tw, tws, tx, a);
+  grouped_ffn_kernel<FFN1, BN, BLK><<<device_sm_count(), kThreads, C::SMEM, s>>>(tw, tws, tx, a);
   return cudaGetLastError();
 }
 
 template <bool FFN1>
 cudaError_t launch_bn(const GroupedFfnArgs& a, cudaStream_t s) {
+  if (a.blockwise) {
+    switch (a.BN) {
+      case 32: return launch_impl<FFN1, 32, true>(a, s);
+      case 64: return launch_impl<FFN1, 64, true>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.BN) {
-    case 32: return launch_impl<FFN1, 32>(a, s);
-    case 64: return launch_impl<FFN1, 64>(a, s);
-    case 128: return launch_impl<FFN1, 128>(a, s);
-    case 256: return launch_impl<FFN1, 256>(a, s);
+    case 32: return launch_impl<FFN1, 32, false>(a, s);
+    case 64: return launch_impl<FFN1, 64, false>(a, s);
+    case 128: return launch_impl<FFN1, 128, false>(a, s);
+    case 256: return launch_impl<FFN1, 256, false>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -100,6 +100,7 @@ struct Plan {
   bool shared;      // fp8 shared expert fused into the grouped GEMMs (rows R..R+T)
   bool shared_bf16; // bf16 shared expert as dense GEMMs (LatentMoE)
   bool mx;          // MXFP4 routed experts
+  bool blockwise;   // fp8 experts with 128 x 128 block scales
   int packed;       // expert weights in tile-major order (moe_pack_weights)
   int act;          // FFN1 activation: 0 SwiGLU, 1 SiTU
   size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
@@ -113,6 +114,13 @@ int choose_bn(const moe_problem* p) {
     if (v == 32 || v == 64 || v == 128 || v == 256) return v;
   }
   const double avg = (double)p->T * p->top_k / (p->E > 0 ? p->E : 1);
+  if (p->wfmt == MOE_W_FP8_E4M3_BLOCK128) {  // block-wise tiles keep sums in registers
+    if (env) {
+      int v = std::atoi(env);
+      if (v == 32 || v == 64) return v;
+    }
+    return avg <= 24.0 ? 32 : 64;
+  }
   if (p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32) {  // block-scaled kernel tiles: 32, 64, 96 rows
     if (env) {
       int v = std::atoi(env);
@@ -140,6 +148,7 @@ Plan make_plan(const moe_problem* p) {
   q.shared_bf16 = p->I_shared > 0 && (p->flags & MOE_F_SHARED_BF16);
   q.shared = p->I_shared > 0 && !q.shared_bf16;
   q.mx = p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32;
+  q.blockwise = p->wfmt == MOE_W_FP8_E4M3_BLOCK128;
   q.packed = (p->flags & MOE_F_PACKED_WEIGHTS) ? 1 : 0;
   q.act = (p->flags & MOE_F_SITU) ? 1 : 0;
   q.RT = q.R + (q.shared ? p->T : 0);
@@ -194,7 +203,8 @@ int check_problem(const moe_problem* p) {
   if (p->H % 128 || p->I % 128 || p->I_shared < 0 || p->I_shared % 128 || p->latent < 0 ||
       p->latent % 128)
     return MOE_ERR_INVALID_ARG;
-  if (p->wfmt != MOE_W_FP8_E4M3_PER_CHANNEL && p->wfmt != MOE_W_MXFP4_E2M1_E8M0_B32)
+  if (p->wfmt != MOE_W_FP8_E4M3_PER_CHANNEL && p->wfmt != MOE_W_MXFP4_E2M1_E8M0_B32 &&
+      p->wfmt != MOE_W_FP8_E4M3_BLOCK128)
     return MOE_ERR_INVALID_ARG;
   if ((int64_t)p->T * p->top_k > (1 << 30) || (int64_t)p->T * p->H > (int64_t)1 << 40)
     return MOE_ERR_INVALID_ARG;
@@ -204,9 +214,13 @@ int check_problem(const moe_problem* p) {
 // Shapes this build runs on the GPU: fp8 experts with an optional fp8 shared
 // expert (I_shared == I, fused into the grouped GEMMs), or the LatentMoE block
 // (latent > 0, optional bf16 shared expert) with fp8 or MXFP4 experts, or
-// MXFP4 experts on their own.
+// MXFP4 experts on their own; block-wise fp8 wherever fp8 runs, with K and I at
+// most 16384 (the block-wise epilogue keeps 128 scales per block row).
 int check_supported(const moe_problem* p) {
   const bool mx = p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32;
+  if (p->wfmt == MOE_W_FP8_E4M3_BLOCK128 &&
+      ((p->latent > 0 ? p->latent : p->H) > 16384 || p->I > 16384))
+    return MOE_ERR_UNSUPPORTED;
   const bool sb = p->I_shared > 0 && (p->flags & MOE_F_SHARED_BF16);
   const bool s8 = p->I_shared > 0 && !sb;
   if (p->latent > 0) {
@@ -270,6 +284,7 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
   a.BN = q.BN;
   a.packed = q.packed;
   a.act = q.act;
+  a.blockwise = q.blockwise ? 1 : 0;
   a.err = err;
   return a;
 }
@@ -279,7 +294,7 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
 bool use_pair_gemm(const Plan& q) {
   const char* env = std::getenv("MOE_GEMM");
   if (env && std::strcmp(env, "1cta") == 0) return false;
-  return q.BN == 256 && q.K % 256 == 0;
+  return !q.blockwise && q.BN == 256 && q.K % 256 == 0;
 }
 
 int run_experts(const Plan& q, const GroupedFfnArgs& a, int rows_total, cudaStream_t s) {
@@ -345,7 +360,8 @@ int moe_describe(const moe_problem* p, char* buf, size_t len) {
       buf, len,
       "ffn1=%s<FFN1,BN=%d> ffn2=%s<FFN2,BN=%d> tile_rows=%d weights=%s%s%s max_items=%d "
       "workspace=%zu",
-      g, q.BN, g, q.BN, q.BN, q.mx ? "mxfp4" : "fp8", q.packed ? ",packed" : "",
+      g, q.BN, g, q.BN, q.BN, q.mx ? "mxfp4" : q.blockwise ? "fp8-block128" : "fp8",
+      q.packed ? ",packed" : "",
       q.L > 0 ? " latent=bf16-pair-gemms" : "", q.max_items, q.total);
   return (n < 0 || (size_t)n >= len) ? MOE_ERR_INVALID_ARG : MOE_OK;
 }

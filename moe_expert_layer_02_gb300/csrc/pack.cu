@@ -119,7 +119,8 @@ extern "C" int moe_pack_weights(const moe_problem* p, const void* w13, const voi
   if (!p || p->E <= 0 || p->I <= 0 || p->I % 128 || p->H <= 0 || p->H % 128 || p->latent < 0 ||
       p->latent % 128)
     return MOE_ERR_INVALID_ARG;
-  if (p->wfmt != MOE_W_FP8_E4M3_PER_CHANNEL && p->wfmt != MOE_W_MXFP4_E2M1_E8M0_B32)
+  if (p->wfmt != MOE_W_FP8_E4M3_PER_CHANNEL && p->wfmt != MOE_W_MXFP4_E2M1_E8M0_B32 &&
+      p->wfmt != MOE_W_FP8_E4M3_BLOCK128)
     return MOE_ERR_INVALID_ARG;
   if (!w13 || !w2 || !w13_packed || !w2_packed) return MOE_ERR_INVALID_ARG;
   if (w13 == w13_packed || w2 == w2_packed) return MOE_ERR_INVALID_ARG;

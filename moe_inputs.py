@@ -81,6 +81,10 @@ CONFIGS = {
     "latent": MoEConfig("latent", T=4096, H=7168, I=3072, E=896, k=16, I_s=6144, L=3584,
                         wfmt="mxfp4", shared_bf16=True),
     "skewed": MoEConfig("skewed", T=8192, H=8192, I=2048, E=256, k=8, I_s=2048, zipf_bias=True),
+    # the decode workload with block-wise fp8 experts (128 x 128 weight blocks,
+    # the format tpu-inference requires)
+    "decode_block": MoEConfig("decode_block", T=512, H=8192, I=2048, E=256, k=8, I_s=2048,
+                              wfmt="fp8_block"),
     # the LatentMoE workload with Kimi K3's own routing and activation (noaux_tc
     # sigmoid routing with a selection bias, SiTU experts)
     "latent_k3": MoEConfig("latent_k3", T=4096, H=7168, I=3072, E=896, k=16, I_s=6144, L=3584,

@@ -38,6 +38,7 @@ def gpu_inputs(cfg: mi.MoEConfig, seed: int = 0) -> dict:
     inp = mi.make_inputs(cfg, device="cuda", seed=seed, expert_weights=reuse)
     if reuse is None:
         _weights_cache.clear()  # keep at most one large weight set resident
+        _host_cache.clear()     # its host copies go with it
         _weights_cache[key] = inp
     return inp
 
@@ -46,7 +47,9 @@ _host_cache: dict = {}
 
 
 def host(inp: dict, keys=None) -> dict:
-    """numpy copies for the oracle (weights cached by identity)."""
+    """numpy copies for the oracle.  Weight copies are cached per device tensor;
+    each entry keeps its tensor alive, so the address in the key cannot be
+    handed to a different tensor while the entry exists."""
     out = {}
     for k, v in inp.items():
         if keys is not None and k not in keys:
@@ -54,13 +57,14 @@ def host(inp: dict, keys=None) -> dict:
         if v is None:
             out[k] = None
             continue
-        ck = (k, v.data_ptr(), tuple(v.shape))
-        if k not in ("x", "router_w", "router_bias") and ck in _host_cache:
-            out[k] = _host_cache[ck]
+        ck = (k, v.data_ptr(), tuple(v.shape), v.dtype)
+        hit = _host_cache.get(ck)
+        if k not in ("x", "router_w", "router_bias") and hit is not None and hit[0] is v:
+            out[k] = hit[1]
             continue
         a = mi.to_numpy({k: v})[k]
         if k not in ("x", "router_w", "router_bias"):
-            _host_cache[ck] = a
+            _host_cache[ck] = (v, a)
         out[k] = a
     return out
 
@@ -100,7 +104,12 @@ def problem(cfg: mi.MoEConfig, packed: bool = False):
     if cfg.shared_bf16:
         flags |= m.F_SHARED_BF16
     return m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, latent=cfg.L,
-                          wfmt=m.W_MXFP4 if cfg.wfmt == "mxfp4" else m.W_FP8, flags=flags)
+                          wfmt=wfmt_code(cfg), flags=flags)
+
+
+def wfmt_code(cfg: mi.MoEConfig) -> int:
+    m = lib()
+    return {"fp8": m.W_FP8, "mxfp4": m.W_MXFP4, "fp8_block": m.W_FP8_BLOCK}[cfg.wfmt]
 
 
 def workspace(p) -> torch.Tensor:
@@ -117,7 +126,17 @@ def bf16_values(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
+    """Half a bf16 unit in the last place at |v| (8 significant bits)."""
+    a = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
+
+
 def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
+    """The bars on the fp32-accumulated output: relative L2 <= REL_L2 and
+    max-abs <= MAX_ABS_RMS x output RMS.  ``got`` is the layer's stored bf16
+    output, whose final rounding adds at most half a bf16 ulp of each element
+    on top of the accumulated value, so the max-abs bar allows that too."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape
@@ -125,9 +144,11 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
     rms = np.sqrt(np.mean(ref ** 2))
     err = got - ref
     rel = np.sqrt(np.sum(err ** 2)) / max(np.sqrt(np.sum(ref ** 2)), 1e-30)
-    mx = np.max(np.abs(err)) if err.size else 0.0
+    excess = np.abs(err) - bf16_half_ulp(got)
+    mx = np.max(excess) if err.size else 0.0
     assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2}"
-    assert mx <= MAX_ABS_RMS * rms, f"{what}: max-abs error {mx:.3e} > {MAX_ABS_RMS} x RMS {rms:.3e}"
+    assert mx <= MAX_ABS_RMS * rms, (
+        f"{what}: max-abs error beyond the bf16 store {mx:.3e} > {MAX_ABS_RMS} x RMS {rms:.3e}")
     return rel, mx / max(rms, 1e-30)
 
 

@@ -168,7 +168,8 @@ def _check_expert_ffn(orc, cfg, rows_sample, act=0):
         rows = G.sample_tokens(cfg.R, rows_sample, seed=3)
     e_of = np.searchsorted(off, rows, side="right") - 1
     off_sub = np.concatenate([[0], np.cumsum(np.bincount(e_of, minlength=cfg.E))]).astype(np.int32)
-    ref = orc.expert_rows(orc.FP8, off_sub, xq[rows], xs[rows], row_w[rows], h["w13"],
+    fmt = orc.FP8_BLOCK if cfg.wfmt == "fp8_block" else orc.FP8
+    ref = orc.expert_rows(fmt, off_sub, xq[rows], xs[rows], row_w[rows], h["w13"],
                           h["w13_scale"], h["w2"], h["w2_scale"], act=act)
     G.assert_close(got[rows], ref, f"expert_ffn {cfg.name}")
 
