@@ -288,6 +288,45 @@ __global__ void __launch_bounds__(256)
   if (threadIdx.x == 0) hs[r] = s;
 }
 
+// The same per-row requantisation with one warp per row: the row (I <= 32 *
+// 8 * MAXV elements) stays in registers between the max and the quantisation,
+// and the max is a shuffle reduction, so many rows are in flight per SM.
+template <int MAXV>
+__global__ void __launch_bounds__(256)
+    requant_warp_kernel(const uint16_t* __restrict__ h, uint8_t* __restrict__ hq,
+                        float* __restrict__ hs, int rows, int I) {
+  const int r = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint4* hr = reinterpret_cast<const uint4*>(h + (size_t)r * I);
+  const int nv = I / 8;
+  uint4 v[MAXV];
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int i = lane + 32 * j;
+    if (i < nv) {
+      v[j] = __ldcs(hr + i);
+      float f[8];
+      unpack_bf16x8(v[j], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+    }
+  }
+  amax = warp_max(amax);
+  const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int i = lane + 32 * j;
+    if (i < nv) {
+      float f[8];
+      unpack_bf16x8(v[j], f);
+      *reinterpret_cast<uint2*>(hq + (size_t)r * I + (size_t)i * 8) = quant8(f, s);
+    }
+  }
+  if (lane == 0) hs[r] = s;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 p = __floats2bfloat162_rn(a, b);  // a -> low half
   return *reinterpret_cast<uint32_t*>(&p);
@@ -475,8 +514,20 @@ cudaError_t launch_quant_scatter(const void* x, const int32_t* perm, void* xq, f
 cudaError_t launch_requant(const void* h, void* hq, float* hs, int rows, int I, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   count_launch();
-  requant_kernel<<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(h), static_cast<uint8_t*>(hq),
-                                      hs, I);
+  const auto* hp = static_cast<const uint16_t*>(h);
+  auto* qp = static_cast<uint8_t*>(hq);
+  const unsigned warps_blocks = (unsigned)(((size_t)rows * 32 + 255) / 256);
+  const int per_lane = (I / 8 + 31) / 32;  // 16-byte vectors per lane
+  if (per_lane <= 4)
+    requant_warp_kernel<4><<<warps_blocks, 256, 0, s>>>(hp, qp, hs, rows, I);
+  else if (per_lane <= 8)
+    requant_warp_kernel<8><<<warps_blocks, 256, 0, s>>>(hp, qp, hs, rows, I);
+  else if (per_lane <= 12)  // I = 3072: fewer registers, more rows per SM
+    requant_warp_kernel<12><<<warps_blocks, 256, 0, s>>>(hp, qp, hs, rows, I);
+  else if (per_lane <= 16)
+    requant_warp_kernel<16><<<warps_blocks, 256, 0, s>>>(hp, qp, hs, rows, I);
+  else
+    requant_kernel<<<rows, 256, 0, s>>>(hp, qp, hs, I);
   return cudaGetLastError();
 }
 
