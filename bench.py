@@ -165,8 +165,9 @@ def dist_setup(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        dist.init_process_group(backend=backend)
+        if not dist.is_initialized():
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
     if torch.cuda.is_available():
         torch.cuda.set_device(local)
     return ws, rank, local
@@ -181,6 +182,13 @@ def max_over_ranks(v: float, ws: int) -> float:
     t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_value(units_per_rank: float, ms: float, ws: int):
+    """Whole-job throughput of ws independent replicas: the units all ranks
+    processed over the slowest rank's time.  Returns (value per second, max ms)."""
+    ms_max = max_over_ranks(ms, ws)
+    return ws * units_per_rank / (ms_max * 1e-3), ms_max
 
 
 def barrier(ws: int):
@@ -332,7 +340,6 @@ def run_ours(args, cfg):
     stage_ms, stage_n = m.moe_profile_read()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1) / args.steps
-    ms_max = max_over_ranks(ms, ws_n)
     rc = m.moe_get_last_error()
     if rc != 0:
         raise SystemExit(f"device error word {rc} after the timed region")
@@ -352,11 +359,9 @@ def run_ours(args, cfg):
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws_n)
-
     bytes_step = work["bytes"]
-    value = ws_n * bytes_step / (ms_max * 1e-3) / 1e9
-    e2e_value = ws_n * bytes_step / (e2e_ms * 1e-3) / 1e9
+    value, ms_max = replica_value(bytes_step / 1e9, ms, ws_n)
+    e2e_value, e2e_ms = replica_value(bytes_step / 1e9, e0.elapsed_time(e1) / e2e_steps, ws_n)
     hbm, bf16, bf16_sus, src = peaks()
     ffn1_ms = stage_ms["ffn1"] / max(stage_n["ffn1"], 1)
     ffn1_bytes = acc.ffn1_launch_bytes(cfg, touched)
