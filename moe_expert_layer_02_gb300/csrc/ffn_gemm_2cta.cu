@@ -285,29 +285,36 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const bool valid = r < it.z && (unsigned)row < (unsigned)g.rows_total;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * P_N;
       uint16_t* orow = static_cast<uint16_t*>(g.out) + (size_t)(valid ? row : 0) * g.ldo;
+      // Columns in groups of 32 (two tcgen05.ld x16 per operand), software
+      // pipelined: the next group's tensor-memory loads are in flight while this
+      // group is scaled and stored, so the load latency is paid once per tile.
       if (EPI == EPI_SWIGLU) {
         const int f0 = nb * 128;
         const float* sc = KIND == KIND_FP8
                               ? (shared ? g.ws_scale : g.w_scale + (size_t)it.x * g.scale_stride)
                               : nullptr;
         const float xs = KIND == KIND_FP8 ? (valid ? g.xscale[row] : 0.0f) : 1.0f;
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 16) {
-          uint32_t vg[16], vu[16];
+        uint32_t va[4][16], vb[4][16];  // g lo, g hi, u lo, u hi
+        auto load = [&](uint32_t (&v)[4][16], int c) {
           __syncwarp();
-          tmem_ld16(tbase + c, vg);
-          tmem_ld16(tbase + 128 + c, vu);
-          tmem_ld_wait();
-          uint32_t packed[8];
+          tmem_ld16(tbase + c, v[0]);
+          tmem_ld16(tbase + c + 16, v[1]);
+          tmem_ld16(tbase + 128 + c, v[2]);
+          tmem_ld16(tbase + 128 + c + 16, v[3]);
+        };
+        auto emit = [&](const uint32_t (&v)[4][16], int c) {
+          uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 16; j += 2) {
+          for (int j = 0; j < 32; j += 2) {
             float hv[2];
 #pragma unroll
             for (int u2 = 0; u2 < 2; ++u2) {
-              float gg = __uint_as_float(vg[j + u2]), uu = __uint_as_float(vu[j + u2]);
+              const int jj = j + u2;
+              float gg = __uint_as_float(v[jj >> 4][jj & 15]);
+              float uu = __uint_as_float(v[2 + (jj >> 4)][jj & 15]);
               if (KIND == KIND_FP8) {
-                gg = (gg * xs) * __ldg(sc + f0 + c + j + u2);
-                uu = (uu * xs) * __ldg(sc + g.I + f0 + c + j + u2);
+                gg = (gg * xs) * __ldg(sc + f0 + c + jj);
+                uu = (uu * xs) * __ldg(sc + g.I + f0 + c + jj);
               }
               hv[u2] = gated_act(g.act, gg, uu);
             }
@@ -315,9 +322,22 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + f0 + c);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                  packed[4 * i + 3]);
           }
+        };
+        load(va, 0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 128; c += 64) {
+          load(vb, c + 32);
+          emit(va, c);
+          tmem_ld_wait();
+          if (c + 64 < 128) load(va, c + 64);
+          emit(vb, c + 32);
+          tmem_ld_wait();
         }
       } else {
         const int c0 = nb * P_N;
@@ -326,16 +346,18 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                             : nullptr;
         const float hs = EPI == EPI_DOWN ? (valid ? g.hs[row] : 0.0f) : 1.0f;
         const float rw = (EPI == EPI_DOWN && valid && !shared && g.row_w) ? g.row_w[row] : 1.0f;
-#pragma unroll 1
-        for (int c = 0; c < P_N; c += 16) {
-          uint32_t v[16];
+        uint32_t va[2][16], vb[2][16];
+        auto load = [&](uint32_t (&v)[2][16], int c) {
           __syncwarp();
-          tmem_ld16(tbase + c, v);
-          tmem_ld_wait();
-          uint32_t packed[8];
+          tmem_ld16(tbase + c, v[0]);
+          tmem_ld16(tbase + c + 16, v[1]);
+        };
+        auto emit = [&](const uint32_t (&v)[2][16], int c) {
+          uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            float y0 = __uint_as_float(v[j]), y1 = __uint_as_float(v[j + 1]);
+          for (int j = 0; j < 32; j += 2) {
+            float y0 = __uint_as_float(v[j >> 4][j & 15]);
+            float y1 = __uint_as_float(v[(j + 1) >> 4][(j + 1) & 15]);
             if (EPI == EPI_DOWN) {
               y0 = ((y0 * hs) * __ldg(sc + c0 + c + j)) * rw;
               y1 = ((y1 * hs) * __ldg(sc + c0 + c + j + 1)) * rw;
@@ -344,9 +366,22 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c0 + c);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                  packed[4 * i + 3]);
           }
+        };
+        load(va, 0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < P_N; c += 64) {
+          load(vb, c + 32);
+          emit(va, c);
+          tmem_ld_wait();
+          if (c + 64 < P_N) load(va, c + 64);
+          emit(vb, c + 32);
+          tmem_ld_wait();
         }
       }
       tc_fence_before();
