@@ -332,46 +332,59 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// One thread per 8 output columns; the grid covers (token, column slice) so a
+// decode-sized batch still fills the GPU.  All k rows of the thread's columns
+// are loaded before the fp32 sum (j ascending, shared expert last), so the
+// loads overlap.
+template <int KMAX>
 __global__ void __launch_bounds__(256)
     combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ perm,
                    const uint16_t* __restrict__ shared, uint16_t* __restrict__ out, int H, int k,
                    int R, int* err) {
-  __shared__ int s_rows[kMaxTopK];
   const int t = blockIdx.x;
-  if (threadIdx.x < k) {
-    int row = perm[(size_t)t * k + threadIdx.x];
-    if ((unsigned)row >= (unsigned)R) {  // invalid permutation entry: contributes nothing
-      record_error(err, kErrInvalidArg);
-      row = -1;
-    }
-    s_rows[threadIdx.x] = row;
-  }
-  __syncthreads();
+  const int v = blockIdx.y * blockDim.x + threadIdx.x;  // 16-byte column group
   const int nv = H / 8;
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    float acc[8];
+  int rows[KMAX];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      if (s_rows[j] < 0) continue;
-      float f[8];
-      unpack_bf16x8(reinterpret_cast<const uint4*>(y + (size_t)s_rows[j] * H)[v], f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+  for (int j = 0; j < KMAX; ++j) {
+    int row = -1;
+    if (j < k) {
+      row = __ldg(perm + (size_t)t * k + j);
+      if ((unsigned)row >= (unsigned)R) {  // invalid permutation entry: contributes nothing
+        if (v == 0) record_error(err, kErrInvalidArg);
+        row = -1;
+      }
     }
-    if (shared) {
-      float f[8];
-      unpack_bf16x8(reinterpret_cast<const uint4*>(shared + (size_t)t * H)[v], f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += f[i];
-    }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = o;
+    rows[j] = row;
   }
+  if (v >= nv) return;
+  uint4 raw[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    if (rows[j] >= 0) raw[j] = __ldcs(reinterpret_cast<const uint4*>(y + (size_t)rows[j] * H) + v);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (rows[j] < 0) continue;
+    float f[8];
+    unpack_bf16x8(raw[j], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += f[i];
+  }
+  if (shared) {
+    float f[8];
+    unpack_bf16x8(reinterpret_cast<const uint4*>(shared + (size_t)t * H)[v], f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += f[i];
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = o;
 }
 
 // LatentMoE: the routed combine feeds RMSNorm on the latent ("Kimi K3 ...
@@ -533,10 +546,20 @@ cudaError_t launch_requant(const void* h, void* hq, float* hs, int rows, int I, 
 
 cudaError_t launch_combine(const void* y, const int32_t* perm, const void* shared, void* out,
                            int T, int H, int k, int* err, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
   count_launch();
-  combine_kernel<<<T, 256, 0, s>>>(static_cast<const uint16_t*>(y), perm,
-                                   static_cast<const uint16_t*>(shared),
-                                   static_cast<uint16_t*>(out), H, k, T * k, err);
+  const dim3 grid(T, (H / 8 + 255) / 256);
+  const auto* yp = static_cast<const uint16_t*>(y);
+  const auto* sp = static_cast<const uint16_t*>(shared);
+  auto* op = static_cast<uint16_t*>(out);
+  if (k <= 4)
+    combine_kernel<4><<<grid, 256, 0, s>>>(yp, perm, sp, op, H, k, T * k, err);
+  else if (k <= 8)
+    combine_kernel<8><<<grid, 256, 0, s>>>(yp, perm, sp, op, H, k, T * k, err);
+  else if (k <= 16)
+    combine_kernel<16><<<grid, 256, 0, s>>>(yp, perm, sp, op, H, k, T * k, err);
+  else
+    combine_kernel<32><<<grid, 256, 0, s>>>(yp, perm, sp, op, H, k, T * k, err);
   return cudaGetLastError();
 }
 
