@@ -64,7 +64,9 @@ constexpr int pow2_at_least(int v) {
 template <bool FFN1, int BN, bool BLK>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK;  // one weight box, 16 KB
-  static constexpr int NA = FFN1 ? 2 : 1;  // W1 and W3 boxes for FFN1
+  // two 128-row weight blocks per stage sharing the activation tile: W1 and
+  // W3 block nb (FFN1), W2 blocks 2nb and 2nb+1 (FFN2)
+  static constexpr int NA = 2;
   static constexpr int B_BYTES = BN * BK;
   static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
   static constexpr int STAGES = cmin(kSmemBudget / STAGE_BYTES, 12);
@@ -95,10 +97,16 @@ __device__ __forceinline__ uint32_t f32_bits_to_bf16(float v) {
 // entries l, l+32, l+64, l+96 (KB <= 128).
 constexpr int kHeld = 4;
 
+// 128-row block index of weight block b (0, 1) of tile column nb.
+template <bool FFN1>
+__device__ __forceinline__ int wblock(const GroupedFfnArgs& a, int b, int nb) {
+  return FFN1 ? (b == 0 ? nb : a.I / BM + nb) : 2 * nb + b;
+}
+
 template <bool FFN1>
 __device__ __forceinline__ void load_block_scales(const GroupedFfnArgs& a, int item, int nb,
-                                                  int KB, int lane, float (&held)[FFN1 ? 2 : 1][kHeld]) {
-  constexpr int NA = FFN1 ? 2 : 1;
+                                                  int KB, int lane, float (&held)[2][kHeld]) {
+  constexpr int NA = 2;
   const int4 it = a.items[item];
   const bool shared = it.x >= a.E;
   const int wrow_blocks = FFN1 ? 2 * a.I / BM : a.K / BM;
@@ -106,11 +114,13 @@ __device__ __forceinline__ void load_block_scales(const GroupedFfnArgs& a, int i
                             : (shared ? a.sw2_scale : a.w2_scale + (size_t)it.x * wrow_blocks * KB);
 #pragma unroll
   for (int b = 0; b < NA; ++b) {
-    const float* srow = sbase + (size_t)(b == 0 ? nb : a.I / BM + nb) * KB;
+    const int blk = wblock<FFN1>(a, b, nb);
+    const float* srow = sbase + (size_t)blk * KB;
+    const bool have = blk < wrow_blocks;  // FFN2 with K % 256 == 128: no second block
 #pragma unroll
     for (int i = 0; i < kHeld; ++i) {
       const int kb = i * 32 + lane;
-      held[b][i] = kb < KB ? __ldg(srow + kb) : 0.0f;
+      held[b][i] = (have && kb < KB) ? __ldg(srow + kb) : 0.0f;
     }
   }
 }
@@ -122,12 +132,12 @@ __device__ __forceinline__ void load_block_scales(const GroupedFfnArgs& a, int i
 template <bool FFN1, int BN, int ACC_COLS, int PBUF>
 __device__ __forceinline__ bool block_epilogue(const GroupedFfnArgs& a, uint32_t tmem, int q,
                                                int lane, int item, int nb, int KB,
-                                               const float (&held)[FFN1 ? 2 : 1][kHeld],
+                                               const float (&held)[2][kHeld],
                                                int next_item, int next_nb,
-                                               float (&held_next)[FFN1 ? 2 : 1][kHeld],
+                                               float (&held_next)[2][kHeld],
                                                uint64_t* tfull, uint64_t* tempty,
                                                volatile int* s_abort, int& pcount) {
-  constexpr int NA = FFN1 ? 2 : 1;
+  constexpr int NA = 2;
   constexpr int RL = (BN + 31) / 32;  // rows per lane for the per-row scalars
   const int4 it = a.items[item];
   const bool shared = it.x >= a.E;
@@ -182,7 +192,8 @@ __device__ __forceinline__ bool block_epilogue(const GroupedFfnArgs& a, uint32_t
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&tempty[pb]));
   }
-  const int f = nb * BM + q * 32 + lane;  // feature (FFN1) / output channel (FFN2)
+  const int f = nb * BM + q * 32 + lane;        // FFN1: feature
+  const int f2 = 2 * nb * BM + q * 32 + lane;   // FFN2: output channel of block 0
 #pragma unroll
   for (int j = 0; j < BN; ++j) {
     const float sj = __shfl_sync(0xffffffffu, rs[j / 32], j % 32);
@@ -192,9 +203,10 @@ __device__ __forceinline__ bool block_epilogue(const GroupedFfnArgs& a, uint32_t
       if (FFN1) {
         const float hv = gated_act(a.act, acc[0][j] * sj, acc[NA - 1][j] * sj);
         static_cast<uint16_t*>(a.h)[(size_t)row * a.I + f] = (uint16_t)f32_bits_to_bf16(hv);
-      } else {
-        static_cast<uint16_t*>(a.y)[(size_t)row * a.K + f] =
-            (uint16_t)f32_bits_to_bf16((acc[0][j] * sj) * wj);
+      } else {  // output channels f (block 2nb) and f + 128 (block 2nb + 1)
+        uint16_t* yr = static_cast<uint16_t*>(a.y) + (size_t)row * a.K;
+        yr[f2] = (uint16_t)f32_bits_to_bf16((acc[0][j] * sj) * wj);
+        if (f2 + BM < a.K) yr[f2 + BM] = (uint16_t)f32_bits_to_bf16((acc[1][j] * sj) * wj);
       }
     }
   }
@@ -247,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  const int NB = FFN1 ? a.I / BM : a.K / BM;  // output blocks per item
+  const int NB = FFN1 ? a.I / BM : (a.K + 2 * BM - 1) / (2 * BM);  // tiles per item
   const int KB = FFN1 ? a.K / BK : a.I / BK;  // K stages per tile
   const int n_items = min(*a.n_items, a.max_items);
   const int n_tiles = n_items * NB;
@@ -272,12 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          // (rows past the last block, FFN2 with K % 256 == 128, read as zeros)
           if (a.packed) {  // tile-major weights: tile (row block, k block) is contiguous
-            tma_load_3d(st, tw, 0, BM * (nb * KB + kb), gc, fb);
-            if (FFN1) tma_load_3d(st + C::A_BYTES, tw, 0, BM * ((a.I / BM + nb) * KB + kb), gc, fb);
+            tma_load_3d(st, tw, 0, BM * (wblock<FFN1>(a, 0, nb) * KB + kb), gc, fb);
+            tma_load_3d(st + C::A_BYTES, tw, 0, BM * (wblock<FFN1>(a, 1, nb) * KB + kb), gc, fb);
           } else {
-            tma_load_3d(st, tw, kb * BK, nb * BM, gc, fb);
-            if (FFN1) tma_load_3d(st + C::A_BYTES, tw, kb * BK, a.I + nb * BM, gc, fb);
+            tma_load_3d(st, tw, kb * BK, wblock<FFN1>(a, 0, nb) * BM, gc, fb);
+            tma_load_3d(st + C::A_BYTES, tw, kb * BK, wblock<FFN1>(a, 1, nb) * BM, gc, fb);
           }
           tma_load_2d(st + C::NA * C::A_BYTES, &tm_x, kb * BK, it.y, fb);
           s_issued[stage] = phase + 1u;
@@ -320,9 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = smem_desc_sw128(b0 + kk * UMMA_K);
             const uint32_t accum = kk ? 1u : 0u;
             mma_f8f6f4(d0, smem_desc_sw128(a0 + kk * UMMA_K), bdesc, idesc, accum);
-            if (FFN1)
-              mma_f8f6f4(d0 + BN, smem_desc_sw128(a0 + C::A_BYTES + kk * UMMA_K), bdesc, idesc,
-                         accum);
+            mma_f8f6f4(d0 + BN, smem_desc_sw128(a0 + C::A_BYTES + kk * UMMA_K), bdesc, idesc,
+                       accum);
           }
           issued_any = true;
           mma_commit(smem_u32(&empty[stage]));
@@ -365,9 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = smem_desc_sw128(b0 + kk * UMMA_K);
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             mma_f8f6f4(d0, smem_desc_sw128(a0 + kk * UMMA_K), bdesc, idesc, accum);
-            if (FFN1)
-              mma_f8f6f4(d0 + BN, smem_desc_sw128(a0 + C::A_BYTES + kk * UMMA_K), bdesc, idesc,
-                         accum);
+            mma_f8f6f4(d0 + BN, smem_desc_sw128(a0 + C::A_BYTES + kk * UMMA_K), bdesc, idesc,
+                       accum);
           }
           issued_any = true;
           mma_commit(smem_u32(&empty[stage]));  // frees the stage once these MMAs finish
@@ -423,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * C::ACC_COLS;
-      const int f = nb * BM + q * 32 + lane;  // feature (FFN1) / output channel (FFN2)
+      const int f = nb * BM + q * 32 + lane;  // feature (FFN1)
       if (FFN1) {
         const float* sc = shared ? a.sw13_scale : a.w13_scale + (size_t)it.x * 2 * a.I;
         const float sg = sc[f], su = sc[a.I + f];
@@ -447,14 +458,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else {
+      } else {  // output channels f2 (block 2nb) and f2 + 128 (block 2nb + 1)
+        const int f2 = 2 * nb * BM + q * 32 + lane;
+        const bool two = f2 + BM < a.K;
         const float* sc = shared ? a.sw2_scale : a.w2_scale + (size_t)it.x * a.K;
-        const float s2 = sc[f];
+        const float s2a = sc[f2], s2b = two ? sc[f2 + BM] : 0.0f;
         uint16_t* yout = static_cast<uint16_t*>(a.y);
         for (int c0 = 0; c0 < rows; c0 += 16) {
-          uint32_t v[16];
+          uint32_t va[16], vb[16];
           __syncwarp();
-          tmem_ld16(tbase + c0, v);
+          tmem_ld16(tbase + c0, va);
+          tmem_ld16(tbase + BN + c0, vb);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -462,8 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = row0 + r;
             if (r < rows && (unsigned)row < (unsigned)a.rows_total) {
               const float rw = (!shared && a.row_w) ? a.row_w[row] : 1.0f;
-              const float yv = ((__uint_as_float(v[j]) * a.hs[row]) * s2) * rw;
-              yout[(size_t)row * a.K + f] = (uint16_t)f32_bits_to_bf16(yv);
+              const float hs = a.hs[row];
+              uint16_t* yr = yout + (size_t)row * a.K;
+              yr[f2] = (uint16_t)f32_bits_to_bf16(((__uint_as_float(va[j]) * hs) * s2a) * rw);
+              if (two)
+                yr[f2 + BM] = (uint16_t)f32_bits_to_bf16(((__uint_as_float(vb[j]) * hs) * s2b) * rw);
             }
           }
         }
