@@ -315,8 +315,12 @@ cudaError_t launch_router_logits(const void* x, const float* wr, const float* bi
     return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
   if (env && std::strcmp(env, "8x16") == 0)
     return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
+  // (also when they make one wave of at least half the SMs: T=512, E=256 runs
+  // in 68 us with large tiles vs 75 us with small ones; T=2048 and T=64 prefer
+  // the small ones)
   const long big_blocks = (long)((T + 31) / 32) * ((E + 31) / 32);
-  if (big_blocks >= 2L * device_sm_count())
+  const long sms = device_sm_count();
+  if (big_blocks >= 2L * sms || (2L * big_blocks >= sms && big_blocks <= sms))
     return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
   return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
 }
