@@ -299,11 +299,11 @@ def run_ours(args, cfg):
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(x=None):
+    def step(x=None, y=None):
         m.moe_forward(p, inp["x"] if x is None else x, inp["router_w"], inp["router_bias"],
                       inp["w13"], inp["w13_scale"], inp["w2"], inp["w2_scale"], inp["sw13"],
                       inp["sw13_scale"], inp["sw2"], inp["sw2_scale"], inp["wd"], inp["wu"],
-                      inp["gamma"], out, wsb)
+                      inp["gamma"], out if y is None else y, wsb)
 
     # touched experts (for algorithmic bytes): routing through the library itself
     logits = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
@@ -321,10 +321,20 @@ def run_ours(args, cfg):
     if rc != 0:
         raise SystemExit(f"device error word {rc} after warm-up")
 
-    clocks = ClockSampler(local)
-    time.sleep(0.2)
+    # per-stage breakdown from a short loop with every stage timed
     m.moe_profile_read()
     m.moe_profile_enable(True)
+    for _ in range(min(args.steps, 20)):
+        step()
+    torch.cuda.synchronize()
+    m.moe_profile_enable(False)
+    stage_ms, stage_n = m.moe_profile_read()
+
+    # the timed region: only the FFN1 launches are bracketed by events (for the
+    # roofline's live kernel time), so the step itself runs as a user's would
+    clocks = ClockSampler(local)
+    time.sleep(0.2)
+    m.moe_profile_enable(True, stages=["ffn1"])
     n0 = m.moe_launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws_n)
@@ -337,33 +347,59 @@ def run_ours(args, cfg):
     barrier(ws_n)
     launches = m.moe_launch_count() - n0
     m.moe_profile_enable(False)
-    stage_ms, stage_n = m.moe_profile_read()
+    ffn1_live_ms, ffn1_live_n = m.moe_profile_read()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1) / args.steps
     rc = m.moe_get_last_error()
     if rc != 0:
         raise SystemExit(f"device error word {rc} after the timed region")
 
-    # end to end through the public call with host buffers
+    # end to end through the public call with host buffers: every step's x is
+    # copied in from pinned host memory and its output copied back, on a copy
+    # stream with two device buffers each way, so step i+1's upload and step
+    # i's download overlap step i's layer (as a serving loop would run them)
     x_host = inp["x"].cpu().pin_memory()
     out_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(inp["x"])
+    x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
+    y_dev = [torch.empty_like(out) for _ in range(2)]
+    copy = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    ev_in, ev_done, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(args.steps // 2, 3)
     barrier(ws_n)
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        step(x_dev)
-        out_host.copy_(out, non_blocking=True)
+    e0.record(copy)
+    with torch.cuda.stream(copy):
+        x_dev[0].copy_(x_host, non_blocking=True)
+        ev_in[0].record(copy)
+    for i in range(e2e_steps):
+        b = i & 1
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])  # step i-2's output has left y_dev[b]
+        step(x_dev[b], y_dev[b])
+        ev_done[b].record(stream)
+        with torch.cuda.stream(copy):
+            if i + 1 < e2e_steps:
+                if i >= 1:
+                    copy.wait_event(ev_done[b ^ 1])  # step i-1 no longer reads x_dev[b^1]
+                x_dev[b ^ 1].copy_(x_host, non_blocking=True)
+                ev_in[b ^ 1].record(copy)
+            copy.wait_event(ev_done[b])
+            out_host.copy_(y_dev[b], non_blocking=True)
+            ev_out[b].record(copy)
+    stream.wait_event(ev_out[(e2e_steps - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
+    # the pipelined steps computed the same layer
+    if not torch.equal(y_dev[(e2e_steps - 1) & 1], out):
+        raise SystemExit("end-to-end output differs from the device-timed output")
     bytes_step = work["bytes"]
     value, ms_max = replica_value(bytes_step / 1e9, ms, ws_n)
     e2e_value, e2e_ms = replica_value(bytes_step / 1e9, e0.elapsed_time(e1) / e2e_steps, ws_n)
     hbm, bf16, bf16_sus, src = peaks()
-    ffn1_ms = stage_ms["ffn1"] / max(stage_n["ffn1"], 1)
+    ffn1_ms = ffn1_live_ms["ffn1"] / max(ffn1_live_n["ffn1"], 1)
     ffn1_bytes = acc.ffn1_launch_bytes(cfg, touched)
     ffn1_flops = acc.ffn1_flops(cfg.R + (cfg.T if cfg.I_s else 0), cfg.K, cfg.I)
     traffic = kernel_traffic("ffn1", cfg.name)

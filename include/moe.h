@@ -301,12 +301,13 @@ int moe_watchdog_selftest(int32_t* role_status, void* stream);
  * Host-side counter, for accounting; never reset. */
 int64_t moe_launch_count(void);
 
-/* Per-stage device timing.  While enabled, every stage launch is bracketed by
- * CUDA events recorded on the launching stream.  moe_profile_read waits for
- * the recorded events, writes the summed milliseconds and launch counts per
- * stage (MOE_STAGE_*, arrays of MOE_STAGE_COUNT) and clears the record.
- * Returns MOE_OK, or MOE_ERR_CUDA. */
-int moe_profile_enable(int on);
+/* Per-stage device timing.  mask selects the stages to time (bit s = stage
+ * MOE_STAGE_s; -1 = all, 0 = off); each launch of a selected stage is
+ * bracketed by CUDA events recorded on the launching stream.  moe_profile_read
+ * waits for the recorded events, writes the summed milliseconds and launch
+ * counts per stage (MOE_STAGE_*, arrays of MOE_STAGE_COUNT) and clears the
+ * record.  Returns MOE_OK, or MOE_ERR_CUDA. */
+int moe_profile_enable(int mask);
 int moe_profile_read(double* stage_ms, int64_t* stage_launches);
 
 #ifdef __cplusplus

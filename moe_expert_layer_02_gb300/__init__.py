@@ -199,8 +199,10 @@ def moe_launch_count() -> int:
     return int(load_library().moe_launch_count())
 
 
-def moe_profile_enable(on: bool = True):
-    load_library().moe_profile_enable(1 if on else 0)
+def moe_profile_enable(on: bool = True, stages=None):
+    """Time every stage (on), the named STAGES only (stages=[...]), or none."""
+    mask = 0 if not on else -1 if stages is None else sum(1 << STAGES.index(s) for s in stages)
+    load_library().moe_profile_enable(mask)
 
 
 def moe_profile_read():

@@ -55,7 +55,7 @@ struct ProfRec {
   int stage;
   cudaEvent_t a, b;
 };
-std::atomic<bool> g_prof_on{false};
+std::atomic<uint32_t> g_prof_mask{0};  // bit s: time stage s
 std::mutex g_prof_mu;
 std::vector<ProfRec> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
@@ -76,7 +76,7 @@ struct StageTimer {
   cudaStream_t s;
   cudaEvent_t a = nullptr;
   StageTimer(int st, cudaStream_t str) : stage(st), s(str) {
-    if (g_prof_on.load(std::memory_order_relaxed)) {
+    if (g_prof_mask.load(std::memory_order_relaxed) & (1u << st)) {
       std::lock_guard<std::mutex> lk(g_prof_mu);
       a = take_event();
       if (a) cudaEventRecord(a, s);
@@ -624,8 +624,8 @@ int moe_get_last_error(void* stream) {
 
 int64_t moe_launch_count(void) { return g_launches.load(); }
 
-int moe_profile_enable(int on) {
-  g_prof_on.store(on != 0);
+int moe_profile_enable(int mask) {
+  g_prof_mask.store(static_cast<uint32_t>(mask));
   return MOE_OK;
 }
 

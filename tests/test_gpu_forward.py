@@ -110,6 +110,14 @@ def test_profile_counts_each_stage():
     assert all(n[k] == 2 for k in base), n
     assert all(ms[k] > 0 for k in base), ms
     assert all(n[k] == 0 for k in n if k not in base)  # LatentMoE stages idle
+    # a stage mask times the named stages only
+    m.moe_profile_enable(True, stages=["ffn1", "combine"])
+    try:
+        run_forward(cfg, inp)
+        ms, n = m.moe_profile_read()
+    finally:
+        m.moe_profile_enable(False)
+    assert n["ffn1"] == 1 and n["combine"] == 1 and sum(n.values()) == 2, n
 
 
 def test_empty_batch_is_a_noop():
