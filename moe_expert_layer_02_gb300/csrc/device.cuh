@@ -139,10 +139,13 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 // ------------------------------------------------------------------ activation
 // Gated activation times the up projection (FFN1 epilogues): act 0 = SwiGLU,
 // silu(g) u; act 1 = SiTU, beta tanh(g / beta) sigmoid(g) u with beta = 4
-// ("Kimi K3 ... feasibility analysis", s.2.6).
+// ("Kimi K3 ... feasibility analysis", s.2.6).  The quotient by 1 + e^-g uses
+// the branch-free approximate divide (within 2 ulp; 0 once e^-g passes 2^126,
+// where the exact quotient is below 1e-36), which lets the compiler overlap
+// the epilogue's independent columns.
 __device__ __forceinline__ float gated_act(int act, float g, float u) {
   const float d = 1.0f + expf(-g);
-  return act ? (4.0f * tanhf(0.25f * g)) / d * u : g / d * u;
+  return __fdividef(act ? 4.0f * tanhf(0.25f * g) : g, d) * u;
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -302,6 +305,40 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
       " [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
+}
+
+// Generic-proxy shared-memory writes become visible to later async-proxy reads
+// (tcgen05.cp) of this thread.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Named barrier `id` over `nthreads` threads that also returns the AND of
+// every participant's `pred` (so the participants take the same branch).
+__device__ __forceinline__ int bar_and(int id, int nthreads, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.b32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r;
 }
 
 // ------------------------------------------------------------------ formats

@@ -17,7 +17,10 @@
 // tile's accumulator (128 rows x 256 fp32 columns per CTA) is double-buffered
 // in tensor memory.
 //
-// Epilogues (thread = one activation row, 16 columns per tcgen05.ld):
+// Epilogues (thread = one activation row, 16 columns per tcgen05.ld; the
+// tile's channel scales staged once in shared memory; each warp's 32 rows x 32
+// output columns transposed through a 64-byte-swizzled shared-memory buffer so
+// that four lanes store one row's 64 contiguous bytes):
 //   SWIGLU: columns 0..127 = g (weight rows f0.., staged by CTA 0), columns
 //           128..255 = u (rows I+f0.., staged by CTA 1); h = bf16(silu(g) u),
 //           with the fp8 per-row and per-channel scales when the operands are fp8.
@@ -51,7 +54,13 @@ constexpr int P_STAGES = 6;
 constexpr int P_ACC_STAGES = 2;
 constexpr int P_TMEM_COLS = 512;
 constexpr int P_NUM_BARS = 2 * P_STAGES + 2 * P_ACC_STAGES + 1;
-constexpr int P_SMEM = 1024 + P_STAGES * P_STAGE + P_NUM_BARS * 8 + 16 + P_STAGES * 4;
+constexpr int P_STG_ROW = 64;                   // transposed output: 32 bf16 columns per row
+constexpr int P_STG_BUF = 32 * P_STG_ROW;       // one epilogue warp's 32 rows
+constexpr int P_STG = 4 * 2 * P_STG_BUF;        // 4 epilogue warps, double-buffered (16 KB)
+constexpr int P_SCL = 2 * P_N * 4;              // a tile's channel scales, double-buffered
+constexpr int P_EPI_BAR = 1;                    // named barrier of the 4 epilogue warps
+constexpr int P_SMEM =
+    1024 + P_STAGES * P_STAGE + P_STG + P_SCL + P_NUM_BARS * 8 + 16 + P_STAGES * 4;
 
 enum { KIND_FP8 = 0, KIND_BF16 = 1 };
 enum { EPI_SWIGLU = 0, EPI_DOWN = 1, EPI_STORE = 2 };
@@ -124,7 +133,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE);
+  uint8_t* stg = smem + P_STAGES * P_STAGE;  // output transpose buffers
+  float* s_scl = reinterpret_cast<float*>(stg + P_STG);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + P_STG + P_SCL);
   uint64_t* full = bars;
   uint64_t* empty = bars + P_STAGES;
   uint64_t* tfull = bars + 2 * P_STAGES;
@@ -268,6 +279,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     const int q = warp & 3;
     const int lrow = q * 32 + lane;  // this thread's row within the CTA's half
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    const uint32_t stg_w = smem_u32(stg + q * 2 * P_STG_BUF);
+    const uint32_t swz = (uint32_t)((lane >> 1) & 3);  // 64-byte swizzle of this row's chunks
+    int grp = 0;  // groups stored by this warp (transpose buffer = grp & 1)
     int it_local = 0;
     for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++it_local) {
       const int item = tile / NB, nb = tile - item * NB;
@@ -275,24 +289,61 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const bool shared = g.items && it.x >= g.E;
       const int acc = it_local % P_ACC_STAGES;
       const uint32_t acc_phase = (uint32_t)(it_local / P_ACC_STAGES) & 1u;
+      // this tile's channel scales: two per thread, read before the wait
+      constexpr bool SCALED = KIND == KIND_FP8 && EPI != EPI_STORE;
+      const int cs = EPI == EPI_SWIGLU ? nb * 128 : nb * P_N;  // first scale column
+      const int cs2 = EPI == EPI_SWIGLU ? g.I + nb * 128 : nb * P_N + 128;
+      float sv0 = 0.0f, sv1 = 0.0f;
+      if (SCALED) {
+        const float* sc = shared ? g.ws_scale : g.w_scale + (size_t)it.x * g.scale_stride;
+        sv0 = __ldg(sc + cs + lrow);
+        sv1 = __ldg(sc + cs2 + lrow);
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait(smem_u32(&tfull[acc]), acc_phase, g.err, s_abort) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      float* scl = s_scl + (it_local & 1) * P_N;
+      if (SCALED) {
+        scl[lrow] = sv0;
+        scl[128 + lrow] = sv1;
+      }
+      // the four warps agree on going on, and the scales are visible to all
+      if (!bar_and(P_EPI_BAR, 128, ok)) break;
       tc_fence_after();
       const int r = lrow + 128 * (int)rank;
       const int row = it.y + r;
       const bool valid = r < it.z && (unsigned)row < (unsigned)g.rows_total;
+      const int wr0 = 128 * (int)rank + q * 32;  // this warp's first row within the item
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * P_N;
-      uint16_t* orow = static_cast<uint16_t*>(g.out) + (size_t)(valid ? row : 0) * g.ldo;
+      // 32 bf16 columns of each of the warp's rows at output column `col`: lane
+      // l writes its row's four 16-byte chunks (chunk i at i ^ swz), then reads
+      // chunk l % 4 of rows l / 4 + 8i, so each store covers 8 rows x 64 bytes
+      auto put = [&](const uint32_t (&packed)[16], int col) {
+        const uint32_t buf = stg_w + (uint32_t)(grp & 1) * P_STG_BUF;
+        ++grp;
+        const uint32_t ra = buf + lane * P_STG_ROW;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          st_shared_v4(ra + (((uint32_t)i ^ swz) << 4), packed[4 * i], packed[4 * i + 1],
+                       packed[4 * i + 2], packed[4 * i + 3]);
+        __syncwarp();
+        const int ch = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 8 * i + (lane >> 2);
+          const uint4 v = ld_shared_v4(buf + rr * P_STG_ROW +
+                                       (((uint32_t)ch ^ ((uint32_t)(rr >> 1) & 3u)) << 4));
+          const int orow_i = it.y + wr0 + rr;
+          if (wr0 + rr < it.z && (unsigned)orow_i < (unsigned)g.rows_total)
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.out) + (size_t)orow_i * g.ldo +
+                                      col + 8 * ch) = v;
+        }
+      };
       // Columns in groups of 32 (two tcgen05.ld x16 per operand), software
       // pipelined: the next group's tensor-memory loads are in flight while this
       // group is scaled and stored, so the load latency is paid once per tile.
       if (EPI == EPI_SWIGLU) {
         const int f0 = nb * 128;
-        const float* sc = KIND == KIND_FP8
-                              ? (shared ? g.ws_scale : g.w_scale + (size_t)it.x * g.scale_stride)
-                              : nullptr;
         const float xs = KIND == KIND_FP8 ? (valid ? g.xscale[row] : 0.0f) : 1.0f;
         uint32_t va[4][16], vb[4][16];  // g lo, g hi, u lo, u hi
         auto load = [&](uint32_t (&v)[4][16], int c) {
@@ -305,28 +356,29 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         auto emit = [&](const uint32_t (&v)[4][16], int c) {
           uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float hv[2];
+          for (int j = 0; j < 32; j += 4) {
+            float4 sg = make_float4(1.0f, 1.0f, 1.0f, 1.0f), su = sg;
+            if (KIND == KIND_FP8) {
+              sg = *reinterpret_cast<const float4*>(scl + c + j);
+              su = *reinterpret_cast<const float4*>(scl + 128 + c + j);
+            }
+            const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
+            float hv[4];
 #pragma unroll
-            for (int u2 = 0; u2 < 2; ++u2) {
+            for (int u2 = 0; u2 < 4; ++u2) {
               const int jj = j + u2;
               float gg = __uint_as_float(v[jj >> 4][jj & 15]);
               float uu = __uint_as_float(v[2 + (jj >> 4)][jj & 15]);
               if (KIND == KIND_FP8) {
-                gg = (gg * xs) * __ldg(sc + f0 + c + jj);
-                uu = (uu * xs) * __ldg(sc + g.I + f0 + c + jj);
+                gg = (gg * xs) * sgv[u2];
+                uu = (uu * xs) * suv[u2];
               }
               hv[u2] = gated_act(g.act, gg, uu);
             }
             packed[j / 2] = pack_bf16x2(hv[0], hv[1]);
+            packed[j / 2 + 1] = pack_bf16x2(hv[2], hv[3]);
           }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + f0 + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                  packed[4 * i + 3]);
-          }
+          put(packed, f0 + c);
         };
         load(va, 0);
         tmem_ld_wait();
@@ -341,9 +393,6 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         }
       } else {
         const int c0 = nb * P_N;
-        const float* sc =
-            EPI == EPI_DOWN ? (shared ? g.ws_scale : g.w_scale + (size_t)it.x * g.scale_stride)
-                            : nullptr;
         const float hs = EPI == EPI_DOWN ? (valid ? g.hs[row] : 0.0f) : 1.0f;
         const float rw = (EPI == EPI_DOWN && valid && !shared && g.row_w) ? g.row_w[row] : 1.0f;
         uint32_t va[2][16], vb[2][16];
@@ -355,22 +404,22 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         auto emit = [&](const uint32_t (&v)[2][16], int c) {
           uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float y0 = __uint_as_float(v[j >> 4][j & 15]);
-            float y1 = __uint_as_float(v[(j + 1) >> 4][(j + 1) & 15]);
-            if (EPI == EPI_DOWN) {
-              y0 = ((y0 * hs) * __ldg(sc + c0 + c + j)) * rw;
-              y1 = ((y1 * hs) * __ldg(sc + c0 + c + j + 1)) * rw;
-            }
-            packed[j / 2] = pack_bf16x2(y0, y1);
-          }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0 + c);
+          for (int j = 0; j < 32; j += 4) {
+            float4 s4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+            if (EPI == EPI_DOWN) s4 = *reinterpret_cast<const float4*>(scl + c + j);
+            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+            float yv[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                  packed[4 * i + 3]);
+            for (int u2 = 0; u2 < 4; ++u2) {
+              const int jj = j + u2;
+              float y0 = __uint_as_float(v[jj >> 4][jj & 15]);
+              if (EPI == EPI_DOWN) y0 = ((y0 * hs) * sv[u2]) * rw;
+              yv[u2] = y0;
+            }
+            packed[j / 2] = pack_bf16x2(yv[0], yv[1]);
+            packed[j / 2 + 1] = pack_bf16x2(yv[2], yv[3]);
           }
+          put(packed, c0 + c);
         };
         load(va, 0);
         tmem_ld_wait();

@@ -115,12 +115,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Generic-proxy shared-memory writes become visible to later async-proxy reads
-// (tcgen05.cp) of this thread.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Shared-memory descriptor of a 32-row x 16-byte scale block, no swizzle: 8-row
 // core matrices of 128 contiguous bytes, 128 bytes apart (both offset fields).
 __device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
