@@ -199,21 +199,17 @@ int orc_default_threads(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }
 /* S1: router logits (fp32, canonical order)                                   */
 /* ------------------------------------------------------------------------- */
 
-/* logit[e] = sum_h float(x[h]) * wr[e,h] (+ bias[e]).  Canonical order: 64
- * partial sums q_{l,p} (l = 0..31, p = 0, 1); q_{l,p} takes the h with
- * (h mod 128) / 4 == l and h mod 2 == p, ascending, through fmaf starting from
- * +0 (so lane l of a 128-wide chunk owns h = 4l..4l+3, its even h in q_{l,0}
- * and its odd h in q_{l,1}); then p_l = q_{l,0} + q_{l,1}, p_l += p_{l+off} for
- * off = 16, 8, 4, 2, 1; the logit is p_0, plus bias[e] as one fp32 add.
- * [LING s.6: routing metadata] */
+/* logit[e] = sum_h float(x[h]) * wr[e,h] (+ bias[e]).  Canonical order: 32
+ * partial sums, partial l takes h = l, l+32, l+64, ... ascending through fmaf
+ * starting from +0; then p_l += p_{l+off} for off = 16, 8, 4, 2, 1; the logit is
+ * p_0, plus bias[e] as one fp32 add.  [LING s.6: routing metadata] */
 static float router_logit_one(int64_t H, const uint16_t* xrow, const float* wrow) {
-  float q[32][2], p[32];
-  for (int l = 0; l < 32; l++) q[l][0] = q[l][1] = 0.0f;
-  for (int64_t h = 0; h < H; h++) {
-    const int l = (int)((h % 128) / 4), par = (int)(h % 2);
-    q[l][par] = fmaf(bf16_to_float(xrow[h]), wrow[h], q[l][par]);
-  }
-  for (int l = 0; l < 32; l++) p[l] = q[l][0] + q[l][1];
+  float p[32];
+  for (int l = 0; l < 32; l++) p[l] = 0.0f;
+  int64_t h0 = 0;
+  for (; h0 + 32 <= H; h0 += 32)
+    for (int l = 0; l < 32; l++) p[l] = fmaf(bf16_to_float(xrow[h0 + l]), wrow[h0 + l], p[l]);
+  for (int l = 0; h0 + l < H; l++) p[l] = fmaf(bf16_to_float(xrow[h0 + l]), wrow[h0 + l], p[l]);
   for (int off = 16; off >= 1; off >>= 1)
     for (int l = 0; l < off; l++) p[l] = p[l] + p[l + off];
   return p[0];

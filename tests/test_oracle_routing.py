@@ -31,8 +31,7 @@ def test_router_logits_vs_fp64(orc, T, H, E):
     xd = _bf16_val(x)
     exact = xd @ wr.astype(np.float64).T
     got = orc.router_logits(x, wr)
-    # fp32 summation bound: |err| <= gamma_n * sum |x||w|, with n at least the
-    # longest chain (H/64 rounded up, +1) plus the pair add and 5 tree steps
+    # fp32 summation bound: |err| <= gamma_n * sum |x||w|, n = H/32 + 5 steps
     n = H // 32 + 1 + 5
     u = 2.0 ** -24
     bound = (n * u / (1 - n * u)) * (np.abs(xd) @ np.abs(wr.astype(np.float64)).T) + 1e-30
@@ -42,30 +41,21 @@ def test_router_logits_vs_fp64(orc, T, H, E):
 
 
 def test_router_logits_is_the_canonical_order(orc):
-    # Cases where the fixed order is visible: partial sums that cancel.  h = 0
-    # and h = 2 feed q_{0,0}; h = 1 feeds q_{0,1}; h = 4 feeds lane 1; h = 64
-    # feeds lane 16, which the tree adds into lane 0 at its first step.
-    H = 128
-
-    def logit(terms):
-        x = np.zeros((1, H), np.float32)
-        w = np.zeros((1, H), np.float32)
-        for h, v in terms:
-            x[0, h], w[0, h] = 1.0, v
-        return orc.router_logits(_bf16_bits(x), w)[0, 0]
-
-    big = 2.0 ** 24
-    # +1 after 2^24 in the same chain is lost: 0 (one chain per lane: also 0)
-    assert logit([(0, big), (2, 1.0), (64, -big)]) == 0.0
-    # ...but survives in lane 1's partial, added after the lanes 0/16 cancel
-    assert logit([(0, big), (4, 1.0), (64, -big)]) == 1.0
-    # even and odd h of a lane are separate chains: 2^24 - 2^24 in q_{0,0},
-    # +1 in q_{0,1} gives 1 (a single chain in h order would lose it: 0)
-    assert logit([(0, big), (1, 1.0), (2, -big)]) == 1.0
-    # h = 32 belongs to lane 8, not lane 0: 2^24 (lane 0) + 1 (lane 8) - 2^24
-    # (lane 16) gives 0 through the tree (16 into 0, then 8 into 0 after the
-    # cancellation: 1); with lanes h mod 32 it would be lane 0 again (0)
-    assert logit([(0, big), (32, 1.0), (64, -big)]) == 1.0
+    # A case where the fixed order is visible: partial sums that cancel.  Lane 0
+    # gets +2^24 then +1 (lost in fp32), lane 16 gets -2^24: tree adds lane 16
+    # into lane 0 at the first step, giving 0 (not 1).
+    H = 64
+    x = np.zeros((1, H), np.float32)
+    w = np.zeros((1, H), np.float32)
+    x[0, 0], w[0, 0] = 1.0, 2.0 ** 24
+    x[0, 32], w[0, 32] = 1.0, 1.0
+    x[0, 16], w[0, 16] = 1.0, -(2.0 ** 24)
+    got = orc.router_logits(_bf16_bits(x), w)
+    assert got[0, 0] == 0.0
+    # moving the +1 to lane 1 makes it survive (different partial)
+    x[0, 32], x[0, 33], w[0, 33] = 0.0, 1.0, 1.0
+    got = orc.router_logits(_bf16_bits(x), w)
+    assert got[0, 0] == 1.0
 
 
 def _topk_by_sort(row, k):
