@@ -144,18 +144,29 @@ def source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def cpu_baseline(cfg, inp_host, n_tokens: int, reps: int = 1):
+def cpu_baseline(cfg, inp_host, n_tokens: int, target_s: float = 10.0):
+    """Time the oracle on the first tokens of the batch, sized to about
+    ``target_s`` seconds of host work (a one-token-per-core probe sets the
+    size) unless ``n_tokens`` fixes it.  Returns (seconds, tokens, threads)."""
     import numpy as np
 
     import oracle
     threads = oracle.threads()
-    n = n_tokens or threads
-    toks = np.arange(min(n, cfg.T), dtype=np.int32)
-    t0 = time.perf_counter()
-    for _ in range(reps):
+
+    def run(n):
+        toks = np.arange(min(n, cfg.T), dtype=np.int32)
+        t0 = time.perf_counter()
         oracle.moe_forward(cfg.oracle_problem(), inp_host, tokens=toks, nthreads=threads)
-    dt = (time.perf_counter() - t0) / reps
-    return dt, len(toks), threads
+        return time.perf_counter() - t0, len(toks)
+
+    if n_tokens:
+        dt, n = run(n_tokens)
+        return dt, n, threads
+    dt, n = run(threads)
+    want = int(n * target_s / max(dt, 1e-3)) // threads * threads
+    if want > n and n < cfg.T:
+        dt, n = run(want)
+    return dt, n, threads
 
 
 def dist_setup(args):

@@ -29,26 +29,41 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- S1 router
-// Block = 8 compute warps (4 token groups x 2 expert groups) + 1 TMA producer
-// warp.  Warp tile TW tokens x EW experts; lane l owns h = l (mod 32) of every
-// chunk, so each logit is one fma chain over h ascending, as the canonical
-// order requires.  Chunks of RT_HK h-values stream through a RT_STAGES-deep
-// shared-memory ring filled by 2-D TMA loads (x tile bf16, router tile fp32;
-// out-of-range rows read as zero).  Pairs of experts share one packed
-// fma.rn.f32x2 (two independent fp32 fused multiply-adds, same rounding).
-constexpr int RT_HK = 128;
-constexpr int RT_STAGES = 4;
+// Block = 8 warps (4 token groups x 2 expert groups); thread 0 also issues the
+// loads.  Warp tile TW tokens x EW experts; lane l owns h = l (mod 32) of every
+// 128-wide chunk, so each logit is one fma chain over h ascending, as the
+// canonical order requires.  Stages of NSUB chunks stream through a
+// shared-memory ring filled by 2-D TMA loads (one [rows][128] box per chunk:
+// x bf16, router fp32; out-of-range rows read as zero).  Pairs of experts share
+// one packed fma.rn.f32x2 (two independent fp32 fused multiply-adds, same
+// rounding as fmaf).
+// No separate producer warp: the register file is handed to a block in groups
+// of four warps, so a ninth warp would cost the eight compute warps a quarter
+// of their registers.
+constexpr int RT_CH = 128;  // h per chunk (one TMA box)
 constexpr int RT_WT = 4, RT_WE = 2;  // warp grid
-constexpr int RT_THREADS = (RT_WT * RT_WE + 1) * 32;
+constexpr int RT_WARPS = RT_WT * RT_WE;
+constexpr int RT_THREADS = RT_WARPS * 32;
 
-template <int TW, int EW>
+template <int TW, int EW, int NSUB_ = 0>
 struct RouterCfg {
-  static constexpr int BT = RT_WT * TW;             // tokens per block
-  static constexpr int BE = RT_WE * EW;             // experts per block
-  static constexpr int X_BYTES = BT * RT_HK * 2;    // bf16 tile
-  static constexpr int W_BYTES = BE * RT_HK * 4;    // fp32 tile
-  static constexpr int STAGE = X_BYTES + W_BYTES;
-  static constexpr int SMEM = 128 + RT_STAGES * STAGE + 2 * RT_STAGES * 8 + 16;
+  static constexpr int BT = RT_WT * TW;  // tokens per block
+  static constexpr int BE = RT_WE * EW;  // experts per block
+  // small warp tiles fit two blocks per SM (128 registers a thread), large
+  // ones one (up to 255)
+  static constexpr int MIN_BLOCKS = (TW * EW <= 64) ? 2 : 1;
+  static constexpr int BUDGET = 216 * 1024 / MIN_BLOCKS;  // ring bytes per block
+  static constexpr int XBOX = BT * RT_CH * 2;            // bf16 [BT][128]
+  static constexpr int WBOX = BE * RT_CH * 4;            // fp32 [BE][128]
+  // every stage costs a barrier round trip and a load-latency bubble, so a
+  // stage carries four chunks when three such stages fit, else two
+  static constexpr int NSUB = NSUB_ ? NSUB_ : (3 * 4 * (XBOX + WBOX) <= BUDGET) ? 4 : 2;
+  static constexpr int HK = NSUB * RT_CH;  // h per stage
+  static constexpr int X_BYTES = NSUB * XBOX;
+  static constexpr int W_BYTES = NSUB * WBOX;
+  static constexpr int STAGE = X_BYTES + W_BYTES;  // NSUB x boxes, then NSUB router boxes
+  static constexpr int STAGES = BUDGET / STAGE;
+  static constexpr int SMEM = 128 + STAGES * STAGE + 2 * STAGES * 8 + 16;
 };
 
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
@@ -63,70 +78,72 @@ __device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
-// Small warp tiles fit two blocks per SM (more warps to hide shared-memory and
-// FMA latency); large ones need one block's worth of registers.
-template <int TW, int EW>
-__global__ void __launch_bounds__(RT_THREADS, (TW * EW <= 64) ? 2 : 1)
+template <int TW, int EW, int NS>
+__global__ void __launch_bounds__(RT_THREADS, RouterCfg<TW, EW, NS>::MIN_BLOCKS)
     router_logits_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ bias,
                          float* __restrict__ logits, int T, int H, int E, int* err) {
-  using C = RouterCfg<TW, EW>;
+  using C = RouterCfg<TW, EW, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RT_STAGES * C::STAGE);
-  uint64_t* empty = full + RT_STAGES;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + RT_STAGES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty = full + C::STAGES;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + C::STAGES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // token tiles are the fast grid dimension: the ~150 concurrent blocks share
-  // each router-weight tile in L2 (T=16384, H=8192, E=256: 1.60 ms, vs 1.70 ms
-  // with expert tiles first; within a single wave the order makes no difference)
+  // token tiles are the fast grid dimension: the concurrent blocks share each
+  // router-weight tile in L2 (T=16384, H=8192, E=256: expert tiles first was
+  // slower; within a single wave the order makes no difference)
   const int t0 = blockIdx.x * C::BT, e0 = blockIdx.y * C::BE;
-  const int nchunk = H / RT_HK;
+  // H % 128 == 0; the chunks of a partly filled last stage beyond H read
+  // zeros, and a zero product leaves a chain unchanged
+  const int nstage = (H + C::HK - 1) / C::HK;
+  const bool producer = threadIdx.x == 0;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < RT_STAGES; ++s) {
+  if (producer) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), RT_WT * RT_WE);
+      mbar_init(smem_u32(&empty[s]), RT_WARPS);
     }
     *s_abort = 0;
     fence_mbarrier_init();
   }
   __syncthreads();
 
-  if (warp == RT_WT * RT_WE) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_x);
-      tma_prefetch_desc(&tm_w);
-      for (int c = 0; c < nchunk; ++c) {
-        const int s = c % RT_STAGES;
-        const uint32_t ph = (uint32_t)(c / RT_STAGES) & 1u;
-        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, err, s_abort)) break;
-        const uint32_t st = smem_u32(smem + s * C::STAGE);
-        const uint32_t fb = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(fb, C::STAGE);
-        tma_load_2d(st, &tm_x, c * RT_HK, t0, fb);
-        tma_load_2d(st + C::X_BYTES, &tm_w, c * RT_HK, e0, fb);
-      }
-      // drain: every issued chunk lands before the block may exit
-      for (int c = max(0, nchunk - RT_STAGES); c < nchunk; ++c)
-        mbar_wait_drain(smem_u32(&full[c % RT_STAGES]), (uint32_t)(c / RT_STAGES) & 1u);
+  auto issue = [&](int c) {  // stage c into slot c % STAGES
+    const uint32_t st = smem_u32(smem + (c % C::STAGES) * C::STAGE);
+    const uint32_t fb = smem_u32(&full[c % C::STAGES]);
+    mbar_arrive_expect_tx(fb, C::STAGE);
+#pragma unroll
+    for (int u = 0; u < C::NSUB; ++u) {
+      tma_load_2d(st + u * C::XBOX, &tm_x, c * C::HK + u * RT_CH, t0, fb);
+      tma_load_2d(st + C::X_BYTES + u * C::WBOX, &tm_w, c * C::HK + u * RT_CH, e0, fb);
     }
-    return;
+  };
+  int issued = 0;  // stages whose loads thread 0 has issued
+  if (producer) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w);
+    for (; issued < C::STAGES && issued < nstage; ++issued) issue(issued);
   }
 
-  // ------------------------------------------------------------ compute warps
   const int tg = warp % RT_WT, eg = warp / RT_WT;
-  uint64_t acc[TW][EW / 2];
+  uint64_t acc[TW][EW / 2];  // {chain of expert 2j, chain of expert 2j+1} for token i
 #pragma unroll
   for (int i = 0; i < TW; ++i)
 #pragma unroll
     for (int j = 0; j < EW / 2; ++j) acc[i][j] = 0;  // +0.0f, +0.0f
   bool ok = true;
-  for (int c = 0; c < nchunk; ++c) {
-    const int s = c % RT_STAGES;
-    const uint32_t ph = (uint32_t)(c / RT_STAGES) & 1u;
+  for (int c = 0; c < nstage; ++c) {
+    // refill stage c-1's slot with the next stage once every warp let go of it
+    if (producer && issued < nstage && c >= 1) {
+      const int p = c - 1;
+      if (mbar_wait(smem_u32(&empty[p % C::STAGES]), (uint32_t)(p / C::STAGES) & 1u, err,
+                    s_abort))
+        issue(issued++);
+    }
+    const int s = c % C::STAGES;
+    const uint32_t ph = (uint32_t)(c / C::STAGES) & 1u;
     int got = 1;
     if (lane == 0) got = mbar_wait(smem_u32(&full[s]), ph, err, s_abort) ? 1 : 0;
     got = __shfl_sync(0xffffffffu, got, 0);
@@ -134,28 +151,40 @@ __global__ void __launch_bounds__(RT_THREADS, (TW * EW <= 64) ? 2 : 1)
       ok = false;
       break;
     }
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + s * C::STAGE) + tg * TW * RT_HK;
-    const float* ws = reinterpret_cast<const float*>(smem + s * C::STAGE + C::X_BYTES) +
-                      eg * EW * RT_HK;
 #pragma unroll
-    for (int q = 0; q < RT_HK / 32; ++q) {
-      const int h = q * 32 + lane;
-      uint64_t wv[EW / 2];
+    for (int u = 0; u < C::NSUB; ++u) {  // the chunks of the stage, h ascending
+      const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + s * C::STAGE + u * C::XBOX) +
+                           tg * TW * RT_CH;
+      const float* ws = reinterpret_cast<const float*>(smem + s * C::STAGE + C::X_BYTES +
+                                                       u * C::WBOX) +
+                        eg * EW * RT_CH;
 #pragma unroll
-      for (int j = 0; j < EW / 2; ++j)
-        wv[j] = pack2(ws[(2 * j) * RT_HK + h], ws[(2 * j + 1) * RT_HK + h]);
+      for (int q = 0; q < RT_CH / 32; ++q) {
+        const int h = q * 32 + lane;
+        uint64_t wv[EW / 2];
 #pragma unroll
-      for (int i = 0; i < TW; ++i) {
-        const float xv = bf16_bits_to_f32(xs[i * RT_HK + h]);
-        const uint64_t xx = pack2(xv, xv);
+        for (int j = 0; j < EW / 2; ++j)
+          wv[j] = pack2(ws[(2 * j) * RT_CH + h], ws[(2 * j + 1) * RT_CH + h]);
 #pragma unroll
-        for (int j = 0; j < EW / 2; ++j) fma2(acc[i][j], xx, wv[j]);
+        for (int i = 0; i < TW; ++i) {
+          const float xv = bf16_bits_to_f32(xs[i * RT_CH + h]);
+          const uint64_t xx = pack2(xv, xv);
+#pragma unroll
+          for (int j = 0; j < EW / 2; ++j) fma2(acc[i][j], xx, wv[j]);
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
   }
-  if (!ok) return;
+  if (!ok) {
+    // a wait gave up: the last STAGES issued stages may still be in flight
+    // (every earlier one was consumed by all warps); let them land before exit
+    if (producer)
+      for (int c = max(0, issued - C::STAGES); c < issued; ++c)
+        mbar_wait_drain(smem_u32(&full[c % C::STAGES]), (uint32_t)(c / C::STAGES) & 1u);
+    return;
+  }
 
 #pragma unroll
   for (int i = 0; i < TW; ++i) {
@@ -266,7 +295,7 @@ __global__ void __launch_bounds__(256)
 namespace {
 
 bool router_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int H,
-                int rows, int box_rows) {
+                int rows, int box_rows) {  // [box_rows][128] boxes
   static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if (!enc) {
     void* p = nullptr;
@@ -279,28 +308,28 @@ bool router_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* b
   }
   cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)H * esize};
-  cuuint32_t box[2] = {(cuuint32_t)RT_HK, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)RT_CH, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int TW, int EW>
+template <int TW, int EW, int NS = 0>
 cudaError_t launch_router_impl(const void* x, const float* wr, const float* bias, float* logits,
                                int T, int H, int E, int* err, cudaStream_t s) {
-  using C = RouterCfg<TW, EW>;
+  using C = RouterCfg<TW, EW, NS>;
   CUtensorMap tx, tw;
   if (!router_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, C::BT) ||
       !router_map(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wr, H, E, C::BE))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<TW, EW>,
+  cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<TW, EW, NS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((T + C::BT - 1) / C::BT, (E + C::BE - 1) / C::BE);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   count_launch();
-  router_logits_kernel<TW, EW><<<grid, RT_THREADS, C::SMEM, s>>>(tx, tw, bias, logits, T, H, E, err);
+  router_logits_kernel<TW, EW, NS><<<grid, RT_THREADS, C::SMEM, s>>>(tx, tw, bias, logits, T, H, E, err);
   return cudaGetLastError();
 }
 
@@ -308,18 +337,26 @@ cudaError_t launch_router_impl(const void* x, const float* wr, const float* bias
 
 cudaError_t launch_router_logits(const void* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, int* err, cudaStream_t s) {
-  // large tiles (8 tokens x 16 experts per warp) when they still give every SM
-  // at least two blocks, else small ones; MOE_ROUTER_TILE=8x8|8x16 overrides
+  // MOE_ROUTER_TILE=8x8|8x16|8x24 (tokens x experts per warp) overrides the choice
   const char* env = std::getenv("MOE_ROUTER_TILE");
   if (env && std::strcmp(env, "8x8") == 0)
     return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
   if (env && std::strcmp(env, "8x16") == 0)
     return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
-  // (also when they make one wave of at least half the SMs: T=512, E=256 runs
-  // in 68 us with large tiles vs 75 us with small ones; T=2048 and T=64 prefer
-  // the small ones)
-  const long big_blocks = (long)((T + 31) / 32) * ((E + 31) / 32);
+  if (env && std::strcmp(env, "8x24") == 0)
+    return launch_router_impl<8, 24>(x, wr, bias, logits, T, H, E, err, s);
   const long sms = device_sm_count();
+  const long ttiles = (T + 31) / 32;
+  // 48-expert blocks reuse each x tile over more experts; worth it when E
+  // splits into them with little padding (E=896, T=4096, H=7168: 1.11 vs
+  // 1.17 ms) and the grid still gives every SM two blocks
+  const long e48 = (E + 47) / 48;
+  if (e48 * 48 <= E + E / 20 && ttiles * e48 >= 2L * sms)
+    return launch_router_impl<8, 24>(x, wr, bias, logits, T, H, E, err, s);
+  // 32-expert blocks when they still give every SM at least two blocks, or
+  // make one wave of at least half the SMs (T=512, E=256: 60 vs 69 us with
+  // 16-expert blocks at two per SM); else 16-expert blocks
+  const long big_blocks = ttiles * ((E + 31) / 32);
   if (big_blocks >= 2L * sms || (2L * big_blocks >= sms && big_blocks <= sms))
     return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
   return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
