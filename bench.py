@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--config", default="decode")
     ap.add_argument("--no-pack", action="store_true",
                     help="time row-major expert weights instead of the packed tile order")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="request MOE_F_FUSED_COMBINE (S7 in the FFN2 epilogue, fp32 sums in "
+                         "an order that is not fixed)")
     ap.add_argument("--ref-tokens", type=int, default=0,
                     help="tokens per oracle step (default: one per host core)")
     return ap.parse_args()
@@ -278,7 +281,8 @@ def run_ours(args, cfg):
     flags = ((m.F_ROUTER_BIAS if (cfg.zipf_bias or cfg.sel_bias) else 0)
              | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
              | (m.F_SIGMOID_ROUTING if cfg.routing == "sigmoid" else 0)
-             | (m.F_SITU if cfg.act == "situ" else 0))
+             | (m.F_SITU if cfg.act == "situ" else 0)
+             | (m.F_FUSED_COMBINE if args.fused_combine else 0))
     wfmt = {"fp8": m.W_FP8, "mxfp4": m.W_MXFP4, "fp8_block": m.W_FP8_BLOCK}[cfg.wfmt]
     pack = not args.no_pack
     if pack:
@@ -403,8 +407,12 @@ def run_ours(args, cfg):
     stream.wait_event(ev_out[(e2e_steps - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
-    # the pipelined steps computed the same layer
-    if not torch.equal(y_dev[(e2e_steps - 1) & 1], out):
+    # the pipelined steps computed the same layer (bit for bit, except that the
+    # fused combine's fp32 sums may round differently in the last bf16 bit)
+    last = y_dev[(e2e_steps - 1) & 1]
+    same = torch.equal(last, out) if not args.fused_combine else bool(
+        ((last.float() - out.float()).abs() <= out.float().abs() * 2.0 ** -7 + 1e-30).all())
+    if not same:
         raise SystemExit("end-to-end output differs from the device-timed output")
     bytes_step = work["bytes"]
     value, ms_max = replica_value(bytes_step / 1e9, ms, ws_n)

@@ -75,6 +75,7 @@ typedef enum {
                                       chosen scores renormalised (K3 report s.2.4) */
 #define MOE_F_SITU 0x10u /* SiTU experts: h = 4 tanh(g/4) sigmoid(g) u instead of
                             SwiGLU's silu(g) u (K3 report s.2.6)                 */
+#define MOE_F_FUSED_COMBINE 0x20u /* S7 in the FFN2 epilogue: see moe_forward     */
 
 typedef struct {
   int32_t T;        /* tokens                                                      */
@@ -267,6 +268,17 @@ int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
  *   latent (L > 0): latent_down [L, H] bf16, latent_up [H, L] bf16,
  *     latent_gamma [L] bf16 (RMSNorm weight, eps 1e-6), Kimi K3 report s.2.4.
  *   out [T, H] bf16 (output); ws / ws_bytes as for moe_permute.
+ * MOE_F_FUSED_COMBINE (the Ling write-up's gather of results done inside the
+ * expert kernel, s.4; the SparseCore gather-reduce of the sglang-jax gap list,
+ * s.8): the FFN2 epilogue adds each routed row, already scaled by its routing
+ * weight, and each shared-expert row straight into an fp32 [T, H] sum in the
+ * workspace (zeroed by S4) with fp32 reductions, and a last pass rounds that
+ * sum to bf16 out.  No y rows are written or read back.  The order of the
+ * top_k + 1 additions per element is not fixed, so two calls can differ in the
+ * last bit of out; without the flag the gather combine sums in a fixed order
+ * and repeats bit for bit.  The flag is a request: it is honoured for fp8
+ * per-channel experts on the single-SM grouped GEMMs without latent (moe_describe
+ * names the combine that runs) and ignored elsewhere.
  * Combinations this build runs (others return MOE_ERR_UNSUPPORTED): without
  * latent, an fp8 shared expert with I_shared = I or none; with latent, a bf16
  * shared expert or none and H, L multiples of 256; MXFP4 experts with K (H or

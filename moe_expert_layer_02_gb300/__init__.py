@@ -19,7 +19,7 @@ __all__ = [
     "moe_profile_read", "moe_pack_weights", "moe_watchdog_selftest", "moe_describe", "STAGES",
     "W_FP8",
     "W_MXFP4", "W_FP8_BLOCK", "F_ROUTER_BIAS", "F_SHARED_BF16", "F_PACKED_WEIGHTS",
-    "F_SIGMOID_ROUTING", "F_SITU",
+    "F_SIGMOID_ROUTING", "F_SITU", "F_FUSED_COMBINE",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +33,7 @@ F_SHARED_BF16 = 0x2
 F_PACKED_WEIGHTS = 0x4
 F_SIGMOID_ROUTING = 0x8
 F_SITU = 0x10
+F_FUSED_COMBINE = 0x20
 STAGES = ("router", "topk", "index", "scatter", "ffn1", "requant", "ffn2", "combine",
           "latent_down", "shared", "latent_up")
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",

@@ -477,10 +477,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r < rows && (unsigned)row < (unsigned)a.rows_total) {
               const float rw = (!shared && a.row_w) ? a.row_w[row] : 1.0f;
               const float hs = a.hs[row];
-              uint16_t* yr = yout + (size_t)row * a.K;
-              yr[f2] = (uint16_t)f32_bits_to_bf16(((__uint_as_float(va[j]) * hs) * s2a) * rw);
-              if (two)
-                yr[f2 + BM] = (uint16_t)f32_bits_to_bf16(((__uint_as_float(vb[j]) * hs) * s2b) * rw);
+              const float ya = ((__uint_as_float(va[j]) * hs) * s2a) * rw;
+              const float yb = ((__uint_as_float(vb[j]) * hs) * s2b) * rw;
+              if (a.out_acc) {  // fused combine: add into the token's fp32 sum
+                const int tok = shared ? row - a.R : a.src[row];
+                if ((unsigned)tok < (unsigned)a.T) {
+                  float* acc_r = a.out_acc + (size_t)tok * a.K;
+                  atomicAdd(acc_r + f2, ya);
+                  if (two) atomicAdd(acc_r + f2 + BM, yb);
+                }
+              } else {
+                uint16_t* yr = yout + (size_t)row * a.K;
+                yr[f2] = (uint16_t)f32_bits_to_bf16(ya);
+                if (two) yr[f2 + BM] = (uint16_t)f32_bits_to_bf16(yb);
+              }
             }
           }
         }

@@ -39,14 +39,19 @@ cudaError_t launch_rank(const int32_t* idx, const float* topk_w, const int32_t* 
                         const int32_t* cbase, int32_t* perm, int32_t* src, float* row_w, int T,
                         int E, int k, cudaStream_t s);
 // Per-token fp8 quantisation of x, copied to each routed row perm[t, :] and
-// (when shared_row0 >= 0) to row shared_row0 + t.
+// (when shared_row0 >= 0) to row shared_row0 + t.  acc_zero [T, H] fp32, when
+// given, is zeroed (the fused combine's sum).
 cudaError_t launch_quant_scatter(const void* x, const int32_t* perm, void* xq, float* xscale,
-                                 int T, int H, int k, int shared_row0, int* err, cudaStream_t s);
+                                 int T, int H, int k, int shared_row0, int* err, cudaStream_t s,
+                                 float* acc_zero = nullptr);
 // Per-row fp8 requantisation of h [rows, I] bf16.
 cudaError_t launch_requant(const void* h, void* hq, float* hs, int rows, int I, cudaStream_t s);
 // out[t] = bf16(sum_j y[perm[t,j]] + shared[t]); shared may be NULL.
 cudaError_t launch_combine(const void* y, const int32_t* perm, const void* shared, void* out,
                            int T, int H, int k, int* err, cudaStream_t s);
+// out = bf16(acc) element-wise, n elements (n % 8 == 0): the fused combine's
+// last pass.
+cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t n, cudaStream_t s);
 // yn[t] = bf16(RMSNorm(sum_j y[perm[t,j]]) * gamma), width L, eps given.
 cudaError_t launch_combine_rmsnorm(const void* y, const int32_t* perm, const void* gamma, void* yn,
                                    int T, int L, int k, float eps, int* err, cudaStream_t s);
@@ -78,6 +83,11 @@ struct GroupedFfnArgs {
   void* hq;               // [rows_total, I] e4m3
   float* hs;              // [rows_total]
   void* y;                // [rows_total, K] bf16
+  float* out_acc;         // [T, K] fp32 or NULL: FFN2 adds rows into out_acc[token]
+                          // with fp32 reductions instead of storing y
+  const int32_t* src;     // [R] token of each routed row (out_acc only)
+  int R;                  // routed rows; rows R.. are the shared expert's (token = row - R)
+  int T;                  // tokens (rows of out_acc)
   int BN;                 // token rows per tile (32, 64, 128, 256)
   int packed;             // fp8 weights in tile-major order (pack.cu)
   int act;                // FFN1 activation: 0 SwiGLU, 1 SiTU (gated_act)

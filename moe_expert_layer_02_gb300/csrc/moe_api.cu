@@ -103,6 +103,8 @@ struct Plan {
   bool blockwise;   // fp8 experts with 128 x 128 block scales
   int packed;       // expert weights in tile-major order (moe_pack_weights)
   int act;          // FFN1 activation: 0 SwiGLU, 1 SiTU
+  bool fused;       // S7 in the FFN2 epilogue (MOE_F_FUSED_COMBINE, where honoured)
+  size_t acc;       // fused combine: fp32 [T, H] sum
   size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
       hq, hs, y, z, yn, hsh, total;
 };
@@ -134,6 +136,8 @@ int choose_bn(const moe_problem* p) {
   return 256;
 }
 
+bool use_pair_gemm(const Plan& q);
+
 Plan make_plan(const moe_problem* p) {
   Plan q{};
   q.T = p->T;
@@ -156,6 +160,9 @@ Plan make_plan(const moe_problem* p) {
   q.BN = choose_bn(p);
   q.max_items = (q.R + q.BN - 1) / q.BN + q.E +
                 (p->I_shared > 0 ? (p->T + q.BN - 1) / q.BN + 1 : 0) + 1;
+  // the fused combine runs in the single-SM fp8 per-channel FFN2 epilogue
+  q.fused = (p->flags & MOE_F_FUSED_COMBINE) && !q.L && !q.mx && !q.blockwise &&
+            !q.shared_bf16 && !use_pair_gemm(q);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -180,7 +187,8 @@ Plan make_plan(const moe_problem* p) {
   q.h = take(RT * (size_t)q.I * 2);
   q.hq = take(RT * (size_t)q.I);
   q.hs = take(RT * 4);
-  q.y = take(RT * (size_t)q.K * 2);
+  q.y = take(q.fused ? 0 : RT * (size_t)q.K * 2);
+  q.acc = take(q.fused ? T * (size_t)q.K * 4 : 0);
   q.z = take(q.L ? T * (size_t)q.L * 2 : 0);
   q.yn = take(q.L ? T * (size_t)q.L * 2 : 0);
   q.hsh = take(q.shared_bf16 ? T * (size_t)q.Is * 2 : 0);
@@ -281,6 +289,8 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
   a.hq = at<void>(ws, q.hq);
   a.hs = at<float>(ws, q.hs);
   a.y = y;
+  a.R = q.R;
+  a.T = q.T;
   a.BN = q.BN;
   a.packed = q.packed;
   a.act = q.act;
@@ -358,11 +368,12 @@ int moe_describe(const moe_problem* p, char* buf, size_t len) {
   const char* g = q.mx ? "grouped_mx_kernel" : pair ? "pair_gemm_kernel" : "grouped_ffn_kernel";
   const int n = std::snprintf(
       buf, len,
-      "ffn1=%s<FFN1,BN=%d> ffn2=%s<FFN2,BN=%d> tile_rows=%d weights=%s%s%s max_items=%d "
-      "workspace=%zu",
+      "ffn1=%s<FFN1,BN=%d> ffn2=%s<FFN2,BN=%d> tile_rows=%d weights=%s%s%s combine=%s "
+      "max_items=%d workspace=%zu",
       g, q.BN, g, q.BN, q.BN, q.mx ? "mxfp4" : q.blockwise ? "fp8-block128" : "fp8",
-      q.packed ? ",packed" : "",
-      q.L > 0 ? " latent=bf16-pair-gemms" : "", q.max_items, q.total);
+      q.packed ? ",packed" : "", q.L > 0 ? " latent=bf16-pair-gemms" : "",
+      q.fused ? "fused-ffn2-fp32-sum" : q.L > 0 ? "gather-rmsnorm" : "gather", q.max_items,
+      q.total);
   return (n < 0 || (size_t)n >= len) ? MOE_ERR_INVALID_ARG : MOE_OK;
 }
 
@@ -553,12 +564,21 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   {
     StageTimer t(MOE_STAGE_SCATTER, s);
     MOE_TRY(launch_quant_scatter(xin, perm, xq, xscale, q.T, q.K, q.k, q.shared ? q.R : -1,
-                                 di->err, s));
+                                 di->err, s, q.fused ? at<float>(ws, q.acc) : nullptr));
   }
   GroupedFfnArgs a = ffn_args(q, ws, xq, xscale, row_w, w13, w13_scale, w2, w2_scale, shared_w13,
                               shared_w13_scale, shared_w2, shared_w2_scale, y, q.RT, di->err);
+  if (q.fused) {
+    a.out_acc = at<float>(ws, q.acc);
+    a.src = at<int32_t>(ws, q.src);
+  }
   st = run_experts(q, a, q.RT, s);
   if (st) return st;
+  if (q.fused) {
+    StageTimer t(MOE_STAGE_COMBINE, s);
+    MOE_TRY(launch_acc_to_bf16(at<float>(ws, q.acc), out, (size_t)q.T * q.H, s));
+    return MOE_OK;
+  }
   if (!q.L) {
     StageTimer t(MOE_STAGE_COMBINE, s);
     MOE_TRY(launch_combine(y, perm, q.shared ? y + (size_t)q.R * q.H : nullptr, out, q.T, q.H, q.k,

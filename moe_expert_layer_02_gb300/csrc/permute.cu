@@ -14,6 +14,8 @@
 // Determinism: counts are order-independent; the rank of a pair inside its
 // 32-token chunk comes from a per-warp bitmask table (popcount of the lanes
 // below), and chunk bases from a prefix scan, so every row index is fixed.
+#include <algorithm>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -226,7 +228,7 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
 __global__ void __launch_bounds__(256)
     quant_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                          uint8_t* __restrict__ xq, float* __restrict__ xscale, int H, int k,
-                         int shared_row0, int R, int* err) {
+                         int shared_row0, int R, int* err, float* __restrict__ acc_zero) {
   __shared__ float s_red[9];
   __shared__ int s_rows[kMaxTopK + 1];
   const int t = blockIdx.x;
@@ -262,6 +264,10 @@ __global__ void __launch_bounds__(256)
       if (s_rows[j] >= 0) *reinterpret_cast<uint2*>(xq + (size_t)s_rows[j] * H + (size_t)v * 8) = q;
   }
   if (threadIdx.x < nrows && s_rows[threadIdx.x] >= 0) xscale[s_rows[threadIdx.x]] = s;
+  if (acc_zero) {  // the fused combine's fp32 sum of this token starts at zero
+    float4* ar = reinterpret_cast<float4*>(acc_zero + (size_t)t * H);
+    for (int v = threadIdx.x; v < H / 4; v += blockDim.x) ar[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 __global__ void __launch_bounds__(256)
@@ -330,6 +336,21 @@ __global__ void __launch_bounds__(256)
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 p = __floats2bfloat162_rn(a, b);  // a -> low half
   return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// out = bf16(acc), eight elements per thread and step.
+__global__ void __launch_bounds__(256)
+    acc_to_bf16_kernel(const float4* __restrict__ acc, uint4* __restrict__ out, size_t n8) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    uint4 u;
+    u.x = pack_bf16x2(a.x, a.y);
+    u.y = pack_bf16x2(a.z, a.w);
+    u.z = pack_bf16x2(b.x, b.y);
+    u.w = pack_bf16x2(b.z, b.w);
+    out[i] = u;
+  }
 }
 
 // One thread per 8 output columns; the grid covers (token, column slice) so a
@@ -516,11 +537,22 @@ cudaError_t launch_rank(const int32_t* idx, const float* topk_w, const int32_t* 
 }
 
 cudaError_t launch_quant_scatter(const void* x, const int32_t* perm, void* xq, float* xscale,
-                                 int T, int H, int k, int shared_row0, int* err, cudaStream_t s) {
+                                 int T, int H, int k, int shared_row0, int* err, cudaStream_t s,
+                                 float* acc_zero) {
   count_launch();
   quant_scatter_kernel<<<T, 256, 0, s>>>(static_cast<const uint16_t*>(x), perm,
                                          static_cast<uint8_t*>(xq), xscale, H, k, shared_row0,
-                                         T * k, err);
+                                         T * k, err, acc_zero);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  count_launch();
+  const size_t n8 = n / 8;
+  const int blocks = (int)std::min<size_t>((n8 + 255) / 256, (size_t)device_sm_count() * 8);
+  acc_to_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(acc),
+                                            static_cast<uint4*>(out), n8);
   return cudaGetLastError();
 }
 

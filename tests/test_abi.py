@@ -124,3 +124,19 @@ def test_describe_names_the_kernels(m):
     buf = ctypes.create_string_buffer(8)
     assert lib.moe_describe(ctypes.byref(p), buf, 8) == 1  # too short
     assert lib.moe_describe(ctypes.byref(m.make_problem(4, 100, 128, 8, 2)), buf, 8) == 1
+
+
+def test_fused_combine_plan(m):
+    # honoured on the single-SM fp8 GEMMs: the fp32 sum [T, H] replaces the
+    # bf16 y rows [T*k + T, H] in the workspace; ignored on the SM-pair GEMMs
+    d = m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048)
+    f = m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048, flags=m.F_FUSED_COMBINE)
+    assert "combine=gather" in m.moe_describe(d)
+    assert "combine=fused" in m.moe_describe(f)
+    wd, wf = m.moe_workspace_bytes(d), m.moe_workspace_bytes(f)
+    assert wd - wf == (512 * 8 + 512) * 8192 * 2 - 512 * 8192 * 4
+    pr = m.make_problem(16384, 8192, 2048, 256, 8, I_shared=2048, flags=m.F_FUSED_COMBINE)
+    assert "combine=gather" in m.moe_describe(pr)
+    lat = m.make_problem(4096, 7168, 3072, 896, 16, I_shared=6144, latent=3584, wfmt=m.W_MXFP4,
+                         flags=m.F_SHARED_BF16 | m.F_FUSED_COMBINE)
+    assert "combine=gather-rmsnorm" in m.moe_describe(lat)
