@@ -44,6 +44,9 @@
 //   warps 2-5   epilogue.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -415,6 +418,296 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- SM pairs
+// The same tiles on pairs of SMs (tcgen05 cta_group::2).  The pair's MMAs
+// cover 256 weight rows, 128 from each CTA's shared memory and tensor memory,
+// and the item's N token rows, N/2 staged by each CTA: each SM stages half of
+// the activation tile that the single-SM kernel stages whole, so a stage moves
+// ~15% fewer bytes through shared memory (the bound of the single-SM kernel).
+// CTA r of a pair runs what would be the single-SM tile column 2p + r (FFN1:
+// W1 and W3 blocks 2p + r; FFN2: W2 blocks 2(2p + r) and 2(2p + r) + 1): it
+// loads that tile's 256-row weight box and its two scale images, and runs that
+// tile's epilogue on its own tensor memory.  Weights and scales must be in
+// moe_pack_weights' order; every copy is a TMA load counted on the even CTA's
+// full barrier.  The even CTA's warp 1 copies both CTAs' scale images into
+// their tensor memory (tcgen05.cp.cta_group::2: each CTA's image from its own
+// shared memory, same offsets) and issues the pair's MMAs; its commits arrive
+// on both CTAs' barriers; both epilogues release accumulators on the even
+// CTA's barrier.  All waits are bounded as in the single-SM kernel.
+template <bool FFN1, int BN>
+struct MxPairCfg {
+  static constexpr int NA = 2;
+  static constexpr int BH = BN / 2;  // activation rows staged per CTA
+  static constexpr int B_BYTES = BH * MX_BK;
+  static constexpr int STAGE_SMEM = NA * MX_A_SMEM + B_BYTES;
+  static constexpr int STAGE_TX = NA * MX_A_TX + B_BYTES + NA * MX_SF_SLOT;  // per CTA
+  static constexpr int STAGES =
+      mx_min((MX_SMEM_BUDGET - MX_SF_SLOT) / (STAGE_SMEM + NA * MX_SF_SLOT), 8);
+  static constexpr int ACC_COLS = NA * BN;
+  static constexpr int ACC_STAGES = 2;
+  static constexpr int SFB_COL = ACC_STAGES * ACC_COLS;
+  static constexpr int SFA_COL = SFB_COL + 8;
+  static constexpr int TMEM_USED = SFA_COL + STAGES * NA * 4;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
+  static constexpr int SF_BYTES = STAGES * NA * MX_SF_SLOT + MX_SF_SLOT;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_SMEM + SF_BYTES + NUM_BARS * 8 + 16 + STAGES * 4;
+  static_assert(TMEM_USED <= TMEM_COLS, "tensor memory budget");
+  static_assert(B_BYTES % 1024 == 0, "operand tiles keep 1024-byte alignment");
+  static_assert(SMEM <= 232448, "dynamic shared memory per block");
+};
+
+__device__ __forceinline__ void mma_mx_pair(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+
+// Both CTAs: a 32-row x 128-bit block from each CTA's shared memory (same
+// offset) into its own tensor memory, replicated to the four lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128_x4_pair(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+
+template <bool FFN1, int BN>
+__global__ void __launch_bounds__(MX_THREADS, 1)
+    grouped_mx_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_x,
+                           const __grid_constant__ CUtensorMap tm_s, const GroupedFfnArgs a) {
+  using C = MxPairCfg<FFN1, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sf = smem + C::STAGES * C::STAGE_SMEM;  // [STAGES][NA][512 B], then the 2^0 block
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sf + C::SF_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + C::ACC_STAGES;
+  uint64_t* drain = tempty + C::ACC_STAGES;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint32_t* s_issued = s_tmem + 4;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  {
+    uint32_t* one = reinterpret_cast<uint32_t*>(sf + C::STAGES * C::NA * MX_SF_SLOT);
+    for (int i = threadIdx.x; i < MX_SF_SLOT / 4; i += blockDim.x) one[i] = 0x7F7F7F7Fu;
+    fence_proxy_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+      s_issued[s] = 0;
+    }
+    for (int s = 0; s < C::ACC_STAGES; ++s) {
+      mbar_init(smem_u32(&tfull[s]), 1);
+      mbar_init(smem_u32(&tempty[s]), 8);  // 4 epilogue warps in each CTA
+    }
+    mbar_init(smem_u32(drain), 1);
+    *s_abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_s);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(s_tmem), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers and the 2^0 blocks of both CTAs exist before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  const int NB = FFN1 ? a.I / MX_BM : a.K / (2 * MX_BM);  // single-SM tile columns per item
+  const int NP = NB / 2;                                 // pair tiles per item
+  const int Kel = FFN1 ? a.K : a.I;
+  const int KB = Kel / MX_BK;
+  const int n_items = min(*a.n_items, a.max_items);
+  const int n_tiles = n_items * NP;
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters) {
+        const int item = tile / NP, nb = 2 * (tile - item * NP) + (int)rank;
+        const int4 it = a.items[item];
+        const int half = min(BN, (it.z + 15) & ~15) / 2;  // this item's N / 2
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = smem_u32(smem + stage * C::STAGE_SMEM);
+          const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT);
+          const uint32_t fb_leader = mapa_shared(smem_u32(&full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * C::STAGE_TX);
+          tma_load_3d_pair(st, &tm_w, 0, C::NA * MX_BM * (nb * KB + kb), it.x, fb_leader);
+          tma_load_2d_pair(st + C::NA * MX_A_SMEM, &tm_x, kb * MX_BK, it.y + (int)rank * half,
+                           fb_leader);
+          tma_load_2d_pair(sfs, &tm_s, 0, ((it.x * NB + nb) * KB + kb) * C::NA, fb_leader);
+          s_issued[stage] = phase + 1u;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (*s_abort && leader) {  // the pair's loads complete on the even CTA's barriers
+        for (int s = 0; s < C::STAGES; ++s)
+          if (s_issued[s]) mbar_wait_drain(smem_u32(&full[s]), s_issued[s] - 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader && lane == 0) {
+      int stage = 0, it_local = 0;
+      uint32_t phase = 0;
+      bool issued_any = false;
+      const uint32_t sfb = tmem + C::SFB_COL;
+      {
+        const uint64_t one = sf_desc(smem_u32(sf + C::STAGES * C::NA * MX_SF_SLOT));
+        tmem_cp_32x128_x4_pair(sfb, one);
+        tmem_cp_32x128_x4_pair(sfb + 4, one);
+      }
+      for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters, ++it_local) {
+        const int item = tile / NP;
+        const int n = min(BN, (a.items[item].z + 15) & ~15);
+        const int acc = it_local % C::ACC_STAGES;
+        const uint32_t acc_phase = (uint32_t)(it_local / C::ACC_STAGES) & 1u;
+        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, a.err, s_abort)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem + acc * C::ACC_COLS;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, a.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * C::STAGE_SMEM);
+          const uint32_t b0 = a0 + C::NA * MX_A_SMEM;
+          const uint32_t sfa = tmem + C::SFA_COL + stage * C::NA * 4;
+          const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT);
+#pragma unroll
+          for (int blk = 0; blk < C::NA; ++blk)
+            tmem_cp_32x128_x4_pair(sfa + blk * 4, sf_desc(sfs + blk * MX_SF_SLOT));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t idesc = idesc_mx(2 * MX_BM, n, kk);
+            const uint64_t bdesc = smem_desc_sw128(b0 + kk * 32);
+            const uint32_t accum = (kb | kk) ? 1u : 0u;
+            mma_mx_pair(d0, smem_desc_sw128(a0 + kk * 32), bdesc, idesc, sfa, sfb, accum);
+            mma_mx_pair(d0 + BN, smem_desc_sw128(a0 + MX_A_SMEM + kk * 32), bdesc, idesc, sfa + 4,
+                        sfb, accum);
+          }
+          issued_any = true;
+          mma_commit_pair(smem_u32(&empty[stage]), 0x3);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(smem_u32(&tfull[acc]), 0x3);
+      }
+      if (*s_abort && issued_any) {
+        mma_commit_pair(smem_u32(drain), 0x1);
+        mbar_wait_drain(smem_u32(drain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    int it_local = 0;
+    for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++it_local) {
+      const int item = tile / NP, nb = 2 * (tile - item * NP) + (int)rank;
+      const int4 it = a.items[item];
+      const int row0 = it.y, rows = it.z;
+      const int acc = it_local % C::ACC_STAGES;
+      const uint32_t acc_phase = (uint32_t)(it_local / C::ACC_STAGES) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(smem_u32(&tfull[acc]), acc_phase, a.err, s_abort) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * C::ACC_COLS;
+      const int f = nb * MX_BM + q * 32 + lane;       // FFN1: h column
+      const int f2 = 2 * nb * MX_BM + q * 32 + lane;  // FFN2: y column of block 0
+      if (FFN1) {
+        uint16_t* hout = static_cast<uint16_t*>(a.h);
+        for (int c0 = 0; c0 < rows; c0 += 16) {
+          uint32_t vg[16], vu[16];
+          __syncwarp();
+          tmem_ld16(tbase + c0, vg);
+          tmem_ld16(tbase + BN + c0, vu);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = c0 + j;
+            const int row = row0 + r;
+            if (r < rows && (unsigned)row < (unsigned)a.rows_total) {
+              const float xs = a.xscale[row];
+              const float g = __uint_as_float(vg[j]) * xs;
+              const float u = __uint_as_float(vu[j]) * xs;
+              hout[(size_t)row * a.I + f] = (uint16_t)f32_to_bf16_bits(gated_act(a.act, g, u));
+            }
+          }
+        }
+      } else {
+        uint16_t* yout = static_cast<uint16_t*>(a.y);
+        for (int c0 = 0; c0 < rows; c0 += 16) {
+          uint32_t v0[16], v1[16];
+          __syncwarp();
+          tmem_ld16(tbase + c0, v0);
+          tmem_ld16(tbase + BN + c0, v1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = c0 + j;
+            const int row = row0 + r;
+            if (r < rows && (unsigned)row < (unsigned)a.rows_total) {
+              const float rw = a.row_w ? a.row_w[row] : 1.0f;
+              const float hs = a.hs[row];
+              uint16_t* yr = yout + (size_t)row * a.K + f2;
+              yr[0] = (uint16_t)f32_to_bf16_bits((__uint_as_float(v0[j]) * hs) * rw);
+              yr[MX_BM] = (uint16_t)f32_to_bf16_bits((__uint_as_float(v1[j]) * hs) * rw);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its peer may still read its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 mx_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -475,8 +768,88 @@ cudaError_t launch_mx_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <bool FFN1, int BN>
+cudaError_t launch_mx_pair_impl(const GroupedFfnArgs& a, cudaStream_t s) {
+  using C = MxPairCfg<FFN1, BN>;
+  auto enc = mx_encoder();
+  if (!enc) return cudaErrorInvalidValue;
+  const int Kel = FFN1 ? a.K : a.I;
+  const int Wrows = FFN1 ? 2 * a.I : a.K;
+  const int NB = FFN1 ? a.I / MX_BM : a.K / (2 * MX_BM);
+  const void* w = FFN1 ? a.w13 : a.w2;
+  const void* x = FFN1 ? a.xq : a.hq;
+  const void* sc = FFN1 ? a.w13_scale : a.w2_scale;
+  if (!a.packed || NB % 2 || (!FFN1 && a.K % (2 * MX_BM)) ||
+      reinterpret_cast<uintptr_t>(sc) % 16)
+    return cudaErrorInvalidValue;
+  CUtensorMap tw, tx, ts;
+  {
+    // moe_pack_weights' order [E][rows/256 * Kel/128 * 256 rows][64 bytes]: one
+    // 256-row box per stage, each 16 packed e2m1 unpacked to 16 bytes
+    const cuuint64_t wr = (cuuint64_t)Wrows * (Kel / MX_BK);
+    cuuint64_t dims[3] = {MX_BK, wr, (cuuint64_t)a.E};
+    cuuint64_t strides[2] = {MX_BK / 2, MX_BK / 2 * wr};
+    cuuint32_t box[3] = {MX_BK, 2 * MX_BM, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(w), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // activation rows: half of the item's rows per CTA
+    cuuint64_t dims[2] = {(cuuint64_t)Kel, (cuuint64_t)a.rows_total};
+    cuuint64_t strides[1] = {(cuuint64_t)Kel};
+    cuuint32_t box[2] = {MX_BK, (cuuint32_t)C::BH};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // packed scale images [E][NB][KB][2][512 B] as rows of 128 words; a
+    // stage's two images are one 2-row box
+    cuuint64_t dims[2] = {MX_SF_SLOT / 4, (cuuint64_t)a.E * NB * (Kel / MX_BK) * C::NA};
+    cuuint64_t strides[1] = {MX_SF_SLOT};
+    cuuint32_t box[2] = {MX_SF_SLOT / 4, (cuuint32_t)C::NA};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(sc), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(grouped_mx_pair_kernel<FFN1, BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((device_sm_count() / 2) * 2);
+  cfg.blockDim = dim3(MX_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launch();
+  e = cudaLaunchKernelEx(&cfg, grouped_mx_pair_kernel<FFN1, BN>, tw, tx, ts, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <bool FFN1>
 cudaError_t launch_mx_bn(const GroupedFfnArgs& a, cudaStream_t s) {
+  if (mx_pair_eligible(a, FFN1)) {
+    switch (a.BN) {
+      case 32: return launch_mx_pair_impl<FFN1, 32>(a, s);
+      case 64: return launch_mx_pair_impl<FFN1, 64>(a, s);
+      case 96: return launch_mx_pair_impl<FFN1, 96>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.BN) {
     case 32: return launch_mx_impl<FFN1, 32>(a, s);
     case 64: return launch_mx_impl<FFN1, 64>(a, s);
@@ -486,6 +859,15 @@ cudaError_t launch_mx_bn(const GroupedFfnArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+// SM pairs need moe_pack_weights' order and an even number of single-SM tile
+// columns; MOE_MX=1cta forces the single-SM kernel.
+bool mx_pair_eligible(const GroupedFfnArgs& a, bool ffn1) {
+  const char* env = std::getenv("MOE_MX");
+  if (env && std::strcmp(env, "1cta") == 0) return false;
+  const int nb = ffn1 ? a.I / MX_BM : a.K / (2 * MX_BM);
+  return a.packed && nb % 2 == 0 && (ffn1 || a.K % (2 * MX_BM) == 0);
+}
 
 cudaError_t launch_ffn1_mx(const GroupedFfnArgs& a, cudaStream_t s) { return launch_mx_bn<true>(a, s); }
 cudaError_t launch_ffn2_mx(const GroupedFfnArgs& a, cudaStream_t s) { return launch_mx_bn<false>(a, s); }

@@ -125,6 +125,8 @@ cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s);
 // ---------------------------------------------------------------- ffn_gemm_mx.cu
 // MXFP4 routed experts (w13/w2 packed e2m1, w13_scale/w2_scale e8m0 bytes);
 // BN in {32, 64, 96}; no shared-expert group.
+// True when the MXFP4 GEMM of FFN1 (ffn1) or FFN2 runs on SM pairs.
+bool mx_pair_eligible(const GroupedFfnArgs& a, bool ffn1);
 cudaError_t launch_ffn1_mx(const GroupedFfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn2_mx(const GroupedFfnArgs& a, cudaStream_t s);
 

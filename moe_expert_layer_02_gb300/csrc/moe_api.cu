@@ -365,12 +365,19 @@ int moe_describe(const moe_problem* p, char* buf, size_t len) {
   if (st) return st;
   const Plan q = make_plan(p);
   const bool pair = !q.mx && use_pair_gemm(q);
-  const char* g = q.mx ? "grouped_mx_kernel" : pair ? "pair_gemm_kernel" : "grouped_ffn_kernel";
+  GroupedFfnArgs mxa{};
+  mxa.packed = q.packed;
+  mxa.I = q.I;
+  mxa.K = q.K;
+  auto gemm = [&](bool ffn1) {
+    if (q.mx) return mx_pair_eligible(mxa, ffn1) ? "grouped_mx_pair_kernel" : "grouped_mx_kernel";
+    return pair ? "pair_gemm_kernel" : "grouped_ffn_kernel";
+  };
   const int n = std::snprintf(
       buf, len,
       "ffn1=%s<FFN1,BN=%d> ffn2=%s<FFN2,BN=%d> tile_rows=%d weights=%s%s%s combine=%s "
       "max_items=%d workspace=%zu",
-      g, q.BN, g, q.BN, q.BN, q.mx ? "mxfp4" : q.blockwise ? "fp8-block128" : "fp8",
+      gemm(true), q.BN, gemm(false), q.BN, q.BN, q.mx ? "mxfp4" : q.blockwise ? "fp8-block128" : "fp8",
       q.packed ? ",packed" : "", q.L > 0 ? " latent=bf16-pair-gemms" : "",
       q.fused ? "fused-ffn2-fp32-sum" : q.L > 0 ? "gather-rmsnorm" : "gather", q.max_items,
       q.total);

@@ -140,3 +140,16 @@ def test_fused_combine_plan(m):
     lat = m.make_problem(4096, 7168, 3072, 896, 16, I_shared=6144, latent=3584, wfmt=m.W_MXFP4,
                          flags=m.F_SHARED_BF16 | m.F_FUSED_COMBINE)
     assert "combine=gather-rmsnorm" in m.moe_describe(lat)
+
+
+def test_mx_pair_plan(m):
+    # the MXFP4 GEMMs run on SM pairs only with packed weights and paired blocks
+    f = m.F_SHARED_BF16
+    lat = dict(I_shared=6144, latent=3584, wfmt=m.W_MXFP4)
+    d = m.moe_describe(m.make_problem(4096, 7168, 3072, 896, 16, flags=f, **lat))
+    assert "ffn1=grouped_mx_kernel" in d and "ffn2=grouped_mx_kernel" in d
+    d = m.moe_describe(m.make_problem(4096, 7168, 3072, 896, 16, flags=f | m.F_PACKED_WEIGHTS, **lat))
+    assert "ffn1=grouped_mx_pair_kernel" in d and "ffn2=grouped_mx_pair_kernel" in d
+    # I = 384 gives three 128-row blocks: FFN1 stays on single SMs
+    d = m.moe_describe(m.make_problem(80, 512, 384, 12, 3, wfmt=m.W_MXFP4, flags=m.F_PACKED_WEIGHTS))
+    assert "ffn1=grouped_mx_kernel" in d and "ffn2=grouped_mx_pair_kernel" in d
