@@ -29,29 +29,32 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------- S1 router
-// Block = 8 warps (4 token groups x 2 expert groups); thread 0 also issues the
-// loads.  Warp tile TW tokens x EW experts; lane l owns h = l (mod 32) of every
-// 128-wide chunk, so each logit is one fma chain over h ascending, as the
-// canonical order requires.  Stages of NSUB chunks stream through a
+// Block = WT x 2 warps (token groups x expert groups); thread 0 also issues
+// the loads.  Warp tile TW tokens x EW experts; lane l owns h = l (mod 32) of
+// every 128-wide chunk, so each logit is one fma chain over h ascending, as
+// the canonical order requires.  Stages of NSUB chunks stream through a
 // shared-memory ring filled by 2-D TMA loads (one [rows][128] box per chunk:
 // x bf16, router fp32; out-of-range rows read as zero).  Pairs of experts share
 // one packed fma.rn.f32x2 (two independent fp32 fused multiply-adds, same
 // rounding as fmaf).
 // No separate producer warp: the register file is handed to a block in groups
 // of four warps, so a ninth warp would cost the eight compute warps a quarter
-// of their registers.
+// of their registers.  Per packed FMA the loop also issues ~0.4 shared loads,
+// and the load pipe and shared-memory bandwidth run at about half their peak
+// beside the FMA pipe's ~60%, so more warps per scheduler (twelve) pay off
+// when the grid is large.
 constexpr int RT_CH = 128;  // h per chunk (one TMA box)
-constexpr int RT_WT = 4, RT_WE = 2;  // warp grid
-constexpr int RT_WARPS = RT_WT * RT_WE;
-constexpr int RT_THREADS = RT_WARPS * 32;
 
-template <int TW, int EW, int NSUB_ = 0>
+template <int TW, int EW, int NSUB_ = 0, int WT_ = 4>
 struct RouterCfg {
-  static constexpr int BT = RT_WT * TW;  // tokens per block
-  static constexpr int BE = RT_WE * EW;  // experts per block
+  static constexpr int WT = WT_, WE = 2;  // warp grid: token groups x expert groups
+  static constexpr int WARPS = WT * WE;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int BT = WT * TW;  // tokens per block
+  static constexpr int BE = WE * EW;  // experts per block
   // small warp tiles fit two blocks per SM (128 registers a thread), large
-  // ones one (up to 255)
-  static constexpr int MIN_BLOCKS = (TW * EW <= 64) ? 2 : 1;
+  // ones one (up to 255 with 8 warps)
+  static constexpr int MIN_BLOCKS = (TW * EW <= 64 && WARPS <= 8) ? 2 : 1;
   static constexpr int BUDGET = 216 * 1024 / MIN_BLOCKS;  // ring bytes per block
   static constexpr int XBOX = BT * RT_CH * 2;            // bf16 [BT][128]
   static constexpr int WBOX = BE * RT_CH * 4;            // fp32 [BE][128]
@@ -78,12 +81,13 @@ __device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
-template <int TW, int EW, int NS>
-__global__ void __launch_bounds__(RT_THREADS, RouterCfg<TW, EW, NS>::MIN_BLOCKS)
+template <int TW, int EW, int NS, int WT>
+__global__ void __launch_bounds__(RouterCfg<TW, EW, NS, WT>::THREADS,
+                                  RouterCfg<TW, EW, NS, WT>::MIN_BLOCKS)
     router_logits_kernel(const __grid_constant__ CUtensorMap tm_x,
                          const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ bias,
                          float* __restrict__ logits, int T, int H, int E, int* err) {
-  using C = RouterCfg<TW, EW, NS>;
+  using C = RouterCfg<TW, EW, NS, WT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(RT_THREADS, RouterCfg<TW, EW, NS>::MIN_BLOCKS)
   if (producer) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), RT_WARPS);
+      mbar_init(smem_u32(&empty[s]), C::WARPS);
     }
     *s_abort = 0;
     fence_mbarrier_init();
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(RT_THREADS, RouterCfg<TW, EW, NS>::MIN_BLOCKS)
     for (; issued < C::STAGES && issued < nstage; ++issued) issue(issued);
   }
 
-  const int tg = warp % RT_WT, eg = warp / RT_WT;
+  const int tg = warp % C::WT, eg = warp / C::WT;
   uint64_t acc[TW][EW / 2];  // {chain of expert 2j, chain of expert 2j+1} for token i
 #pragma unroll
   for (int i = 0; i < TW; ++i)
@@ -315,21 +319,21 @@ bool router_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* b
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int TW, int EW, int NS = 0>
+template <int TW, int EW, int NS = 0, int WT = 4>
 cudaError_t launch_router_impl(const void* x, const float* wr, const float* bias, float* logits,
                                int T, int H, int E, int* err, cudaStream_t s) {
-  using C = RouterCfg<TW, EW, NS>;
+  using C = RouterCfg<TW, EW, NS, WT>;
   CUtensorMap tx, tw;
   if (!router_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, C::BT) ||
       !router_map(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wr, H, E, C::BE))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<TW, EW, NS>,
+  cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<TW, EW, NS, WT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((T + C::BT - 1) / C::BT, (E + C::BE - 1) / C::BE);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   count_launch();
-  router_logits_kernel<TW, EW, NS><<<grid, RT_THREADS, C::SMEM, s>>>(tx, tw, bias, logits, T, H, E, err);
+  router_logits_kernel<TW, EW, NS, WT><<<grid, C::THREADS, C::SMEM, s>>>(tx, tw, bias, logits, T, H, E, err);
   return cudaGetLastError();
 }
 
@@ -337,28 +341,34 @@ cudaError_t launch_router_impl(const void* x, const float* wr, const float* bias
 
 cudaError_t launch_router_logits(const void* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, int* err, cudaStream_t s) {
-  // MOE_ROUTER_TILE=8x8|8x16|8x24 (tokens x experts per warp) overrides the choice
+  // MOE_ROUTER_TILE overrides the choice: 8x8 (8 warps of 8 tokens x 8 experts,
+  // two blocks per SM), 8x16 (8 warps of 8 x 16), 8x16s4 (the same with four
+  // chunks per stage), 12w8x16 (12 warps of 8 x 16: 48 tokens x 32 experts)
   const char* env = std::getenv("MOE_ROUTER_TILE");
   if (env && std::strcmp(env, "8x8") == 0)
     return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
   if (env && std::strcmp(env, "8x16") == 0)
     return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
-  if (env && std::strcmp(env, "8x24") == 0)
-    return launch_router_impl<8, 24>(x, wr, bias, logits, T, H, E, err, s);
+  if (env && std::strcmp(env, "8x16s4") == 0)
+    return launch_router_impl<8, 16, 4>(x, wr, bias, logits, T, H, E, err, s);
+  if (env && std::strcmp(env, "12w8x16") == 0)
+    return launch_router_impl<8, 16, 0, 6>(x, wr, bias, logits, T, H, E, err, s);
   const long sms = device_sm_count();
-  const long ttiles = (T + 31) / 32;
-  // 48-expert blocks reuse each x tile over more experts; worth it when E
-  // splits into them with little padding (E=896, T=4096, H=7168: 1.11 vs
-  // 1.17 ms) and the grid still gives every SM two blocks
-  const long e48 = (E + 47) / 48;
-  if (e48 * 48 <= E + E / 20 && ttiles * e48 >= 2L * sms)
-    return launch_router_impl<8, 24>(x, wr, bias, logits, T, H, E, err, s);
-  // 32-expert blocks when they still give every SM at least two blocks, or
-  // make one wave of at least half the SMs (T=512, E=256: 60 vs 69 us with
-  // 16-expert blocks at two per SM); else 16-expert blocks
-  const long big_blocks = ttiles * ((E + 31) / 32);
-  if (big_blocks >= 2L * sms || (2L * big_blocks >= sms && big_blocks <= sms))
+  const long e32 = (E + 31) / 32;
+  // Twelve warps (three per scheduler, 168 registers) hide more latency and
+  // share each stage over 48 x 32 (token, expert) pairs; they need at least
+  // two blocks per SM (T=16384, H=8192, E=256: 1.36 vs 1.44 ms with eight
+  // warps; T=4096, H=7168, E=896: 1.08 ms)
+  if ((long)((T + 47) / 48) * e32 >= 2L * sms)
+    return launch_router_impl<8, 16, 0, 6>(x, wr, bias, logits, T, H, E, err, s);
+  // eight warps of 8 x 16 when they still give every SM two blocks; in a
+  // single wave of at least half the SMs, with four chunks per stage (T=512,
+  // E=256: 56 us vs 59 us with two and 69 us with 8 x 8 tiles at two per SM)
+  const long big_blocks = (long)((T + 31) / 32) * e32;
+  if (big_blocks >= 2L * sms)
     return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
+  if (2L * big_blocks >= sms && big_blocks <= sms)
+    return launch_router_impl<8, 16, 4>(x, wr, bias, logits, T, H, E, err, s);
   return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
 }
 
