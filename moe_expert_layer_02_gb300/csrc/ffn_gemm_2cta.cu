@@ -35,6 +35,9 @@
 // barrier.  All waits are bounded as in ffn_gemm.cu.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -78,6 +81,7 @@ struct PairGemm {
   int packed;             // first-segment weights in tile-major order (pack.cu)
   int act;                // SwiGLU epilogue: 0 SwiGLU, 1 SiTU
   int rows_total;         // rows of A (and of the output)
+  int small;              // grouped: items of <= 128 rows run as M = 128 tiles
   const float* xscale;    // fp8 SWIGLU: per-row activation scale
   const float* w_scale;   // fp8: per-channel scale of group 0 (stride scale_stride)
   const float* ws_scale;  // fp8: per-channel scale of the shared expert
@@ -100,12 +104,21 @@ __device__ __forceinline__ int4 tile_item(const PairGemm& g, int item) {
   return make_int4(0, row0, min(2 * P_ROWS, g.dense_rows - row0), 0);
 }
 
+// Grouped items of at most 128 rows run as M = 128 tiles: each CTA stages 64
+// activation rows, and the tile's accumulator lands in tensor-memory columns
+// 0..127 of the pair: lanes 0..63 hold rows 0..63 of the CTA's half for output
+// columns 0..127, lanes 64..127 the same rows for columns 128..255 (read back
+// from the hardware; an M = 256 tile puts row i in lane i, all 256 columns).
+__device__ __forceinline__ bool is_small(const PairGemm& g, const int4& it) {
+  return g.small && g.items && it.z <= 2 * 64;
+}
+
 template <int KIND>
-__device__ __forceinline__ uint32_t pair_idesc() {
-  // f32 accumulate, K-major A and B, M = 256 (pair), N = 256
+__device__ __forceinline__ uint32_t pair_idesc(int M = 2 * P_ROWS) {
+  // f32 accumulate, K-major A and B, M = 256 (or 128) for the pair, N = 256
   const uint32_t fmt = KIND == KIND_FP8 ? 0u : 1u;  // e4m3 (kind::f8f6f4) / bf16 (kind::f16)
   return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(P_N >> 3) << 17) |
-         ((uint32_t)((2 * P_ROWS) >> 4) << 24);
+         ((uint32_t)(M >> 4) << 24);
 }
 
 template <int KIND>
@@ -128,7 +141,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
                      const __grid_constant__ CUtensorMap tm_ws,
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_w2,
-                     const __grid_constant__ CUtensorMap tm_x2, const PairGemm g) {
+                     const __grid_constant__ CUtensorMap tm_x2,
+                     const __grid_constant__ CUtensorMap tm_xh,
+                     const __grid_constant__ CUtensorMap tm_wh,
+                     const __grid_constant__ CUtensorMap tm_wsh, const PairGemm g) {
   constexpr int EL = KIND == KIND_FP8 ? P_BK : P_BK / 2;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -171,6 +187,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       tma_prefetch_desc(&tm_w2);
       tma_prefetch_desc(&tm_x2);
     }
+    if (g.small) {
+      tma_prefetch_desc(&tm_xh);
+      tma_prefetch_desc(&tm_wh);
+      tma_prefetch_desc(&tm_wsh);
+    }
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(s_tmem), P_TMEM_COLS);
   tc_fence_before();
@@ -199,6 +220,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         const int gc = shared ? 0 : it.x;
         const int wrow = EPI == EPI_SWIGLU ? (rank == 0 ? nb * 128 : g.I + nb * 128)
                                            : nb * P_N + 128 * (int)rank;
+        // M = 128 tile: 64 activation rows per CTA; for SWIGLU each CTA stages
+        // the W1 and the W3 half-block of its 64 features (so g and u of a
+        // feature meet in one tensor-memory lane half)
+        const bool small = is_small(g, it);
+        const CUtensorMap* twh = shared ? &tm_wsh : &tm_wh;
+        auto load_w = [&](uint32_t dst, const CUtensorMap* m, int row, int kb, uint32_t fb) {
+          if (g.packed)  // tile-major weights: (row block, k block) is contiguous
+            tma_load_3d_pair(dst, m, 0, 128 * ((row / 128) * g.kb1 + kb) + row % 128, gc, fb);
+          else
+            tma_load_3d_pair(dst, m, kb * EL, row, gc, fb);
+        };
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, g.err, s_abort)) {
@@ -207,14 +239,21 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
           const uint32_t st = smem_u32(smem + stage * P_STAGE);
           const uint32_t fb_leader = mapa_shared(smem_u32(&full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * P_STAGE);
-          if (kb < g.kb1) {
+          if (leader)
+            mbar_arrive_expect_tx(smem_u32(&full[stage]),
+                                  small ? 2 * (P_A_BYTES / 2 + P_B_BYTES) : 2 * P_STAGE);
+          if (small) {
+            tma_load_2d_pair(st, &tm_xh, kb * EL, it.y + 64 * (int)rank, fb_leader);
+            if (EPI == EPI_SWIGLU) {
+              load_w(st + P_A_BYTES, twh, nb * 128 + 64 * (int)rank, kb, fb_leader);
+              load_w(st + P_A_BYTES + P_B_BYTES / 2, twh, g.I + nb * 128 + 64 * (int)rank, kb,
+                     fb_leader);
+            } else {
+              load_w(st + P_A_BYTES, tw, wrow, kb, fb_leader);
+            }
+          } else if (kb < g.kb1) {
             tma_load_2d_pair(st, &tm_x, kb * EL, it.y + 128 * (int)rank, fb_leader);
-            if (g.packed)  // tile-major weights: (row block, k block) is contiguous
-              tma_load_3d_pair(st + P_A_BYTES, tw, 0, 128 * ((wrow / 128) * g.kb1 + kb), gc,
-                               fb_leader);
-            else
-              tma_load_3d_pair(st + P_A_BYTES, tw, kb * EL, wrow, gc, fb_leader);
+            load_w(st + P_A_BYTES, tw, wrow, kb, fb_leader);
           } else {
             const int k2 = (kb - g.kb1) * EL;
             tma_load_2d_pair(st, &tm_x2, k2, it.y + 128 * (int)rank, fb_leader);
@@ -239,8 +278,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int stage = 0, it_local = 0;
       uint32_t phase = 0;
       bool issued_any = false;
-      const uint32_t idesc = pair_idesc<KIND>();
+      const uint32_t idesc256 = pair_idesc<KIND>(), idesc128 = pair_idesc<KIND>(128);
       for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters, ++it_local) {
+        const uint32_t idesc = is_small(g, tile_item(g, tile / NB)) ? idesc128 : idesc256;
         const int acc = it_local % P_ACC_STAGES;
         const uint32_t acc_phase = (uint32_t)(it_local / P_ACC_STAGES) & 1u;
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, g.err, s_abort)) break;
@@ -310,10 +350,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       // the four warps agree on going on, and the scales are visible to all
       if (!bar_and(P_EPI_BAR, 128, ok)) break;
       tc_fence_after();
-      const int r = lrow + 128 * (int)rank;
+      // M = 128 tiles: warps 0, 1 hold rows 0..63 of this CTA's half for the
+      // first 128 output columns, warps 2, 3 the same rows for the last 128
+      const bool small = is_small(g, it);
+      const int hq = q >> 1;
+      const int wr0 = small ? 64 * (int)rank + 32 * (q & 1)  // this warp's first row
+                            : 128 * (int)rank + q * 32;     // within the item
+      const int r = wr0 + lane;
       const int row = it.y + r;
       const bool valid = r < it.z && (unsigned)row < (unsigned)g.rows_total;
-      const int wr0 = 128 * (int)rank + q * 32;  // this warp's first row within the item
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * P_N;
       // 32 bf16 columns of each of the warp's rows at output column `col`: lane
       // l writes its row's four 16-byte chunks (chunk i at i ^ swz), then reads
@@ -344,14 +389,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       // group is scaled and stored, so the load latency is paid once per tile.
       if (EPI == EPI_SWIGLU) {
         const int f0 = nb * 128;
+        const int uo = small ? 64 : 128;     // tensor-memory column of u after g
+        const int co = small ? 64 * hq : 0;  // this thread's first feature in the tile
+        const int ncol = small ? 64 : 128;
         const float xs = KIND == KIND_FP8 ? (valid ? g.xscale[row] : 0.0f) : 1.0f;
         uint32_t va[4][16], vb[4][16];  // g lo, g hi, u lo, u hi
         auto load = [&](uint32_t (&v)[4][16], int c) {
           __syncwarp();
           tmem_ld16(tbase + c, v[0]);
           tmem_ld16(tbase + c + 16, v[1]);
-          tmem_ld16(tbase + 128 + c, v[2]);
-          tmem_ld16(tbase + 128 + c + 16, v[3]);
+          tmem_ld16(tbase + uo + c, v[2]);
+          tmem_ld16(tbase + uo + c + 16, v[3]);
         };
         auto emit = [&](const uint32_t (&v)[4][16], int c) {
           uint32_t packed[16];
@@ -359,8 +407,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           for (int j = 0; j < 32; j += 4) {
             float4 sg = make_float4(1.0f, 1.0f, 1.0f, 1.0f), su = sg;
             if (KIND == KIND_FP8) {
-              sg = *reinterpret_cast<const float4*>(scl + c + j);
-              su = *reinterpret_cast<const float4*>(scl + 128 + c + j);
+              sg = *reinterpret_cast<const float4*>(scl + co + c + j);
+              su = *reinterpret_cast<const float4*>(scl + 128 + co + c + j);
             }
             const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
             float hv[4];
@@ -378,21 +426,22 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             packed[j / 2] = pack_bf16x2(hv[0], hv[1]);
             packed[j / 2 + 1] = pack_bf16x2(hv[2], hv[3]);
           }
-          put(packed, f0 + c);
+          put(packed, f0 + co + c);
         };
         load(va, 0);
         tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 128; c += 64) {
+        for (int c = 0; c < ncol; c += 64) {
           load(vb, c + 32);
           emit(va, c);
           tmem_ld_wait();
-          if (c + 64 < 128) load(va, c + 64);
+          if (c + 64 < ncol) load(va, c + 64);
           emit(vb, c + 32);
           tmem_ld_wait();
         }
       } else {
         const int c0 = nb * P_N;
+        const int co = small ? 128 * hq : 0;  // this thread's first output column in the tile
+        const int ncol = small ? 128 : P_N;
         const float hs = EPI == EPI_DOWN ? (valid ? g.hs[row] : 0.0f) : 1.0f;
         const float rw = (EPI == EPI_DOWN && valid && !shared && g.row_w) ? g.row_w[row] : 1.0f;
         uint32_t va[2][16], vb[2][16];
@@ -406,7 +455,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             float4 s4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-            if (EPI == EPI_DOWN) s4 = *reinterpret_cast<const float4*>(scl + c + j);
+            if (EPI == EPI_DOWN) s4 = *reinterpret_cast<const float4*>(scl + co + c + j);
             const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
             float yv[4];
 #pragma unroll
@@ -419,16 +468,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
             packed[j / 2] = pack_bf16x2(yv[0], yv[1]);
             packed[j / 2 + 1] = pack_bf16x2(yv[2], yv[3]);
           }
-          put(packed, c0 + c);
+          put(packed, c0 + co + c);
         };
         load(va, 0);
         tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < P_N; c += 64) {
+        for (int c = 0; c < ncol; c += 64) {
           load(vb, c + 32);
           emit(va, c);
           tmem_ld_wait();
-          if (c + 64 < P_N) load(va, c + 64);
+          if (c + 64 < ncol) load(va, c + 64);
           emit(vb, c + 32);
           tmem_ld_wait();
         }
@@ -449,6 +497,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   }
 }
 
+// Grouped items of <= 128 rows as M = 128 tiles unless MOE_PAIR_SMALL=0.
+bool pair_small_tiles() {
+  const char* env = std::getenv("MOE_PAIR_SMALL");
+  return !(env && std::strcmp(env, "0") == 0);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -463,15 +517,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 // Map over a row-major [groups][rows][inner] tensor of 1-byte (fp8) or
-// 2-byte (bf16) elements; box = 128 bytes x 128 rows, 128-byte swizzle.
+// 2-byte (bf16) elements; box = 128 bytes x box_rows rows (128, or 64 for the
+// halves of M = 128 tiles), 128-byte swizzle.
 bool pair_map(CUtensorMap* m, int kind, int rank, const void* base, uint64_t inner,
-              uint64_t rows, uint64_t groups) {
+              uint64_t rows, uint64_t groups, uint32_t box_rows = P_ROWS) {
   auto enc = encoder();
   if (!enc || !base) return false;
   const int es = kind == KIND_FP8 ? 1 : 2;
   cuuint64_t dims[3] = {inner, rows, groups};
   cuuint64_t strides[2] = {inner * es, inner * rows * es};
-  cuuint32_t box[3] = {(cuuint32_t)(P_BK / es), (cuuint32_t)P_ROWS, 1};
+  cuuint32_t box[3] = {(cuuint32_t)(P_BK / es), box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, kind == KIND_FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
              rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -481,8 +536,9 @@ bool pair_map(CUtensorMap* m, int kind, int rank, const void* base, uint64_t inn
 
 template <int KIND, int EPI>
 cudaError_t launch_pair_gemm(const CUtensorMap& tw, const CUtensorMap& tws, const CUtensorMap& tx,
-                             const CUtensorMap& tw2, const CUtensorMap& tx2, const PairGemm& g,
-                             cudaStream_t s) {
+                             const CUtensorMap& tw2, const CUtensorMap& tx2,
+                             const CUtensorMap& txh, const CUtensorMap& twh,
+                             const CUtensorMap& twsh, const PairGemm& g, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<KIND, EPI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
   if (e != cudaSuccess) return e;
@@ -499,7 +555,8 @@ cudaError_t launch_pair_gemm(const CUtensorMap& tw, const CUtensorMap& tws, cons
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launch();
-  e = cudaLaunchKernelEx(&cfg, pair_gemm_kernel<KIND, EPI>, tw, tws, tx, tw2, tx2, g);
+  e = cudaLaunchKernelEx(&cfg, pair_gemm_kernel<KIND, EPI>, tw, tws, tx, tw2, tx2, txh, twh, twsh,
+                         g);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -514,9 +571,13 @@ cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   CUtensorMap tw, tws, tx;
   const uint64_t winner = a.packed ? P_BK : K;
   const uint64_t wrows = a.packed ? (uint64_t)Wrows * (K / P_BK) : Wrows;
+  CUtensorMap twh, twsh, txh;
   if (!pair_map(&tw, KIND_FP8, 3, w, winner, wrows, a.E) ||
       !pair_map(&tws, KIND_FP8, 3, ws ? ws : w, winner, wrows, 1) ||
-      !pair_map(&tx, KIND_FP8, 2, x, K, a.rows_total, 1))
+      !pair_map(&tx, KIND_FP8, 2, x, K, a.rows_total, 1) ||
+      !pair_map(&twh, KIND_FP8, 3, w, winner, wrows, a.E, 64) ||
+      !pair_map(&twsh, KIND_FP8, 3, ws ? ws : w, winner, wrows, 1, 64) ||
+      !pair_map(&txh, KIND_FP8, 2, x, K, a.rows_total, 1, 64))
     return cudaErrorInvalidValue;
   PairGemm g{};
   g.items = a.items;
@@ -530,6 +591,7 @@ cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   g.packed = a.packed;
   g.act = a.act;
   g.rows_total = a.rows_total;
+  g.small = pair_small_tiles() ? 1 : 0;
   g.xscale = a.xscale;
   g.w_scale = FFN1 ? a.w13_scale : a.w2_scale;
   g.ws_scale = FFN1 ? a.sw13_scale : a.sw2_scale;
@@ -539,8 +601,8 @@ cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   g.out = FFN1 ? a.h : a.y;
   g.ldo = FFN1 ? a.I : a.K;
   g.err = a.err;
-  if (FFN1) return launch_pair_gemm<KIND_FP8, EPI_SWIGLU>(tw, tws, tx, tw, tx, g, s);
-  return launch_pair_gemm<KIND_FP8, EPI_DOWN>(tw, tws, tx, tw, tx, g, s);
+  if (FFN1) return launch_pair_gemm<KIND_FP8, EPI_SWIGLU>(tw, tws, tx, tw, tx, txh, twh, twsh, g, s);
+  return launch_pair_gemm<KIND_FP8, EPI_DOWN>(tw, tws, tx, tw, tx, txh, twh, twsh, g, s);
 }
 
 }  // namespace
@@ -580,8 +642,9 @@ cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s) {
   g.out = d.out;
   g.ldo = d.N;
   g.err = d.err;
-  if (d.swiglu) return launch_pair_gemm<KIND_BF16, EPI_SWIGLU>(tw, tw, tx, tw2, tx2, g, s);
-  return launch_pair_gemm<KIND_BF16, EPI_STORE>(tw, tw, tx, tw2, tx2, g, s);
+  // dense launches have no small tiles: the half-box maps are never read
+  if (d.swiglu) return launch_pair_gemm<KIND_BF16, EPI_SWIGLU>(tw, tw, tx, tw2, tx2, tx, tw, tw, g, s);
+  return launch_pair_gemm<KIND_BF16, EPI_STORE>(tw, tw, tx, tw2, tx2, tx, tw, tw, g, s);
 }
 
 }  // namespace moe

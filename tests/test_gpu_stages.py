@@ -132,13 +132,17 @@ def _expert_problem(orc, cfg, h):
     return off, q[src], s[src], row_w
 
 
-@pytest.mark.parametrize("bn", [32, 64, 128, 256, "256-1cta"])
+@pytest.mark.parametrize("bn", [32, 64, 128, 256, "256-1cta", "256-nosmall"])
 @pytest.mark.parametrize("cfg", [mi.CONFIGS["toy"], RAGGED, KE, E3, SKEW_SMALL], ids=ids)
 def test_expert_ffn_all_tiles(orc, cfg, bn, monkeypatch):
-    # 256-row tiles run on SM pairs when H % 256 == 0; "256-1cta" forces the
-    # single-SM kernel for the same tiles
+    # 256-row tiles run on SM pairs when H % 256 == 0, items of <= 128 rows as
+    # M = 128 tiles; "256-nosmall" runs those as padded M = 256 tiles and
+    # "256-1cta" forces the single-SM kernel for the same tiles
     if bn == "256-1cta":
         monkeypatch.setenv("MOE_GEMM", "1cta")
+        bn = 256
+    if bn == "256-nosmall":
+        monkeypatch.setenv("MOE_PAIR_SMALL", "0")
         bn = 256
     monkeypatch.setenv("MOE_TILE_N", str(bn))
     _check_expert_ffn(orc, cfg, rows_sample=None)
