@@ -35,6 +35,15 @@ cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t
                         int shared_row0, int shared_rows, cudaStream_t s);
 cudaError_t launch_items_from_offsets(const int32_t* off, int E, int4* items, int32_t* n_items,
                                       int max_items, int BN, cudaStream_t s);
+// count + scan + rank in one single-block launch, for T <= 1024 when the
+// per-chunk masks and bases ([nch][E] words each) fit kIndexSmallSmem bytes of
+// shared memory.
+constexpr size_t kIndexSmallSmem = 96 * 1024;
+bool index_small_fits(int T, int E);
+cudaError_t launch_index_small(const int32_t* idx, const float* topk_w, int32_t* cnt, int32_t* off,
+                               int32_t* perm, int32_t* src, float* row_w, int T, int E, int k,
+                               int4* items, int32_t* n_items, int max_items, int BN,
+                               int shared_row0, int shared_rows, int* err, cudaStream_t s);
 cudaError_t launch_rank(const int32_t* idx, const float* topk_w, const int32_t* off,
                         const int32_t* cbase, int32_t* perm, int32_t* src, float* row_w, int T,
                         int E, int k, cudaStream_t s);

@@ -299,6 +299,14 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
   return a;
 }
 
+// Small batches build the permutation in one single-block launch
+// (index_small_kernel); MOE_INDEX=3pass forces the three-kernel path.
+bool use_index_small(const Plan& q) {
+  const char* env = std::getenv("MOE_INDEX");
+  if (env && std::strcmp(env, "3pass") == 0) return false;
+  return index_small_fits(q.T, q.E);
+}
+
 // Large batches (256-row tiles) run the grouped GEMMs on SM pairs; MOE_GEMM=1cta
 // forces the single-SM kernels.
 bool use_pair_gemm(const Plan& q) {
@@ -440,11 +448,16 @@ int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
     StageTimer t(MOE_STAGE_INDEX, s);
-    MOE_TRY(launch_count(topk_idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
-    MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), counts, offsets, q.T, q.E,
-                        q.k, nullptr, nullptr, 0, q.BN, 0, 0, s));
-    MOE_TRY(launch_rank(topk_idx, nullptr, offsets, at<int32_t>(ws, q.cbase), perm, src_row,
-                        nullptr, q.T, q.E, q.k, s));
+    if (use_index_small(q)) {
+      MOE_TRY(launch_index_small(topk_idx, nullptr, counts, offsets, perm, src_row, nullptr, q.T,
+                                 q.E, q.k, nullptr, nullptr, 0, q.BN, 0, 0, di->err, s));
+    } else {
+      MOE_TRY(launch_count(topk_idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
+      MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), counts, offsets, q.T,
+                          q.E, q.k, nullptr, nullptr, 0, q.BN, 0, 0, s));
+      MOE_TRY(launch_rank(topk_idx, nullptr, offsets, at<int32_t>(ws, q.cbase), perm, src_row,
+                          nullptr, q.T, q.E, q.k, s));
+    }
   }
   {
     StageTimer t(MOE_STAGE_SCATTER, s);
@@ -561,12 +574,19 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   }
   {
     StageTimer t(MOE_STAGE_INDEX, s);
-    MOE_TRY(launch_count(idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
-    MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), at<int32_t>(ws, q.cnt), off,
-                        q.T, q.E, q.k, at<int4>(ws, q.items), at<int32_t>(ws, q.n_items),
-                        q.max_items, q.BN, q.R, q.shared ? q.T : 0, s));
-    MOE_TRY(launch_rank(idx, tw, off, at<int32_t>(ws, q.cbase), perm, at<int32_t>(ws, q.src), row_w,
-                        q.T, q.E, q.k, s));
+    if (use_index_small(q)) {
+      MOE_TRY(launch_index_small(idx, tw, at<int32_t>(ws, q.cnt), off, perm, at<int32_t>(ws, q.src),
+                                 row_w, q.T, q.E, q.k, at<int4>(ws, q.items),
+                                 at<int32_t>(ws, q.n_items), q.max_items, q.BN, q.R,
+                                 q.shared ? q.T : 0, di->err, s));
+    } else {
+      MOE_TRY(launch_count(idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
+      MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), at<int32_t>(ws, q.cnt),
+                          off, q.T, q.E, q.k, at<int4>(ws, q.items), at<int32_t>(ws, q.n_items),
+                          q.max_items, q.BN, q.R, q.shared ? q.T : 0, s));
+      MOE_TRY(launch_rank(idx, tw, off, at<int32_t>(ws, q.cbase), perm, at<int32_t>(ws, q.src),
+                          row_w, q.T, q.E, q.k, s));
+    }
   }
   {
     StageTimer t(MOE_STAGE_SCATTER, s);

@@ -179,6 +179,93 @@ __global__ void __launch_bounds__(1024)
   if (items) build_items(s_cnt, E, BN, shared_row0, shared_rows, items, n_items, max_items, s_warp);
 }
 
+// S3 for small batches (T <= 1024) in one block of 1024 threads: the
+// per-chunk expert masks, the per-expert chunk scans, the expert offsets, the
+// tile list and the stable ranks of count_kernel, scan_kernel and rank_kernel,
+// with the masks and chunk bases in shared memory ([nch][E] words each) and one
+// launch instead of three.  Warp c owns chunk c and lane l its token, whose
+// top-k indices and weights are loaded once, up front, into registers.  Same
+// results bit for bit.  KMAX >= k bounds the per-lane register arrays.
+template <int KMAX>
+__global__ void __launch_bounds__(1024)
+    index_small_kernel(const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
+                       int32_t* __restrict__ cnt, int32_t* __restrict__ off,
+                       int32_t* __restrict__ perm, int32_t* __restrict__ src,
+                       float* __restrict__ row_w, int T, int E, int k, int nch, int4* items,
+                       int32_t* n_items, int max_items, int BN, int shared_row0,
+                       int shared_rows, int* err) {
+  extern __shared__ uint32_t s_dyn[];
+  uint32_t* bits = s_dyn;                                   // [nch][E] lane masks
+  int* cb = reinterpret_cast<int*>(s_dyn + (size_t)nch * E);  // [nch][E] chunk bases
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_warp[33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = warp;  // nch <= 32: one chunk per warp at most
+  const int t = c * kChunk + lane;
+  const bool mine = c < nch && t < T;
+  int ev[KMAX];
+  float wv[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    ev[j] = (mine && j < k) ? idx[(size_t)t * k + j] : -1;
+    wv[j] = (mine && j < k && row_w) ? topk_w[(size_t)t * k + j] : 0.0f;
+  }
+  if (c < nch) {
+    uint32_t* b = bits + (size_t)c * E;
+    for (int e = lane; e < E; e += 32) b[e] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j >= k || !mine) continue;
+      if ((unsigned)ev[j] < (unsigned)E)
+        atomicOr(&b[ev[j]], 1u << lane);
+      else
+        record_error(err, kErrInvalidArg);
+    }
+  }
+  __syncthreads();
+  for (int e = warp; e < E; e += 32) {
+    const int v = lane < nch ? __popc(bits[(size_t)lane * E + e]) : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane < nch) cb[(size_t)lane * E + e] = x - v;
+    if (lane == 31) s_off[e] = x;
+  }
+  __syncthreads();
+  const int v = threadIdx.x < E ? s_off[threadIdx.x] : 0;
+  int total;
+  const int ex = block_exclusive_scan(v, s_warp, &total);
+  if (threadIdx.x < E) {
+    cnt[threadIdx.x] = v;
+    off[threadIdx.x] = ex;
+    s_off[threadIdx.x] = ex;
+  }
+  if (threadIdx.x == 0) {
+    off[E] = total;
+    s_off[E] = total;
+  }
+  __syncthreads();
+  if (items) build_items(s_off, E, BN, shared_row0, shared_rows, items, n_items, max_items, s_warp);
+  if (!mine) return;
+  const uint32_t below = (1u << lane) - 1u;
+  const uint32_t* b = bits + (size_t)c * E;
+  const int* base = cb + (size_t)c * E;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j >= k) break;
+    const int e = ev[j];
+    if ((unsigned)e >= (unsigned)E) continue;
+    const int row = s_off[e] + base[e] + __popc(b[e] & below);
+    perm[(size_t)t * k + j] = row;
+    src[row] = t;
+    if (row_w) row_w[row] = wv[j];
+  }
+}
+
 __global__ void __launch_bounds__(1024)
     items_kernel(const int32_t* __restrict__ off, int E, int4* items, int32_t* n_items,
                  int max_items, int BN) {
@@ -515,6 +602,34 @@ cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t
   scan_kernel<<<1, 1024, 0, s>>>(cc, cbase, cnt, off, E, num_chunks(T), T * k, items, n_items,
                                  max_items, BN, shared_row0, shared_rows);
   return cudaGetLastError();
+}
+
+bool index_small_fits(int T, int E) {
+  return num_chunks(T) <= 32 &&
+         (size_t)num_chunks(T) * E * 2 * sizeof(uint32_t) <= kIndexSmallSmem;
+}
+
+cudaError_t launch_index_small(const int32_t* idx, const float* topk_w, int32_t* cnt, int32_t* off,
+                               int32_t* perm, int32_t* src, float* row_w, int T, int E, int k,
+                               int4* items, int32_t* n_items, int max_items, int BN,
+                               int shared_row0, int shared_rows, int* err, cudaStream_t s) {
+  const int nch = num_chunks(T);
+  const size_t smem = (size_t)nch * E * 2 * sizeof(uint32_t);
+  if (nch > 32 || smem > kIndexSmallSmem) return cudaErrorInvalidValue;
+  auto go = [&](auto kern) {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kIndexSmallSmem);
+      if (e != cudaSuccess) return e;
+    }
+    count_launch();
+    kern<<<1, 1024, smem, s>>>(idx, topk_w, cnt, off, perm, src, row_w, T, E, k, nch, items,
+                               n_items, max_items, BN, shared_row0, shared_rows, err);
+    return cudaGetLastError();
+  };
+  if (k <= 8) return go(index_small_kernel<8>);
+  if (k <= 16) return go(index_small_kernel<16>);
+  return go(index_small_kernel<kMaxTopK>);
 }
 
 cudaError_t launch_items_from_offsets(const int32_t* off, int E, int4* items, int32_t* n_items,

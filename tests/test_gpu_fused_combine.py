@@ -59,7 +59,7 @@ def test_fused_matches_gather_and_repeats():
 
 
 def test_fused_launches_and_zeroing():
-    # ten launches, as with the gather combine; a second call on a reused
+    # as many launches as with the gather combine; a second call on a reused
     # workspace must not see the first call's sums (S4 zeroes them)
     m = G.lib()
     cfg = SHARED_SMALL
@@ -73,7 +73,7 @@ def test_fused_launches_and_zeroing():
     n0 = m.moe_launch_count()
     m.moe_forward(*args)
     first = out.clone()
-    assert m.moe_launch_count() - n0 == 10
+    assert m.moe_launch_count() - n0 == 8
     m.moe_forward(*args)
     assert m.moe_get_last_error() == 0
     d = (out.float() - first.float()).abs()

@@ -76,8 +76,13 @@ def test_topk_ties_lower_index(orc):
     assert np.allclose(gw.cpu().numpy(), w, rtol=1e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("path", ["auto", "3pass"])
 @pytest.mark.parametrize("cfg", SMALL + FULL, ids=ids)
-def test_permute_bit_exact(orc, cfg):
+def test_permute_bit_exact(orc, cfg, path, monkeypatch):
+    # small batches build the permutation in one single-block launch; "3pass"
+    # forces the count / scan / rank kernels that large batches use
+    if path == "3pass":
+        monkeypatch.setenv("MOE_INDEX", "3pass")
     m = G.lib()
     inp = G.gpu_inputs(cfg)
     h = G.host(inp, keys=("x", "router_w", "router_bias"))
