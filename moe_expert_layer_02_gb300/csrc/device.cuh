@@ -307,6 +307,22 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned),
+// cached in L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// The mbarrier receives one arrival (counted in its expected count) once every
+// cp.async this thread issued before has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Generic-proxy shared-memory writes become visible to later async-proxy reads
 // (tcgen05.cp) of this thread.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -81,7 +81,9 @@ struct Cfg {
   static_assert(!BLK || BN <= 64, "block-wise tiles keep their sums in registers");
   static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * ACC_COLS);
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + STAGES * 4;
+  // + the tile's token list (FFN1 row gather)
+  static constexpr int SMEM =
+      1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + STAGES * 4 + BN * 4;
   static_assert(B_BYTES % 1024 == 0, "operand tiles must keep 1024-byte alignment");
   static_assert(ACC_BUFS * ACC_COLS <= 512, "tensor memory holds 512 columns");
   static_assert(STAGES >= 2, "need at least two pipeline stages");
@@ -231,12 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   uint32_t* s_issued = s_tmem + 4;  // per stage: 0 = never, else phase + 1
+  int* s_tok = reinterpret_cast<int*>(s_issued + C::STAGES);  // [BN] tokens of the tile's rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // FFN1 row gather: the producer warp's 32 lanes copy the activation rows, each
+  // lane's cp.async completion arriving on the stage's full barrier
+  const bool gat = FFN1 && !BLK && a.gather;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&full[s]), gat ? 1 + 32 : 1);
       mbar_init(smem_u32(&empty[s]), 1);
       s_issued[s] = 0;
     }
@@ -266,42 +272,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (gat || lane == 0) {  // the whole warp when it gathers rows, else lane 0
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && !*s_abort; tile += gridDim.x) {
+      const uint8_t* xtok = static_cast<const uint8_t*>(a.xq);
+      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        int stop = lane == 0 ? *s_abort : 0;
+        if (gat) stop = __shfl_sync(0xffffffffu, stop, 0);
+        if (stop) break;
         const int item = tile / NB, nb = tile - item * NB;
         const int4 it = a.items[item];
         const bool shared = it.x >= a.E;
         const CUtensorMap* tw = shared ? &tm_ws : &tm_w;
         const int gc = shared ? 0 : it.x;
+        const int n = min(BN, (it.z + 15) & ~15);  // rows the MMAs read
+        if (gat) {
+          // token of each row the MMAs read; the padding rows repeat a real one
+          for (int i = lane; i < n; i += 32) {
+            const int r = it.y + min(i, it.z - 1);
+            int t = shared ? r - a.R : a.src[r];
+            s_tok[i] = (unsigned)t < (unsigned)a.T ? t : 0;
+          }
+          __syncwarp();
+        }
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort)) {
+          int got = 1;
+          if (lane == 0) got = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort) ? 1 : 0;
+          if (gat) got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
             ok = false;
             break;
           }
           const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          // (rows past the last block, FFN2 with K % 256 == 128, read as zeros)
-          if (a.packed) {  // tile-major weights: tile (row block, k block) is contiguous
-            tma_load_3d(st, tw, 0, BM * (wblock<FFN1>(a, 0, nb) * KB + kb), gc, fb);
-            tma_load_3d(st + C::A_BYTES, tw, 0, BM * (wblock<FFN1>(a, 1, nb) * KB + kb), gc, fb);
-          } else {
-            tma_load_3d(st, tw, kb * BK, wblock<FFN1>(a, 0, nb) * BM, gc, fb);
-            tma_load_3d(st + C::A_BYTES, tw, kb * BK, wblock<FFN1>(a, 1, nb) * BM, gc, fb);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, gat ? C::NA * C::A_BYTES : C::STAGE_BYTES);
+            // (rows past the last block, FFN2 with K % 256 == 128, read as zeros)
+            if (a.packed) {  // tile-major weights: tile (row block, k block) is contiguous
+              tma_load_3d(st, tw, 0, BM * (wblock<FFN1>(a, 0, nb) * KB + kb), gc, fb);
+              tma_load_3d(st + C::A_BYTES, tw, 0, BM * (wblock<FFN1>(a, 1, nb) * KB + kb), gc, fb);
+            } else {
+              tma_load_3d(st, tw, kb * BK, wblock<FFN1>(a, 0, nb) * BM, gc, fb);
+              tma_load_3d(st + C::A_BYTES, tw, kb * BK, wblock<FFN1>(a, 1, nb) * BM, gc, fb);
+            }
+            if (!gat) tma_load_2d(st + C::NA * C::A_BYTES, &tm_x, kb * BK, it.y, fb);
+            s_issued[stage] = phase + 1u;
           }
-          tma_load_2d(st + C::NA * C::A_BYTES, &tm_x, kb * BK, it.y, fb);
-          s_issued[stage] = phase + 1u;
+          if (gat) {
+            // row i of the 128-byte-swizzled tile: 16-byte chunk c at chunk c ^ (i % 8)
+            const uint32_t b0 = st + C::NA * C::A_BYTES;
+            for (int qc = lane; qc < n * 8; qc += 32) {
+              const int i = qc >> 3, c = qc & 7;
+              cp_async16(b0 + i * BK + ((c ^ (i & 7)) << 4),
+                         xtok + (size_t)s_tok[i] * a.K + kb * BK + c * 16);
+            }
+            cp_async_arrive_noinc(fb);
+            __syncwarp();
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
+        if (gat) __syncwarp();  // s_tok is rewritten for the next tile
       }
-      if (*s_abort) {  // let our own copies land before the CTA can exit
+      if (gat) cp_async_wait_all();  // no copy into this CTA's shared memory outlives it
+      if (lane == 0 && *s_abort) {  // let our own copies land before the CTA can exit
         for (int s = 0; s < C::STAGES; ++s)
           if (s_issued[s]) mbar_wait_drain(smem_u32(&full[s]), s_issued[s] - 1u);
       }
@@ -370,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          if (gat) fence_proxy_async_smem();  // gathered rows came through the generic proxy
           const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t b0 = a0 + C::NA * C::A_BYTES;
 #pragma unroll
@@ -450,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = c0 + j;
             const int row = row0 + r;
             if (r < rows && (unsigned)row < (unsigned)a.rows_total) {
-              const float xs = a.xscale[row];
+              const float xs = gat ? a.xscale[shared ? row - a.R : a.src[row]] : a.xscale[row];
               const float g = (__uint_as_float(vg[j]) * xs) * sg;
               const float u = (__uint_as_float(vu[j]) * xs) * su;
               const float hv = gated_act(a.act, g, u);

@@ -108,15 +108,6 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// The mbarrier receives one arrival (counted in its expected count) once every
-// cp.async this thread issued before has landed.
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
 
 // Shared-memory descriptor of a 32-row x 16-byte scale block, no swizzle: 8-row
 // core matrices of 128 contiguous bytes, 128 bytes apart (both offset fields).

@@ -100,6 +100,9 @@ struct GroupedFfnArgs {
   int BN;                 // token rows per tile (32, 64, 128, 256)
   int packed;             // fp8 weights in tile-major order (pack.cu)
   int act;                // FFN1 activation: 0 SwiGLU, 1 SiTU (gated_act)
+  int gather;             // FFN1 (single-SM, per-channel): xq / xscale hold one row per
+                          // token; the producer gathers row r of a tile from token
+                          // src[r] (routed) or r - R (shared expert)
   int blockwise;          // fp8 weights with fp32 scales per 128 x 128 block:
                           // w13_scale [E][2I/128][K/128], w2_scale [E][K/128][I/128]
   int* err;

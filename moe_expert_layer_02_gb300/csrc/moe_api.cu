@@ -104,6 +104,7 @@ struct Plan {
   int packed;       // expert weights in tile-major order (moe_pack_weights)
   int act;          // FFN1 activation: 0 SwiGLU, 1 SiTU
   bool fused;       // S7 in the FFN2 epilogue (MOE_F_FUSED_COMBINE, where honoured)
+  bool gather;      // S4 quantises per token; the FFN1 producer gathers the rows
   size_t acc;       // fused combine: fp32 [T, H] sum
   size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
       hq, hs, y, z, yn, hsh, total;
@@ -163,6 +164,12 @@ Plan make_plan(const moe_problem* p) {
   // the fused combine runs in the single-SM fp8 per-channel FFN2 epilogue
   q.fused = (p->flags & MOE_F_FUSED_COMBINE) && !q.L && !q.mx && !q.blockwise &&
             !q.shared_bf16 && !use_pair_gemm(q);
+  // the single-SM fp8 per-channel FFN1 gathers its rows by token (MOE_GATHER=0:
+  // S4 writes the permuted rows instead)
+  {
+    const char* env = std::getenv("MOE_GATHER");
+    q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && !(env && std::strcmp(env, "0") == 0);
+  }
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -383,9 +390,9 @@ int moe_describe(const moe_problem* p, char* buf, size_t len) {
   };
   const int n = std::snprintf(
       buf, len,
-      "ffn1=%s<FFN1,BN=%d> ffn2=%s<FFN2,BN=%d> tile_rows=%d weights=%s%s%s combine=%s "
-      "max_items=%d workspace=%zu",
-      gemm(true), q.BN, gemm(false), q.BN, q.BN, q.mx ? "mxfp4" : q.blockwise ? "fp8-block128" : "fp8",
+      "ffn1=%s<FFN1,BN=%d> ffn2=%s<FFN2,BN=%d> tile_rows=%d ffn1_rows=%s weights=%s%s%s "
+      "combine=%s max_items=%d workspace=%zu",
+      gemm(true), q.BN, gemm(false), q.BN, q.BN, q.gather ? "gathered" : "permuted", q.mx ? "mxfp4" : q.blockwise ? "fp8-block128" : "fp8",
       q.packed ? ",packed" : "", q.L > 0 ? " latent=bf16-pair-gemms" : "",
       q.fused ? "fused-ffn2-fp32-sum" : q.L > 0 ? "gather-rmsnorm" : "gather", q.max_items,
       q.total);
@@ -590,15 +597,18 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   }
   {
     StageTimer t(MOE_STAGE_SCATTER, s);
-    MOE_TRY(launch_quant_scatter(xin, perm, xq, xscale, q.T, q.K, q.k, q.shared ? q.R : -1,
-                                 di->err, s, q.fused ? at<float>(ws, q.acc) : nullptr));
+    if (q.gather)  // one fp8 row per token (rows 0..T-1 of xq); FFN1 gathers them
+      MOE_TRY(launch_quant_scatter(xin, nullptr, xq, xscale, q.T, q.K, 0, 0, di->err, s,
+                                   q.fused ? at<float>(ws, q.acc) : nullptr));
+    else
+      MOE_TRY(launch_quant_scatter(xin, perm, xq, xscale, q.T, q.K, q.k, q.shared ? q.R : -1,
+                                   di->err, s, q.fused ? at<float>(ws, q.acc) : nullptr));
   }
   GroupedFfnArgs a = ffn_args(q, ws, xq, xscale, row_w, w13, w13_scale, w2, w2_scale, shared_w13,
                               shared_w13_scale, shared_w2, shared_w2_scale, y, q.RT, di->err);
-  if (q.fused) {
-    a.out_acc = at<float>(ws, q.acc);
-    a.src = at<int32_t>(ws, q.src);
-  }
+  a.src = at<int32_t>(ws, q.src);
+  a.gather = q.gather ? 1 : 0;
+  if (q.fused) a.out_acc = at<float>(ws, q.acc);
   st = run_experts(q, a, q.RT, s);
   if (st) return st;
   if (q.fused) {

@@ -153,3 +153,13 @@ def test_mx_pair_plan(m):
     # I = 384 gives three 128-row blocks: FFN1 stays on single SMs
     d = m.moe_describe(m.make_problem(80, 512, 384, 12, 3, wfmt=m.W_MXFP4, flags=m.F_PACKED_WEIGHTS))
     assert "ffn1=grouped_mx_kernel" in d and "ffn2=grouped_mx_pair_kernel" in d
+
+
+def test_row_gather_plan(m):
+    # the single-SM fp8 per-channel path gathers FFN1 rows by token; the SM-pair,
+    # block-wise and MXFP4 paths read permuted rows
+    assert "ffn1_rows=gathered" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048))
+    assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(16384, 8192, 2048, 256, 8,
+                                                                 I_shared=2048))
+    assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8,
+                                                                 wfmt=m.W_FP8_BLOCK))

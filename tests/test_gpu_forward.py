@@ -39,6 +39,15 @@ def _check(orc, cfg, n_sample):
     return G.assert_close(got, ref_f, f"moe_forward {cfg.name}")
 
 
+@pytest.mark.parametrize("cfg", [SHARED_SMALL, RAGGED, KE], ids=ids)
+def test_forward_small_permuted_rows(orc, cfg, monkeypatch):
+    # S4 writes the permuted fp8 rows and FFN1 reads them by TMA, instead of the
+    # default per-token rows gathered by the FFN1 producer
+    monkeypatch.setenv("MOE_GATHER", "0")
+    assert "ffn1_rows=permuted" in G.lib().moe_describe(G.problem(cfg))
+    _check(orc, cfg, n_sample=cfg.T)
+
+
 @pytest.mark.parametrize("cfg", SMALL, ids=ids)
 def test_forward_small(orc, cfg):
     _check(orc, cfg, n_sample=10 ** 9)
