@@ -165,7 +165,8 @@ Plan make_plan(const moe_problem* p) {
   q.fused = (p->flags & MOE_F_FUSED_COMBINE) && !q.L && !q.mx && !q.blockwise &&
             !q.shared_bf16 && !use_pair_gemm(q);
   // the single-SM fp8 per-channel FFN1 gathers its rows by token (MOE_GATHER=0:
-  // S4 writes the permuted rows instead)
+  // S4 writes the permuted rows instead).  The SM-pair FFN1 reads permuted rows:
+  // gathering 128 rows per stage with 16-byte cp.async made it 3x slower.
   {
     const char* env = std::getenv("MOE_GATHER");
     q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && !(env && std::strcmp(env, "0") == 0);

@@ -156,7 +156,7 @@ def test_mx_pair_plan(m):
 
 
 def test_row_gather_plan(m):
-    # the single-SM fp8 per-channel path gathers FFN1 rows by token; the SM-pair,
+    # the single-SM fp8 per-channel FFN1 gathers its rows by token; the SM-pair,
     # block-wise and MXFP4 paths read permuted rows
     assert "ffn1_rows=gathered" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048))
     assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(16384, 8192, 2048, 256, 8,

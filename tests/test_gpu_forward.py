@@ -6,7 +6,7 @@ import torch
 
 import _gpu as G
 import moe_inputs as mi
-from test_gpu_stages import BIASED, E3, KE, MAXE, RAGGED, T1
+from test_gpu_stages import BIASED, E3, KE, MAXE, RAGGED, SKEW_SMALL, T1
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +45,19 @@ def test_forward_small_permuted_rows(orc, cfg, monkeypatch):
     # default per-token rows gathered by the FFN1 producer
     monkeypatch.setenv("MOE_GATHER", "0")
     assert "ffn1_rows=permuted" in G.lib().moe_describe(G.problem(cfg))
+    _check(orc, cfg, n_sample=cfg.T)
+
+
+@pytest.mark.parametrize("small", ["m128", "m256"])
+@pytest.mark.parametrize("cfg", [SHARED_SMALL, RAGGED, SKEW_SMALL.with_(I_s=256)], ids=ids)
+def test_forward_sm_pairs(orc, cfg, small, monkeypatch):
+    # 256-row tiles on SM pairs for a small batch: items of <= 128 rows as
+    # M = 128 tiles, or as padded M = 256 tiles
+    monkeypatch.setenv("MOE_TILE_N", "256")
+    if small == "m256":
+        monkeypatch.setenv("MOE_PAIR_SMALL", "0")
+    d = G.lib().moe_describe(G.problem(cfg))
+    assert "ffn1=pair_gemm_kernel" in d and "ffn1_rows=permuted" in d, d
     _check(orc, cfg, n_sample=cfg.T)
 
 
