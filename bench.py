@@ -64,6 +64,7 @@ def workload_name(cfg):
     kind = {"decode": "Ling-style decode", "prefill": "Ling-style prefill",
             "decode_e32": "Ling-style decode, 32 experts (profiling case)",
             "prefill_e32": "Ling-style prefill, 32 experts (profiling case)",
+            "mid": "Ling-style mid-size batch",
             "latent": "Kimi-K3-style LatentMoE",
             "latent_e64": "Kimi-K3-style LatentMoE, 64 experts (profiling case)",
             "latent_k3": "Kimi-K3-style LatentMoE with K3 routing and activation",

@@ -164,12 +164,15 @@ Plan make_plan(const moe_problem* p) {
   // the fused combine runs in the single-SM fp8 per-channel FFN2 epilogue
   q.fused = (p->flags & MOE_F_FUSED_COMBINE) && !q.L && !q.mx && !q.blockwise &&
             !q.shared_bf16 && !use_pair_gemm(q);
-  // the single-SM fp8 per-channel FFN1 gathers its rows by token (MOE_GATHER=0:
-  // S4 writes the permuted rows instead).  The SM-pair FFN1 reads permuted rows:
-  // gathering 128 rows per stage with 16-byte cp.async made it 3x slower.
+  // With 32-row tiles the single-SM fp8 per-channel FFN1 gathers its rows by
+  // token (MOE_GATHER=0: S4 writes the permuted rows instead).  Larger tiles
+  // read permuted rows: the producer's 16-byte cp.async copies (8 per row and
+  // stage) and the proxy fence before each stage's MMAs cost more than they
+  // save (T=2048, 128-row tiles: FFN1 1.84 vs 1.28 ms; SM pairs: 3x slower).
   {
     const char* env = std::getenv("MOE_GATHER");
-    q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && !(env && std::strcmp(env, "0") == 0);
+    q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && q.BN <= 32 &&
+               !(env && std::strcmp(env, "0") == 0);
   }
   size_t o = 0;
   auto take = [&](size_t bytes) {

@@ -98,6 +98,9 @@ CONFIGS = {
                             wfmt="mxfp4", shared_bf16=True),
     # profiling stand-in for "prefill": ~512 rows per expert, 32 experts
     "prefill_e32": MoEConfig("prefill_e32", T=2048, H=8192, I=2048, E=32, k=8, I_s=2048),
+    # between decode and prefill: Ling shapes, ~64 rows per expert (64-row
+    # tiles on single SMs)
+    "mid": MoEConfig("mid", T=2048, H=8192, I=2048, E=256, k=8, I_s=2048),
 }
 
 
