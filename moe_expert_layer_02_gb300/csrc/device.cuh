@@ -253,6 +253,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// The same without release semantics: the arrival does not wait for this
+// thread's earlier global stores.  For handing a tensor-memory accumulator back
+// to the MMA thread after tcgen05.wait::ld (the reads have completed) and
+// tcgen05.fence::before_thread_sync.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // TMA loads into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair (cta_group::2).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, int c0, int c1,

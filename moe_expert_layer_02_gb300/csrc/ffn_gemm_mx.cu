@@ -685,7 +685,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+      // the accumulator is free once this warp's tensor-memory loads are done
+      // (each group waited above); the output stores need not be complete
+      if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader0 + acc * 8);
     }
   }
 
