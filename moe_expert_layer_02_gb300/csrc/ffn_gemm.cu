@@ -596,8 +596,7 @@ cudaError_t launch_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   if (!make_map(&tws, 3, ws ? ws : w, winner, wrows, 1, BM)) return cudaErrorInvalidValue;
   if (!make_map(&tx, 2, x, K, a.rows_total, 1, BN)) return cudaErrorInvalidValue;
   if (BLK && (K / BK > C::MAX_KB || (FFN1 ? a.I : a.K) % BM)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(grouped_ffn_kernel<FFN1, BN, BLK>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = ensure_max_smem<grouped_ffn_kernel<FFN1, BN, BLK>>(C::SMEM);
   if (e != cudaSuccess) return e;
   count_launch();
   grouped_ffn_kernel<FFN1, BN, BLK><<<device_sm_count(), kThreads, C::SMEM, s>>>(tw, tws, tx, a);

@@ -541,8 +541,7 @@ cudaError_t launch_pair_gemm(const CUtensorMap& tw, const CUtensorMap& tws, cons
                              const CUtensorMap& tw2, const CUtensorMap& tx2,
                              const CUtensorMap& txh, const CUtensorMap& twh,
                              const CUtensorMap& twsh, const PairGemm& g, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<KIND, EPI>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
+  cudaError_t e = ensure_max_smem<pair_gemm_kernel<KIND, EPI>>(P_SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((device_sm_count() / 2) * 2);

@@ -753,8 +753,7 @@ cudaError_t launch_mx_impl(const GroupedFfnArgs& a, cudaStream_t s) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(grouped_mx_kernel<FFN1, BN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = ensure_max_smem<grouped_mx_kernel<FFN1, BN>>(C::SMEM);
   if (e != cudaSuccess) return e;
   count_launch();
   grouped_mx_kernel<FFN1, BN><<<device_sm_count(), MX_THREADS, C::SMEM, s>>>(tw, tx, a);
@@ -812,8 +811,7 @@ cudaError_t launch_mx_pair_impl(const GroupedFfnArgs& a, cudaStream_t s) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(grouped_mx_pair_kernel<FFN1, BN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = ensure_max_smem<grouped_mx_pair_kernel<FFN1, BN>>(C::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((device_sm_count() / 2) * 2);

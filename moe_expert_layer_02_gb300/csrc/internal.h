@@ -3,12 +3,31 @@
 #pragma once
 
 #include <cuda.h>
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace moe {
 
 // Tokens per warp chunk in the index kernels (one token per lane).
+// Raise kernel K's dynamic shared-memory limit to `bytes`, once per device
+// (the attribute belongs to the device's context; setting it on every launch
+// costs host time and is not needed inside a stream capture).  `bytes` must be
+// the same on every call for a given K.
+template <auto K>
+inline cudaError_t ensure_max_smem(int bytes) {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 constexpr int kChunk = 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;

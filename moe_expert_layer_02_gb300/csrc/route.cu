@@ -327,8 +327,7 @@ cudaError_t launch_router_impl(const void* x, const float* wr, const float* bias
   if (!router_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, C::BT) ||
       !router_map(&tw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, wr, H, E, C::BE))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<TW, EW, NS, WT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = ensure_max_smem<router_logits_kernel<TW, EW, NS, WT>>(C::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 grid((T + C::BT - 1) / C::BT, (E + C::BE - 1) / C::BE);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
