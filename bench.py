@@ -370,6 +370,30 @@ def run_ours(args, cfg):
     if rc != 0:
         raise SystemExit(f"device error word {rc} after the timed region")
 
+    # the same step replayed from a CUDA graph (as a serving loop would run a
+    # captured layer): the kernels' launch cost leaves the host entirely
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        g.replay()
+        torch.cuda.synchronize()
+        reps = max(min(args.steps, 100), 3)
+        gev0, gev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        gev1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = gev0.elapsed_time(gev1) / reps
+        del g
+    except RuntimeError as e:  # capture refused: report the eager numbers only
+        print(f"graph replay not measured: {e}", file=sys.stderr)
+    rc = m.moe_get_last_error()
+    if rc != 0:
+        raise SystemExit(f"device error word {rc} after the graph replays")
+
     # end to end through the public call with host buffers: every step's x is
     # copied in from pinned host memory and its output copied back, on a copy
     # stream with two device buffers each way, so step i+1's upload and step
@@ -462,6 +486,7 @@ def run_ours(args, cfg):
         "roofline": roof,
         "stages_ms": {k: v / max(stage_n[k], 1) for k, v in stage_ms.items()},
         "gpu_launches": launches,
+        "graph_ms_per_step": graph_ms,
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
