@@ -148,6 +148,19 @@ __device__ __forceinline__ float gated_act(int act, float g, float u) {
   return __fdividef(act ? 4.0f * tanhf(0.25f * g) : g, d) * u;
 }
 
+// ------------------------------------------------------------------ launches
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor on the stream is still
+// running.  pdl_wait() blocks until the predecessor has completed and its
+// memory is visible (a no-op for an ordinary launch); every kernel of the layer
+// calls it before its first global-memory access.  pdl_release() then lets
+// the next kernel start launching (it starts once every CTA of this grid has
+// released or exited).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  pdl_wait();  // the previous kernel's outputs are complete and visible
 
   const int NB = FFN1 ? a.I / BM : (a.K + 2 * BM - 1) / (2 * BM);  // tiles per item
   const int KB = FFN1 ? a.K / BK : a.I / BK;  // K stages per tile
@@ -543,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  pdl_release();  // the next kernel may start launching: this one is done
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -599,7 +601,9 @@ cudaError_t launch_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   cudaError_t e = ensure_max_smem<grouped_ffn_kernel<FFN1, BN, BLK>>(C::SMEM);
   if (e != cudaSuccess) return e;
   count_launch();
-  grouped_ffn_kernel<FFN1, BN, BLK><<<device_sm_count(), kThreads, C::SMEM, s>>>(tw, tws, tx, a);
+  e = launch_kernel(grouped_ffn_kernel<FFN1, BN, BLK>, dim3(device_sm_count()), dim3(kThreads),
+                    C::SMEM, s, 1, tw, tws, tx, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   cluster_sync();  // barriers of both CTAs exist before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  pdl_wait();  // the previous kernel's outputs are complete and visible
 
   const int NB = g.nb;
   const int KB = g.kb1 + g.kb2;
@@ -493,6 +494,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // neither CTA leaves while its peer may still signal it
+  pdl_release();  // the next kernel may start launching: this one is done
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, P_TMEM_COLS);
@@ -543,21 +545,9 @@ cudaError_t launch_pair_gemm(const CUtensorMap& tw, const CUtensorMap& tws, cons
                              const CUtensorMap& twsh, const PairGemm& g, cudaStream_t s) {
   cudaError_t e = ensure_max_smem<pair_gemm_kernel<KIND, EPI>>(P_SMEM);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((device_sm_count() / 2) * 2);
-  cfg.blockDim = dim3(P_THREADS);
-  cfg.dynamicSmemBytes = P_SMEM;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   count_launch();
-  e = cudaLaunchKernelEx(&cfg, pair_gemm_kernel<KIND, EPI>, tw, tws, tx, tw2, tx2, txh, twh, twsh,
-                         g);
+  e = launch_kernel(pair_gemm_kernel<KIND, EPI>, dim3((device_sm_count() / 2) * 2), dim3(P_THREADS),
+                    P_SMEM, s, 2, tw, tws, tx, tw2, tx2, txh, twh, twsh, g);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

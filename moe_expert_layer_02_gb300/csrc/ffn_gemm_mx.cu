@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  pdl_wait();  // the previous kernel's outputs are complete and visible
 
   const int NB = FFN1 ? a.I / MX_BM : a.K / (2 * MX_BM);  // tiles per item
   const int Kel = FFN1 ? a.K : a.I;  // reduction width in elements
@@ -403,6 +404,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  pdl_release();  // the next kernel may start launching: this one is done
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -519,6 +521,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   cluster_sync();  // barriers and the 2^0 blocks of both CTAs exist before any cross-CTA use
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  pdl_wait();  // the previous kernel's outputs are complete and visible
 
   const int NB = FFN1 ? a.I / MX_BM : a.K / (2 * MX_BM);  // single-SM tile columns per item
   const int NP = NB / 2;                                 // pair tiles per item
@@ -695,6 +698,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // neither CTA leaves while its peer may still read its shared memory
+  pdl_release();  // the next kernel may start launching: this one is done
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, C::TMEM_COLS);
@@ -756,7 +760,9 @@ cudaError_t launch_mx_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   cudaError_t e = ensure_max_smem<grouped_mx_kernel<FFN1, BN>>(C::SMEM);
   if (e != cudaSuccess) return e;
   count_launch();
-  grouped_mx_kernel<FFN1, BN><<<device_sm_count(), MX_THREADS, C::SMEM, s>>>(tw, tx, a);
+  e = launch_kernel(grouped_mx_kernel<FFN1, BN>, dim3(device_sm_count()), dim3(MX_THREADS), C::SMEM,
+                    s, 1, tw, tx, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -813,20 +819,9 @@ cudaError_t launch_mx_pair_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   }
   cudaError_t e = ensure_max_smem<grouped_mx_pair_kernel<FFN1, BN>>(C::SMEM);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((device_sm_count() / 2) * 2);
-  cfg.blockDim = dim3(MX_THREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   count_launch();
-  e = cudaLaunchKernelEx(&cfg, grouped_mx_pair_kernel<FFN1, BN>, tw, tx, ts, a);
+  e = launch_kernel(grouped_mx_pair_kernel<FFN1, BN>, dim3((device_sm_count() / 2) * 2),
+                    dim3(MX_THREADS), C::SMEM, s, 2, tw, tx, ts, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

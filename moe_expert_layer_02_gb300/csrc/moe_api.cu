@@ -352,6 +352,14 @@ int device_sm_count() {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* env = std::getenv("MOE_PDL");
+    return !(env && std::strcmp(env, "0") == 0);
+  }();
+  return on;
+}
+
 int* device_error_word() {
   DeviceInfo* d = device_info();
   return d ? d->err : nullptr;

@@ -46,6 +46,8 @@ __device__ __forceinline__ void build_chunk_bits(const int32_t* __restrict__ idx
 __global__ void __launch_bounds__(kWarps * 32)
     count_kernel(const int32_t* __restrict__ idx, int32_t* __restrict__ cc, int T, int E, int k,
                  int nch, int* err) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   extern __shared__ uint32_t s_bits[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
@@ -60,6 +62,8 @@ __global__ void __launch_bounds__(kWarps * 32)
                 const int32_t* __restrict__ off, const int32_t* __restrict__ cbase,
                 int32_t* __restrict__ perm, int32_t* __restrict__ src, float* __restrict__ row_w,
                 int T, int E, int k, int nch) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   extern __shared__ uint32_t s_bits[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
@@ -143,6 +147,8 @@ __global__ void __launch_bounds__(1024)
     scan_kernel(const int32_t* __restrict__ cc, int32_t* __restrict__ cbase, int32_t* cnt,
                 int32_t* off, int E, int nch, int R, int4* items, int32_t* n_items, int max_items,
                 int BN, int shared_row0, int shared_rows) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   __shared__ int s_cnt[kMaxExperts + 1];
   __shared__ int s_warp[33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,6 +200,8 @@ __global__ void __launch_bounds__(1024)
                        float* __restrict__ row_w, int T, int E, int k, int nch, int4* items,
                        int32_t* n_items, int max_items, int BN, int shared_row0,
                        int shared_rows, int* err) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   extern __shared__ uint32_t s_dyn[];
   uint32_t* bits = s_dyn;                                   // [nch][E] lane masks
   int* cb = reinterpret_cast<int*>(s_dyn + (size_t)nch * E);  // [nch][E] chunk bases
@@ -269,6 +277,8 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(1024)
     items_kernel(const int32_t* __restrict__ off, int E, int4* items, int32_t* n_items,
                  int max_items, int BN) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_warp[33];
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = off[e];
@@ -316,6 +326,8 @@ __global__ void __launch_bounds__(256)
     quant_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                          uint8_t* __restrict__ xq, float* __restrict__ xscale, int H, int k,
                          int shared_row0, int R, int* err, float* __restrict__ acc_zero) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   __shared__ float s_red[9];
   __shared__ int s_rows[kMaxTopK + 1];
   const int t = blockIdx.x;
@@ -360,6 +372,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     requant_kernel(const uint16_t* __restrict__ h, uint8_t* __restrict__ hq, float* __restrict__ hs,
                    int I) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   __shared__ float s_red[9];
   const size_t r = blockIdx.x;
   const uint4* hr = reinterpret_cast<const uint4*>(h + r * I);
@@ -388,6 +402,8 @@ template <int MAXV>
 __global__ void __launch_bounds__(256)
     requant_warp_kernel(const uint16_t* __restrict__ h, uint8_t* __restrict__ hq,
                         float* __restrict__ hs, int rows, int I) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   const int r = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -428,6 +444,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // out = bf16(acc), eight elements per thread and step.
 __global__ void __launch_bounds__(256)
     acc_to_bf16_kernel(const float4* __restrict__ acc, uint4* __restrict__ out, size_t n8) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = acc[2 * i], b = acc[2 * i + 1];
@@ -449,6 +467,8 @@ __global__ void __launch_bounds__(256)
     combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ perm,
                    const uint16_t* __restrict__ shared, uint16_t* __restrict__ out, int H, int k,
                    int R, int* err) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   const int t = blockIdx.x;
   const int v = blockIdx.y * blockDim.x + threadIdx.x;  // 16-byte column group
   const int nv = H / 8;
@@ -503,6 +523,8 @@ __global__ void __launch_bounds__(256)
     combine_rmsnorm_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ perm,
                            const uint16_t* __restrict__ gamma, uint16_t* __restrict__ yn, int L,
                            int k, int R, float eps, int* err) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   extern __shared__ float s_acc[];  // [L]
   __shared__ int s_rows[kMaxTopK];
   __shared__ float s_red[9];
@@ -579,10 +601,9 @@ cudaError_t launch_combine_rmsnorm(const void* y, const int32_t* perm, const voi
     if (e != cudaSuccess) return e;
   }
   count_launch();
-  combine_rmsnorm_kernel<<<T, 256, smem, s>>>(static_cast<const uint16_t*>(y), perm,
-                                              static_cast<const uint16_t*>(gamma),
-                                              static_cast<uint16_t*>(yn), L, k, T * k, eps, err);
-  return cudaGetLastError();
+  return launch_kernel(combine_rmsnorm_kernel, dim3(T), dim3(256), smem, s, 1,
+                       static_cast<const uint16_t*>(y), perm, static_cast<const uint16_t*>(gamma),
+                       static_cast<uint16_t*>(yn), L, k, T * k, eps, err);
 }
 
 cudaError_t launch_count(const int32_t* idx, int32_t* cc, int T, int E, int k, int* err,
@@ -591,17 +612,17 @@ cudaError_t launch_count(const int32_t* idx, int32_t* cc, int T, int E, int k, i
   const int blocks = (nch + kWarps - 1) / kWarps;
   const size_t smem = (size_t)kWarps * E * sizeof(uint32_t);
   count_launch();
-  count_kernel<<<blocks, kWarps * 32, smem, s>>>(idx, cc, T, E, k, nch, err);
-  return cudaGetLastError();
+  return launch_kernel(count_kernel, dim3(blocks), dim3(kWarps * 32), smem, s, 1, idx, cc, T, E, k,
+                       nch, err);
 }
 
 cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t* off, int T, int E,
                         int k, int4* items, int32_t* n_items, int max_items, int BN,
                         int shared_row0, int shared_rows, cudaStream_t s) {
   count_launch();
-  scan_kernel<<<1, 1024, 0, s>>>(cc, cbase, cnt, off, E, num_chunks(T), T * k, items, n_items,
-                                 max_items, BN, shared_row0, shared_rows);
-  return cudaGetLastError();
+  return launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, s, 1, cc, cbase, cnt, off, E,
+                       num_chunks(T), T * k, items, n_items, max_items, BN, shared_row0,
+                       shared_rows);
 }
 
 bool index_small_fits(int T, int E) {
@@ -623,9 +644,9 @@ cudaError_t launch_index_small(const int32_t* idx, const float* topk_w, int32_t*
       if (e != cudaSuccess) return e;
     }
     count_launch();
-    kern<<<1, 1024, smem, s>>>(idx, topk_w, cnt, off, perm, src, row_w, T, E, k, nch, items,
-                               n_items, max_items, BN, shared_row0, shared_rows, err);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(1), dim3(1024), smem, s, 1, idx, topk_w, cnt, off, perm, src,
+                         row_w, T, E, k, nch, items, n_items, max_items, BN, shared_row0,
+                         shared_rows, err);
   };
   if (k <= 8) return go(index_small_kernel<8>);
   if (k <= 16) return go(index_small_kernel<16>);
@@ -635,8 +656,8 @@ cudaError_t launch_index_small(const int32_t* idx, const float* topk_w, int32_t*
 cudaError_t launch_items_from_offsets(const int32_t* off, int E, int4* items, int32_t* n_items,
                                       int max_items, int BN, cudaStream_t s) {
   count_launch();
-  items_kernel<<<1, 1024, 0, s>>>(off, E, items, n_items, max_items, BN);
-  return cudaGetLastError();
+  return launch_kernel(items_kernel, dim3(1), dim3(1024), 0, s, 1, off, E, items, n_items, max_items,
+                       BN);
 }
 
 cudaError_t launch_rank(const int32_t* idx, const float* topk_w, const int32_t* off,
@@ -646,19 +667,17 @@ cudaError_t launch_rank(const int32_t* idx, const float* topk_w, const int32_t* 
   const int blocks = (nch + kWarps - 1) / kWarps;
   const size_t smem = (size_t)kWarps * E * sizeof(uint32_t);
   count_launch();
-  rank_kernel<<<blocks, kWarps * 32, smem, s>>>(idx, topk_w, off, cbase, perm, src, row_w, T, E,
-                                                 k, nch);
-  return cudaGetLastError();
+  return launch_kernel(rank_kernel, dim3(blocks), dim3(kWarps * 32), smem, s, 1, idx, topk_w, off,
+                       cbase, perm, src, row_w, T, E, k, nch);
 }
 
 cudaError_t launch_quant_scatter(const void* x, const int32_t* perm, void* xq, float* xscale,
                                  int T, int H, int k, int shared_row0, int* err, cudaStream_t s,
                                  float* acc_zero) {
   count_launch();
-  quant_scatter_kernel<<<T, 256, 0, s>>>(static_cast<const uint16_t*>(x), perm,
-                                         static_cast<uint8_t*>(xq), xscale, H, k, shared_row0,
-                                         T * k, err, acc_zero);
-  return cudaGetLastError();
+  return launch_kernel(quant_scatter_kernel, dim3(T), dim3(256), 0, s, 1,
+                       static_cast<const uint16_t*>(x), perm, static_cast<uint8_t*>(xq), xscale, H, k,
+                       shared_row0, T * k, err, acc_zero);
 }
 
 cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t n, cudaStream_t s) {
@@ -666,9 +685,8 @@ cudaError_t launch_acc_to_bf16(const float* acc, void* out, size_t n, cudaStream
   count_launch();
   const size_t n8 = n / 8;
   const int blocks = (int)std::min<size_t>((n8 + 255) / 256, (size_t)device_sm_count() * 8);
-  acc_to_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(acc),
-                                            static_cast<uint4*>(out), n8);
-  return cudaGetLastError();
+  return launch_kernel(acc_to_bf16_kernel, dim3(blocks), dim3(256), 0, s, 1,
+                       reinterpret_cast<const float4*>(acc), static_cast<uint4*>(out), n8);
 }
 
 cudaError_t launch_requant(const void* h, void* hq, float* hs, int rows, int I, cudaStream_t s) {
@@ -679,16 +697,19 @@ cudaError_t launch_requant(const void* h, void* hq, float* hs, int rows, int I, 
   const unsigned warps_blocks = (unsigned)(((size_t)rows * 32 + 255) / 256);
   const int per_lane = (I / 8 + 31) / 32;  // 16-byte vectors per lane
   if (per_lane <= 4)
-    requant_warp_kernel<4><<<warps_blocks, 256, 0, s>>>(hp, qp, hs, rows, I);
+    return launch_kernel(requant_warp_kernel<4>, dim3(warps_blocks), dim3(256), 0, s, 1, hp, qp, hs,
+                         rows, I);
   else if (per_lane <= 8)
-    requant_warp_kernel<8><<<warps_blocks, 256, 0, s>>>(hp, qp, hs, rows, I);
+    return launch_kernel(requant_warp_kernel<8>, dim3(warps_blocks), dim3(256), 0, s, 1, hp, qp, hs,
+                         rows, I);
   else if (per_lane <= 12)  // I = 3072: fewer registers, more rows per SM
-    requant_warp_kernel<12><<<warps_blocks, 256, 0, s>>>(hp, qp, hs, rows, I);
+    return launch_kernel(requant_warp_kernel<12>, dim3(warps_blocks), dim3(256), 0, s, 1, hp, qp, hs,
+                         rows, I);
   else if (per_lane <= 16)
-    requant_warp_kernel<16><<<warps_blocks, 256, 0, s>>>(hp, qp, hs, rows, I);
+    return launch_kernel(requant_warp_kernel<16>, dim3(warps_blocks), dim3(256), 0, s, 1, hp, qp, hs,
+                         rows, I);
   else
-    requant_kernel<<<rows, 256, 0, s>>>(hp, qp, hs, I);
-  return cudaGetLastError();
+    return launch_kernel(requant_kernel, dim3(rows), dim3(256), 0, s, 1, hp, qp, hs, I);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* perm, const void* shared, void* out,
@@ -700,14 +721,17 @@ cudaError_t launch_combine(const void* y, const int32_t* perm, const void* share
   const auto* sp = static_cast<const uint16_t*>(shared);
   auto* op = static_cast<uint16_t*>(out);
   if (k <= 4)
-    combine_kernel<4><<<grid, 256, 0, s>>>(yp, perm, sp, op, H, k, T * k, err);
+    return launch_kernel(combine_kernel<4>, grid, dim3(256), 0, s, 1, yp, perm, sp, op, H, k, T * k,
+                         err);
   else if (k <= 8)
-    combine_kernel<8><<<grid, 256, 0, s>>>(yp, perm, sp, op, H, k, T * k, err);
+    return launch_kernel(combine_kernel<8>, grid, dim3(256), 0, s, 1, yp, perm, sp, op, H, k, T * k,
+                         err);
   else if (k <= 16)
-    combine_kernel<16><<<grid, 256, 0, s>>>(yp, perm, sp, op, H, k, T * k, err);
+    return launch_kernel(combine_kernel<16>, grid, dim3(256), 0, s, 1, yp, perm, sp, op, H, k, T * k,
+                         err);
   else
-    combine_kernel<32><<<grid, 256, 0, s>>>(yp, perm, sp, op, H, k, T * k, err);
-  return cudaGetLastError();
+    return launch_kernel(combine_kernel<32>, grid, dim3(256), 0, s, 1, yp, perm, sp, op, H, k, T * k,
+                         err);
 }
 
 }  // namespace moe

@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(RouterCfg<TW, EW, NS, WT>::THREADS,
     fence_mbarrier_init();
   }
   __syncthreads();
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
 
   auto issue = [&](int c) {  // stage c into slot c % STAGES
     const uint32_t st = smem_u32(smem + (c % C::STAGES) * C::STAGE);
@@ -243,6 +245,8 @@ __global__ void __launch_bounds__(256)
     topk_kernel(const float* __restrict__ logits, const float* __restrict__ sel_bias,
                 int32_t* __restrict__ idx, float* __restrict__ w, int T, int E, int k,
                 int sigmoid) {
+  pdl_wait();  // the previous kernel's outputs are complete and visible
+  pdl_release();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -332,7 +336,9 @@ cudaError_t launch_router_impl(const void* x, const float* wr, const float* bias
   const dim3 grid((T + C::BT - 1) / C::BT, (E + C::BE - 1) / C::BE);
   if (grid.y > 65535u) return cudaErrorInvalidValue;
   count_launch();
-  router_logits_kernel<TW, EW, NS, WT><<<grid, C::THREADS, C::SMEM, s>>>(tx, tw, bias, logits, T, H, E, err);
+  e = launch_kernel(router_logits_kernel<TW, EW, NS, WT>, grid, dim3(C::THREADS), C::SMEM, s, 1, tx,
+                    tw, bias, logits, T, H, E, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -377,18 +383,23 @@ cudaError_t launch_topk(const float* logits, const float* sel_bias, int sigmoid,
   count_launch();
   const int vpl = (E + 31) / 32;
   if (vpl <= 1)
-    topk_kernel<1><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
+    return launch_kernel(topk_kernel<1>, dim3(blocks), dim3(256), 0, s, 1, logits, sel_bias, idx, w,
+                         T, E, k, sigmoid);
   else if (vpl <= 2)
-    topk_kernel<2><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
+    return launch_kernel(topk_kernel<2>, dim3(blocks), dim3(256), 0, s, 1, logits, sel_bias, idx, w,
+                         T, E, k, sigmoid);
   else if (vpl <= 4)
-    topk_kernel<4><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
+    return launch_kernel(topk_kernel<4>, dim3(blocks), dim3(256), 0, s, 1, logits, sel_bias, idx, w,
+                         T, E, k, sigmoid);
   else if (vpl <= 8)
-    topk_kernel<8><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
+    return launch_kernel(topk_kernel<8>, dim3(blocks), dim3(256), 0, s, 1, logits, sel_bias, idx, w,
+                         T, E, k, sigmoid);
   else if (vpl <= 16)
-    topk_kernel<16><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
+    return launch_kernel(topk_kernel<16>, dim3(blocks), dim3(256), 0, s, 1, logits, sel_bias, idx, w,
+                         T, E, k, sigmoid);
   else
-    topk_kernel<32><<<blocks, 256, 0, s>>>(logits, sel_bias, idx, w, T, E, k, sigmoid);
-  return cudaGetLastError();
+    return launch_kernel(topk_kernel<32>, dim3(blocks), dim3(256), 0, s, 1, logits, sel_bias, idx, w,
+                         T, E, k, sigmoid);
 }
 
 }  // namespace moe
