@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(256)
 // feasibility analysis", s.2.4: routed experts -> routed_expert_norm ->
 // up_proj).  acc = sum_j y[perm[t,j]] in fp32 (j ascending), then
 // yn = bf16(acc / sqrt(mean(acc^2) + eps) * gamma).
+template <int KMAX>
 __global__ void __launch_bounds__(256)
     combine_rmsnorm_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ perm,
                            const uint16_t* __restrict__ gamma, uint16_t* __restrict__ yn, int L,
@@ -541,13 +542,20 @@ __global__ void __launch_bounds__(256)
   const int nv = L / 8;
   float sq = 0.0f;
   for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    // all k row loads in flight before the sum (j ascending, as in the gather)
+    uint4 raw[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k && s_rows[j] >= 0)
+        raw[j] = __ldcs(reinterpret_cast<const uint4*>(y + (size_t)s_rows[j] * L) + v);
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      if (s_rows[j] < 0) continue;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j >= k || s_rows[j] < 0) continue;
       float f[8];
-      unpack_bf16x8(reinterpret_cast<const uint4*>(y + (size_t)s_rows[j] * L)[v], f);
+      unpack_bf16x8(raw[j], f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] += f[i];
     }
@@ -595,15 +603,21 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_combine_rmsnorm(const void* y, const int32_t* perm, const void* gamma, void* yn,
                                    int T, int L, int k, float eps, int* err, cudaStream_t s) {
   const size_t smem = (size_t)L * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(combine_rmsnorm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  count_launch();
-  return launch_kernel(combine_rmsnorm_kernel, dim3(T), dim3(256), smem, s, 1,
-                       static_cast<const uint16_t*>(y), perm, static_cast<const uint16_t*>(gamma),
-                       static_cast<uint16_t*>(yn), L, k, T * k, eps, err);
+  auto go = [&](auto kern) {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    count_launch();
+    return launch_kernel(kern, dim3(T), dim3(256), smem, s, 1, static_cast<const uint16_t*>(y),
+                         perm, static_cast<const uint16_t*>(gamma), static_cast<uint16_t*>(yn), L,
+                         k, T * k, eps, err);
+  };
+  if (k <= 4) return go(combine_rmsnorm_kernel<4>);
+  if (k <= 8) return go(combine_rmsnorm_kernel<8>);
+  if (k <= 16) return go(combine_rmsnorm_kernel<16>);
+  return go(combine_rmsnorm_kernel<kMaxTopK>);
 }
 
 cudaError_t launch_count(const int32_t* idx, int32_t* cc, int T, int E, int k, int* err,
