@@ -264,16 +264,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  pdl_wait();  // the previous kernel's outputs are complete and visible
+  // (with programmatic dependent launch the tile list is final here: it is
+  // written by an index kernel that releases its dependents only at its end,
+  // at least one launch before this one; everything else the previous
+  // kernel writes is read only after pdl_wait)
 
   const int NB = FFN1 ? a.I / BM : (a.K + 2 * BM - 1) / (2 * BM);  // tiles per item
   const int KB = FFN1 ? a.K / BK : a.I / BK;  // K stages per tile
   const int n_items = min(*a.n_items, a.max_items);
   const int n_tiles = n_items * NB;
 
+  auto load_weights = [&](int tile, int kb, uint32_t st, uint32_t fb) {
+    const int4 it = a.items[tile / NB];
+    const int nb = tile % NB;
+    const bool shared = it.x >= a.E;
+    const CUtensorMap* tw = shared ? &tm_ws : &tm_w;
+    const int gc = shared ? 0 : it.x;
+    // (rows past the last block, FFN2 with K % 256 == 128, read as zeros)
+    if (a.packed) {  // tile-major weights: tile (row block, k block) is contiguous
+      tma_load_3d(st, tw, 0, BM * (wblock<FFN1>(a, 0, nb) * KB + kb), gc, fb);
+      tma_load_3d(st + C::A_BYTES, tw, 0, BM * (wblock<FFN1>(a, 1, nb) * KB + kb), gc, fb);
+    } else {
+      tma_load_3d(st, tw, kb * BK, wblock<FFN1>(a, 0, nb) * BM, gc, fb);
+      tma_load_3d(st + C::A_BYTES, tw, kb * BK, wblock<FFN1>(a, 1, nb) * BM, gc, fb);
+    }
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (gat || lane == 0) {  // the whole warp when it gathers rows, else lane 0
+      // The weights of the first STAGES stages do not depend on the previous
+      // kernel: their loads start before pdl_wait (while that kernel still
+      // runs); the activation rows of those stages follow after it.
+      int pre = 0;
+      if (lane == 0) {
+        int tile = blockIdx.x, kb = 0;
+        for (; pre < C::STAGES && tile < n_tiles; ++pre) {
+          const uint32_t fb = smem_u32(&full[pre]);
+          mbar_arrive_expect_tx(fb, gat ? C::NA * C::A_BYTES : C::STAGE_BYTES);
+          load_weights(tile, kb, smem_u32(smem + pre * C::STAGE_BYTES), fb);
+          s_issued[pre] = 1u;
+          if (++kb == KB) {
+            kb = 0;
+            tile += gridDim.x;
+          }
+        }
+      }
+      if (gat) pre = __shfl_sync(0xffffffffu, pre, 0);
+      pdl_wait();  // the previous kernel's outputs are complete and visible
+      int seq = 0;  // stages handled so far
       int stage = 0;
       uint32_t phase = 0;
       const uint8_t* xtok = static_cast<const uint8_t*>(a.xq);
@@ -281,11 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stop = lane == 0 ? *s_abort : 0;
         if (gat) stop = __shfl_sync(0xffffffffu, stop, 0);
         if (stop) break;
-        const int item = tile / NB, nb = tile - item * NB;
+        const int item = tile / NB;
         const int4 it = a.items[item];
         const bool shared = it.x >= a.E;
-        const CUtensorMap* tw = shared ? &tm_ws : &tm_w;
-        const int gc = shared ? 0 : it.x;
         const int n = min(BN, (it.z + 15) & ~15);  // rows the MMAs read
         if (gat) {
           // token of each row the MMAs read; the padding rows repeat a real one
@@ -297,26 +334,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
-          int got = 1;
-          if (lane == 0) got = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort) ? 1 : 0;
-          if (gat) got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
-            ok = false;
-            break;
-          }
+        for (int kb = 0; kb < KB; ++kb, ++seq) {
           const uint32_t st = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t fb = smem_u32(&full[stage]);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(fb, gat ? C::NA * C::A_BYTES : C::STAGE_BYTES);
-            // (rows past the last block, FFN2 with K % 256 == 128, read as zeros)
-            if (a.packed) {  // tile-major weights: tile (row block, k block) is contiguous
-              tma_load_3d(st, tw, 0, BM * (wblock<FFN1>(a, 0, nb) * KB + kb), gc, fb);
-              tma_load_3d(st + C::A_BYTES, tw, 0, BM * (wblock<FFN1>(a, 1, nb) * KB + kb), gc, fb);
-            } else {
-              tma_load_3d(st, tw, kb * BK, wblock<FFN1>(a, 0, nb) * BM, gc, fb);
-              tma_load_3d(st + C::A_BYTES, tw, kb * BK, wblock<FFN1>(a, 1, nb) * BM, gc, fb);
+          if (seq >= pre) {  // (the first stages' weights are already on their way)
+            int got = 1;
+            if (lane == 0)
+              got = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, a.err, s_abort) ? 1 : 0;
+            if (gat) got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+              ok = false;
+              break;
             }
+            if (lane == 0) {
+              mbar_arrive_expect_tx(fb, gat ? C::NA * C::A_BYTES : C::STAGE_BYTES);
+              load_weights(tile, kb, st, fb);
+            }
+          }
+          if (lane == 0) {
             if (!gat) tma_load_2d(st + C::NA * C::A_BYTES, &tm_x, kb * BK, it.y, fb);
             s_issued[stage] = phase + 1u;
           }
@@ -347,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    pdl_wait();
     if (lane == 0 && BLK) {
       // one partial sum per stage, into buffer pcount % ACC_STAGES
       int stage = 0, pcount = 0;
@@ -437,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait();
     const int q = warp & 3;  // tensor-memory lane quarter this warp may access
     int it_local = 0;
     if (BLK) {

@@ -148,7 +148,6 @@ __global__ void __launch_bounds__(1024)
                 int32_t* off, int E, int nch, int R, int4* items, int32_t* n_items, int max_items,
                 int BN, int shared_row0, int shared_rows) {
   pdl_wait();  // the previous kernel's outputs are complete and visible
-  pdl_release();
   __shared__ int s_cnt[kMaxExperts + 1];
   __shared__ int s_warp[33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,6 +182,11 @@ __global__ void __launch_bounds__(1024)
   }
   __syncthreads();
   if (items) build_items(s_cnt, E, BN, shared_row0, shared_rows, items, n_items, max_items, s_warp);
+  // the tile list is final and visible before the next kernels may launch:
+  // the expert GEMMs read it before their pdl_wait
+  __threadfence();
+  __syncthreads();
+  pdl_release();
 }
 
 // S3 for small batches (T <= 1024) in one block of 1024 threads: the
@@ -201,7 +205,6 @@ __global__ void __launch_bounds__(1024)
                        int32_t* n_items, int max_items, int BN, int shared_row0,
                        int shared_rows, int* err) {
   pdl_wait();  // the previous kernel's outputs are complete and visible
-  pdl_release();
   extern __shared__ uint32_t s_dyn[];
   uint32_t* bits = s_dyn;                                   // [nch][E] lane masks
   int* cb = reinterpret_cast<int*>(s_dyn + (size_t)nch * E);  // [nch][E] chunk bases
@@ -258,6 +261,11 @@ __global__ void __launch_bounds__(1024)
   }
   __syncthreads();
   if (items) build_items(s_off, E, BN, shared_row0, shared_rows, items, n_items, max_items, s_warp);
+  // the tile list is final and visible before the next kernels may launch:
+  // the expert GEMMs read it before their pdl_wait
+  __threadfence();
+  __syncthreads();
+  pdl_release();
   if (!mine) return;
   const uint32_t below = (1u << lane) - 1u;
   const uint32_t* b = bits + (size_t)c * E;
@@ -278,12 +286,16 @@ __global__ void __launch_bounds__(1024)
     items_kernel(const int32_t* __restrict__ off, int E, int4* items, int32_t* n_items,
                  int max_items, int BN) {
   pdl_wait();  // the previous kernel's outputs are complete and visible
-  pdl_release();
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_warp[33];
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = off[e];
   __syncthreads();
   build_items(s_off, E, BN, 0, 0, items, n_items, max_items, s_warp);
+  // the tile list is final and visible before the next kernels may launch:
+  // the expert GEMMs read it before their pdl_wait
+  __threadfence();
+  __syncthreads();
+  pdl_release();
 }
 
 // Block-wide max of non-negative floats (blockDim.x == 256).
