@@ -32,10 +32,19 @@
 //     scale changes every 128 K, so the K-sum cannot run in one accumulator.
 //     With BLK the MMAs write each stage's partial sum into one of four (FFN1)
 //     or eight (FFN2) tensor-memory buffers (restarted per stage), and the
-//     epilogue warps add
-//     s[nb][kb] * partial into fp32 registers, stage by stage, before applying
+//     epilogue warps add s[nb][kb] * partial into fp32 registers, stage by
+//     stage, before applying
 //     the per-token scale and the activation at the end of the tile (tiles of
 //     at most 64 token rows, the registers' limit).
+//   * Row gather (FFN1 with 32-row tiles): the activations arrive as one fp8
+//     row per token, and the producer warp's 32 lanes copy each tile's rows
+//     (routed row r -> token src[r]) with 16-byte cp.async into the swizzled
+//     layout; each lane's completion arrives on the stage's full barrier and
+//     the MMA thread fences the generic proxy before reading the stage
+//     ("Optimising Ling-2.6-1T ...", s.4: tokens gathered inside the kernel).
+//   * Programmatic dependent launch: the producer issues the weight loads of
+//     its first ring stages before griddepcontrol.wait, so the weight stream
+//     starts while the previous kernel still runs.
 //   * Every pipeline wait is bounded; on timeout the CTA records
 //     MOE_ERR_TIMEOUT, drains its own TMA loads and MMAs and frees its tensor
 //     memory before returning.

@@ -32,7 +32,12 @@
 // warps 2-5 epilogue.  Both CTAs' TMA loads complete on the even CTA's `full`
 // barrier; the even CTA's commits arrive on both CTAs' `empty` / `tfull`
 // barriers; both epilogues release an accumulator on the even CTA's `tempty`
-// barrier.  All waits are bounded as in ffn_gemm.cu.
+// barrier (a relaxed arrive: the warp's tensor-memory loads have completed, its
+// output stores need not have).  All waits are bounded as in ffn_gemm.cu.
+//
+// Grouped items of at most 128 rows run as M = 128 MMAs (64 activation rows
+// per CTA), so an expert's small last item is not padded to 256 rows; see
+// is_small() for the accumulator layout of those tiles.
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
