@@ -163,3 +163,6 @@ def test_row_gather_plan(m):
                                                                  I_shared=2048))
     assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8,
                                                                  wfmt=m.W_FP8_BLOCK))
+    # 128-row single-SM tiles (~64 rows per expert) read permuted rows too
+    d = m.moe_describe(m.make_problem(2048, 8192, 2048, 256, 8, I_shared=2048))
+    assert "ffn1=grouped_ffn_kernel<FFN1,BN=128>" in d and "ffn1_rows=permuted" in d, d
