@@ -111,26 +111,20 @@ struct Plan {
 };
 
 int choose_bn(const moe_problem* p) {
+  // MOE_TILE_N overrides the choice with a tile height the weight format has
+  // kernels for; any other value is ignored
   const char* env = std::getenv("MOE_TILE_N");
-  if (env) {
-    int v = std::atoi(env);
-    if (v == 32 || v == 64 || v == 128 || v == 256) return v;
-  }
+  const int v = env ? std::atoi(env) : 0;
   const double avg = (double)p->T * p->top_k / (p->E > 0 ? p->E : 1);
   if (p->wfmt == MOE_W_FP8_E4M3_BLOCK128) {  // block-wise tiles keep sums in registers
-    if (env) {
-      int v = std::atoi(env);
-      if (v == 32 || v == 64) return v;
-    }
+    if (v == 32 || v == 64) return v;
     return avg <= 24.0 ? 32 : 64;
   }
   if (p->wfmt == MOE_W_MXFP4_E2M1_E8M0_B32) {  // block-scaled kernel tiles: 32, 64, 96 rows
-    if (env) {
-      int v = std::atoi(env);
-      if (v == 32 || v == 64 || v == 96) return v;
-    }
+    if (v == 32 || v == 64 || v == 96) return v;
     return avg <= 24.0 ? 32 : avg <= 48.0 ? 64 : 96;
   }
+  if (v == 32 || v == 64 || v == 128 || v == 256) return v;
   if (avg <= 24.0) return 32;
   if (avg <= 48.0) return 64;
   if (avg <= 96.0) return 128;

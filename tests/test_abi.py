@@ -166,3 +166,17 @@ def test_row_gather_plan(m):
     # 128-row single-SM tiles (~64 rows per expert) read permuted rows too
     d = m.moe_describe(m.make_problem(2048, 8192, 2048, 256, 8, I_shared=2048))
     assert "ffn1=grouped_ffn_kernel<FFN1,BN=128>" in d and "ffn1_rows=permuted" in d, d
+
+
+@pytest.mark.parametrize("tile,want", [("32", (32, 32, 32)), ("64", (64, 64, 64)),
+                                       ("96", (None, None, 96)), ("128", (128, None, None)),
+                                       ("256", (256, None, None)), ("48", (None, None, None))])
+def test_tile_override_respects_the_format(m, monkeypatch, tile, want):
+    # MOE_TILE_N takes a tile height only where the format has kernels for it
+    # (fp8 per-channel 32/64/128/256, block-wise 32/64, MXFP4 32/64/96);
+    # anything else leaves the automatic choice (~16 rows per expert: 32)
+    monkeypatch.setenv("MOE_TILE_N", tile)
+    for fmt, w in zip((m.W_FP8, m.W_FP8_BLOCK, m.W_MXFP4), want):
+        d = m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, wfmt=fmt))
+        bn = int(re.search(r"ffn1=\w+<FFN1,BN=(\d+)>", d).group(1))
+        assert bn == (w if w is not None else 32), (fmt, d)

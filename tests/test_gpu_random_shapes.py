@@ -1,0 +1,86 @@
+"""GPU parity of the whole layer on seeded random shapes and launch choices.
+
+Each case draws, from its own seed, a problem inside the shapes the library
+accepts (T, H, I, E, k, a shared expert or none, a latent projection or none,
+the weight format, softmax or sigmoid routing, SwiGLU or SiTU, row-major or
+packed weights) and the launch knobs a caller can set (tile height, the row
+path of FFN1, the index kernels, single-SM or SM-pair GEMMs, the router tile),
+runs moe_forward once, and compares every token with the oracle under the
+layer's tolerance.  The draws cover corners the named cases do not: one
+expert, k = E, ragged tails of every tile height, single-token batches."""
+import numpy as np
+import pytest
+
+import _gpu as G
+import moe_inputs as mi
+from test_gpu_forward import run_forward
+
+pytestmark = pytest.mark.gpu
+
+KINDS = ("fp8", "fp8_shared", "fp8_block", "mxfp4", "latent")
+N_CASES = 25
+
+
+def draw(seed: int):
+    r = np.random.default_rng(7000 + seed)
+    kind = KINDS[seed % len(KINDS)]
+    mx = kind in ("mxfp4", "latent")
+    H = int(256 * r.integers(1, 4)) if mx else int(128 * r.integers(1, 7))
+    I = int(128 * r.integers(1, 5))
+    E = int(r.choice([1, 2, 3, 5, 8, 13, 24, 40, 64]))
+    k = int(r.integers(1, min(E, 8) + 1))
+    T = int(r.choice([1, 2, 7, 33, 64, 100, 161, 257, 400]))
+    kw = dict(T=T, H=H, I=I, E=E, k=k)
+    if kind == "fp8_shared" or (kind == "fp8_block" and r.random() < 0.5):
+        kw["I_s"] = I
+    if kind == "fp8_block":
+        kw["wfmt"] = "fp8_block"
+    if kind == "mxfp4":
+        kw["wfmt"] = "mxfp4"
+    if kind == "latent":
+        kw["L"] = int(256 * r.integers(1, H // 256 + 1))
+        kw["wfmt"] = str(r.choice(["mxfp4", "fp8", "fp8_block"]))
+        kw["I_s"] = int(128 * r.integers(0, 4))
+        kw["shared_bf16"] = kw["I_s"] > 0
+    if r.random() < 0.3:
+        kw.update(routing="sigmoid", sel_bias=True)
+    elif r.random() < 0.3:
+        kw["zipf_bias"] = True
+    if r.random() < 0.3:
+        kw["act"] = "situ"
+    cfg = mi.MoEConfig(f"rand{seed}_{kind}", **kw)
+
+    tiles = {"fp8": (32, 64, 128, 256), "fp8_block": (32, 64), "mxfp4": (32, 64, 96)}[
+        "mxfp4" if cfg.wfmt == "mxfp4" else cfg.wfmt]
+    env = {}
+    if r.random() < 0.6:
+        env["MOE_TILE_N"] = str(int(r.choice(tiles)))
+    if r.random() < 0.3:
+        env["MOE_GATHER"] = "0"
+    if r.random() < 0.3:
+        env["MOE_INDEX"] = "3pass"
+    if r.random() < 0.2:
+        env["MOE_GEMM"] = "1cta"
+    if r.random() < 0.2:
+        env["MOE_PAIR_SMALL"] = "0"
+    if r.random() < 0.3:
+        env["MOE_MX"] = "1cta"
+    if r.random() < 0.5:
+        env["MOE_ROUTER_TILE"] = str(r.choice(["8x8", "8x16", "8x16s4", "12w8x16"]))
+    packed = bool(r.random() < 0.5)
+    return cfg, env, packed
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_forward_random_shape(orc, seed, monkeypatch):
+    cfg, env, packed = draw(seed)
+    for key, val in env.items():
+        monkeypatch.setenv(key, val)
+    m = G.lib()
+    p = G.problem(cfg, packed=packed)
+    what = f"{cfg} env={env} packed={packed} plan: {m.moe_describe(p)}"
+    inp = G.gpu_inputs(cfg)
+    out = run_forward(cfg, G.pack(cfg, inp) if packed else inp, packed=packed)
+    assert m.moe_get_last_error() == 0, what
+    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), G.host(inp))
+    G.assert_close(G.bf16_values(G.bf16_bits(out)), ref, what)
