@@ -28,7 +28,7 @@
  *   Formats: OCP 8-bit floating point spec (E4M3FN) and OCP Microscaling
  *   Formats v1.0 (E2M1, E8M0).
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *   - router logits are fp32 in one canonical order (32 strided fma chains,
  *     then a halving tree), so that top-k can be compared bit-exactly;
  *   - top-k ties go to the lower expert index; weights are the softmax over the
