@@ -1,13 +1,15 @@
 """GPU parity of the whole layer on seeded random shapes and launch choices.
 
-Each case draws, from its own seed, a problem inside the shapes the library
-accepts (T, H, I, E, k, a shared expert or none, a latent projection or none,
-the weight format, softmax or sigmoid routing, SwiGLU or SiTU, row-major or
-packed weights) and the launch knobs a caller can set (tile height, the row
-path of FFN1, the index kernels, single-SM or SM-pair GEMMs, the router tile),
-runs moe_forward once, and compares every token with the oracle under the
-layer's tolerance.  The draws cover corners the named cases do not: one
-expert, k = E, ragged tails of every tile height, single-token batches."""
+Each case draws, from its own seed, one of six problem kinds (fp8 per-channel
+experts with and without the shared expert, the same on SM pairs, block-wise
+fp8, MXFP4, LatentMoE) inside the shapes the library accepts (T, H, I, E, k,
+the shared expert and the latent projection, softmax or sigmoid routing,
+SwiGLU or SiTU, row-major or packed weights) and the launch knobs a caller can
+set (tile height, the row path of FFN1, the index kernels, single-SM or
+SM-pair GEMMs, the router tile), runs moe_forward once, and compares every
+token with the oracle under the layer's tolerance.  The draws cover corners
+the named cases do not: one expert, k = E, ragged tails of every tile height,
+single-token batches."""
 import numpy as np
 import pytest
 
@@ -17,21 +19,23 @@ from test_gpu_forward import run_forward
 
 pytestmark = pytest.mark.gpu
 
-KINDS = ("fp8", "fp8_shared", "fp8_block", "mxfp4", "latent")
-N_CASES = 25
+KINDS = ("fp8", "fp8_shared", "fp8_block", "mxfp4", "latent", "fp8_pair")
+N_CASES = 60
 
 
 def draw(seed: int):
     r = np.random.default_rng(7000 + seed)
     kind = KINDS[seed % len(KINDS)]
-    mx = kind in ("mxfp4", "latent")
-    H = int(256 * r.integers(1, 4)) if mx else int(128 * r.integers(1, 7))
+    wide = kind in ("mxfp4", "latent", "fp8_pair")  # H a multiple of 256
+    H = int(256 * r.integers(1, 4)) if wide else int(128 * r.integers(1, 7))
     I = int(128 * r.integers(1, 5))
     E = int(r.choice([1, 2, 3, 5, 8, 13, 24, 40, 64]))
     k = int(r.integers(1, min(E, 8) + 1))
     T = int(r.choice([1, 2, 7, 33, 64, 100, 161, 257, 400]))
+    if kind == "fp8_pair":  # enough rows for both M = 256 and M = 128 pair tiles
+        T = int(r.choice([64, 257, 400, 700]))
     kw = dict(T=T, H=H, I=I, E=E, k=k)
-    if kind == "fp8_shared" or (kind == "fp8_block" and r.random() < 0.5):
+    if kind in ("fp8_shared", "fp8_pair") or (kind == "fp8_block" and r.random() < 0.5):
         kw["I_s"] = I
     if kind == "fp8_block":
         kw["wfmt"] = "fp8_block"
@@ -59,7 +63,9 @@ def draw(seed: int):
         env["MOE_GATHER"] = "0"
     if r.random() < 0.3:
         env["MOE_INDEX"] = "3pass"
-    if r.random() < 0.2:
+    if kind == "fp8_pair":  # 256-row tiles on SM pairs
+        env["MOE_TILE_N"] = "256"
+    elif r.random() < 0.2:
         env["MOE_GEMM"] = "1cta"
     if r.random() < 0.2:
         env["MOE_PAIR_SMALL"] = "0"
@@ -67,7 +73,8 @@ def draw(seed: int):
         env["MOE_MX"] = "1cta"
     if r.random() < 0.5:
         env["MOE_ROUTER_TILE"] = str(r.choice(["8x8", "8x16", "8x16s4", "12w8x16"]))
-    packed = bool(r.random() < 0.5)
+    # the MXFP4 SM-pair kernels need packed weights
+    packed = bool(r.random() < (0.8 if cfg.wfmt == "mxfp4" else 0.5))
     return cfg, env, packed
 
 
