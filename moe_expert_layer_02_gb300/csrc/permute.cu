@@ -324,14 +324,18 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&f)[8]) {
   }
 }
 
+// e4m3 codes of four values (round-to-nearest-even, saturating), the first
+// in the low byte; two values per conversion instruction.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
 // q = e4m3(v / s) for 8 values (fp32 IEEE division, round-to-nearest-even).
 __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) lo |= (uint32_t)f32_to_e4m3(f[i] / s) << (8 * i);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) hi |= (uint32_t)f32_to_e4m3(f[4 + i] / s) << (8 * i);
-  return make_uint2(lo, hi);
+  return make_uint2(e4m3x4(f[0] / s, f[1] / s, f[2] / s, f[3] / s),
+                    e4m3x4(f[4] / s, f[5] / s, f[6] / s, f[7] / s));
 }
 
 __global__ void __launch_bounds__(256)

@@ -111,6 +111,37 @@ def test_permute_bit_exact(orc, cfg, path, monkeypatch):
         assert np.array_equal(xq[rows], q[src[rows]])
 
 
+def test_permute_quantisation_every_bf16_value(orc):
+    # S4's fp8 codes and scales against the oracle's x / s for every finite
+    # bf16 value: row i = [a_i, then every bf16 v with |v| <= a_i, both signs,
+    # and -0], where a_i runs over every 64th positive finite bf16 (subnormal
+    # to largest, so s = a_i / 448 also takes values below 2^-100, whose rows
+    # divide every element), one expert, k = 1 (rows stay in token order)
+    m = G.lib()
+    H = 65536
+    pos = np.arange(1, 0x7F80, dtype=np.uint16)  # positive finite bf16 patterns, ascending
+    amax = np.unique(np.concatenate([pos[::64], pos[-1:]]))
+    x = np.zeros((amax.size, H), np.uint16)
+    for i, a in enumerate(amax):
+        mags = pos[pos <= a]
+        vals = np.concatenate([[a], mags, mags | np.uint16(0x8000), [np.uint16(0x8000)]])
+        x[i, :vals.size] = vals
+    T = amax.size
+    s, q = orc.quant_rows(x)
+    p = m.make_problem(T, H, 128, 1, 1)
+    ws = G.workspace(p)
+    d = lambda *shape, dt=torch.int32: torch.empty(*shape, dtype=dt, device="cuda")
+    g_xq, g_xs = d(T, H, dt=torch.uint8), d(T, dt=torch.float32)
+    xt = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    m.moe_permute(p, torch.zeros(T, 1, dtype=torch.int32, device="cuda"), xt, d(1), d(2),
+                  d(T, 1), d(T), g_xq, g_xs, ws)
+    assert m.moe_get_last_error() == 0
+    assert np.array_equal(g_xs.cpu().numpy().view(np.uint32), s.view(np.uint32))
+    got = g_xq.cpu().numpy()
+    bad = np.nonzero(got != q)
+    assert bad[0].size == 0, (bad[0][:5], bad[1][:5], got[bad][:5], q[bad][:5])
+
+
 def test_permute_rejects_bad_indices_without_writing_out_of_range():
     m = G.lib()
     T, E, k, H = 40, 8, 2, 128
