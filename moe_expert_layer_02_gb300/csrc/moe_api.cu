@@ -125,8 +125,13 @@ int choose_bn(const moe_problem* p) {
     return avg <= 24.0 ? 32 : avg <= 48.0 ? 64 : 96;
   }
   if (v == 32 || v == 64 || v == 128 || v == 256) return v;
-  if (avg <= 24.0) return 32;
-  if (avg <= 48.0) return 64;
+  // fp8 per-channel: 128-row tiles up to ~96 rows per expert, even when
+  // experts hold far fewer rows (the MMAs read only the item's rows rounded
+  // up to 16).  A tile's stage then carries 48 KB, so four stages fill the
+  // shared memory, and four stages stream the weights fastest: T=512, H=8192,
+  // I=2048, E=256 top-8, FFN1 1.22 ms with 128-row tiles vs 1.34 ms with
+  // 32-row tiles and six stages, 1.23 ms with 64-row tiles and four stages,
+  // 1.26 ms with five
   if (avg <= 96.0) return 128;
   return 256;
 }
@@ -158,15 +163,15 @@ Plan make_plan(const moe_problem* p) {
   // the fused combine runs in the single-SM fp8 per-channel FFN2 epilogue
   q.fused = (p->flags & MOE_F_FUSED_COMBINE) && !q.L && !q.mx && !q.blockwise &&
             !q.shared_bf16 && !use_pair_gemm(q);
-  // With 32-row tiles the single-SM fp8 per-channel FFN1 gathers its rows by
-  // token (MOE_GATHER=0: S4 writes the permuted rows instead).  Larger tiles
-  // read permuted rows: the producer's 16-byte cp.async copies (8 per row and
-  // stage) and the proxy fence before each stage's MMAs cost more than they
-  // save (T=2048, 128-row tiles: FFN1 1.84 vs 1.28 ms; SM pairs: 3x slower).
+  // MOE_GATHER=1: the single-SM fp8 per-channel FFN1 gathers its rows by
+  // token and S4 writes one row per token.  Off by default: the producer's
+  // 16-byte cp.async copies (8 per row and stage) and the proxy fence before
+  // each stage's MMAs cost more than the smaller S4 saves (T=512, H=8192,
+  // I=2048, E=256 top-8, 128-row tiles: FFN1 1.35 vs 1.22 ms, S4 10.0 vs
+  // 12.9 us; T=2048: 1.84 vs 1.28 ms; on SM pairs 3x slower, not offered).
   {
     const char* env = std::getenv("MOE_GATHER");
-    q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && q.BN <= 32 &&
-               !(env && std::strcmp(env, "0") == 0);
+    q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && env && std::strcmp(env, "1") == 0;
   }
   size_t o = 0;
   auto take = [&](size_t bytes) {

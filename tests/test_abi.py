@@ -114,7 +114,7 @@ def test_binding_names_match_c_names(m):
 
 def test_describe_names_the_kernels(m):
     p = m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048)
-    assert m.moe_describe(p).startswith("ffn1=grouped_ffn_kernel<FFN1,BN=32>")
+    assert m.moe_describe(p).startswith("ffn1=grouped_ffn_kernel<FFN1,BN=128>")
     q = m.make_problem(16384, 8192, 2048, 256, 8, I_shared=2048)
     assert "pair_gemm_kernel<FFN1,BN=256>" in m.moe_describe(q)
     x = m.make_problem(4096, 7168, 3072, 896, 16, I_shared=6144, latent=3584, wfmt=m.W_MXFP4,
@@ -155,17 +155,24 @@ def test_mx_pair_plan(m):
     assert "ffn1=grouped_mx_kernel" in d and "ffn2=grouped_mx_pair_kernel" in d
 
 
-def test_row_gather_plan(m):
-    # the single-SM fp8 per-channel FFN1 gathers its rows by token; the SM-pair,
-    # block-wise and MXFP4 paths read permuted rows
-    assert "ffn1_rows=gathered" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048))
+def test_row_gather_plan(m, monkeypatch):
+    # MOE_GATHER=1: the single-SM fp8 per-channel FFN1 gathers its rows by
+    # token, at any tile height; the SM-pair, block-wise and MXFP4 paths read
+    # permuted rows, and so does everything by default
+    dec = lambda: m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048))
+    d = dec()
+    assert "ffn1=grouped_ffn_kernel<FFN1,BN=128>" in d and "ffn1_rows=permuted" in d, d
+    monkeypatch.setenv("MOE_GATHER", "1")
+    assert "ffn1_rows=gathered" in dec()
+    monkeypatch.setenv("MOE_TILE_N", "32")
+    assert "BN=32> " in dec() and "ffn1_rows=gathered" in dec()
+    monkeypatch.delenv("MOE_TILE_N")
     assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(16384, 8192, 2048, 256, 8,
                                                                  I_shared=2048))
     assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8,
                                                                  wfmt=m.W_FP8_BLOCK))
-    # 128-row single-SM tiles (~64 rows per expert) read permuted rows too
-    d = m.moe_describe(m.make_problem(2048, 8192, 2048, 256, 8, I_shared=2048))
-    assert "ffn1=grouped_ffn_kernel<FFN1,BN=128>" in d and "ffn1_rows=permuted" in d, d
+    assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8,
+                                                                 wfmt=m.W_MXFP4))
 
 
 @pytest.mark.parametrize("tile,want", [("32", (32, 32, 32)), ("64", (64, 64, 64)),
@@ -174,9 +181,10 @@ def test_row_gather_plan(m):
 def test_tile_override_respects_the_format(m, monkeypatch, tile, want):
     # MOE_TILE_N takes a tile height only where the format has kernels for it
     # (fp8 per-channel 32/64/128/256, block-wise 32/64, MXFP4 32/64/96);
-    # anything else leaves the automatic choice (~16 rows per expert: 32)
+    # anything else leaves the automatic choice (~16 rows per expert: 128 for
+    # fp8 per-channel, 32 for the others)
     monkeypatch.setenv("MOE_TILE_N", tile)
-    for fmt, w in zip((m.W_FP8, m.W_FP8_BLOCK, m.W_MXFP4), want):
+    for fmt, w, auto in zip((m.W_FP8, m.W_FP8_BLOCK, m.W_MXFP4), want, (128, 32, 32)):
         d = m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, wfmt=fmt))
         bn = int(re.search(r"ffn1=\w+<FFN1,BN=(\d+)>", d).group(1))
-        assert bn == (w if w is not None else 32), (fmt, d)
+        assert bn == (w if w is not None else auto), (fmt, d)

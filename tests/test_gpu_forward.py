@@ -39,12 +39,15 @@ def _check(orc, cfg, n_sample):
     return G.assert_close(got, ref_f, f"moe_forward {cfg.name}")
 
 
+@pytest.mark.parametrize("bn", [32, 128])
 @pytest.mark.parametrize("cfg", [SHARED_SMALL, RAGGED, KE], ids=ids)
-def test_forward_small_permuted_rows(orc, cfg, monkeypatch):
-    # S4 writes the permuted fp8 rows and FFN1 reads them by TMA, instead of the
-    # default per-token rows gathered by the FFN1 producer
-    monkeypatch.setenv("MOE_GATHER", "0")
-    assert "ffn1_rows=permuted" in G.lib().moe_describe(G.problem(cfg))
+def test_forward_small_gathered_rows(orc, cfg, bn, monkeypatch):
+    # MOE_GATHER=1: S4 writes one fp8 row per token and the FFN1 producer
+    # gathers each tile's rows by token, instead of the default permuted rows
+    # that FFN1 reads by TMA
+    monkeypatch.setenv("MOE_GATHER", "1")
+    monkeypatch.setenv("MOE_TILE_N", str(bn))
+    assert "ffn1_rows=gathered" in G.lib().moe_describe(G.problem(cfg))
     _check(orc, cfg, n_sample=cfg.T)
 
 

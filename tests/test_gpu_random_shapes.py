@@ -60,7 +60,7 @@ def draw(seed: int):
     if r.random() < 0.6:
         env["MOE_TILE_N"] = str(int(r.choice(tiles)))
     if r.random() < 0.3:
-        env["MOE_GATHER"] = "0"
+        env["MOE_GATHER"] = "1"
     if r.random() < 0.3:
         env["MOE_INDEX"] = "3pass"
     if kind == "fp8_pair":  # 256-row tiles on SM pairs
