@@ -80,9 +80,10 @@ struct Cfg {
   static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
   // At most four stages (32 KB of weights each) in flight: with five or six
   // the weight stream ran slower (T=512, H=8192, I=2048, E=256: FFN2 0.65 vs
-  // 0.69 ms with 32-row tiles, FFN1 1.23 vs 1.26 ms with 64-row tiles), and
-  // with three slower again (1.27 ms).  Block-wise tiles keep the deeper ring.
-  static constexpr int STAGES = cmin(kSmemBudget / STAGE_BYTES, BLK ? 12 : 4);
+  // 0.69 ms with 32-row tiles, FFN1 1.23 vs 1.26 ms with 64-row tiles;
+  // block-wise scales, 32-row tiles: layer 2.07 ms with four stages, 2.12
+  // with five, 2.20 with six), and with three slower again.
+  static constexpr int STAGES = cmin(kSmemBudget / STAGE_BYTES, 4);
   static constexpr int ACC_COLS = NA * BN;
   // accumulators per tile, or (BLK) per-stage partial-sum buffers, so the MMAs
   // can run that many stages ahead of the warps that scale and add them: four
