@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -140,11 +141,16 @@ def kernel_traffic(kernel: str, cfg_name: str):
 
 
 def source_sha() -> str:
+    """Hash of the expert-GEMM sources the traffic figure depends on: code only
+    (comments and whitespace do not change the kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_layer_02_gb300", "csrc")
     for n in ("ffn_gemm.cu", "device.cuh", "internal.h"):
-        with open(os.path.join(csrc, n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, n)) as f:
+            code = f.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -25,8 +25,9 @@
 //     [E][rows][K], activation rows through a 2-D map, 128-byte swizzle),
 //     warp 1 = MMA issuer (tcgen05.mma kind::f8f6f4, commit to mbarriers),
 //     warps 2-5 = epilogue (tcgen05.ld, scales, SiLU*gate or routing weight,
-//     bf16 stores).  Multi-stage smem ring + double-buffered accumulators
-//     (the write-up's "weight double-buffering" becomes this ring).
+//     bf16 stores).  A smem ring of at most four stages + double-buffered
+//     accumulators (the write-up's "weight double-buffering" becomes this
+//     ring; deeper rings streamed the weights more slowly).
 //   * Block-wise fp8 weights (one fp32 scale per 128 x 128 block, the format
 //     tpu-inference requires, "Kimi K3 ... feasibility analysis" s.3.7): the
 //     scale changes every 128 K, so the K-sum cannot run in one accumulator.
@@ -36,8 +37,8 @@
 //     stage, before applying
 //     the per-token scale and the activation at the end of the tile (tiles of
 //     at most 64 token rows, the registers' limit).
-//   * Row gather (FFN1 with 32-row tiles): the activations arrive as one fp8
-//     row per token, and the producer warp's 32 lanes copy each tile's rows
+//   * Row gather (FFN1, opt-in): the activations arrive as one fp8 row per
+//     token, and the producer warp's 32 lanes copy each tile's rows
 //     (routed row r -> token src[r]) with 16-byte cp.async into the swizzled
 //     layout; each lane's completion arrives on the stage's full barrier and
 //     the MMA thread fences the generic proxy before reading the stage
