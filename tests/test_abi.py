@@ -188,3 +188,16 @@ def test_tile_override_respects_the_format(m, monkeypatch, tile, want):
         d = m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, wfmt=fmt))
         bn = int(re.search(r"ffn1=\w+<FFN1,BN=(\d+)>", d).group(1))
         assert bn == (w if w is not None else auto), (fmt, d)
+
+
+@pytest.mark.parametrize("T,want", [(1, "grouped_ffn_kernel<FFN1,BN=128>"),
+                                    (512, "grouped_ffn_kernel<FFN1,BN=128>"),
+                                    (3072, "grouped_ffn_kernel<FFN1,BN=128>"),  # 96 rows / expert
+                                    (3104, "pair_gemm_kernel<FFN1,BN=256>"),    # 97 rows / expert
+                                    (16384, "pair_gemm_kernel<FFN1,BN=256>")])
+def test_tile_height_follows_rows_per_expert(m, T, want):
+    # fp8 per-channel: 128-row single-SM tiles up to 96 mean rows per expert
+    # (the weight stream is fastest there with a four-stage ring), 256-row
+    # tiles on SM pairs above
+    d = m.moe_describe(m.make_problem(T, 8192, 2048, 256, 8, I_shared=2048))
+    assert d.startswith("ffn1=" + want), d
