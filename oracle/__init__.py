@@ -98,6 +98,7 @@ def lib():
         L.orc_expert_rows.argtypes = [i32, i32, i64, i64, i64, P, P, P, P, P, P, P, P, P, P, P, P,
                                       ctypes.c_int]
         L.orc_combine.argtypes = [i64, i64, ctypes.c_int, P, P, P, P]
+        L.orc_latent_down.argtypes = [i64, i64, P, P, P, i64, P, ctypes.c_int]
         _lib = L
     return _lib
 
@@ -220,6 +221,20 @@ def quant_rows(x_bf16_u16):
     q = np.empty((T, H), dtype=np.uint8)
     lib().orc_quant_rows(T, H, _p(x), _p(s), _p(q))
     return s, q
+
+
+def latent_down(x_bf16_u16, wd_bf16_u16, tokens=None, nthreads: int = 0):
+    """LatentMoE down projection z = bf16(x Wd^T) (exact products, fp64 sum,
+    one nearest-even rounding) for the listed tokens: uint16 [n, L]."""
+    x = _c(x_bf16_u16, np.uint16)
+    wd = _c(wd_bf16_u16, np.uint16)
+    T, H = x.shape
+    L = wd.shape[0]
+    assert wd.shape[1] == H
+    toks = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
+    z = np.empty((toks.shape[0], L), dtype=np.uint16)
+    lib().orc_latent_down(H, L, _p(x), _p(wd), _p(toks), toks.shape[0], _p(z), nthreads)
+    return z
 
 
 def expert_rows(wfmt, off, xq, xs, row_w, w13, w13_scale, w2, w2_scale, want_h=False,

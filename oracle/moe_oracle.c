@@ -582,6 +582,38 @@ static void expert_slice(int fmt, int64_t K, int64_t I, int64_t e, const uint8_t
   }
 }
 
+/* z = bf16(x Wd^T) for one token [K3 s.2.4 routed_expert_down_proj]: each
+ * product of two bf16 values is exact in fp64 and the sum is taken in fp64
+ * (h ascending), then rounded once to nearest-even bf16. */
+static void latent_down_row(int64_t H, int64_t L, const uint16_t* xrow, const uint16_t* wd,
+                            uint16_t* z) {
+  for (int64_t l = 0; l < L; l++) {
+    double a = 0.0;
+    for (int64_t h = 0; h < H; h++) a += orc_bf16_decode(xrow[h]) * orc_bf16_decode(wd[l * H + h]);
+    z[l] = orc_bf16_from_double(a);
+  }
+}
+
+typedef struct {
+  int64_t H, L;
+  const uint16_t* x;
+  const uint16_t* wd;
+  const int32_t* tokens;
+  uint16_t* z;
+} down_ctx;
+
+static void down_body(int64_t i, void* c) {
+  down_ctx* d = (down_ctx*)c;
+  latent_down_row(d->H, d->L, d->x + (int64_t)d->tokens[i] * d->H, d->wd, d->z + i * d->L);
+}
+
+/* The LatentMoE down projection alone, for the listed tokens: z [n, L] bf16. */
+void orc_latent_down(int64_t H, int64_t L, const uint16_t* x, const uint16_t* wd,
+                     const int32_t* tokens, int64_t n_tokens, uint16_t* z, int nthreads) {
+  down_ctx c = {H, L, x, wd, tokens, z};
+  orc_parallel_for(n_tokens, nthreads, down_body, &c);
+}
+
 static void token_forward(int64_t i, void* c) {
   fwd_ctx* f = (fwd_ctx*)c;
   const orc_problem* p = f->p;
@@ -608,13 +640,8 @@ static void token_forward(int64_t i, void* c) {
 
   float sx;
   if (p->L > 0) {
-    /* z = bf16(x Wd^T) [K3 s.2.4 routed_expert_down_proj] */
     uint16_t* z = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)K);
-    for (int64_t l = 0; l < K; l++) {
-      double a = 0.0;
-      for (int64_t h = 0; h < H; h++) a += orc_bf16_decode(xrow[h]) * orc_bf16_decode(w->wd[l * H + h]);
-      z[l] = orc_bf16_from_double(a);
-    }
+    latent_down_row(H, K, xrow, w->wd, z);
     sx = quant_row_bf16(K, z, xq);
     free(z);
   } else {
