@@ -40,6 +40,12 @@
  *     Nothing aborts, throws or falls back to another implementation.
  *   - Shapes: H, I, I_shared (and latent) must be multiples of 128; T >= 0
  *     (T = 0 is a no-op); 1 <= top_k <= min(E, 32); E <= 1024.
+ *   - Per-device state: the library looks up, once per device and then keeps,
+ *     the device addresses of its own global variables (the error word, the
+ *     scratch array of moe_permute_static) and raises kernel attributes.  All
+ *     of it belongs to the device's primary context, which cudaDeviceReset
+ *     destroys: do not reset a device that this library has run on while the
+ *     process goes on calling the library.
  */
 #ifndef MOE_GB300_MOE_H_
 #define MOE_GB300_MOE_H_
@@ -116,7 +122,8 @@ const char* moe_status_string(int status);
  * run.  For logs and benchmarks; the text format may change. */
 int moe_describe(const moe_problem* p, char* buf, size_t len);
 
-/* Bytes of device workspace that moe_forward, moe_permute and moe_expert_ffn
+/* Bytes of device workspace that moe_forward, moe_permute, moe_expert_ffn and
+ * moe_latent_down
  * need for problem `p` (0 if `p` is invalid).  Pure host computation. */
 size_t moe_workspace_bytes(const moe_problem* p);
 
@@ -147,6 +154,23 @@ int moe_router_logits(const moe_problem* p, const void* x, const float* router_w
  *   else ignored) -> topk_idx [T, top_k] int32, topk_w [T, top_k] fp32 */
 int moe_route(const moe_problem* p, const float* logits, const float* bias, int32_t* topk_idx,
               float* topk_w, void* stream);
+
+/* S9 (LatentMoE) -- down projection onto the latent on which the routed experts
+ * run ("Kimi K3 ... feasibility analysis", s.2.4 routed_expert_down_proj):
+ * z[t,l] = bf16(sum_h x[t,h] * latent_down[l,h]), rounded to nearest-even from
+ * the exact dot product, so that the per-token fp8 quantisation of z that
+ * follows is reproducible bit for bit.  A tensor-core GEMM with short fp32
+ * accumulations computes every element; the elements lying so near a bf16
+ * rounding boundary that its remaining error could matter are recomputed
+ * exactly (two-fp32 sums of the exact bf16 products).  moe_forward runs this
+ * as its first latent step.
+ *   x [T, H] bf16, latent_down [latent, H] bf16 -> z [T, latent] bf16 (output)
+ *   ws / ws_bytes: workspace of at least moe_workspace_bytes(p) (per-element
+ *   recompute flags live there)
+ * Needs latent > 0; H and latent multiples of 256 and 4 H + 2 latent <=
+ * 163840 (else MOE_ERR_UNSUPPORTED); pointers 16-byte aligned. */
+int moe_latent_down(const moe_problem* p, const void* x, const void* latent_down, void* z,
+                    void* ws, size_t ws_bytes, void* stream);
 
 /* S3 + S4 -- expert-contiguous permutation and per-token fp8 quantisation.
  * counts[e] = #{(t,j): idx[t,j] = e}; offsets[e] = sum_{e'<e} counts[e'],
@@ -183,7 +207,9 @@ int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, in
  * cudaFree or allocating library routine.  All calls on a device share the
  * array and it keeps the last call's contents; every entry a call reads is
  * written earlier in the same call, but calls whose kernels overlap on the
- * GPU (other streams or threads) race on it and must be serialised. */
+ * GPU (other streams or threads) race on it and must be serialised.  The
+ * cached address does not survive a cudaDeviceReset of the device (see
+ * "Per-device state" above). */
 int moe_permute_static(const moe_problem* p, const int32_t* topk_idx, const void* x,
                        int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* src_row,
                        void* xq_perm, float* xscale_perm, void* stream);
@@ -312,6 +338,38 @@ int moe_watchdog_selftest(int32_t* role_status, void* stream);
 /* Number of kernels this library has launched in this process (all devices).
  * Host-side counter, for accounting; never reset. */
 int64_t moe_launch_count(void);
+
+/* Launch choices that change no result, only which kernels run and how
+ * (process-wide, every device).  At its first use the library reads them once
+ * from the environment -- MOE_TILE_N=<rows>, MOE_GATHER=1, MOE_INDEX=3pass,
+ * MOE_GEMM=1cta, MOE_PAIR_SMALL=0, MOE_MX=1cta,
+ * MOE_ROUTER_TILE=8x8|8x16|8x16s4|12w8x16, MOE_PDL=0 -- and moe_set_tuning
+ * replaces them for every later call.  For benchmarks and tests; the defaults
+ * are the measured best. */
+typedef struct {
+  int32_t tile_n;      /* 0 automatic; else token rows per grouped-GEMM tile where the
+                          weight format has kernels for it (fp8 per-channel 32, 64,
+                          128, 256; block-wise 32, 64; MXFP4 32, 64, 96), ignored
+                          otherwise                                                  */
+  int32_t ffn1_gather; /* 1: the single-SM fp8 per-channel FFN1 gathers its rows by
+                          token and S4 writes one row per token                      */
+  int32_t index_3pass; /* 1: count / scan / rank kernels even where one block would do */
+  int32_t gemm_1cta;   /* 1: single-SM fp8 grouped GEMMs for 256-row tiles as well    */
+  int32_t pair_small;  /* 1 (default): SM-pair items of <= 128 rows as M = 128 tiles  */
+  int32_t mx_1cta;     /* 1: single-SM MXFP4 grouped GEMMs                             */
+  int32_t router_tile; /* 0 automatic; 1: 8 warps of 8 tokens x 8 experts, 2: 8 x 16,
+                          3: 8 x 16 with four chunks a stage, 4: 12 warps of 8 x 16   */
+  int32_t pdl;         /* 1 (default): programmatic dependent launch between kernels */
+} moe_tuning;
+
+/* Current launch choices.  MOE_ERR_INVALID_ARG if t is NULL. */
+int moe_get_tuning(moe_tuning* t);
+
+/* Replace the launch choices (host only; takes effect for calls made after it
+ * returns).  MOE_ERR_INVALID_ARG, changing nothing, if t is NULL or a field is
+ * out of range (tile_n not 0/32/64/96/128/256, flags not 0/1, router_tile
+ * not 0..4). */
+int moe_set_tuning(const moe_tuning* t);
 
 /* Per-stage device timing.  mask selects the stages to time (bit s = stage
  * MOE_STAGE_s; -1 = all, 0 = off); each launch of a selected stage is

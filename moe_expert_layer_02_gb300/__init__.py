@@ -14,12 +14,13 @@ import os
 __all__ = [
     "MoEError", "MoEProblem", "make_problem", "load_library", "moe_workspace_bytes",
     "moe_router_logits", "moe_route", "moe_permute", "moe_permute_static", "moe_expert_ffn",
-    "moe_unpermute",
+    "moe_unpermute", "moe_latent_down",
     "moe_forward", "moe_get_last_error", "moe_launch_count", "moe_profile_enable",
     "moe_profile_read", "moe_pack_weights", "moe_watchdog_selftest", "moe_describe", "STAGES",
     "W_FP8",
     "W_MXFP4", "W_FP8_BLOCK", "F_ROUTER_BIAS", "F_SHARED_BF16", "F_PACKED_WEIGHTS",
-    "F_SIGMOID_ROUTING", "F_SITU", "F_FUSED_COMBINE",
+    "F_SIGMOID_ROUTING", "F_SITU", "F_FUSED_COMBINE", "MoETuning", "moe_get_tuning",
+    "moe_set_tuning", "tuned",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -52,6 +53,14 @@ class MoEProblem(ctypes.Structure):
                 ("latent", ctypes.c_int32), ("wfmt", ctypes.c_int32), ("flags", ctypes.c_uint32)]
 
 
+class MoETuning(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("tile_n", "ffn1_gather", "index_3pass", "gemm_1cta",
+                                             "pair_small", "mx_1cta", "router_tile", "pdl")]
+
+
+ROUTER_TILES = {"auto": 0, "8x8": 1, "8x16": 2, "8x16s4": 3, "12w8x16": 4}
+
+
 def make_problem(T, H, I, E, top_k, I_shared=0, latent=0, wfmt=W_FP8, flags=0) -> MoEProblem:
     return MoEProblem(T=T, H=H, I=I, E=E, top_k=top_k, I_shared=I_shared, latent=latent,
                       wfmt=wfmt, flags=flags)
@@ -61,7 +70,8 @@ _lib = None
 _EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_router_logits", "moe_route",
             "moe_permute", "moe_permute_static", "moe_expert_ffn", "moe_unpermute", "moe_forward",
             "moe_get_last_error", "moe_launch_count", "moe_profile_enable", "moe_profile_read",
-            "moe_pack_weights", "moe_watchdog_selftest", "moe_describe")
+            "moe_pack_weights", "moe_watchdog_selftest", "moe_describe", "moe_latent_down",
+            "moe_get_tuning", "moe_set_tuning")
 
 
 def load_library(path: str = LIB_PATH):
@@ -86,6 +96,9 @@ def load_library(path: str = LIB_PATH):
     L.moe_describe.argtypes = [PP, ctypes.c_char_p, ctypes.c_size_t]
     L.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_unpermute.argtypes = [PP, P, P, P, P, P]
+    L.moe_latent_down.argtypes = [PP, P, P, P, P, ctypes.c_size_t, P]
+    L.moe_get_tuning.argtypes = [ctypes.POINTER(MoETuning)]
+    L.moe_set_tuning.argtypes = [ctypes.POINTER(MoETuning)]
     L.moe_forward.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P]
     L.moe_get_last_error.argtypes = [P]
     L.moe_launch_count.restype = ctypes.c_int64
@@ -171,6 +184,12 @@ def moe_unpermute(p, y_rows, perm, shared, out, stream=None):
                                         _ptr(out), _stream(stream)), "moe_unpermute")
 
 
+def moe_latent_down(p, x, latent_down, z, ws, stream=None):
+    _check(load_library().moe_latent_down(ctypes.byref(p), _ptr(x), _ptr(latent_down), _ptr(z),
+                                          _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream(stream)), "moe_latent_down")
+
+
 def moe_forward(p, x, router_w, router_bias, w13, w13_scale, w2, w2_scale, shared_w13,
                 shared_w13_scale, shared_w2, shared_w2_scale, latent_down, latent_up,
                 latent_gamma, out, ws, stream=None):
@@ -194,6 +213,42 @@ def moe_describe(p) -> str:
     buf = ctypes.create_string_buffer(512)
     _check(load_library().moe_describe(ctypes.byref(p), buf, len(buf)), "moe_describe")
     return buf.value.decode()
+
+
+def moe_get_tuning() -> dict:
+    """The library's launch choices (moe_tuning) as a dict."""
+    t = MoETuning()
+    _check(load_library().moe_get_tuning(ctypes.byref(t)), "moe_get_tuning")
+    return {n: getattr(t, n) for n, _ in MoETuning._fields_}
+
+
+def moe_set_tuning(**kw):
+    """Change some launch choices (names of moe_tuning's fields; router_tile also
+    takes the names in ROUTER_TILES); the others keep their current values."""
+    cur = moe_get_tuning()
+    for k, v in kw.items():
+        if k not in cur:
+            raise KeyError(k)
+        cur[k] = ROUTER_TILES[v] if (k == "router_tile" and isinstance(v, str)) else int(v)
+    t = MoETuning(**cur)
+    _check(load_library().moe_set_tuning(ctypes.byref(t)), "moe_set_tuning")
+
+
+class tuned:
+    """Context manager: ``with tuned(tile_n=32): ...`` restores the previous
+    launch choices on exit."""
+
+    def __init__(self, **kw):
+        self.kw = kw
+
+    def __enter__(self):
+        self.saved = moe_get_tuning()
+        moe_set_tuning(**self.kw)
+        return self
+
+    def __exit__(self, *exc):
+        moe_set_tuning(**self.saved)
+        return False
 
 
 def moe_launch_count() -> int:

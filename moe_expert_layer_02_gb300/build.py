@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "_lib", "libmoe.so")
 SOURCES = ["route.cu", "permute.cu", "ffn_gemm.cu", "ffn_gemm_2cta.cu", "ffn_gemm_mx.cu",
-           "moe_api.cu", "permute_static.cu", "pack.cu", "watchdog.cu"]
+           "moe_api.cu", "permute_static.cu", "pack.cu", "watchdog.cu", "latent_down.cu"]
 HEADERS = [os.path.join(CSRC, "device.cuh"), os.path.join(CSRC, "internal.h"),
            os.path.join(ROOT, "include", "moe.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

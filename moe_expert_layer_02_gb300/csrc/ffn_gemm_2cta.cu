@@ -509,11 +509,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   }
 }
 
-// Grouped items of <= 128 rows as M = 128 tiles unless MOE_PAIR_SMALL=0.
-bool pair_small_tiles() {
-  const char* env = std::getenv("MOE_PAIR_SMALL");
-  return !(env && std::strcmp(env, "0") == 0);
-}
+// Grouped items of <= 128 rows as M = 128 tiles unless tuning().pair_small is 0.
+bool pair_small_tiles() { return tuning().pair_small != 0; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -847,10 +847,9 @@ cudaError_t launch_mx_bn(const GroupedFfnArgs& a, cudaStream_t s) {
 }  // namespace
 
 // SM pairs need moe_pack_weights' order and an even number of single-SM tile
-// columns; MOE_MX=1cta forces the single-SM kernel.
+// columns; tuning().mx_1cta forces the single-SM kernel.
 bool mx_pair_eligible(const GroupedFfnArgs& a, bool ffn1) {
-  const char* env = std::getenv("MOE_MX");
-  if (env && std::strcmp(env, "1cta") == 0) return false;
+  if (tuning().mx_1cta) return false;
   const int nb = ffn1 ? a.I / MX_BM : a.K / (2 * MX_BM);
   return a.packed && nb % 2 == 0 && (ffn1 || a.K % (2 * MX_BM) == 0);
 }

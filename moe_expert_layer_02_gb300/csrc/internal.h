@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
 
 // Tokens per warp chunk in the index kernels (one token per lane).
@@ -28,9 +30,13 @@ inline cudaError_t ensure_max_smem(int bytes) {
   return e;
 }
 
+// The launch choices of moe_tuning (include/moe.h): read once from the MOE_*
+// environment variables, replaced by moe_set_tuning; a snapshot per call.
+moe_tuning tuning();
+
 // Launch `kernel` on `s` with programmatic stream serialization (unless
-// MOE_PDL=0) and, when cluster_x > 1, clusters of cluster_x CTAs.  The kernel
-// must call pdl_wait() before touching global memory.
+// tuning().pdl is 0) and, when cluster_x > 1, clusters of cluster_x CTAs.  The
+// kernel must call pdl_wait() before touching global memory.
 bool pdl_enabled();
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -184,6 +190,15 @@ struct DenseGemmArgs {
 };
 cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s);
 
+// ---------------------------------------------------------------- latent_down.cu
+// z [T, L] = nearest-even bf16 of the exact x Wd^T (x [T, H], Wd [L, H] bf16):
+// a chunked SM-pair GEMM, then an exact recomputation of the elements whose
+// rounding the GEMM's remaining error could change.  flags: workspace of
+// latent_down_flag_bytes(T, L).  H % 128 == 0, L % 128 == 0, 4 H + 2 L <= 160 KiB.
+size_t latent_down_flag_bytes(int T, int L);
+cudaError_t launch_latent_down(const void* x, const void* wd, void* z, uint32_t* flags, int T,
+                               int H, int L, int* err, cudaStream_t s);
+
 // ---------------------------------------------------------------- ffn_gemm_mx.cu
 // MXFP4 routed experts (w13/w2 packed e2m1, w13_scale/w2_scale e8m0 bytes);
 // BN in {32, 64, 96}; no shared-expert group.
@@ -193,6 +208,9 @@ cudaError_t launch_ffn1_mx(const GroupedFfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn2_mx(const GroupedFfnArgs& a, cudaStream_t s);
 
 // Shared helpers (moe_api.cu)
+// Host-side validation of a problem (moe_status): the checks every entry point
+// that takes a moe_problem applies before it launches anything.
+int check_problem(const moe_problem* p);
 int device_sm_count();
 void count_launch();
 int* device_error_word();  // device address of the current device's error word

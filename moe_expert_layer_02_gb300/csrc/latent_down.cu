@@ -1,0 +1,484 @@
+// latent_down.cu -- the LatentMoE down projection z = bf16(x Wd^T), rounded
+// exactly ("Kimi K3 ... feasibility analysis", s.2.4: routed_expert_down_proj
+// maps the hidden x [T, H] to the latent [T, L] on which the routed experts
+// run).  x [T, H] and Wd [L, H] are bf16; z [T, L] is the nearest-even bf16 of
+// the exact dot product.
+//
+// Why exactly.  z is quantised per token to fp8 before the experts.  A z that
+// is one bf16 ulp off moves an e4m3 code now and then, and one moved code
+// perturbs h of every routed row of the token by ~0.1%, which shifts the bf16
+// rounding of some rows' amax and so their whole per-row fp8 requantisation.
+// A single tensor-core accumulation over K = 7168 misses the exactly rounded
+// bf16 in 0.4% of the elements (measured on a GB300; the share grows linearly
+// with K, 0.06% at K = 1024, so the accumulation error is systematic, not a
+// random walk), and through that cascade 7.6% of LatentMoE tokens ended more
+// than 5% of the output RMS away from the exact layer.
+//
+// How.
+//  1. latent_down_kernel: a GEMM on SM pairs (tcgen05.mma cta_group::2,
+//     kind::f16, bf16 operands, fp32 accumulation in tensor memory).  A tile is
+//     256 token rows (128 per CTA) x 128 latent features (64 weight rows staged
+//     per CTA).  The accumulation restarts every kChunkStages K stages (128 K,
+//     eight MMAs) in the next of four tensor-memory buffers, and eight epilogue
+//     warps (two per lane quarter, 64 columns each) add every chunk's partial
+//     sums into registers: S in fp32 (the dot product) and A in bf16 (the sum
+//     of the partials' magnitudes, which scales the remaining error).  Short
+//     accumulations keep the tensor core's own error ~30x smaller than one
+//     long one (0.014% of roundings off instead of 0.40%).  At the tile's end
+//     each element is rounded to bf16 from S and flagged when a bf16 rounding
+//     boundary lies within MOE_ZFLAG_ULPS * 2^-23 * A of S: only there can the
+//     remaining error change the rounding.
+//  2. latent_fix_kernel: one block per token recomputes every flagged element
+//     on the CUDA cores in two-fp32 arithmetic -- a product of two bf16 values
+//     is exact in fp32, and TwoSum keeps every addition's rounding error -- and
+//     rounds the unevaluated sum hi + lo to nearest-even bf16.
+//
+// Pipeline and waits follow ffn_gemm_2cta.cu: warp 0 TMA producer, warp 1 MMA
+// issuer (even CTA), warps 2-9 epilogue; both CTAs' loads complete on the even
+// CTA's `full` barriers; commits multicast to both CTAs; the epilogues hand a
+// buffer back on the even CTA's `tempty` barrier.  Every wait is bounded.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "device.cuh"
+#include "internal.h"
+
+// Margin of the flag test in units of 2^-23 * A (A = sum of the chunk partials'
+// magnitudes).  Calibrated on a GB300 at the LatentMoE shape (x [4096, 7168]
+// N(0,1), Wd N(0, 1/7168), 14.7 M elements, margin -> elements whose bf16
+// rounding still differed from the exact one): 0 -> 2013, 0.5 -> 12, 1 -> 1,
+// 2 -> 0.  Three units leave a factor 1.5 over the last; a larger margin only
+// sends more elements to the exact recomputation.
+#ifndef MOE_ZFLAG_ULPS
+#define MOE_ZFLAG_ULPS 3.0f
+#endif
+
+namespace moe {
+
+namespace {
+
+constexpr int LD_ROWS = 128;            // token rows per CTA (M = 256 per pair)
+constexpr int LD_N = 128;               // latent features per tile
+constexpr int LD_BK = 128;              // K bytes per stage (64 bf16)
+constexpr int LD_EL = LD_BK / 2;        // K elements per stage
+constexpr int LD_UMMA_B = 32;           // K bytes per tcgen05.mma (16 bf16)
+constexpr int LD_A_BYTES = LD_ROWS * LD_BK;         // 16 KB
+constexpr int LD_B_BYTES = (LD_N / 2) * LD_BK;      // 8 KB (this CTA's 64 weight rows)
+constexpr int LD_STAGE = LD_A_BYTES + LD_B_BYTES;   // 24 KB
+constexpr int LD_STAGES = 8;
+constexpr int kChunkStages = 2;         // K stages per tensor-core accumulation
+constexpr int LD_BUFS = 4;              // partial-sum buffers in tensor memory
+constexpr int LD_TMEM_COLS = LD_BUFS * LD_N;  // 512
+constexpr int LD_EPI_WARPS = 8;
+constexpr int LD_THREADS = 64 + 32 * LD_EPI_WARPS;  // 320
+constexpr int LD_NUM_BARS = 2 * LD_STAGES + 2 * LD_BUFS + 1;
+constexpr int LD_SMEM = 1024 + LD_STAGES * LD_STAGE + LD_NUM_BARS * 8 + 16 + LD_STAGES * 4;
+
+struct LatentDown {
+  int T, H, L;
+  void* z;           // [T, L] bf16
+  uint32_t* flags;   // [T, L / 32]: bit j of word w = element (t, 32 w + j) needs recomputing
+  int* err;
+};
+
+// f32 accumulate (bits 4-5 = 1), bf16 A and B (kind::f16 format 1 at bits 7-9
+// and 10-12), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__device__ __forceinline__ uint32_t ld_idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(LD_N >> 3) << 17) |
+         ((uint32_t)((2 * LD_ROWS) >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// True when rounding s to bf16 may differ from rounding the exact value, given
+// |exact - s| <= margin.  The bf16 rounding boundaries of |s| in [lo, lo + ulp)
+// are lo - ulp/2 (or lo - ulp/4 when lo is a power of two) and lo + ulp/2.
+__device__ __forceinline__ bool near_bf16_boundary(float s, float margin) {
+  const uint32_t u = __float_as_uint(s) & 0x7FFFFFFFu;
+  const uint32_t e = u >> 23;
+  if (e <= 8u) return margin > 0.0f;  // |s| < 2^-118 (or zero): recompute
+  const float ulp = __uint_as_float((e - 7u) << 23);        // bf16 ulp at |s|
+  const float mid = __uint_as_float((u & 0xFFFF0000u) | 0x8000u);
+  return margin >= 0.25f * ulp || fabsf(__uint_as_float(u) - mid) <= margin;
+}
+
+// 320 threads, one CTA per SM.  Ten warps put three on two of the four SM
+// sub-partitions, whose 16K registers then cap a thread at 168: the epilogue
+// keeps 64 fp32 sums, 64 loaded values and the magnitudes as 32 bf16 pairs.
+__global__ void __launch_bounds__(LD_THREADS, 1)
+    latent_down_kernel(const __grid_constant__ CUtensorMap tm_x,
+                       const __grid_constant__ CUtensorMap tm_w, const LatentDown g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LD_STAGES * LD_STAGE);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + LD_STAGES;
+  uint64_t* tfull = bars + 2 * LD_STAGES;
+  uint64_t* tempty = tfull + LD_BUFS;
+  uint64_t* drain = tempty + LD_BUFS;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + LD_NUM_BARS);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint32_t* s_issued = s_tmem + 4;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < LD_STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+      s_issued[s] = 0;
+    }
+    for (int b = 0; b < LD_BUFS; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 2 * LD_EPI_WARPS);  // the epilogue warps of both CTAs
+    }
+    mbar_init(smem_u32(drain), 1);
+    *s_abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(s_tmem), LD_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  pdl_wait();
+
+  const int n_rt = (g.T + 2 * LD_ROWS - 1) / (2 * LD_ROWS);
+  const int n_ct = g.L / LD_N;
+  const int n_tiles = n_rt * n_ct;
+  const int KB = g.H / LD_EL;               // K stages per tile
+  const int NCH = KB / kChunkStages;        // chunks per tile
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < n_tiles && ok && !*s_abort; tile += n_clusters) {
+        const int rt = tile / n_ct, ct = tile - rt * n_ct;
+        const int row0 = rt * 2 * LD_ROWS + LD_ROWS * (int)rank;
+        const int wrow0 = ct * LD_N + (LD_N / 2) * (int)rank;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, g.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = smem_u32(smem + stage * LD_STAGE);
+          const uint32_t fb_leader = mapa_shared(smem_u32(&full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * LD_STAGE);
+          tma_load_2d_pair(st, &tm_x, kb * LD_EL, row0, fb_leader);
+          tma_load_2d_pair(st + LD_A_BYTES, &tm_w, kb * LD_EL, wrow0, fb_leader);
+          s_issued[stage] = phase + 1u;
+          if (++stage == LD_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*s_abort && leader) {  // the pair's loads complete on the even CTA's barriers
+        for (int s = 0; s < LD_STAGES; ++s)
+          if (s_issued[s]) mbar_wait_drain(smem_u32(&full[s]), s_issued[s] - 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader && lane == 0) {
+      int stage = 0, chunk = 0;
+      uint32_t phase = 0;
+      bool issued_any = false, ok = true;
+      const uint32_t idesc = ld_idesc();
+      for (int tile = cluster; tile < n_tiles && ok && !*s_abort; tile += n_clusters) {
+        for (int c = 0; c < NCH && ok; ++c, ++chunk) {
+          const int buf = chunk % LD_BUFS;
+          const uint32_t bphase = (uint32_t)(chunk / LD_BUFS) & 1u;
+          if (!mbar_wait(smem_u32(&tempty[buf]), bphase ^ 1u, g.err, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + buf * LD_N;
+          for (int s = 0; s < kChunkStages; ++s) {
+            if (!mbar_wait(smem_u32(&full[stage]), phase, g.err, s_abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem + stage * LD_STAGE);
+            const uint32_t b0 = a0 + LD_A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < LD_BK / LD_UMMA_B; ++kk)
+              mma_bf16_pair(d, smem_desc_sw128(a0 + kk * LD_UMMA_B),
+                            smem_desc_sw128(b0 + kk * LD_UMMA_B), idesc, (s | kk) ? 1u : 0u);
+            issued_any = true;
+            mma_commit_pair(smem_u32(&empty[stage]), 0x3);
+            if (++stage == LD_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) mma_commit_pair(smem_u32(&tfull[buf]), 0x3);
+        }
+      }
+      if (*s_abort && issued_any) {
+        mma_commit_pair(smem_u32(drain), 0x1);
+        mbar_wait_drain(smem_u32(drain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int q = warp & 3;          // tensor-memory lane quarter this warp may read
+    const int half = ew >> 2;        // which 64 of the tile's 128 columns
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    int chunk = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters) {
+      const int rt = tile / n_ct, ct = tile - rt * n_ct;
+      float S[64];
+      __nv_bfloat162 A[32];  // sums of |partial| (only a margin: 8 bits suffice)
+#pragma unroll
+      for (int j = 0; j < 64; ++j) S[j] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) A[j] = __floats2bfloat162_rn(0.0f, 0.0f);
+      for (int c = 0; c < NCH; ++c, ++chunk) {
+        const int buf = chunk % LD_BUFS;
+        const uint32_t bphase = (uint32_t)(chunk / LD_BUFS) & 1u;
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(smem_u32(&tfull[buf]), bphase, g.err, s_abort) ? 1 : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // all 64 columns in flight at once, so the load latency is paid once
+        // per chunk; the buffer goes back as soon as they have landed
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + buf * LD_N + half * 64;
+        uint32_t v[4][16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_ld16(tb + 16 * i, v[i]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader0 + buf * 8);
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) {
+          const float p0 = __uint_as_float(v[j >> 4][j & 15]);
+          const float p1 = __uint_as_float(v[j >> 4][(j & 15) + 1]);
+          S[j] += p0;
+          S[j + 1] += p1;
+          A[j >> 1] = __hadd2(A[j >> 1], __floats2bfloat162_rn(fabsf(p0), fabsf(p1)));
+        }
+      }
+      if (!ok) break;
+      const int row = rt * 2 * LD_ROWS + LD_ROWS * (int)rank + q * 32 + lane;
+      if (row < g.T) {
+        const int col0 = ct * LD_N + half * 64;
+        uint32_t fw[2] = {0u, 0u};
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) {
+          // margin from the magnitude sums, widened by 1/8 for their bf16
+          // rounding: a sum of n positive terms rounded at every step stays
+          // within n * 2^-9 of the exact one, at most 1/8 for the <= 64
+          // chunks of K <= 8192 (and ~1% in practice)
+          const float2 a = __bfloat1622float2(A[j >> 1]);
+          const float m0 = (MOE_ZFLAG_ULPS * 1.125f * 0x1p-23f) * a.x;
+          const float m1 = (MOE_ZFLAG_ULPS * 1.125f * 0x1p-23f) * a.y;
+          if (near_bf16_boundary(S[j], m0)) fw[j >> 5] |= 1u << (j & 31);
+          if (near_bf16_boundary(S[j + 1], m1)) fw[(j + 1) >> 5] |= 1u << ((j + 1) & 31);
+          __nv_bfloat162 b = __floats2bfloat162_rn(S[j], S[j + 1]);
+          pk[j >> 1] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.z) + (size_t)row * g.L + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        uint32_t* fdst = g.flags + (size_t)row * (g.L / 32) + col0 / 32;
+        fdst[0] = fw[0];
+        fdst[1] = fw[1];
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its peer may still signal it
+  pdl_release();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, LD_TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- exact fixup
+// s + e == a + b exactly (Knuth's TwoSum; no ordering of |a|, |b| needed).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float aa = __fsub_rn(s, bb);
+  e = __fadd_rn(__fsub_rn(a, aa), __fsub_rn(b, bb));
+}
+
+// Nearest-even bf16 of the exact value hi + lo, where (hi, lo) = TwoSum output
+// (|lo| <= ulp(hi) / 2).  Every bf16 rounding boundary is an fp32 value, so
+// hi + lo lies on hi's side of it unless hi is the boundary itself; then lo's
+// sign decides, and lo == 0 is an exact tie (to even).
+__device__ __forceinline__ uint16_t bf16_of_sum(float hi, float lo) {
+  const uint32_t u = __float_as_uint(hi);
+  uint32_t r = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;  // nearest-even of hi
+  if ((u & 0xFFFFu) == 0x8000u && lo != 0.0f) {
+    const bool up_mag = (lo > 0.0f) == (hi > 0.0f);  // |hi + lo| beyond the midpoint
+    r = up_mag ? (u >> 16) + 1u : (u >> 16);
+  }
+  return (uint16_t)r;
+}
+
+constexpr int FX_THREADS = 256;
+constexpr int FX_SMEM_MAX = 160 * 1024;  // x row as fp32 + flagged-column list: 4 H + 2 L bytes
+
+// One block per token: x[t] goes to shared memory as fp32, then each warp
+// takes flagged elements in turn.  Lane j sums the products of columns
+// 8 (j + 32 m) .. 8 (j + 32 m) + 7 (m ascending) with TwoSum, and the warp
+// combines the lanes' (hi, lo) pairs.
+__global__ void __launch_bounds__(FX_THREADS)
+    latent_fix_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wd,
+                      uint16_t* __restrict__ z, const uint32_t* __restrict__ flags, int T, int H,
+                      int L) {
+  extern __shared__ float4 fx_smem[];
+  float* xs = reinterpret_cast<float*>(fx_smem);
+  uint16_t* list = reinterpret_cast<uint16_t*>(xs + H);  // flagged columns of this token
+  __shared__ int n_list;
+  pdl_wait();
+  const int t = blockIdx.x;
+  if (t >= T) return;
+  const int W = L / 32;
+  if (threadIdx.x == 0) n_list = 0;
+  __syncthreads();
+  for (int w = threadIdx.x; w < W; w += FX_THREADS) {
+    uint32_t bits = flags[(size_t)t * W + w];
+    while (bits) {
+      const int j = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      list[atomicAdd(&n_list, 1)] = (uint16_t)(32 * w + j);
+    }
+  }
+  const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * H);
+  for (int i = threadIdx.x; i < H / 4; i += FX_THREADS) {  // 4 bf16 -> 4 fp32
+    const uint2 v = xr[i];
+    fx_smem[i] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                             __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+  }
+  __syncthreads();
+  const int n = n_list;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < n; i += FX_THREADS / 32) {
+    const int l = list[i];
+    const uint4* wr = reinterpret_cast<const uint4*>(wd + (size_t)l * H);
+    float hi = 0.0f, lo = 0.0f;
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 wv = __ldg(wr + c);
+      const float4 xa = fx_smem[2 * c], xb = fx_smem[2 * c + 1];
+      // products of bf16 values: 16 significant bits, exact in fp32
+      const float p[8] = {
+          __fmul_rn(xa.x, __uint_as_float(wv.x << 16)), __fmul_rn(xa.y, __uint_as_float(wv.x & 0xFFFF0000u)),
+          __fmul_rn(xa.z, __uint_as_float(wv.y << 16)), __fmul_rn(xa.w, __uint_as_float(wv.y & 0xFFFF0000u)),
+          __fmul_rn(xb.x, __uint_as_float(wv.z << 16)), __fmul_rn(xb.y, __uint_as_float(wv.z & 0xFFFF0000u)),
+          __fmul_rn(xb.z, __uint_as_float(wv.w << 16)), __fmul_rn(xb.w, __uint_as_float(wv.w & 0xFFFF0000u))};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float s, e;
+        two_sum(hi, p[k], s, e);
+        hi = s;
+        lo = __fadd_rn(lo, e);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+      float s, e;
+      two_sum(hi, h2, s, e);
+      hi = s;
+      lo = __fadd_rn(__fadd_rn(lo, l2), e);
+    }
+    if (lane == 0) {
+      float s, e;
+      two_sum(hi, lo, s, e);  // renormalise: |e| <= ulp(s) / 2
+      z[(size_t)t * L + l] = bf16_of_sum(s, e);
+    }
+  }
+  pdl_release();
+}
+
+bool ld_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)LD_EL, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t latent_down_flag_bytes(int T, int L) { return (size_t)T * (L / 32) * 4; }
+
+cudaError_t launch_latent_down(const void* x, const void* wd, void* z, uint32_t* flags, int T,
+                               int H, int L, int* err, cudaStream_t s) {
+  if (T <= 0 || H % (LD_EL * kChunkStages) || L % LD_N || !flags) return cudaErrorInvalidValue;
+  CUtensorMap tx, tw;
+  if (!ld_map(&tx, x, H, T, LD_ROWS) || !ld_map(&tw, wd, H, L, LD_N / 2))
+    return cudaErrorInvalidValue;
+  LatentDown g{T, H, L, z, flags, err};
+  cudaError_t e = ensure_max_smem<latent_down_kernel>(LD_SMEM);
+  if (e != cudaSuccess) return e;
+  const int tiles = ((T + 2 * LD_ROWS - 1) / (2 * LD_ROWS)) * (L / LD_N);
+  const int clusters = std::min(device_sm_count() / 2, tiles);
+  count_launch();
+  e = launch_kernel(latent_down_kernel, dim3(2 * clusters), dim3(LD_THREADS), LD_SMEM, s, 2, tx, tw,
+                    g);
+  if (e != cudaSuccess) return e;
+  const size_t fx_smem = (size_t)H * 4 + (size_t)L * 2;
+  if (fx_smem > (size_t)FX_SMEM_MAX) return cudaErrorInvalidValue;
+  e = ensure_max_smem<latent_fix_kernel>(FX_SMEM_MAX);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  e = launch_kernel(latent_fix_kernel, dim3(T), dim3(FX_THREADS), fx_smem, s, 1,
+                    static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wd),
+                    static_cast<uint16_t*>(z), static_cast<const uint32_t*>(flags), T, H, L);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace moe

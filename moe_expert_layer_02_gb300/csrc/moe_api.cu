@@ -24,8 +24,11 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int64_t> g_launches{0};
 
+// Filled once per device under g_dev_mu; `ready` is published with a release
+// store after sms and err are written, and read with an acquire load, so a
+// thread that sees it set also sees both fields.
 struct DeviceInfo {
-  bool ready = false;
+  std::atomic<bool> ready{false};
   int sms = 0;
   int* err = nullptr;
 };
@@ -36,15 +39,17 @@ DeviceInfo* device_info() {
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
   DeviceInfo& di = g_dev[d];
-  if (!di.ready) {
+  if (!di.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!di.ready) {
-      if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+    if (!di.ready.load(std::memory_order_relaxed)) {
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
         return nullptr;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+      di.sms = sms;
       di.err = static_cast<int*>(p);
-      di.ready = true;
+      di.ready.store(true, std::memory_order_release);
     }
   }
   return &di;
@@ -107,14 +112,13 @@ struct Plan {
   bool gather;      // S4 quantises per token; the FFN1 producer gathers the rows
   size_t acc;       // fused combine: fp32 [T, H] sum
   size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
-      hq, hs, y, z, yn, hsh, total;
+      hq, hs, y, z, zflag, yn, hsh, total;
 };
 
 int choose_bn(const moe_problem* p) {
-  // MOE_TILE_N overrides the choice with a tile height the weight format has
-  // kernels for; any other value is ignored
-  const char* env = std::getenv("MOE_TILE_N");
-  const int v = env ? std::atoi(env) : 0;
+  // tuning().tile_n overrides the choice with a tile height the weight format
+  // has kernels for; any other value is ignored
+  const int v = tuning().tile_n;
   const double avg = (double)p->T * p->top_k / (p->E > 0 ? p->E : 1);
   if (p->wfmt == MOE_W_FP8_E4M3_BLOCK128) {  // block-wise tiles keep sums in registers
     if (v == 32 || v == 64) return v;
@@ -163,16 +167,13 @@ Plan make_plan(const moe_problem* p) {
   // the fused combine runs in the single-SM fp8 per-channel FFN2 epilogue
   q.fused = (p->flags & MOE_F_FUSED_COMBINE) && !q.L && !q.mx && !q.blockwise &&
             !q.shared_bf16 && !use_pair_gemm(q);
-  // MOE_GATHER=1: the single-SM fp8 per-channel FFN1 gathers its rows by
+  // tuning().ffn1_gather: the single-SM fp8 per-channel FFN1 gathers its rows by
   // token and S4 writes one row per token.  Off by default: the producer's
   // 16-byte cp.async copies (8 per row and stage) and the proxy fence before
   // each stage's MMAs cost more than the smaller S4 saves (T=512, H=8192,
   // I=2048, E=256 top-8, 128-row tiles: FFN1 1.35 vs 1.22 ms, S4 10.0 vs
   // 12.9 us; T=2048: 1.84 vs 1.28 ms; on SM pairs 3x slower, not offered).
-  {
-    const char* env = std::getenv("MOE_GATHER");
-    q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && env && std::strcmp(env, "1") == 0;
-  }
+  q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && tuning().ffn1_gather;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -200,6 +201,7 @@ Plan make_plan(const moe_problem* p) {
   q.y = take(q.fused ? 0 : RT * (size_t)q.K * 2);
   q.acc = take(q.fused ? T * (size_t)q.K * 4 : 0);
   q.z = take(q.L ? T * (size_t)q.L * 2 : 0);
+  q.zflag = take(q.L ? latent_down_flag_bytes(q.T, q.L) : 0);
   q.yn = take(q.L ? T * (size_t)q.L * 2 : 0);
   q.hsh = take(q.shared_bf16 ? T * (size_t)q.Is * 2 : 0);
   q.total = o;
@@ -213,6 +215,8 @@ T* at(void* ws, size_t off) {
 
 // ------------------------------------------------------------------ checks
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
 
 int check_problem(const moe_problem* p) {
   if (!p) return MOE_ERR_INVALID_ARG;
@@ -229,6 +233,8 @@ int check_problem(const moe_problem* p) {
   return MOE_OK;
 }
 
+namespace {
+
 // Shapes this build runs on the GPU: fp8 experts with an optional fp8 shared
 // expert (I_shared == I, fused into the grouped GEMMs), or the LatentMoE block
 // (latent > 0, optional bf16 shared expert) with fp8 or MXFP4 experts, or
@@ -244,6 +250,8 @@ int check_supported(const moe_problem* p) {
   if (p->latent > 0) {
     if (s8) return MOE_ERR_UNSUPPORTED;
     if (p->H % 256 || p->latent % 256) return MOE_ERR_UNSUPPORTED;
+    // the exact down projection keeps an fp32 row of x and a column list in shared memory
+    if (4 * (int64_t)p->H + 2 * (int64_t)p->latent > 160 * 1024) return MOE_ERR_UNSUPPORTED;
   } else {
     if (sb) return MOE_ERR_UNSUPPORTED;
     if (mx && s8) return MOE_ERR_UNSUPPORTED;
@@ -310,18 +318,16 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
 }
 
 // Small batches build the permutation in one single-block launch
-// (index_small_kernel); MOE_INDEX=3pass forces the three-kernel path.
+// (index_small_kernel); tuning().index_3pass forces the three-kernel path.
 bool use_index_small(const Plan& q) {
-  const char* env = std::getenv("MOE_INDEX");
-  if (env && std::strcmp(env, "3pass") == 0) return false;
+  if (tuning().index_3pass) return false;
   return index_small_fits(q.T, q.E);
 }
 
-// Large batches (256-row tiles) run the grouped GEMMs on SM pairs; MOE_GEMM=1cta
-// forces the single-SM kernels.
+// Large batches (256-row tiles) run the grouped GEMMs on SM pairs;
+// tuning().gemm_1cta forces the single-SM kernels.
 bool use_pair_gemm(const Plan& q) {
-  const char* env = std::getenv("MOE_GEMM");
-  if (env && std::strcmp(env, "1cta") == 0) return false;
+  if (tuning().gemm_1cta) return false;
   return !q.blockwise && q.BN == 256 && q.K % 256 == 0;
 }
 
@@ -351,12 +357,54 @@ int device_sm_count() {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+namespace {
+
+// moe_tuning, field by field, so that readers never see a half-written set.
+std::atomic<int32_t> g_tune[8];
+std::once_flag g_tune_once;
+
+bool env_is(const char* name, const char* value) {
+  const char* v = std::getenv(name);
+  return v && std::strcmp(v, value) == 0;
+}
+
+void tuning_from_env() {
+  const char* tn = std::getenv("MOE_TILE_N");
+  int rt = 0;
+  if (env_is("MOE_ROUTER_TILE", "8x8")) rt = 1;
+  if (env_is("MOE_ROUTER_TILE", "8x16")) rt = 2;
+  if (env_is("MOE_ROUTER_TILE", "8x16s4")) rt = 3;
+  if (env_is("MOE_ROUTER_TILE", "12w8x16")) rt = 4;
+  const int32_t v[8] = {tn ? std::atoi(tn) : 0,
+                        env_is("MOE_GATHER", "1") ? 1 : 0,
+                        env_is("MOE_INDEX", "3pass") ? 1 : 0,
+                        env_is("MOE_GEMM", "1cta") ? 1 : 0,
+                        env_is("MOE_PAIR_SMALL", "0") ? 0 : 1,
+                        env_is("MOE_MX", "1cta") ? 1 : 0,
+                        rt,
+                        env_is("MOE_PDL", "0") ? 0 : 1};
+  for (int i = 0; i < 8; ++i) g_tune[i].store(v[i], std::memory_order_relaxed);
+}
+
+}  // namespace
+
+moe_tuning tuning() {
+  std::call_once(g_tune_once, tuning_from_env);
+  moe_tuning t;
+  t.tile_n = g_tune[0].load(std::memory_order_relaxed);
+  t.ffn1_gather = g_tune[1].load(std::memory_order_relaxed);
+  t.index_3pass = g_tune[2].load(std::memory_order_relaxed);
+  t.gemm_1cta = g_tune[3].load(std::memory_order_relaxed);
+  t.pair_small = g_tune[4].load(std::memory_order_relaxed);
+  t.mx_1cta = g_tune[5].load(std::memory_order_relaxed);
+  t.router_tile = g_tune[6].load(std::memory_order_relaxed);
+  t.pdl = g_tune[7].load(std::memory_order_relaxed);
+  return t;
+}
+
 bool pdl_enabled() {
-  static const bool on = [] {
-    const char* env = std::getenv("MOE_PDL");
-    return !(env && std::strcmp(env, "0") == 0);
-  }();
-  return on;
+  std::call_once(g_tune_once, tuning_from_env);
+  return g_tune[7].load(std::memory_order_relaxed) != 0;
 }
 
 int* device_error_word() {
@@ -513,6 +561,25 @@ int moe_expert_ffn(const moe_problem* p, const int32_t* offsets, const void* xq_
   return run_experts(q, a, q.R, s);
 }
 
+int moe_latent_down(const moe_problem* p, const void* x, const void* latent_down, void* z,
+                    void* ws, size_t ws_bytes, void* stream) {
+  int st = check_problem(p);
+  if (st) return st;
+  if (p->latent <= 0 || !x || !latent_down || !z) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(latent_down, 16) || !aligned(z, 16)) return MOE_ERR_INVALID_ARG;
+  st = check_supported(p);
+  if (st) return st;
+  const Plan q = make_plan(p);
+  if (!ws || ws_bytes < q.total || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  if (p->T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  StageTimer t(MOE_STAGE_LATENT_DOWN, s);
+  return cuda_status(launch_latent_down(x, latent_down, z, at<uint32_t>(ws, q.zflag), q.T, q.H,
+                                        q.L, di->err, s));
+}
+
 int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
                   const void* shared, void* out, void* stream) {
   int st = check_problem(p);
@@ -579,15 +646,8 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   const void* xin = x;
   if (q.L) {
     StageTimer t(MOE_STAGE_LATENT_DOWN, s);
-    DenseGemmArgs d{};
-    d.x = x;
-    d.w = latent_down;
-    d.K1 = q.H;
-    d.rows = q.T;
-    d.N = q.L;
-    d.out = at<void>(ws, q.z);
-    d.err = di->err;
-    MOE_TRY(launch_dense_bf16(d, s));
+    MOE_TRY(launch_latent_down(x, latent_down, at<void>(ws, q.z), at<uint32_t>(ws, q.zflag), q.T,
+                               q.H, q.L, di->err, s));
     xin = at<void>(ws, q.z);
   }
   {
@@ -691,6 +751,26 @@ int moe_get_last_error(void* stream) {
 }
 
 int64_t moe_launch_count(void) { return g_launches.load(); }
+
+int moe_get_tuning(moe_tuning* t) {
+  if (!t) return MOE_ERR_INVALID_ARG;
+  *t = tuning();
+  return MOE_OK;
+}
+
+int moe_set_tuning(const moe_tuning* t) {
+  if (!t) return MOE_ERR_INVALID_ARG;
+  const int32_t v[8] = {t->tile_n, t->ffn1_gather, t->index_3pass, t->gemm_1cta,
+                        t->pair_small, t->mx_1cta, t->router_tile, t->pdl};
+  const bool tile_ok = v[0] == 0 || v[0] == 32 || v[0] == 64 || v[0] == 96 || v[0] == 128 ||
+                       v[0] == 256;
+  if (!tile_ok || v[6] < 0 || v[6] > 4) return MOE_ERR_INVALID_ARG;
+  for (int i : {1, 2, 3, 4, 5, 7})
+    if (v[i] != 0 && v[i] != 1) return MOE_ERR_INVALID_ARG;
+  std::call_once(g_tune_once, tuning_from_env);  // the environment never overrides a set
+  for (int i = 0; i < 8; ++i) g_tune[i].store(v[i], std::memory_order_relaxed);
+  return MOE_OK;
+}
 
 int moe_profile_enable(int mask) {
   g_prof_mask.store(static_cast<uint32_t>(mask));

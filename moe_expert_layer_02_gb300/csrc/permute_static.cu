@@ -61,10 +61,8 @@ extern "C" int moe_permute_static(const moe_problem* p, const int32_t* topk_idx,
                                   int32_t* counts, int32_t* offsets, int32_t* perm,
                                   int32_t* src_row, void* xq_perm, float* xscale_perm,
                                   void* stream) {
-  if (!p) return MOE_ERR_INVALID_ARG;
-  if (p->T < 0 || p->H <= 0 || p->H % 128 || p->E <= 0 || p->E > kMaxExperts || p->top_k <= 0 ||
-      p->top_k > p->E || p->top_k > kMaxTopK || p->latent < 0 || p->latent % 128)
-    return MOE_ERR_INVALID_ARG;
+  const int st = check_problem(p);  // the same checks as moe_permute
+  if (st) return st;
   if (!topk_idx || !x || !counts || !offsets || !perm || !src_row || !xq_perm || !xscale_perm)
     return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(xq_perm)) % 16)

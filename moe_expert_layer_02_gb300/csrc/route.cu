@@ -346,18 +346,16 @@ cudaError_t launch_router_impl(const void* x, const float* wr, const float* bias
 
 cudaError_t launch_router_logits(const void* x, const float* wr, const float* bias, float* logits,
                                  int T, int H, int E, int* err, cudaStream_t s) {
-  // MOE_ROUTER_TILE overrides the choice: 8x8 (8 warps of 8 tokens x 8 experts,
-  // two blocks per SM), 8x16 (8 warps of 8 x 16), 8x16s4 (the same with four
-  // chunks per stage), 12w8x16 (12 warps of 8 x 16: 48 tokens x 32 experts)
-  const char* env = std::getenv("MOE_ROUTER_TILE");
-  if (env && std::strcmp(env, "8x8") == 0)
-    return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
-  if (env && std::strcmp(env, "8x16") == 0)
-    return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
-  if (env && std::strcmp(env, "8x16s4") == 0)
-    return launch_router_impl<8, 16, 4>(x, wr, bias, logits, T, H, E, err, s);
-  if (env && std::strcmp(env, "12w8x16") == 0)
-    return launch_router_impl<8, 16, 0, 6>(x, wr, bias, logits, T, H, E, err, s);
+  // tuning().router_tile overrides the choice: 1 = 8 warps of 8 tokens x 8
+  // experts (two blocks per SM), 2 = 8 warps of 8 x 16, 3 = the same with four
+  // chunks per stage, 4 = 12 warps of 8 x 16 (48 tokens x 32 experts)
+  switch (tuning().router_tile) {
+    case 1: return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
+    case 2: return launch_router_impl<8, 16>(x, wr, bias, logits, T, H, E, err, s);
+    case 3: return launch_router_impl<8, 16, 4>(x, wr, bias, logits, T, H, E, err, s);
+    case 4: return launch_router_impl<8, 16, 0, 6>(x, wr, bias, logits, T, H, E, err, s);
+    default: break;
+  }
   const long sms = device_sm_count();
   const long e32 = (E + 31) / 32;
   // Twelve warps (three per scheduler, 168 registers) hide more latency and

@@ -1,8 +1,9 @@
 """Shared helpers for the -m gpu parity tests: seeded inputs on the device, their
 host copies for the oracle, the C-ABI problem struct, and the output tolerance.
 
-Tolerance (fp32-accumulated output, stated for this layer): relative L2 error
-<= 1e-2 and max-abs error <= 5e-2 x RMS(reference).  Integer and byte outputs
+Tolerance (stated for this layer): relative L2 error <= 1e-2 and max-abs
+error <= 5e-2 x RMS(reference), on the stored bf16 output against the oracle's
+unrounded output (block-wise fp8 weights: see assert_close).  Integer and byte outputs
 (routing indices, counts, offsets, permutation, fp8 codes) are compared
 bit for bit.
 """
@@ -132,11 +133,18 @@ def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
 
 
-def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
-    """The bars on the fp32-accumulated output: relative L2 <= REL_L2 and
-    max-abs <= MAX_ABS_RMS x output RMS.  ``got`` is the layer's stored bf16
-    output, whose final rounding adds at most half a bf16 ulp of each element
-    on top of the accumulated value, so the max-abs bar allows that too."""
+def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "",
+                 bf16_store_allowance: bool = False):
+    """The layer's bars: relative L2 <= REL_L2 and max-abs <= MAX_ABS_RMS x
+    output RMS, on the stored bf16 output against the oracle's exact (fp64,
+    unrounded) output.
+
+    ``bf16_store_allowance`` is for block-wise fp8 weights only: their 16x block
+    gains give outputs of up to ~25x RMS, where the final bf16 store alone
+    moves an element by up to half an ulp, ~5% of RMS.  There the max-abs bar
+    is applied to |got - ref| minus half a bf16 ulp of ``got``.  Every other
+    weight format meets the bar on the raw difference.  The message reports
+    both figures."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape
@@ -144,12 +152,15 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
     rms = np.sqrt(np.mean(ref ** 2))
     err = got - ref
     rel = np.sqrt(np.sum(err ** 2)) / max(np.sqrt(np.sum(ref ** 2)), 1e-30)
-    excess = np.abs(err) - bf16_half_ulp(got)
-    mx = np.max(excess) if err.size else 0.0
+    raw = np.max(np.abs(err)) if err.size else 0.0
+    adj = np.max(np.abs(err) - bf16_half_ulp(got)) if err.size else 0.0
+    mx = adj if bf16_store_allowance else raw
+    rms_ = max(rms, 1e-30)
     assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2}"
     assert mx <= MAX_ABS_RMS * rms, (
-        f"{what}: max-abs error beyond the bf16 store {mx:.3e} > {MAX_ABS_RMS} x RMS {rms:.3e}")
-    return rel, mx / max(rms, 1e-30)
+        f"{what}: max-abs error {raw / rms_:.4f} x RMS (beyond the bf16 store {adj / rms_:.4f} x RMS)"
+        f" > {MAX_ABS_RMS}" + (" [bar applied beyond the bf16 store]" if bf16_store_allowance else ""))
+    return rel, raw / rms_
 
 
 def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
@@ -158,4 +169,32 @@ def sample_tokens(T: int, n: int, seed: int = 0) -> np.ndarray:
         return np.arange(T, dtype=np.int32)
     rng = np.random.default_rng(seed)
     pick = set(rng.choice(T, n - 2, replace=False).tolist()) | {0, T - 1}
+    return np.array(sorted(pick), dtype=np.int32)
+
+
+def edge_tokens(orc, cfg: mi.MoEConfig, h: dict, n: int, seed: int = 0,
+                max_experts: int = 1024) -> np.ndarray:
+    """Token sample for full-size checks that reaches the kernels' edge paths:
+    the token of every expert's last routed row (its last, usually partly
+    filled, tile item; at most ``max_experts`` experts, a seeded choice), up to
+    32 tokens of the most loaded expert, the first and last tokens, and a
+    seeded random fill up to ``n``.  The routing is the oracle's."""
+    if cfg.routing == "sigmoid":
+        lg = orc.router_logits(h["x"], h["router_w"])
+        idx, _ = orc.topk(lg, cfg.k, routing="sigmoid", bias=h["router_bias"])
+    else:
+        lg = orc.router_logits(h["x"], h["router_w"], h["router_bias"])
+        idx, _ = orc.topk(lg, cfg.k)
+    cnt, off, _, src = orc.permute(idx, cfg.E)
+    rng = np.random.default_rng(seed)
+    experts = np.nonzero(cnt)[0]
+    if len(experts) > max_experts:
+        experts = np.sort(rng.choice(experts, max_experts, replace=False))
+    pick = {int(src[off[e + 1] - 1]) for e in experts}
+    hot = int(np.argmax(cnt))
+    pick |= {int(t) for t in src[off[hot]:off[hot + 1]][:32]}
+    pick |= {0, cfg.T - 1}
+    rest = np.setdiff1d(np.arange(cfg.T), np.fromiter(pick, np.int64))
+    if len(pick) < n and len(rest):
+        pick |= {int(t) for t in rng.choice(rest, min(n - len(pick), len(rest)), replace=False)}
     return np.array(sorted(pick), dtype=np.int32)

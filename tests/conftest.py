@@ -37,3 +37,16 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture
+def tuning():
+    """Set the library's launch choices (moe_tuning fields as keywords) for one
+    test; the previous choices come back at teardown."""
+    import moe_expert_layer_02_gb300 as m
+    from moe_expert_layer_02_gb300 import build
+    build.build()
+    m.load_library()
+    saved = m.moe_get_tuning()
+    yield m.moe_set_tuning
+    m.moe_set_tuning(**saved)

@@ -155,18 +155,18 @@ def test_mx_pair_plan(m):
     assert "ffn1=grouped_mx_kernel" in d and "ffn2=grouped_mx_pair_kernel" in d
 
 
-def test_row_gather_plan(m, monkeypatch):
-    # MOE_GATHER=1: the single-SM fp8 per-channel FFN1 gathers its rows by
+def test_row_gather_plan(m, tuning):
+    # ffn1_gather: the single-SM fp8 per-channel FFN1 gathers its rows by
     # token, at any tile height; the SM-pair, block-wise and MXFP4 paths read
     # permuted rows, and so does everything by default
     dec = lambda: m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048))
     d = dec()
     assert "ffn1=grouped_ffn_kernel<FFN1,BN=128>" in d and "ffn1_rows=permuted" in d, d
-    monkeypatch.setenv("MOE_GATHER", "1")
+    tuning(ffn1_gather=1)
     assert "ffn1_rows=gathered" in dec()
-    monkeypatch.setenv("MOE_TILE_N", "32")
+    tuning(tile_n=32)
     assert "BN=32> " in dec() and "ffn1_rows=gathered" in dec()
-    monkeypatch.delenv("MOE_TILE_N")
+    tuning(tile_n=0)
     assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(16384, 8192, 2048, 256, 8,
                                                                  I_shared=2048))
     assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8,
@@ -175,15 +175,15 @@ def test_row_gather_plan(m, monkeypatch):
                                                                  wfmt=m.W_MXFP4))
 
 
-@pytest.mark.parametrize("tile,want", [("32", (32, 32, 32)), ("64", (64, 64, 64)),
-                                       ("96", (None, None, 96)), ("128", (128, None, None)),
-                                       ("256", (256, None, None)), ("48", (None, None, None))])
-def test_tile_override_respects_the_format(m, monkeypatch, tile, want):
-    # MOE_TILE_N takes a tile height only where the format has kernels for it
-    # (fp8 per-channel 32/64/128/256, block-wise 32/64, MXFP4 32/64/96);
-    # anything else leaves the automatic choice (~16 rows per expert: 128 for
+@pytest.mark.parametrize("tile,want", [(32, (32, 32, 32)), (64, (64, 64, 64)),
+                                       (96, (None, None, 96)), (128, (128, None, None)),
+                                       (256, (256, None, None)), (0, (None, None, None))])
+def test_tile_override_respects_the_format(m, tuning, tile, want):
+    # a tile height is taken only where the format has kernels for it (fp8
+    # per-channel 32/64/128/256, block-wise 32/64, MXFP4 32/64/96); anything
+    # else, and 0, leaves the automatic choice (~16 rows per expert: 128 for
     # fp8 per-channel, 32 for the others)
-    monkeypatch.setenv("MOE_TILE_N", tile)
+    tuning(tile_n=tile)
     for fmt, w, auto in zip((m.W_FP8, m.W_FP8_BLOCK, m.W_MXFP4), want, (128, 32, 32)):
         d = m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, wfmt=fmt))
         bn = int(re.search(r"ffn1=\w+<FFN1,BN=(\d+)>", d).group(1))
@@ -201,3 +201,21 @@ def test_tile_height_follows_rows_per_expert(m, T, want):
     # tiles on SM pairs above
     d = m.moe_describe(m.make_problem(T, 8192, 2048, 256, 8, I_shared=2048))
     assert d.startswith("ffn1=" + want), d
+
+
+def test_tuning_round_trip_and_range_checks(m, tuning):
+    base = m.moe_get_tuning()
+    assert base["pair_small"] in (0, 1) and base["pdl"] in (0, 1)
+    tuning(tile_n=64, router_tile="8x16s4", pdl=0)
+    t = m.moe_get_tuning()
+    assert t["tile_n"] == 64 and t["router_tile"] == 3 and t["pdl"] == 0
+    for bad in (dict(tile_n=48), dict(router_tile=5), dict(ffn1_gather=2), dict(pdl=-1)):
+        with pytest.raises(m.MoEError) as ei:
+            m.moe_set_tuning(**bad)
+        assert ei.value.status == 1  # MOE_ERR_INVALID_ARG, nothing changed
+        assert m.moe_get_tuning() == t
+    lib = m.load_library()
+    assert lib.moe_get_tuning(None) == 1 and lib.moe_set_tuning(None) == 1
+    with m.tuned(tile_n=32):
+        assert m.moe_get_tuning()["tile_n"] == 32
+    assert m.moe_get_tuning() == t

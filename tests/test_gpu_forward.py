@@ -41,24 +41,24 @@ def _check(orc, cfg, n_sample):
 
 @pytest.mark.parametrize("bn", [32, 128])
 @pytest.mark.parametrize("cfg", [SHARED_SMALL, RAGGED, KE], ids=ids)
-def test_forward_small_gathered_rows(orc, cfg, bn, monkeypatch):
-    # MOE_GATHER=1: S4 writes one fp8 row per token and the FFN1 producer
+def test_forward_small_gathered_rows(orc, cfg, bn, tuning):
+    # ffn1_gather: S4 writes one fp8 row per token and the FFN1 producer
     # gathers each tile's rows by token, instead of the default permuted rows
     # that FFN1 reads by TMA
-    monkeypatch.setenv("MOE_GATHER", "1")
-    monkeypatch.setenv("MOE_TILE_N", str(bn))
+    tuning(ffn1_gather=1)
+    tuning(tile_n=bn)
     assert "ffn1_rows=gathered" in G.lib().moe_describe(G.problem(cfg))
     _check(orc, cfg, n_sample=cfg.T)
 
 
 @pytest.mark.parametrize("small", ["m128", "m256"])
 @pytest.mark.parametrize("cfg", [SHARED_SMALL, RAGGED, SKEW_SMALL.with_(I_s=256)], ids=ids)
-def test_forward_sm_pairs(orc, cfg, small, monkeypatch):
+def test_forward_sm_pairs(orc, cfg, small, tuning):
     # 256-row tiles on SM pairs for a small batch: items of <= 128 rows as
     # M = 128 tiles, or as padded M = 256 tiles
-    monkeypatch.setenv("MOE_TILE_N", "256")
+    tuning(tile_n=256)
     if small == "m256":
-        monkeypatch.setenv("MOE_PAIR_SMALL", "0")
+        tuning(pair_small=0)
     d = G.lib().moe_describe(G.problem(cfg))
     assert "ffn1=pair_gemm_kernel" in d and "ffn1_rows=permuted" in d, d
     _check(orc, cfg, n_sample=cfg.T)
@@ -91,20 +91,38 @@ def test_forward_packed_weights_small(orc, cfg):
     G.assert_close(G.bf16_values(G.bf16_bits(out)), ref, f"packed {cfg.name}")
 
 
+def full_size_tokens(orc, cfg, h, seed):
+    """Every token of the decode batch; for the larger batches at least 256
+    tokens, among them the token of every expert's last routed row (its last,
+    partly filled tile item) and tokens of the most loaded expert."""
+    if cfg.T <= 512:
+        return np.arange(cfg.T, dtype=np.int32)
+    return G.edge_tokens(orc, cfg, h, 256, seed=seed)
+
+
 @pytest.mark.parametrize("cfg", FULL, ids=ids)
 def test_forward_packed_weights_full_size(orc, cfg):
     m = G.lib()
     inp = G.gpu_inputs(cfg)
     out = run_forward(cfg, G.pack(cfg, inp), packed=True)
     assert m.moe_get_last_error() == 0
-    toks = G.sample_tokens(cfg.T, 16, seed=21)
-    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), G.host(inp), tokens=toks)
+    h = G.host(inp)
+    toks = full_size_tokens(orc, cfg, h, seed=21)
+    assert len(toks) >= min(cfg.T, 256)
+    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), h, tokens=toks)
     G.assert_close(G.bf16_values(G.bf16_bits(out))[toks], ref, f"packed {cfg.name}")
 
 
 @pytest.mark.parametrize("cfg", FULL, ids=ids)
-def test_forward_full_size_sampled(orc, cfg):
-    _check(orc, cfg, n_sample=24)
+def test_forward_full_size(orc, cfg):
+    m = G.lib()
+    inp = G.gpu_inputs(cfg)
+    out = run_forward(cfg, inp)
+    assert m.moe_get_last_error() == 0
+    h = G.host(inp)
+    toks = full_size_tokens(orc, cfg, h, seed=11)
+    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), h, tokens=toks)
+    G.assert_close(G.bf16_values(G.bf16_bits(out))[toks], ref, f"moe_forward {cfg.name}")
 
 
 def test_forward_deterministic_and_counted():

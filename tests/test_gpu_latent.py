@@ -38,8 +38,8 @@ def _latent_rows(orc, cfg, seed=9):
 @pytest.mark.parametrize("bn", [32, 64, 96])
 @pytest.mark.parametrize("cfg", [MX_PLAIN, LAT_SMALL, MX_PLAIN.with_(name="mx_situ", act="situ")],
                          ids=ids)
-def test_mxfp4_expert_ffn(orc, cfg, bn, monkeypatch):
-    monkeypatch.setenv("MOE_TILE_N", str(bn))
+def test_mxfp4_expert_ffn(orc, cfg, bn, tuning):
+    tuning(tile_n=bn)
     m = G.lib()
     inp, h, off, xq, xs, row_w = _latent_rows(orc, cfg)
     p = G.problem(cfg)
@@ -112,25 +112,22 @@ def _latent_full(orc, packed=False):
     cfg = mi.CONFIGS["latent"]
     inp = G.gpu_inputs(cfg)
     out = _forward(cfg, G.pack(cfg, inp) if packed else inp, packed=packed)
-    toks = G.sample_tokens(cfg.T, 24, seed=5)
-    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), G.host(inp), tokens=toks)
+    h = G.host(inp)
+    # 256 tokens: the last routed row of 200 experts (their last tile items),
+    # tokens of the most loaded expert, and a random fill
+    toks = G.edge_tokens(orc, cfg, h, 256, seed=5, max_experts=200)
+    ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), h, tokens=toks)
     return G.bf16_values(G.bf16_bits(out))[toks], ref
 
 
+# z = bf16(x Wd^T) is exactly rounded on both sides (moe_latent_down), so the
+# per-token fp8 quantisation of z agrees code for code and the whole LatentMoE
+# layer meets both bars on the raw difference
 @pytest.mark.parametrize("packed", [False, True], ids=["row-major", "packed"])
-def test_latent_full_size_sampled_rel_l2(orc, packed):
+def test_latent_full_size_sampled(orc, packed):
     got, ref = _latent_full(orc, packed)
-    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-    assert rel <= G.REL_L2, rel
-
-
-# z = bf16(x Wd^T) from tensor-core fp32 accumulation differs from the exact
-# rounding in ~0.4% of elements by one ulp; through the per-token fp8
-# quantisation of z and the per-row requantisation of h that can shift whole
-# rows of codes, so this is the tightest of the checks.
-def test_latent_full_size_sampled_max_abs(orc):
-    got, ref = _latent_full(orc)
-    G.assert_close(got, ref, "moe_forward latent")
+    assert len(got) >= 256
+    G.assert_close(got, ref, f"moe_forward latent ({'packed' if packed else 'row-major'})")
 
 
 def test_latent_routing_bit_exact(orc):

@@ -32,8 +32,8 @@ def forward(cfg, inp):
 
 @pytest.mark.parametrize("bn", [32, 64, 96])
 @pytest.mark.parametrize("cfg", [MX_PAIR, MX_PAIR_RAGGED, LAT_PAIR, ONE_EXPERT], ids=ids)
-def test_mx_pair_forward(orc, cfg, bn, monkeypatch):
-    monkeypatch.setenv("MOE_TILE_N", str(bn))
+def test_mx_pair_forward(orc, cfg, bn, tuning):
+    tuning(tile_n=bn)
     m = G.lib()
     d = m.moe_describe(G.problem(cfg, packed=True))
     assert "ffn1=grouped_mx_pair_kernel" in d and "ffn2=grouped_mx_pair_kernel" in d, d
@@ -43,11 +43,11 @@ def test_mx_pair_forward(orc, cfg, bn, monkeypatch):
     G.assert_close(got, ref, f"mxfp4 pair {cfg.name} BN={bn}")
 
 
-def test_mx_pair_matches_single_sm(monkeypatch):
+def test_mx_pair_matches_single_sm(tuning):
     cfg = MX_PAIR_RAGGED
     inp = G.pack(cfg, G.gpu_inputs(cfg))
     pair = forward(cfg, inp)
-    monkeypatch.setenv("MOE_MX", "1cta")
+    tuning(mx_1cta=1)
     assert "grouped_mx_pair_kernel" not in G.lib().moe_describe(G.problem(cfg, packed=True))
     single = forward(cfg, inp)
     G.assert_close(pair, single, "pair vs single-SM")

@@ -56,38 +56,38 @@ def draw(seed: int):
 
     tiles = {"fp8": (32, 64, 128, 256), "fp8_block": (32, 64), "mxfp4": (32, 64, 96)}[
         "mxfp4" if cfg.wfmt == "mxfp4" else cfg.wfmt]
-    env = {}
+    knobs = {}
     if r.random() < 0.6:
-        env["MOE_TILE_N"] = str(int(r.choice(tiles)))
+        knobs["tile_n"] = int(r.choice(tiles))
     if r.random() < 0.3:
-        env["MOE_GATHER"] = "1"
+        knobs["ffn1_gather"] = 1
     if r.random() < 0.3:
-        env["MOE_INDEX"] = "3pass"
+        knobs["index_3pass"] = 1
     if kind == "fp8_pair":  # 256-row tiles on SM pairs
-        env["MOE_TILE_N"] = "256"
+        knobs["tile_n"] = 256
     elif r.random() < 0.2:
-        env["MOE_GEMM"] = "1cta"
+        knobs["gemm_1cta"] = 1
     if r.random() < 0.2:
-        env["MOE_PAIR_SMALL"] = "0"
+        knobs["pair_small"] = 0
     if r.random() < 0.3:
-        env["MOE_MX"] = "1cta"
+        knobs["mx_1cta"] = 1
     if r.random() < 0.5:
-        env["MOE_ROUTER_TILE"] = str(r.choice(["8x8", "8x16", "8x16s4", "12w8x16"]))
+        knobs["router_tile"] = str(r.choice(["8x8", "8x16", "8x16s4", "12w8x16"]))
     # the MXFP4 SM-pair kernels need packed weights
     packed = bool(r.random() < (0.8 if cfg.wfmt == "mxfp4" else 0.5))
-    return cfg, env, packed
+    return cfg, knobs, packed
 
 
 @pytest.mark.parametrize("seed", range(N_CASES))
-def test_forward_random_shape(orc, seed, monkeypatch):
-    cfg, env, packed = draw(seed)
-    for key, val in env.items():
-        monkeypatch.setenv(key, val)
+def test_forward_random_shape(orc, seed, tuning):
+    cfg, knobs, packed = draw(seed)
+    tuning(**knobs)
     m = G.lib()
     p = G.problem(cfg, packed=packed)
-    what = f"{cfg} env={env} packed={packed} plan: {m.moe_describe(p)}"
+    what = f"{cfg} tuning={knobs} packed={packed} plan: {m.moe_describe(p)}"
     inp = G.gpu_inputs(cfg)
     out = run_forward(cfg, G.pack(cfg, inp) if packed else inp, packed=packed)
     assert m.moe_get_last_error() == 0, what
     ref, _, _, _ = orc.moe_forward(cfg.oracle_problem(), G.host(inp))
-    G.assert_close(G.bf16_values(G.bf16_bits(out)), ref, what)
+    G.assert_close(G.bf16_values(G.bf16_bits(out)), ref, what,
+                   bf16_store_allowance=cfg.wfmt == "fp8_block")

@@ -20,6 +20,7 @@ BIASED = mi.MoEConfig("biased", T=300, H=256, I=128, E=64, k=6, zipf_bias=True)
 SKEW_SMALL = mi.MoEConfig("skew_small", T=640, H=512, I=256, E=16, k=4, zipf_bias=True)
 SMALL = [mi.CONFIGS["toy"], RAGGED, MAXE, T1, KE, E3, BIASED]
 FULL = [mi.CONFIGS["decode"], mi.CONFIGS["skewed"], mi.CONFIGS["prefill"]]
+LATENT = mi.CONFIGS["latent"]  # routing on x [4096, 7168] over 896 experts, top-16
 ids = lambda c: c.name
 
 
@@ -44,7 +45,7 @@ def test_router_logits_bit_exact(orc, cfg):
     assert m.moe_get_last_error() == 0
 
 
-@pytest.mark.parametrize("cfg", SMALL + FULL[:2], ids=ids)
+@pytest.mark.parametrize("cfg", SMALL + FULL + [LATENT], ids=ids)
 def test_topk_bit_exact(orc, cfg):
     m = G.lib()
     inp = G.gpu_inputs(cfg)
@@ -77,25 +78,28 @@ def test_topk_ties_lower_index(orc):
 
 
 @pytest.mark.parametrize("path", ["auto", "3pass"])
-@pytest.mark.parametrize("cfg", SMALL + FULL, ids=ids)
-def test_permute_bit_exact(orc, cfg, path, monkeypatch):
+@pytest.mark.parametrize("cfg", SMALL + FULL + [LATENT], ids=ids)
+def test_permute_bit_exact(orc, cfg, path, tuning):
     # small batches build the permutation in one single-block launch; "3pass"
     # forces the count / scan / rank kernels that large batches use
     if path == "3pass":
-        monkeypatch.setenv("MOE_INDEX", "3pass")
+        tuning(index_3pass=1)
     m = G.lib()
     inp = G.gpu_inputs(cfg)
-    h = G.host(inp, keys=("x", "router_w", "router_bias"))
+    h = G.host(inp, keys=("x", "router_w", "router_bias", "wd"))
     _, idx, _ = _routing(orc, cfg, h)
     cnt, off, perm, src = orc.permute(idx, cfg.E)
-    s, q = orc.quant_rows(h["x"])
+    # the LatentMoE experts (and so the permutation's rows) take the latent z
+    xin = orc.latent_down(h["x"], h["wd"]) if cfg.L else h["x"]
+    s, q = orc.quant_rows(xin)
     p = G.problem(cfg)
     ws = G.workspace(p)
     d = lambda *shape, dt=torch.int32: torch.empty(*shape, dtype=dt, device="cuda")
     g_cnt, g_off, g_perm, g_src = d(cfg.E), d(cfg.E + 1), d(cfg.T, cfg.k), d(cfg.R)
-    g_xq = d(cfg.R, cfg.H, dt=torch.uint8)
+    g_xq = d(cfg.R, cfg.K, dt=torch.uint8)
     g_xs = d(cfg.R, dt=torch.float32)
-    m.moe_permute(p, torch.from_numpy(idx).cuda(), inp["x"], g_cnt, g_off, g_perm, g_src, g_xq,
+    x_dev = torch.from_numpy(xin.view(np.int16)).view(torch.bfloat16).cuda() if cfg.L else inp["x"]
+    m.moe_permute(p, torch.from_numpy(idx).cuda(), x_dev, g_cnt, g_off, g_perm, g_src, g_xq,
                   g_xs, ws)
     assert m.moe_get_last_error() == 0
     assert np.array_equal(g_cnt.cpu().numpy(), cnt)
@@ -170,17 +174,17 @@ def _expert_problem(orc, cfg, h):
 
 @pytest.mark.parametrize("bn", [32, 64, 128, 256, "256-1cta", "256-nosmall"])
 @pytest.mark.parametrize("cfg", [mi.CONFIGS["toy"], RAGGED, KE, E3, SKEW_SMALL], ids=ids)
-def test_expert_ffn_all_tiles(orc, cfg, bn, monkeypatch):
+def test_expert_ffn_all_tiles(orc, cfg, bn, tuning):
     # 256-row tiles run on SM pairs when H % 256 == 0, items of <= 128 rows as
     # M = 128 tiles; "256-nosmall" runs those as padded M = 256 tiles and
     # "256-1cta" forces the single-SM kernel for the same tiles
     if bn == "256-1cta":
-        monkeypatch.setenv("MOE_GEMM", "1cta")
+        tuning(gemm_1cta=1)
         bn = 256
     if bn == "256-nosmall":
-        monkeypatch.setenv("MOE_PAIR_SMALL", "0")
+        tuning(pair_small=0)
         bn = 256
-    monkeypatch.setenv("MOE_TILE_N", str(bn))
+    tuning(tile_n=bn)
     _check_expert_ffn(orc, cfg, rows_sample=None)
 
 
@@ -211,7 +215,8 @@ def _check_expert_ffn(orc, cfg, rows_sample, act=0):
     fmt = orc.FP8_BLOCK if cfg.wfmt == "fp8_block" else orc.FP8
     ref = orc.expert_rows(fmt, off_sub, xq[rows], xs[rows], row_w[rows], h["w13"],
                           h["w13_scale"], h["w2"], h["w2_scale"], act=act)
-    G.assert_close(got[rows], ref, f"expert_ffn {cfg.name}")
+    G.assert_close(got[rows], ref, f"expert_ffn {cfg.name}",
+                   bf16_store_allowance=cfg.wfmt == "fp8_block")
 
 
 @pytest.mark.parametrize("cfg", [mi.CONFIGS["toy"], RAGGED, MAXE, T1], ids=ids)

@@ -55,6 +55,19 @@ def test_static_permute_matches_workspace_version_two_calls_in_a_row():
             assert np.array_equal(a, b), name
 
 
+@pytest.mark.gpu
+def test_static_permute_fills_its_scratch_exactly():
+    # E * ceil(T/32) == 2^19: the largest problem the fixed tables admit, so the
+    # last entry of each table (and the second table's start) is used
+    T, E, k, H = 16384, 1024, 2, 128
+    assert E * ((T + 31) // 32) == STATIC_TABLE
+    ref, got = _outputs(T, E, k, H, 3)
+    for a, b in zip(ref, got):
+        if a.dtype == np.float32:
+            a, b = a.view(np.uint32), b.view(np.uint32)
+        assert np.array_equal(a, b)
+
+
 def test_static_permute_refuses_problems_beyond_its_scratch():
     m = G.lib()
     E = 1024
