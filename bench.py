@@ -1,7 +1,9 @@
 """Benchmark of the fused MoE expert layer on GB300 (one JSON line on stdout).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config decode|prefill|skewed|toy]
+                    [--config decode|prefill|skewed|latent|toy|...]
+                    [--also prefill,skewed,latent] [--also-steps 30]
+    python bench.py --stage router|route --dims A B C [--steps K]
 
 A step is one moe_forward over one batch (router logits -> top-k -> permute +
 fp8 quant -> grouped FFN1 -> requant -> grouped FFN2 -> gather + shared),
@@ -12,6 +14,12 @@ step, so no flush is needed.  ``value`` is algorithmic bytes per step (touched
 expert weights + scales, shared weights, router, x, out) / step time, summed
 over ranks; replicas run independent copies (the layer does not shard here).
 ``--impl reference`` times the CPU oracle on a bounded token sample instead.
+
+On one GPU the line also carries ``workloads``: the other workloads (Ling
+prefill T=16384, the skewed-routing T=8192 batch, the Kimi-K3-style LatentMoE
+T=4096 batch by default), each timed in the same process after the headline
+one, with its own step time, dominant-kernel roofline, grouped-GEMM tensor
+rate, clocks and per-stage times.  ``--stage`` times one entry point alone.
 """
 from __future__ import annotations
 
@@ -48,6 +56,15 @@ def parse():
                          "an order that is not fixed)")
     ap.add_argument("--ref-tokens", type=int, default=0,
                     help="tokens per oracle step (default: one per host core)")
+    ap.add_argument("--also", default="prefill,skewed,latent",
+                    help="other workloads timed after the headline one and reported as nested "
+                         "records of the same line (comma list; 'none' for none; one GPU only)")
+    ap.add_argument("--also-steps", type=int, default=30,
+                    help="timed steps of each nested workload")
+    ap.add_argument("--stage", choices=["router", "route"], default=None,
+                    help="time one entry point alone instead of the layer (see run_stage)")
+    ap.add_argument("--dims", type=int, nargs=3, default=None,
+                    help="with --stage: T H E (router) or T E k (route)")
     return ap.parse_args()
 
 
@@ -269,13 +286,197 @@ def run_reference(args, cfg):
     return 0
 
 
+def load_workload(m, cfg, dev, pack: bool, fused_combine: bool = False, base=None):
+    """Device inputs, problem, workspace and output buffer for ``cfg``.  Expert
+    weights (and their packed copies) of ``base``, a workload loaded before
+    with the same weight shapes, are reused instead of regenerated."""
+    import torch
+
+    import moe_inputs as mi
+    from moe_expert_layer_02_gb300 import accounting as acc
+    shape = (cfg.E, cfg.I, cfg.K, cfg.I_s, cfg.wfmt, cfg.shared_bf16, cfg.H, cfg.L)
+    reuse = base if base is not None and base["shape"] == shape else None
+    raw = mi.make_inputs(cfg, device=dev, seed=0,
+                         expert_weights=reuse["raw"] if reuse is not None else None)
+    flags = ((m.F_ROUTER_BIAS if (cfg.zipf_bias or cfg.sel_bias) else 0)
+             | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
+             | (m.F_SIGMOID_ROUTING if cfg.routing == "sigmoid" else 0)
+             | (m.F_SITU if cfg.act == "situ" else 0)
+             | (m.F_FUSED_COMBINE if fused_combine else 0))
+    wfmt = {"fp8": m.W_FP8, "mxfp4": m.W_MXFP4, "fp8_block": m.W_FP8_BLOCK}[cfg.wfmt]
+    packed = {}
+    if pack and reuse is not None:
+        packed = reuse["packed"]
+    elif pack:
+        # one-time load-time weight preparation (untimed): tile-major expert weights
+        pp = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, latent=cfg.L, wfmt=wfmt)
+        w13p, w2p = torch.empty_like(raw["w13"]), torch.empty_like(raw["w2"])
+        packed = dict(w13=w13p, w2=w2p)
+        if cfg.wfmt == "mxfp4":  # e8m0 scales regrouped into per-stage tensor-memory images
+            s13p, s2p = torch.empty_like(raw["w13_scale"]), torch.empty_like(raw["w2_scale"])
+            m.moe_pack_weights(pp, raw["w13"], raw["w2"], raw["w13_scale"], raw["w2_scale"], w13p,
+                               w2p, s13p, s2p)
+            packed.update(w13_scale=s13p, w2_scale=s2p)
+        else:
+            m.moe_pack_weights(pp, raw["w13"], raw["w2"], None, None, w13p, w2p)
+        if cfg.I_s and not cfg.shared_bf16:
+            ps = m.make_problem(cfg.T, cfg.H, cfg.I_s, 1, 1)
+            s13, s2 = torch.empty_like(raw["sw13"]), torch.empty_like(raw["sw2"])
+            m.moe_pack_weights(ps, raw["sw13"], raw["sw2"], None, None, s13, s2)
+            packed.update(sw13=s13, sw2=s2)
+        torch.cuda.synchronize()
+    if pack:
+        flags |= m.F_PACKED_WEIGHTS
+    inp = dict(raw, **packed)
+    p = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, latent=cfg.L,
+                       wfmt=wfmt, flags=flags)
+    wsb = torch.empty(m.moe_workspace_bytes(p), dtype=torch.uint8, device=dev)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    # touched experts (for algorithmic bytes): routing through the library itself
+    logits = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
+    tidx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+    tw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+    m.moe_router_logits(p, raw["x"], raw["router_w"], raw["router_bias"], logits)
+    m.moe_route(p, logits, raw["router_bias"], tidx, tw)
+    touched = int(torch.unique(tidx).numel())
+    del logits, tidx, tw
+
+    def step(x=None, y=None):
+        m.moe_forward(p, inp["x"] if x is None else x, inp["router_w"], inp["router_bias"],
+                      inp["w13"], inp["w13_scale"], inp["w2"], inp["w2_scale"], inp["sw13"],
+                      inp["sw13_scale"], inp["sw2"], inp["sw2_scale"], inp["wd"], inp["wu"],
+                      inp["gamma"], out if y is None else y, wsb)
+
+    return {"cfg": cfg, "shape": shape, "raw": raw, "packed": packed, "inp": inp, "p": p,
+            "wsb": wsb, "out": out, "touched": touched, "work": acc.layer_work(cfg, touched),
+            "step": step, "pack": pack}
+
+
+def timed_run(m, W, steps: int, warmup: int, ws_n: int, local: int):
+    """Warm-up, a per-stage table (every stage timed, up to 20 steps), then the
+    timed region: ``steps`` steps bracketed by CUDA events on the launching
+    stream, with only the grouped-GEMM launches (FFN1, FFN2) also bracketed
+    for their live kernel times, and the SM clocks sampled meanwhile."""
+    import torch
+    step = W["step"]
+    stream = torch.cuda.current_stream()
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    rc = m.moe_get_last_error()
+    if rc != 0:
+        raise SystemExit(f"device error word {rc} after warm-up ({W['cfg'].name})")
+    m.moe_profile_read()
+    m.moe_profile_enable(True)
+    for _ in range(min(steps, 20)):
+        step()
+    torch.cuda.synchronize()
+    m.moe_profile_enable(False)
+    stage_ms, stage_n = m.moe_profile_read()
+
+    clocks = ClockSampler(local)
+    time.sleep(0.2)
+    m.moe_profile_enable(True, stages=["ffn1", "ffn2"])
+    n0 = m.moe_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    launches = m.moe_launch_count() - n0
+    m.moe_profile_enable(False)
+    live_ms, live_n = m.moe_profile_read()
+    clk = clocks.stop()
+    rc = m.moe_get_last_error()
+    if rc != 0:
+        raise SystemExit(f"device error word {rc} after the timed region ({W['cfg'].name})")
+    return {"ms": ev0.elapsed_time(ev1) / steps, "launches": launches, "clocks": clk,
+            "stages_ms": {k: v / max(stage_n[k], 1) for k, v in stage_ms.items()},
+            "ffn1_ms": live_ms["ffn1"] / max(live_n["ffn1"], 1),
+            "ffn2_ms": live_ms["ffn2"] / max(live_n["ffn2"], 1)}
+
+
+def peak_clock_mhz():
+    """Median SM clock under which the sustained bf16 peak was measured."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["clocks_under_load"]["sm_mhz_median"])
+    except Exception:
+        return None
+
+
+def roofline_record(m, W, R, ms_step):
+    """The dominant kernel's roofline (FFN1, from its live CUDA-event time) and
+    the grouped GEMMs' tensor rate against the fp8 peak."""
+    from moe_expert_layer_02_gb300 import accounting as acc
+    cfg, touched = W["cfg"], W["touched"]
+    hbm, bf16, bf16_sus, src = peaks()
+    rows = cfg.R + (cfg.T if (cfg.I_s and not cfg.shared_bf16) else 0)
+    ffn1_bytes = acc.ffn1_launch_bytes(cfg, touched)
+    ffn1_flops = acc.ffn1_flops(rows, cfg.K, cfg.I)
+    ffn2_flops = acc.ffn2_flops(rows, cfg.K, cfg.I)
+    # decode-like batches stream weights (HBM-bound); large batches are bound by
+    # the fp8 tensor rate, taken as 2 x the measured bf16 rate (nominal ratio),
+    # sustained figure because the kernel runs inside a seconds-long loop
+    fp8_peak = 2.0 * (bf16_sus or bf16)
+    t_hbm = ffn1_bytes / (hbm * 1e9)
+    t_mma = ffn1_flops / (fp8_peak * 1e12)
+    ms1 = R["ffn1_ms"]
+    if t_hbm >= t_mma:
+        ach = ffn1_bytes / (ms1 * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "peak_source": f"hbm_gbs of {src}"}
+    else:
+        ach = ffn1_flops / (ms1 * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": ach / fp8_peak,
+                "peak_source": f"2 x bf16_tflops_sustained of {src} (fp8 = 2 x bf16 nominal ratio)"}
+    plan = m.moe_describe(W["p"])
+    ffn1_kernel = plan.split()[0].split("=", 1)[1]
+    work = W["work"]
+    roof.update({"kernel": f"{ffn1_kernel} (W1|W3 + SiLU*gate)",
+                 "traffic": kernel_traffic("ffn1", cfg.name),
+                 "algorithmic_bytes_per_launch": ffn1_bytes, "flops_per_launch": ffn1_flops,
+                 "avg_launch_ms": ms1,
+                 "layer_hbm_frac": (work["bytes"] / (ms_step * 1e-3) / 1e9) / hbm,
+                 "layer_tensor_frac": (work["flops_fp8"] / (ms_step * 1e-3) / 1e12) / fp8_peak})
+    # grouped expert GEMMs (FFN1 + FFN2) against the fp8 tensor peak, and the
+    # same at the clock the peak was measured under (time x SM MHz on both sides)
+    gg_tflops = (ffn1_flops + ffn2_flops) / ((R["ffn1_ms"] + R["ffn2_ms"]) * 1e-3) / 1e12
+    pk_mhz = peak_clock_mhz()
+    run_mhz = (R["clocks"] or {}).get("sm_mhz")
+    gg = {"ffn1_ms": R["ffn1_ms"], "ffn2_ms": R["ffn2_ms"], "flops": ffn1_flops + ffn2_flops,
+          "tflops": gg_tflops, "fp8_peak_tflops": fp8_peak, "frac_of_fp8_peak": gg_tflops / fp8_peak,
+          "peak_sm_mhz": pk_mhz, "run_sm_mhz": run_mhz,
+          "frac_of_fp8_peak_at_run_clock": (gg_tflops / (fp8_peak * run_mhz / pk_mhz)
+                                            if (pk_mhz and run_mhz) else None)}
+    return roof, gg, plan
+
+
+def workload_record(m, W, args, ws_n, local, steps):
+    """One nested record of the bench line: another workload timed in the same
+    process after the headline one."""
+    cfg = W["cfg"]
+    R = timed_run(m, W, steps, args.warmup, ws_n, local)
+    value, ms_max = replica_value(W["work"]["bytes"] / 1e9, R["ms"], ws_n)
+    roof, gg, plan = roofline_record(m, W, R, ms_max)
+    return {"workload": workload_name(cfg), "steps": steps, "ms_per_step": ms_max,
+            "value": value, "unit": "GB/s", "latency_us": ms_max * 1e3,
+            "tflops_fp8": W["work"]["flops_fp8"] / (ms_max * 1e-3) / 1e12,
+            "touched_experts": W["touched"], "roofline": roof, "grouped_gemms": gg,
+            "clocks": R["clocks"], "stages_ms": R["stages_ms"], "gpu_launches": R["launches"],
+            "plan": plan}
+
+
 def run_ours(args, cfg):
-    import numpy as np
     import torch
 
     import moe_expert_layer_02_gb300 as m
     import moe_inputs as mi
-    from moe_expert_layer_02_gb300 import accounting as acc
     from moe_expert_layer_02_gb300 import build as mb
 
     ws_n, rank, local = dist_setup(args)
@@ -284,97 +485,13 @@ def run_ours(args, cfg):
     mb.build()
     m.load_library()
     dev = torch.device("cuda", local)
-    inp = mi.make_inputs(cfg, device=dev, seed=0)
-    flags = ((m.F_ROUTER_BIAS if (cfg.zipf_bias or cfg.sel_bias) else 0)
-             | (m.F_SHARED_BF16 if cfg.shared_bf16 else 0)
-             | (m.F_SIGMOID_ROUTING if cfg.routing == "sigmoid" else 0)
-             | (m.F_SITU if cfg.act == "situ" else 0)
-             | (m.F_FUSED_COMBINE if args.fused_combine else 0))
-    wfmt = {"fp8": m.W_FP8, "mxfp4": m.W_MXFP4, "fp8_block": m.W_FP8_BLOCK}[cfg.wfmt]
     pack = not args.no_pack
-    if pack:
-        # one-time load-time weight preparation (untimed): tile-major expert weights
-        pp = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, latent=cfg.L, wfmt=wfmt)
-        w13p, w2p = torch.empty_like(inp["w13"]), torch.empty_like(inp["w2"])
-        packed = dict(w13=w13p, w2=w2p)
-        if cfg.wfmt == "mxfp4":  # e8m0 scales regrouped into per-stage tensor-memory images
-            s13p, s2p = torch.empty_like(inp["w13_scale"]), torch.empty_like(inp["w2_scale"])
-            m.moe_pack_weights(pp, inp["w13"], inp["w2"], inp["w13_scale"], inp["w2_scale"], w13p,
-                               w2p, s13p, s2p)
-            packed.update(w13_scale=s13p, w2_scale=s2p)
-        else:
-            m.moe_pack_weights(pp, inp["w13"], inp["w2"], None, None, w13p, w2p)
-        if cfg.I_s and not cfg.shared_bf16:
-            ps = m.make_problem(cfg.T, cfg.H, cfg.I_s, 1, 1)
-            s13, s2 = torch.empty_like(inp["sw13"]), torch.empty_like(inp["sw2"])
-            m.moe_pack_weights(ps, inp["sw13"], inp["sw2"], None, None, s13, s2)
-            packed.update(sw13=s13, sw2=s2)
-        torch.cuda.synchronize()
-        host_inp = inp  # the oracle reads the original layout
-        inp = dict(inp, **packed)
-        flags |= m.F_PACKED_WEIGHTS
-    else:
-        host_inp = inp
-    p = m.make_problem(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, I_shared=cfg.I_s, latent=cfg.L,
-                       wfmt=wfmt, flags=flags)
-    wsb = torch.empty(m.moe_workspace_bytes(p), dtype=torch.uint8, device=dev)
-    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    W = load_workload(m, cfg, dev, pack, fused_combine=args.fused_combine)
+    p, inp, out, step = W["p"], W["inp"], W["out"], W["step"]
+    work = W["work"]
     stream = torch.cuda.current_stream()
-
-    def step(x=None, y=None):
-        m.moe_forward(p, inp["x"] if x is None else x, inp["router_w"], inp["router_bias"],
-                      inp["w13"], inp["w13_scale"], inp["w2"], inp["w2_scale"], inp["sw13"],
-                      inp["sw13_scale"], inp["sw2"], inp["sw2_scale"], inp["wd"], inp["wu"],
-                      inp["gamma"], out if y is None else y, wsb)
-
-    # touched experts (for algorithmic bytes): routing through the library itself
-    logits = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
-    tidx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
-    tw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
-    m.moe_router_logits(p, inp["x"], inp["router_w"], inp["router_bias"], logits)
-    m.moe_route(p, logits, inp["router_bias"], tidx, tw)
-    touched = int(torch.unique(tidx).numel())
-    work = acc.layer_work(cfg, touched)
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    rc = m.moe_get_last_error()
-    if rc != 0:
-        raise SystemExit(f"device error word {rc} after warm-up")
-
-    # per-stage breakdown from a short loop with every stage timed
-    m.moe_profile_read()
-    m.moe_profile_enable(True)
-    for _ in range(min(args.steps, 20)):
-        step()
-    torch.cuda.synchronize()
-    m.moe_profile_enable(False)
-    stage_ms, stage_n = m.moe_profile_read()
-
-    # the timed region: only the FFN1 launches are bracketed by events (for the
-    # roofline's live kernel time), so the step itself runs as a user's would
-    clocks = ClockSampler(local)
-    time.sleep(0.2)
-    m.moe_profile_enable(True, stages=["ffn1"])
-    n0 = m.moe_launch_count()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(ws_n)
-    torch.cuda.synchronize()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(ws_n)
-    launches = m.moe_launch_count() - n0
-    m.moe_profile_enable(False)
-    ffn1_live_ms, ffn1_live_n = m.moe_profile_read()
-    clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    rc = m.moe_get_last_error()
-    if rc != 0:
-        raise SystemExit(f"device error word {rc} after the timed region")
+    R = timed_run(m, W, args.steps, args.warmup, ws_n, local)
+    ms = R["ms"]
 
     # the same step replayed from a CUDA graph (as a serving loop would run a
     # captured layer): the kernels' launch cost leaves the host entirely
@@ -448,63 +565,50 @@ def run_ours(args, cfg):
     bytes_step = work["bytes"]
     value, ms_max = replica_value(bytes_step / 1e9, ms, ws_n)
     e2e_value, e2e_ms = replica_value(bytes_step / 1e9, e0.elapsed_time(e1) / e2e_steps, ws_n)
-    hbm, bf16, bf16_sus, src = peaks()
-    ffn1_ms = ffn1_live_ms["ffn1"] / max(ffn1_live_n["ffn1"], 1)
-    ffn1_bytes = acc.ffn1_launch_bytes(cfg, touched)
-    ffn1_flops = acc.ffn1_flops(cfg.R + (cfg.T if cfg.I_s else 0), cfg.K, cfg.I)
-    traffic = kernel_traffic("ffn1", cfg.name)
-    fl = work["flops_fp8"]
-    # decode-like batches stream weights (HBM-bound); large batches are bound by
-    # the fp8 tensor rate, taken as 2 x the measured bf16 rate (nominal ratio),
-    # sustained figure because the kernel runs inside a seconds-long loop
-    t_hbm = ffn1_bytes / (hbm * 1e9)
-    fp8_peak = 2.0 * (bf16_sus or bf16)
-    t_mma = ffn1_flops / (fp8_peak * 1e12)
-    if t_hbm >= t_mma:
-        ach = ffn1_bytes / (ffn1_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "peak_source": f"hbm_gbs of {src}"}
-    else:
-        ach = ffn1_flops / (ffn1_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": ach / fp8_peak,
-                "peak_source": f"2 x bf16_tflops_sustained of {src} (fp8 = 2 x bf16 nominal ratio)"}
-    plan = m.moe_describe(p)
-    ffn1_kernel = plan.split()[0].split("=", 1)[1]
-    roof.update({"kernel": f"{ffn1_kernel} (W1|W3 + SiLU*gate)", "traffic": traffic,
-                 "algorithmic_bytes_per_launch": ffn1_bytes, "flops_per_launch": ffn1_flops,
-                 "avg_launch_ms": ffn1_ms,
-                 "layer_hbm_frac": (bytes_step / (ms_max * 1e-3) / 1e9) / hbm,
-                 "layer_tensor_frac": (fl / (ms_max * 1e-3) / 1e12) / fp8_peak})
+    roof, gg, plan = roofline_record(m, W, R, ms_max)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_n, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
         "config": {"workload": workload_name(cfg), "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
-                   "top_k": cfg.k, "I_shared": cfg.I_s, "touched_experts": touched,
+                   "top_k": cfg.k, "I_shared": cfg.I_s, "touched_experts": W["touched"],
                    "parallelism": "replicas" if ws_n > 1 else "single",
                    "weights": "tile-major (moe_pack_weights, untimed)" if pack else "row-major",
                    "plan": plan,
                    "l2": "inputs larger than L2 (%.1f GB of weights per step), no flush" % (
                        (work["bytes_weights_routed"] + work["bytes_weights_shared"]) / 1e9)},
         "latency_us": ms_max * 1e3,
-        "tflops_fp8": fl / (ms_max * 1e-3) / 1e12,
+        "tflops_fp8": work["flops_fp8"] / (ms_max * 1e-3) / 1e12,
         "roofline": roof,
-        "stages_ms": {k: v / max(stage_n[k], 1) for k, v in stage_ms.items()},
-        "gpu_launches": launches,
+        "grouped_gemms": gg,
+        "stages_ms": R["stages_ms"],
+        "gpu_launches": R["launches"],
         "graph_ms_per_step": graph_ms,
-        "clocks": clk,
+        "clocks": R["clocks"],
         "e2e": {"value": e2e_value, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
     }
+    del x_dev, y_dev, x_host, out_host
     if rank == 0 and ws_n == 1:
-        host = mi.to_numpy({k: v for k, v in host_inp.items()})
+        host = mi.to_numpy({k: v for k, v in W["raw"].items()})
         dt, n, cores = cpu_baseline(cfg, host, args.ref_tokens)
+        del host
         frac = n / cfg.T
         line["cpu_baseline"] = {
             "value": bytes_step * frac / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"first {n} of {cfg.T} tokens, whole layer per token, bytes scaled by {frac:.4f}",
             "seconds": dt}
+    # the other workloads of the layer, each timed in this process after the
+    # headline one (weights of equal shape are shared with it)
+    extra = [] if (ws_n > 1 or args.also in ("", "none")) else [
+        n for n in args.also.split(",") if n and n != cfg.name]
+    if extra:
+        line["workloads"] = {}
+        for name in extra:
+            Wx = load_workload(m, mi.CONFIGS[name], dev, pack, base=W)
+            line["workloads"][name] = workload_record(m, Wx, args, ws_n, local, args.also_steps)
+            del Wx
+            torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws_n > 1:
@@ -513,8 +617,62 @@ def run_ours(args, cfg):
     return 0
 
 
+def run_stage(args):
+    """Time one entry point alone on seeded inputs (for profiling a stage under
+    ncu without a whole layer's weights on the device): ``--stage router
+    --dims T H E`` (moe_router_logits) or ``--stage route --dims T E k``
+    (moe_route).  x ~ N(0,1) bf16, router weights ~ N(0,1/H) fp32, logits ~
+    N(0,1), generated on the device from seed 0."""
+    import torch
+
+    import moe_expert_layer_02_gb300 as m
+    from moe_expert_layer_02_gb300 import build as mb
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --stage needs a CUDA device")
+    mb.build()
+    m.load_library()
+    g = torch.Generator(device="cuda").manual_seed(0)
+    if args.stage == "router":
+        T, H, E = args.dims
+        x = torch.randn(T, H, device="cuda", generator=g).to(torch.bfloat16)
+        w = torch.randn(E, H, device="cuda", generator=g) / H ** 0.5
+        out = torch.empty(T, E, device="cuda")
+        p = m.make_problem(T, H, 128, E, 1)
+        call = lambda: m.moe_router_logits(p, x, w, None, out)  # noqa: E731
+        work, unit = 2.0 * T * H * E, "TFLOP/s"
+    else:
+        T, E, k = args.dims
+        logits = torch.randn(T, E, device="cuda", generator=g)
+        idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+        wt = torch.empty(T, k, device="cuda")
+        p = m.make_problem(T, 128, 128, E, k)
+        call = lambda: m.moe_route(p, logits, None, idx, wt)  # noqa: E731
+        work, unit = 4.0 * T * E, "GB/s"
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(args.steps):
+        call()
+    ev[1].record()
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    status = m.moe_get_last_error()
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"stage": args.stage, "dims": args.dims, "us_per_call": ms * 1e3,
+                      "rate": rate, "unit": unit, "status": status}), flush=True)
+    if status:
+        raise SystemExit(f"device error {status}")
+    return 0
+
+
 def main():
     args = parse()
+    if args.stage:
+        if not args.dims:
+            raise SystemExit("--stage needs --dims")
+        return run_stage(args)
     import moe_inputs as mi
     cfg = mi.CONFIGS[args.config]
     if args.impl == "reference":
