@@ -112,6 +112,27 @@ __device__ __forceinline__ int4 tile_item(const PairGemm& g, int item) {
   return make_int4(0, row0, min(2 * P_ROWS, g.dense_rows - row0), 0);
 }
 
+// Tile t -> (item, output block).  Dense launches and groups without the
+// count in the item's fourth field go item by item (t = item * NB + nb).  A
+// group's items carry {index within the group, items in the group} there, and
+// its tiles go output block by output block instead: the group's n items of
+// one block are n consecutive tiles, which neighbouring SM pairs run at the
+// same time, so they stream the same expert weights while those are in L2.
+// (A group cut short by the end of the list keeps the item-by-item order.)
+__device__ __forceinline__ int2 tile_coords(const PairGemm& g, int tile, int NB, int n_items) {
+  int item = tile / NB, nb = tile - item * NB;
+  if (g.items) {
+    const int w = g.items[item].w;
+    const int first = item - (w & 0xFFFF), n = w >> 16;
+    if (w && first >= 0 && first + n <= n_items) {
+      const int local = tile - first * NB;
+      item = first + local % n;
+      nb = local / n;
+    }
+  }
+  return make_int2(item, nb);
+}
+
 // Grouped items of at most 128 rows run as M = 128 tiles: each CTA stages 64
 // activation rows, and the tile's accumulator lands in tensor-memory columns
 // 0..127 of the pair: lanes 0..63 hold rows 0..63 of the CTA's half for output
@@ -222,7 +243,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters) {
-        const int item = tile / NB, nb = tile - item * NB;
+        const int2 tc = tile_coords(g, tile, NB, n_items);
+        const int item = tc.x, nb = tc.y;
         const int4 it = tile_item(g, item);
         const bool shared = g.items && it.x >= g.E;
         const CUtensorMap* tw = shared ? &tm_ws : &tm_w;
@@ -289,7 +311,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       bool issued_any = false;
       const uint32_t idesc256 = pair_idesc<KIND>(), idesc128 = pair_idesc<KIND>(128);
       for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters, ++it_local) {
-        const uint32_t idesc = is_small(g, tile_item(g, tile / NB)) ? idesc128 : idesc256;
+        const uint32_t idesc =
+            is_small(g, tile_item(g, tile_coords(g, tile, NB, n_items).x)) ? idesc128 : idesc256;
         const int acc = it_local % P_ACC_STAGES;
         const uint32_t acc_phase = (uint32_t)(it_local / P_ACC_STAGES) & 1u;
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, g.err, s_abort)) break;
@@ -333,7 +356,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     int grp = 0;  // groups stored by this warp (transpose buffer = grp & 1)
     int it_local = 0;
     for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++it_local) {
-      const int item = tile / NB, nb = tile - item * NB;
+      const int2 tc = tile_coords(g, tile, NB, n_items);
+      const int item = tc.x, nb = tc.y;
       const int4 it = tile_item(g, item);
       const bool shared = g.items && it.x >= g.E;
       const int acc = it_local % P_ACC_STAGES;
