@@ -17,24 +17,25 @@
 // How.
 //  1. latent_down_kernel: a GEMM on SM pairs (tcgen05.mma cta_group::2,
 //     kind::f16, bf16 operands, fp32 accumulation in tensor memory).  A tile is
-//     256 token rows (128 per CTA) x 128 latent features (64 weight rows staged
-//     per CTA).  The accumulation restarts every kChunkStages K stages (128 K,
-//     eight MMAs) in the next of four tensor-memory buffers, and eight epilogue
-//     warps (two per lane quarter, 64 columns each) add every chunk's partial
-//     sums into registers: S in fp32 (the dot product) and A in bf16 (the sum
-//     of the partials' magnitudes, which scales the remaining error).  Short
-//     accumulations keep the tensor core's own error ~30x smaller than one
-//     long one (0.014% of roundings off instead of 0.40%).  At the tile's end
-//     each element is rounded to bf16 from S and flagged when a bf16 rounding
-//     boundary lies within MOE_ZFLAG_ULPS * 2^-23 * A of S: only there can the
-//     remaining error change the rounding.
+//     256 token rows (128 per CTA) x 256 latent features (128 weight rows
+//     staged per CTA).  The accumulation restarts every kChunkStages K stages
+//     (128 K, eight MMAs) in the other of two tensor-memory buffers, and eight
+//     epilogue warps (two per lane quarter, 128 columns each) add every chunk's
+//     partial sums into registers: S in fp32 (the dot product) and Q in bf16
+//     (the sum of the partials' squares, which scales the remaining error:
+//     the chunks' rounding errors add like independent terms of their size).
+//     Short accumulations keep the tensor core's own error ~30x smaller than
+//     one long one (0.014% of roundings off instead of 0.40%).  At the tile's
+//     end each element is rounded to bf16 from S and flagged when a bf16
+//     rounding boundary lies within MOE_ZFLAG_ULPS * 2^-23 * sqrt(Q) of S:
+//     only there can the remaining error change the rounding.
 //  2. latent_fix_kernel: one block per token recomputes every flagged element
 //     on the CUDA cores in two-fp32 arithmetic -- a product of two bf16 values
 //     is exact in fp32, and TwoSum keeps every addition's rounding error -- and
 //     rounds the unevaluated sum hi + lo to nearest-even bf16.
 //
 // Pipeline and waits follow ffn_gemm_2cta.cu: warp 0 TMA producer, warp 1 MMA
-// issuer (even CTA), warps 2-9 epilogue; both CTAs' loads complete on the even
+// issuer (even CTA), warps 4-11 epilogue; both CTAs' loads complete on the even
 // CTA's `full` barriers; commits multicast to both CTAs; the epilogues hand a
 // buffer back on the even CTA's `tempty` barrier.  Every wait is bounded.
 #include <cudaTypedefs.h>
@@ -44,14 +45,17 @@
 #include "device.cuh"
 #include "internal.h"
 
-// Margin of the flag test in units of 2^-23 * A (A = sum of the chunk partials'
-// magnitudes).  Calibrated on a GB300 at the LatentMoE shape (x [4096, 7168]
-// N(0,1), Wd N(0, 1/7168), 14.7 M elements, margin -> elements whose bf16
-// rounding still differed from the exact one): 0 -> 2013, 0.5 -> 12, 1 -> 1,
-// 2 -> 0.  Three units leave a factor 1.5 over the last; a larger margin only
-// sends more elements to the exact recomputation.
+// Margin of the flag test in units of 2^-23 * sqrt(Q), Q = the sum of the
+// squared chunk partials.  Calibrated on a GB300 at the LatentMoE shape (x
+// [4096, 7168] N(0,1), Wd N(0, 1/7168), 14.7 M elements; margin -> share
+// flagged, elements whose bf16 rounding still differed from the exact one):
+// 0 -> 0.003%, 2013; 4 -> 0.14%, 2; 6 -> 0.20%, 1; 8 -> 0.26%, 0; 12 -> 0.37%,
+// 0; 16 -> 0.48%, 0.  Twelve leaves a factor 1.5 over the first margin without
+// a miss and 2 over the last with one; a larger margin only sends more
+// elements to the exact recomputation.  (A margin from the sum of the
+// partials' magnitudes needed 0.41% flagged for its first zero.)
 #ifndef MOE_ZFLAG_ULPS
-#define MOE_ZFLAG_ULPS 3.0f
+#define MOE_ZFLAG_ULPS 12.0f
 #endif
 
 namespace moe {
@@ -59,21 +63,42 @@ namespace moe {
 namespace {
 
 constexpr int LD_ROWS = 128;            // token rows per CTA (M = 256 per pair)
-constexpr int LD_N = 128;               // latent features per tile
 constexpr int LD_BK = 128;              // K bytes per stage (64 bf16)
 constexpr int LD_EL = LD_BK / 2;        // K elements per stage
 constexpr int LD_UMMA_B = 32;           // K bytes per tcgen05.mma (16 bf16)
-constexpr int LD_A_BYTES = LD_ROWS * LD_BK;         // 16 KB
-constexpr int LD_B_BYTES = (LD_N / 2) * LD_BK;      // 8 KB (this CTA's 64 weight rows)
-constexpr int LD_STAGE = LD_A_BYTES + LD_B_BYTES;   // 24 KB
-constexpr int LD_STAGES = 8;
+constexpr int LD_A_BYTES = LD_ROWS * LD_BK;  // 16 KB
 constexpr int kChunkStages = 2;         // K stages per tensor-core accumulation
-constexpr int LD_BUFS = 4;              // partial-sum buffers in tensor memory
-constexpr int LD_TMEM_COLS = LD_BUFS * LD_N;  // 512
-constexpr int LD_EPI_WARPS = 8;
-constexpr int LD_THREADS = 64 + 32 * LD_EPI_WARPS;  // 320
-constexpr int LD_NUM_BARS = 2 * LD_STAGES + 2 * LD_BUFS + 1;
-constexpr int LD_SMEM = 1024 + LD_STAGES * LD_STAGE + LD_NUM_BARS * 8 + 16 + LD_STAGES * 4;
+constexpr int LD_EPI_WARPS = 8;         // two per tensor-memory lane quarter
+
+// Tiles of N = 256 latent features (128 weight rows staged per CTA), two
+// partial-sum buffers filling the 512 tensor-memory columns, twelve warps:
+// warp 0 loads, warp 1 issues the MMAs, warps 2-3 idle, warps 4-11 add the
+// partials, 128 columns each.  The first warp group gives its registers up
+// (setmaxnreg) so that the epilogue threads can hold 128 fp32 sums and 64 bf16
+// pairs of squares.  x is read from L2 L/256 times, and a K stage moves 32 KB into each
+// SM's shared memory per 2.1 M multiply-adds.  (A first version with 128-wide
+// tiles and ten warps, within the 168 registers a thread gets when three warps
+// share a scheduler, read x twice as often and moved 24 KB per 1.05 M
+// multiply-adds: 0.30 ms at the LatentMoE shape, tensor pipe 31% busy.)
+template <int N>
+struct LdCfg {
+  static_assert(N == 256, "the register split below is laid out for 256-wide tiles");
+  static constexpr int WIDE = 1;
+  static constexpr int WARPS = 12;
+  static constexpr int THREADS = 32 * WARPS;
+  static constexpr int EPI0 = 4;             // first epilogue warp
+  static constexpr int COLS = N / 2;         // columns per epilogue thread
+  static constexpr int BUFS = 512 / N;
+  static constexpr int B_BYTES = (N / 2) * LD_BK;
+  static constexpr int STAGE = LD_A_BYTES + B_BYTES;
+  static constexpr int STAGES = 6;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * BUFS + 1;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + NUM_BARS * 8 + 16 + STAGES * 4;
+  // the wide kernel's register split: launched at 168 a thread (384 x 168 =
+  // 64512), the first warp group drops to 40 and the two epilogue groups rise
+  // to 232 (4 x 32 x 40 + 8 x 32 x 232 = 64512)
+  static constexpr int LAUNCH_REGS = 168, LOW_REGS = 40, HIGH_REGS = 232;
+};
 
 struct LatentDown {
   int T, H, L;
@@ -84,8 +109,9 @@ struct LatentDown {
 
 // f32 accumulate (bits 4-5 = 1), bf16 A and B (kind::f16 format 1 at bits 7-9
 // and 10-12), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+template <int N>
 __device__ __forceinline__ uint32_t ld_idesc() {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(LD_N >> 3) << 17) |
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)((2 * LD_ROWS) >> 4) << 24);
 }
 
@@ -96,6 +122,32 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d, uint64_t adesc, uint64
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
+}
+
+// Two fp32 additions in one instruction (round to nearest, as two adds).
+__device__ __forceinline__ void add_f32x2(uint64_t& acc, uint32_t lo, uint32_t hi) {
+  asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tadd.rn.f32x2 %0, %0, t;\n\t}"
+      : "+l"(acc)
+      : "r"(lo), "r"(hi));
+}
+
+// acc (two bf16) += (lo^2, hi^2), with lo and hi rounded to bf16 first.
+__device__ __forceinline__ uint32_t add_sq_bf16x2(uint32_t acc, uint32_t lo, uint32_t hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b32 t;\n\tcvt.rn.bf16x2.f32 t, %2, %1;\n\t"
+      "fma.rn.bf16x2 %0, t, t, %3;\n\t}"
+      : "=r"(r)
+      : "r"(lo), "r"(hi), "r"(acc));
+  return r;
+}
+
+template <int R>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
 }
 
 // True when rounding s to bf16 may differ from rounding the exact value, given
@@ -110,22 +162,22 @@ __device__ __forceinline__ bool near_bf16_boundary(float s, float margin) {
   return margin >= 0.25f * ulp || fabsf(__uint_as_float(u) - mid) <= margin;
 }
 
-// 320 threads, one CTA per SM.  Ten warps put three on two of the four SM
-// sub-partitions, whose 16K registers then cap a thread at 168: the epilogue
-// keeps 64 fp32 sums, 64 loaded values and the magnitudes as 32 bf16 pairs.
-__global__ void __launch_bounds__(LD_THREADS, 1)
+template <int N>
+__global__ void __launch_bounds__(LdCfg<N>::THREADS, 1)
     latent_down_kernel(const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_w, const LatentDown g) {
+  using C = LdCfg<N>;
+  constexpr int COLS = C::COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LD_STAGES * LD_STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
   uint64_t* full = bars;
-  uint64_t* empty = bars + LD_STAGES;
-  uint64_t* tfull = bars + 2 * LD_STAGES;
-  uint64_t* tempty = tfull + LD_BUFS;
-  uint64_t* drain = tempty + LD_BUFS;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + LD_NUM_BARS);
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + C::BUFS;
+  uint64_t* drain = tempty + C::BUFS;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   uint32_t* s_issued = s_tmem + 4;
 
@@ -134,12 +186,12 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < LD_STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
       s_issued[s] = 0;
     }
-    for (int b = 0; b < LD_BUFS; ++b) {
+    for (int b = 0; b < C::BUFS; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
       mbar_init(smem_u32(&tempty[b]), 2 * LD_EPI_WARPS);  // the epilogue warps of both CTAs
     }
@@ -151,7 +203,7 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_w);
   }
-  if (warp == 1) tmem_alloc_pair(smem_u32(s_tmem), LD_TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(smem_u32(s_tmem), 512);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // barriers of both CTAs exist before any cross-CTA signal
@@ -160,12 +212,15 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
   pdl_wait();
 
   const int n_rt = (g.T + 2 * LD_ROWS - 1) / (2 * LD_ROWS);
-  const int n_ct = g.L / LD_N;
+  const int n_ct = g.L / N;
   const int n_tiles = n_rt * n_ct;
   const int KB = g.H / LD_EL;               // K stages per tile
   const int NCH = KB / kChunkStages;        // chunks per tile
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
 
+  if (warp < C::EPI0) {
+    // the first warp group (all four warps together) hands registers over
+    if (C::WIDE) regs_dec<C::LOW_REGS>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -175,26 +230,26 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
       for (int tile = cluster; tile < n_tiles && ok && !*s_abort; tile += n_clusters) {
         const int rt = tile / n_ct, ct = tile - rt * n_ct;
         const int row0 = rt * 2 * LD_ROWS + LD_ROWS * (int)rank;
-        const int wrow0 = ct * LD_N + (LD_N / 2) * (int)rank;
+        const int wrow0 = ct * N + (N / 2) * (int)rank;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, g.err, s_abort)) {
             ok = false;
             break;
           }
-          const uint32_t st = smem_u32(smem + stage * LD_STAGE);
+          const uint32_t st = smem_u32(smem + stage * C::STAGE);
           const uint32_t fb_leader = mapa_shared(smem_u32(&full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * LD_STAGE);
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * C::STAGE);
           tma_load_2d_pair(st, &tm_x, kb * LD_EL, row0, fb_leader);
           tma_load_2d_pair(st + LD_A_BYTES, &tm_w, kb * LD_EL, wrow0, fb_leader);
           s_issued[stage] = phase + 1u;
-          if (++stage == LD_STAGES) {
+          if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (*s_abort && leader) {  // the pair's loads complete on the even CTA's barriers
-        for (int s = 0; s < LD_STAGES; ++s)
+        for (int s = 0; s < C::STAGES; ++s)
           if (s_issued[s]) mbar_wait_drain(smem_u32(&full[s]), s_issued[s] - 1u);
       }
     }
@@ -204,24 +259,24 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
       int stage = 0, chunk = 0;
       uint32_t phase = 0;
       bool issued_any = false, ok = true;
-      const uint32_t idesc = ld_idesc();
+      const uint32_t idesc = ld_idesc<N>();
       for (int tile = cluster; tile < n_tiles && ok && !*s_abort; tile += n_clusters) {
         for (int c = 0; c < NCH && ok; ++c, ++chunk) {
-          const int buf = chunk % LD_BUFS;
-          const uint32_t bphase = (uint32_t)(chunk / LD_BUFS) & 1u;
+          const int buf = chunk % C::BUFS;
+          const uint32_t bphase = (uint32_t)(chunk / C::BUFS) & 1u;
           if (!mbar_wait(smem_u32(&tempty[buf]), bphase ^ 1u, g.err, s_abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem + buf * LD_N;
+          const uint32_t d = tmem + buf * N;
           for (int s = 0; s < kChunkStages; ++s) {
             if (!mbar_wait(smem_u32(&full[stage]), phase, g.err, s_abort)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(smem + stage * LD_STAGE);
+            const uint32_t a0 = smem_u32(smem + stage * C::STAGE);
             const uint32_t b0 = a0 + LD_A_BYTES;
 #pragma unroll
             for (int kk = 0; kk < LD_BK / LD_UMMA_B; ++kk)
@@ -229,7 +284,7 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
                             smem_desc_sw128(b0 + kk * LD_UMMA_B), idesc, (s | kk) ? 1u : 0u);
             issued_any = true;
             mma_commit_pair(smem_u32(&empty[stage]), 0x3);
-            if (++stage == LD_STAGES) {
+            if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
@@ -242,25 +297,28 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
         mbar_wait_drain(smem_u32(drain), 0);
       }
     }
+  }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;
+    if (C::WIDE) regs_inc<C::HIGH_REGS>();
+    const int ew = warp - C::EPI0;
     const int q = warp & 3;          // tensor-memory lane quarter this warp may read
-    const int half = ew >> 2;        // which 64 of the tile's 128 columns
+    const int half = ew >> 2;        // which half of the tile's columns
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
     int chunk = 0;
     bool ok = true;
     for (int tile = cluster; tile < n_tiles && ok; tile += n_clusters) {
       const int rt = tile / n_ct, ct = tile - rt * n_ct;
-      float S[64];
-      __nv_bfloat162 A[32];  // sums of |partial| (only a margin: 8 bits suffice)
+      uint64_t S[COLS / 2];  // fp32 sums of columns 2j, 2j + 1
+      uint32_t Q[COLS / 2];  // bf16 sums of partial^2 (only a margin: 8 bits suffice)
 #pragma unroll
-      for (int j = 0; j < 64; ++j) S[j] = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) A[j] = __floats2bfloat162_rn(0.0f, 0.0f);
+      for (int j = 0; j < COLS / 2; ++j) {
+        S[j] = 0ull;
+        Q[j] = 0u;
+      }
       for (int c = 0; c < NCH; ++c, ++chunk) {
-        const int buf = chunk % LD_BUFS;
-        const uint32_t bphase = (uint32_t)(chunk / LD_BUFS) & 1u;
+        const int buf = chunk % C::BUFS;
+        const uint32_t bphase = (uint32_t)(chunk / C::BUFS) & 1u;
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait(smem_u32(&tfull[buf]), bphase, g.err, s_abort) ? 1 : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -269,52 +327,57 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
           break;
         }
         tc_fence_after();
-        // all 64 columns in flight at once, so the load latency is paid once
-        // per chunk; the buffer goes back as soon as they have landed
-        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + buf * LD_N + half * 64;
-        uint32_t v[4][16];
+        const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + buf * N + half * COLS;
+        // 32 columns per wait (registers are the limit); the buffer goes back
+        // once the last group has landed
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tmem_ld16(tb + 16 * i, v[i]);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader0 + buf * 8);
+        for (int r = 0; r < COLS / 32; ++r) {
+          uint32_t v[32];
+          tmem_ld16(tb + 32 * r, *reinterpret_cast<uint32_t(*)[16]>(v));
+          tmem_ld16(tb + 32 * r + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          tmem_ld_wait();
+          if (r == COLS / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader0 + buf * 8);
+          }
 #pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          const float p0 = __uint_as_float(v[j >> 4][j & 15]);
-          const float p1 = __uint_as_float(v[j >> 4][(j & 15) + 1]);
-          S[j] += p0;
-          S[j + 1] += p1;
-          A[j >> 1] = __hadd2(A[j >> 1], __floats2bfloat162_rn(fabsf(p0), fabsf(p1)));
+          for (int j = 0; j < 32; j += 2) {
+            add_f32x2(S[16 * r + (j >> 1)], v[j], v[j + 1]);
+            Q[16 * r + (j >> 1)] = add_sq_bf16x2(Q[16 * r + (j >> 1)], v[j], v[j + 1]);
+          }
         }
       }
       if (!ok) break;
       const int row = rt * 2 * LD_ROWS + LD_ROWS * (int)rank + q * 32 + lane;
       if (row < g.T) {
-        const int col0 = ct * LD_N + half * 64;
-        uint32_t fw[2] = {0u, 0u};
-        uint32_t pk[32];
+        const int col0 = ct * N + half * COLS;
+        uint32_t fw[COLS / 32];
 #pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          // margin from the magnitude sums, widened by 1/8 for their bf16
-          // rounding: a sum of n positive terms rounded at every step stays
-          // within n * 2^-9 of the exact one, at most 1/8 for the <= 64
-          // chunks of K <= 8192 (and ~1% in practice)
-          const float2 a = __bfloat1622float2(A[j >> 1]);
-          const float m0 = (MOE_ZFLAG_ULPS * 1.125f * 0x1p-23f) * a.x;
-          const float m1 = (MOE_ZFLAG_ULPS * 1.125f * 0x1p-23f) * a.y;
-          if (near_bf16_boundary(S[j], m0)) fw[j >> 5] |= 1u << (j & 31);
-          if (near_bf16_boundary(S[j + 1], m1)) fw[(j + 1) >> 5] |= 1u << ((j + 1) & 31);
-          __nv_bfloat162 b = __floats2bfloat162_rn(S[j], S[j + 1]);
-          pk[j >> 1] = *reinterpret_cast<uint32_t*>(&b);
-        }
+        for (int i = 0; i < COLS / 32; ++i) fw[i] = 0u;
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.z) + (size_t)row * g.L + col0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int j0 = 0; j0 < COLS; j0 += 8) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = j0; j < j0 + 8; j += 2) {
+            // margin from the partials' root sum of squares (the chunks'
+            // rounding errors add like independent terms of their size)
+            const float m0 = (MOE_ZFLAG_ULPS * 0x1p-23f) * sqrtf(__uint_as_float(Q[j >> 1] << 16));
+            const float m1 =
+                (MOE_ZFLAG_ULPS * 0x1p-23f) * sqrtf(__uint_as_float(Q[j >> 1] & 0xFFFF0000u));
+            float s0, s1;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(S[j >> 1]));
+            if (near_bf16_boundary(s0, m0)) fw[j >> 5] |= 1u << (j & 31);
+            if (near_bf16_boundary(s1, m1)) fw[(j + 1) >> 5] |= 1u << ((j + 1) & 31);
+            __nv_bfloat162 b = __floats2bfloat162_rn(s0, s1);
+            pk[(j - j0) >> 1] = *reinterpret_cast<uint32_t*>(&b);
+          }
+          dst[j0 / 8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
         uint32_t* fdst = g.flags + (size_t)row * (g.L / 32) + col0 / 32;
-        fdst[0] = fw[0];
-        fdst[1] = fw[1];
+#pragma unroll
+        for (int i = 0; i < COLS / 32; ++i) fdst[i] = fw[i];
       }
     }
   }
@@ -326,7 +389,7 @@ __global__ void __launch_bounds__(LD_THREADS, 1)
   pdl_release();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc_pair(tmem, LD_TMEM_COLS);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -450,24 +513,44 @@ bool ld_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uin
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// True when the kernel was built with exactly the per-thread register count
+// its setmaxnreg split assumes: a block launched with fewer registers could
+// never complete the split.
+bool wide_kernel_usable() {
+  static const bool ok = [] {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, latent_down_kernel<256>) == cudaSuccess &&
+           fa.numRegs == LdCfg<256>::LAUNCH_REGS;
+  }();
+  return ok;
+}
+
+template <int N>
+cudaError_t launch_down_gemm(const void* x, const void* wd, const LatentDown& g, cudaStream_t s) {
+  using C = LdCfg<N>;
+  CUtensorMap tx, tw;
+  if (!ld_map(&tx, x, g.H, g.T, LD_ROWS) || !ld_map(&tw, wd, g.H, g.L, N / 2))
+    return cudaErrorInvalidValue;
+  cudaError_t e = ensure_max_smem<latent_down_kernel<N>>(C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int tiles = ((g.T + 2 * LD_ROWS - 1) / (2 * LD_ROWS)) * (g.L / N);
+  const int clusters = std::min(device_sm_count() / 2, tiles);
+  count_launch();
+  return launch_kernel(latent_down_kernel<N>, dim3(2 * clusters), dim3(C::THREADS), C::SMEM, s,
+                       2, tx, tw, g);
+}
+
 }  // namespace
 
 size_t latent_down_flag_bytes(int T, int L) { return (size_t)T * (L / 32) * 4; }
 
 cudaError_t launch_latent_down(const void* x, const void* wd, void* z, uint32_t* flags, int T,
                                int H, int L, int* err, cudaStream_t s) {
-  if (T <= 0 || H % (LD_EL * kChunkStages) || L % LD_N || !flags) return cudaErrorInvalidValue;
-  CUtensorMap tx, tw;
-  if (!ld_map(&tx, x, H, T, LD_ROWS) || !ld_map(&tw, wd, H, L, LD_N / 2))
-    return cudaErrorInvalidValue;
+  if (T <= 0 || H % (LD_EL * kChunkStages) || L % 128 || !flags) return cudaErrorInvalidValue;
   LatentDown g{T, H, L, z, flags, err};
-  cudaError_t e = ensure_max_smem<latent_down_kernel>(LD_SMEM);
-  if (e != cudaSuccess) return e;
-  const int tiles = ((T + 2 * LD_ROWS - 1) / (2 * LD_ROWS)) * (L / LD_N);
-  const int clusters = std::min(device_sm_count() / 2, tiles);
-  count_launch();
-  e = launch_kernel(latent_down_kernel, dim3(2 * clusters), dim3(LD_THREADS), LD_SMEM, s, 2, tx, tw,
-                    g);
+  // never launch a register split the build cannot complete (it would wait forever)
+  if (L % 256 || !wide_kernel_usable()) return cudaErrorInvalidDeviceFunction;
+  cudaError_t e = launch_down_gemm<256>(x, wd, g, s);
   if (e != cudaSuccess) return e;
   const size_t fx_smem = (size_t)H * 4 + (size_t)L * 2;
   if (fx_smem > (size_t)FX_SMEM_MAX) return cudaErrorInvalidValue;
