@@ -556,10 +556,16 @@ def run_ours(args, cfg):
     e1.record(stream)
     torch.cuda.synchronize()
     # the pipelined steps computed the same layer (bit for bit, except that the
-    # fused combine's fp32 sums may round differently in the last bf16 bit)
+    # fused combine's fp32 sums add in an order that is not fixed: there the
+    # outputs may differ by a bf16 ulp, and by more near zero, where the
+    # cancelling terms' rounding shows)
     last = y_dev[(e2e_steps - 1) & 1]
-    same = torch.equal(last, out) if not args.fused_combine else bool(
-        ((last.float() - out.float()).abs() <= out.float().abs() * 2.0 ** -7 + 1e-30).all())
+    if not args.fused_combine:
+        same = torch.equal(last, out)
+    else:
+        o = out.float()
+        rms = float(o.pow(2).mean().sqrt())
+        same = bool(((last.float() - o).abs() <= o.abs() * 2.0 ** -7 + 2.0 ** -7 * rms).all())
     if not same:
         raise SystemExit("end-to-end output differs from the device-timed output")
     bytes_step = work["bytes"]
