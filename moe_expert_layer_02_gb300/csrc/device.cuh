@@ -295,6 +295,20 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Four rows of a 2-D map whose box is one row high, rows r[0..3] at inner
+// coordinate c0 (a multiple of 16 bytes), into four consecutive box rows at
+// dst; out-of-range rows read as zeros.  Completion counted on an mbarrier of
+// either CTA of the pair (cta_group::2).
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* m, int c0,
+                                                 const int (&r)[4], uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]),
+      "r"(bar_cluster)
+      : "memory");
+}
+
 // Tensor-memory allocation shared by the pair: one warp of each CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),

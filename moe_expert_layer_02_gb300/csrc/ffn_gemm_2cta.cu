@@ -38,6 +38,14 @@
 // Grouped items of at most 128 rows run as M = 128 MMAs (64 activation rows
 // per CTA), so an expert's small last item is not padded to 256 rows; see
 // is_small() for the accumulator layout of those tiles.
+//
+// Row gather (FFN1, opt-in, tuning().ffn1_gather): the activations arrive as
+// one fp8 row per token; the producer warp's lanes each copy four of the
+// tile's rows per stage with one TMA tile::gather4 (a map whose box is one row
+// high; rows past the item read out-of-range zeros), straight into the
+// swizzled stage, completing on the even CTA's barrier like the other loads.
+// Correct, but the gathered stages arrive far slower than one 128-row box
+// (prefill FFN1 12.06 vs 3.70 ms), so permuted rows stay the default.
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
@@ -98,6 +106,12 @@ struct PairGemm {
   const float* row_w;     // DOWN: routing weight per row (nullptr = 1)
   void* out;              // bf16 output, row stride ldo elements
   int ldo;
+  int gather;             // fp8 SWIGLU: tm_x holds one row per token (box one row
+                          // high); the producer gathers row r of a tile from token
+                          // src[r] (r < R) or r - R (shared expert), and the
+                          // epilogue takes that token's activation scale
+  const int32_t* src;     // [R] token of each routed row (gather only)
+  int R, T;               // routed rows, tokens (gather only)
   int* err;
 };
 
@@ -239,10 +253,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // With the row gather the whole warp works: lane 0 waits, arms the stage
+    // and loads the weights, and every lane gathers four activation rows.
+    const bool gat = KIND == KIND_FP8 && EPI == EPI_SWIGLU && g.gather;
+    if (gat || lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters) {
+      for (int tile = cluster; tile < n_tiles; tile += n_clusters) {
+        int stop = lane == 0 ? *s_abort : 0;
+        if (gat) stop = __shfl_sync(0xffffffffu, stop, 0);
+        if (stop) break;
         const int2 tc = tile_coords(g, tile, NB, n_items);
         const int item = tc.x, nb = tc.y;
         const int4 it = tile_item(g, item);
@@ -262,14 +282,58 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           else
             tma_load_3d_pair(dst, m, kb * EL, row, gc, fb);
         };
+        // gather: the tokens of this CTA's rows 4 lane .. 4 lane + 3 (rows past
+        // the item read token T: out of range, so zeros)
+        const int cta_rows = small ? 64 : 128;
+        int tok[4] = {0, 0, 0, 0};
+        if (gat) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int local = cta_rows * (int)rank + 4 * lane + j;  // row within the item
+            const int r = it.y + local;
+            int t = g.T;
+            if (4 * lane + j < cta_rows && local < it.z && (unsigned)r < (unsigned)g.rows_total) {
+              t = r < g.R ? g.src[r] : r - g.R;
+              if ((unsigned)t >= (unsigned)g.T) t = g.T;
+            }
+            tok[j] = t;
+          }
+        }
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, g.err, s_abort)) {
+          int got = 1;
+          if (lane == 0) got = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, g.err, s_abort);
+          if (gat) got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
             ok = false;
             break;
           }
           const uint32_t st = smem_u32(smem + stage * P_STAGE);
           const uint32_t fb_leader = mapa_shared(smem_u32(&full[stage]), 0);
+          if (gat) {
+            if (lane == 0) {
+              if (leader)
+                mbar_arrive_expect_tx(smem_u32(&full[stage]),
+                                      small ? 2 * (P_A_BYTES / 2 + P_B_BYTES) : 2 * P_STAGE);
+              if (small) {
+                load_w(st + P_A_BYTES, twh, nb * 128 + 64 * (int)rank, kb, fb_leader);
+                load_w(st + P_A_BYTES + P_B_BYTES / 2, twh, g.I + nb * 128 + 64 * (int)rank, kb,
+                       fb_leader);
+              } else {
+                load_w(st + P_A_BYTES, tw, wrow, kb, fb_leader);
+              }
+              s_issued[stage] = phase + 1u;
+            }
+            // four 128-byte rows per copy, landing at rows 4 lane .. 4 lane + 3
+            // of the swizzled tile (the swizzle follows the shared address)
+            if (4 * lane < cta_rows)
+              tma_gather4_pair(st + 512 * lane, &tm_x, kb * EL, tok, fb_leader);
+            if (++stage == P_STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (leader)
             mbar_arrive_expect_tx(smem_u32(&full[stage]),
                                   small ? 2 * (P_A_BYTES / 2 + P_B_BYTES) : 2 * P_STAGE);
@@ -298,7 +362,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         }
         if (!ok) break;
       }
-      if (*s_abort && leader) {  // the pair's loads complete on the even CTA's barriers
+      if (lane == 0 && *s_abort && leader) {  // the pair's loads complete on the even CTA's barriers
         for (int s = 0; s < P_STAGES; ++s)
           if (s_issued[s]) mbar_wait_drain(smem_u32(&full[s]), s_issued[s] - 1u);
       }
@@ -425,7 +489,16 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         const int uo = small ? 64 : 128;     // tensor-memory column of u after g
         const int co = small ? 64 * hq : 0;  // this thread's first feature in the tile
         const int ncol = small ? 64 : 128;
-        const float xs = KIND == KIND_FP8 ? (valid ? g.xscale[row] : 0.0f) : 1.0f;
+        float xs = 1.0f;
+        if (KIND == KIND_FP8) {
+          xs = 0.0f;
+          if (valid && g.gather) {  // one scale per token
+            const int t = row < g.R ? g.src[row] : row - g.R;
+            if ((unsigned)t < (unsigned)g.T) xs = g.xscale[t];
+          } else if (valid) {
+            xs = g.xscale[row];
+          }
+        }
         uint32_t va[4][16], vb[4][16];  // g lo, g hi, u lo, u hi
         auto load = [&](uint32_t (&v)[4][16], int c) {
           __syncwarp();
@@ -592,9 +665,12 @@ cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   const uint64_t winner = a.packed ? P_BK : K;
   const uint64_t wrows = a.packed ? (uint64_t)Wrows * (K / P_BK) : Wrows;
   CUtensorMap twh, twsh, txh;
+  const bool gather = FFN1 && a.gather;
+  // gathered rows: one row per token, read by four-row gathers (box one row high)
+  const bool xmap = gather ? pair_map(&tx, KIND_FP8, 2, x, K, a.T, 1, 1)
+                           : pair_map(&tx, KIND_FP8, 2, x, K, a.rows_total, 1);
   if (!pair_map(&tw, KIND_FP8, 3, w, winner, wrows, a.E) ||
-      !pair_map(&tws, KIND_FP8, 3, ws ? ws : w, winner, wrows, 1) ||
-      !pair_map(&tx, KIND_FP8, 2, x, K, a.rows_total, 1) ||
+      !pair_map(&tws, KIND_FP8, 3, ws ? ws : w, winner, wrows, 1) || !xmap ||
       !pair_map(&twh, KIND_FP8, 3, w, winner, wrows, a.E, 64) ||
       !pair_map(&twsh, KIND_FP8, 3, ws ? ws : w, winner, wrows, 1, 64) ||
       !pair_map(&txh, KIND_FP8, 2, x, K, a.rows_total, 1, 64))
@@ -620,6 +696,10 @@ cudaError_t launch_grouped_pair(const GroupedFfnArgs& a, cudaStream_t s) {
   g.row_w = a.row_w;
   g.out = FFN1 ? a.h : a.y;
   g.ldo = FFN1 ? a.I : a.K;
+  g.gather = gather ? 1 : 0;
+  g.src = a.src;
+  g.R = a.R;
+  g.T = a.T;
   g.err = a.err;
   if (FFN1) return launch_pair_gemm<KIND_FP8, EPI_SWIGLU>(tw, tws, tx, tw, tx, txh, twh, twsh, g, s);
   return launch_pair_gemm<KIND_FP8, EPI_DOWN>(tw, tws, tx, tw, tx, txh, twh, twsh, g, s);

@@ -167,13 +167,15 @@ Plan make_plan(const moe_problem* p) {
   // the fused combine runs in the single-SM fp8 per-channel FFN2 epilogue
   q.fused = (p->flags & MOE_F_FUSED_COMBINE) && !q.L && !q.mx && !q.blockwise &&
             !q.shared_bf16 && !use_pair_gemm(q);
-  // tuning().ffn1_gather: the single-SM fp8 per-channel FFN1 gathers its rows by
-  // token and S4 writes one row per token.  Off by default: the producer's
-  // 16-byte cp.async copies (8 per row and stage) and the proxy fence before
-  // each stage's MMAs cost more than the smaller S4 saves (T=512, H=8192,
-  // I=2048, E=256 top-8, 128-row tiles: FFN1 1.35 vs 1.22 ms, S4 10.0 vs
-  // 12.9 us; T=2048: 1.84 vs 1.28 ms; on SM pairs 3x slower, not offered).
-  q.gather = !q.mx && !q.blockwise && !use_pair_gemm(q) && tuning().ffn1_gather;
+  // tuning().ffn1_gather: the fp8 per-channel FFN1 gathers its rows by token
+  // and S4 writes one row per token.  Off by default.  Single SM: the
+  // producer's 16-byte cp.async copies (8 per row and stage) and the proxy
+  // fence before each stage's MMAs cost more than the smaller S4 saves (T=512,
+  // H=8192, I=2048, E=256 top-8, 128-row tiles: FFN1 1.35 vs 1.22 ms, S4 10.0
+  // vs 12.9 us; T=2048: 1.84 vs 1.28 ms).  SM pairs: four-row TMA gathers
+  // (tile::gather4, 32 per stage and CTA); T=16384: FFN1 12.06 vs 3.70 ms, S4
+  // 0.099 vs 0.225 ms; T=8192 skewed: FFN1 5.63 vs 1.55 ms.
+  q.gather = !q.mx && !q.blockwise && tuning().ffn1_gather;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;

@@ -156,9 +156,9 @@ def test_mx_pair_plan(m):
 
 
 def test_row_gather_plan(m, tuning):
-    # ffn1_gather: the single-SM fp8 per-channel FFN1 gathers its rows by
-    # token, at any tile height; the SM-pair, block-wise and MXFP4 paths read
-    # permuted rows, and so does everything by default
+    # ffn1_gather: the fp8 per-channel FFN1 (single-SM or SM pairs) gathers
+    # its rows by token, at any tile height; the block-wise and MXFP4 paths
+    # read permuted rows, and so does everything by default
     dec = lambda: m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8, I_shared=2048))
     d = dec()
     assert "ffn1=grouped_ffn_kernel<FFN1,BN=128>" in d and "ffn1_rows=permuted" in d, d
@@ -167,7 +167,8 @@ def test_row_gather_plan(m, tuning):
     tuning(tile_n=32)
     assert "BN=32> " in dec() and "ffn1_rows=gathered" in dec()
     tuning(tile_n=0)
-    assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(16384, 8192, 2048, 256, 8,
+    # SM pairs gather with four-row TMA copies
+    assert "ffn1_rows=gathered" in m.moe_describe(m.make_problem(16384, 8192, 2048, 256, 8,
                                                                  I_shared=2048))
     assert "ffn1_rows=permuted" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8,
                                                                  wfmt=m.W_FP8_BLOCK))

@@ -51,16 +51,18 @@ def test_forward_small_gathered_rows(orc, cfg, bn, tuning):
     _check(orc, cfg, n_sample=cfg.T)
 
 
+@pytest.mark.parametrize("rows", ["permuted", "gathered"])
 @pytest.mark.parametrize("small", ["m128", "m256"])
 @pytest.mark.parametrize("cfg", [SHARED_SMALL, RAGGED, SKEW_SMALL.with_(I_s=256)], ids=ids)
-def test_forward_sm_pairs(orc, cfg, small, tuning):
+def test_forward_sm_pairs(orc, cfg, small, rows, tuning):
     # 256-row tiles on SM pairs for a small batch: items of <= 128 rows as
-    # M = 128 tiles, or as padded M = 256 tiles
-    tuning(tile_n=256)
+    # M = 128 tiles, or as padded M = 256 tiles; FFN1 reads permuted rows or
+    # gathers one row per token with four-row TMA copies
+    tuning(tile_n=256, ffn1_gather=int(rows == "gathered"))
     if small == "m256":
         tuning(pair_small=0)
     d = G.lib().moe_describe(G.problem(cfg))
-    assert "ffn1=pair_gemm_kernel" in d and "ffn1_rows=permuted" in d, d
+    assert "ffn1=pair_gemm_kernel" in d and f"ffn1_rows={rows}" in d, d
     _check(orc, cfg, n_sample=cfg.T)
 
 
