@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config decode|prefill|skewed|latent|toy|...]
                     [--also prefill,skewed,latent] [--also-steps 30]
-    python bench.py --stage router|route --dims A B C [--steps K]
+    python bench.py --stage router|route|latent_down --dims A B C [--steps K]
 
 A step is one moe_forward over one batch (router logits -> top-k -> permute +
 fp8 quant -> grouped FFN1 -> requant -> grouped FFN2 -> gather + shared),
@@ -61,10 +61,10 @@ def parse():
                          "records of the same line (comma list; 'none' for none; one GPU only)")
     ap.add_argument("--also-steps", type=int, default=30,
                     help="timed steps of each nested workload")
-    ap.add_argument("--stage", choices=["router", "route"], default=None,
+    ap.add_argument("--stage", choices=["router", "route", "latent_down"], default=None,
                     help="time one entry point alone instead of the layer (see run_stage)")
     ap.add_argument("--dims", type=int, nargs=3, default=None,
-                    help="with --stage: T H E (router) or T E k (route)")
+                    help="with --stage: T H E (router), T E k (route) or T H L (latent_down)")
     return ap.parse_args()
 
 
@@ -626,9 +626,10 @@ def run_ours(args, cfg):
 def run_stage(args):
     """Time one entry point alone on seeded inputs (for profiling a stage under
     ncu without a whole layer's weights on the device): ``--stage router
-    --dims T H E`` (moe_router_logits) or ``--stage route --dims T E k``
-    (moe_route).  x ~ N(0,1) bf16, router weights ~ N(0,1/H) fp32, logits ~
-    N(0,1), generated on the device from seed 0."""
+    --dims T H E`` (moe_router_logits), ``--stage route --dims T E k``
+    (moe_route) or ``--stage latent_down --dims T H L`` (moe_latent_down).
+    x ~ N(0,1) bf16, router weights ~ N(0,1/H) fp32, logits ~ N(0,1), Wd ~
+    N(0,1/H) bf16, generated on the device from seed 0."""
     import torch
 
     import moe_expert_layer_02_gb300 as m
@@ -646,6 +647,15 @@ def run_stage(args):
         p = m.make_problem(T, H, 128, E, 1)
         call = lambda: m.moe_router_logits(p, x, w, None, out)  # noqa: E731
         work, unit = 2.0 * T * H * E, "TFLOP/s"
+    elif args.stage == "latent_down":
+        T, H, L = args.dims
+        x = torch.randn(T, H, device="cuda", generator=g).to(torch.bfloat16)
+        wd = (torch.randn(L, H, device="cuda", generator=g) / H ** 0.5).to(torch.bfloat16)
+        z = torch.empty(T, L, dtype=torch.bfloat16, device="cuda")
+        p = m.make_problem(T, H, 128, 8, 1, latent=L, wfmt=m.W_MXFP4)
+        wsb = torch.empty(m.moe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+        call = lambda: m.moe_latent_down(p, x, wd, z, wsb)  # noqa: E731
+        work, unit = 2.0 * T * H * L, "TFLOP/s"
     else:
         T, E, k = args.dims
         logits = torch.randn(T, E, device="cuda", generator=g)
