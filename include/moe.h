@@ -122,8 +122,8 @@ const char* moe_status_string(int status);
  * run.  For logs and benchmarks; the text format may change. */
 int moe_describe(const moe_problem* p, char* buf, size_t len);
 
-/* Bytes of device workspace that moe_forward, moe_permute, moe_expert_ffn and
- * moe_latent_down
+/* Bytes of device workspace that moe_forward, moe_permute, moe_expert_ffn,
+ * moe_router_topk and moe_latent_down
  * need for problem `p` (0 if `p` is invalid).  Pure host computation. */
 size_t moe_workspace_bytes(const moe_problem* p);
 
@@ -154,6 +154,27 @@ int moe_router_logits(const moe_problem* p, const void* x, const float* router_w
  *   else ignored) -> topk_idx [T, top_k] int32, topk_w [T, top_k] fp32 */
 int moe_route(const moe_problem* p, const float* logits, const float* bias, int32_t* topk_idx,
               float* topk_w, void* stream);
+
+/* S1 + S2 in one call: the routing moe_router_logits followed by moe_route
+ * gives, bit for bit in topk_idx (Ling write-up, s.1 top-8 routing; "Kimi K3
+ * ... feasibility analysis", s.2.4), computed the way moe_forward does it.
+ * Large batches (at least sixteen 256 x 256 logit tiles) compute the logits on
+ * the tensor cores: every fp32 router weight is split exactly into three bf16
+ * pieces, x . w is one tensor-core accumulation of exact products, and a
+ * token's selection is accepted only when every adjacent gap among its k + 1
+ * best keys exceeds the two keys' error margins (a multiple of 2^-23 |x_t|
+ * |w_e|); otherwise the canonical logits of every expert that could still
+ * place are computed in moe_router_logits' order and the top k taken among
+ * them.  topk_w is the softmax (or sigmoid share) of the logits the selection
+ * used, within 1e-5 relative of moe_route's.  Smaller batches run
+ * moe_router_logits and moe_route.
+ *   x [T, H] bf16, router_w [E, H] fp32, bias as for moe_router_logits (softmax
+ *   routing) or moe_route (MOE_F_SIGMOID_ROUTING)
+ *   topk_idx [T, top_k] int32, topk_w [T, top_k] fp32 (outputs)
+ *   ws / ws_bytes: workspace of at least moe_workspace_bytes(p) */
+int moe_router_topk(const moe_problem* p, const void* x, const float* router_w,
+                    const float* bias, int32_t* topk_idx, float* topk_w, void* ws,
+                    size_t ws_bytes, void* stream);
 
 /* S9 (LatentMoE) -- down projection onto the latent on which the routed experts
  * run ("Kimi K3 ... feasibility analysis", s.2.4 routed_expert_down_proj):
@@ -343,7 +364,7 @@ int64_t moe_launch_count(void);
  * (process-wide, every device).  At its first use the library reads them once
  * from the environment -- MOE_TILE_N=<rows>, MOE_GATHER=1, MOE_INDEX=3pass,
  * MOE_GEMM=1cta, MOE_PAIR_SMALL=0, MOE_MX=1cta,
- * MOE_ROUTER_TILE=8x8|8x16|8x16s4|12w8x16, MOE_PDL=0 -- and moe_set_tuning
+ * MOE_ROUTER_TILE=8x8|8x16|8x16s4|12w8x16|tc, MOE_PDL=0 -- and moe_set_tuning
  * replaces them for every later call.  For benchmarks and tests; the defaults
  * are the measured best. */
 typedef struct {
@@ -357,8 +378,10 @@ typedef struct {
   int32_t gemm_1cta;   /* 1: single-SM fp8 grouped GEMMs for 256-row tiles as well    */
   int32_t pair_small;  /* 1 (default): SM-pair items of <= 128 rows as M = 128 tiles  */
   int32_t mx_1cta;     /* 1: single-SM MXFP4 grouped GEMMs                             */
-  int32_t router_tile; /* 0 automatic; 1: 8 warps of 8 tokens x 8 experts, 2: 8 x 16,
-                          3: 8 x 16 with four chunks a stage, 4: 12 warps of 8 x 16   */
+  int32_t router_tile; /* 0 automatic; CUDA-core router: 1: 8 warps of 8 tokens x 8
+                          experts, 2: 8 x 16, 3: 8 x 16 with four chunks a stage,
+                          4: 12 warps of 8 x 16; 6: tensor-core logits with the
+                          selection made exact (moe_router_topk), at any size    */
   int32_t pdl;         /* 1 (default): programmatic dependent launch between kernels */
 } moe_tuning;
 
@@ -368,7 +391,7 @@ int moe_get_tuning(moe_tuning* t);
 /* Replace the launch choices (host only; takes effect for calls made after it
  * returns).  MOE_ERR_INVALID_ARG, changing nothing, if t is NULL or a field is
  * out of range (tile_n not 0/32/64/96/128/256, flags not 0/1, router_tile
- * not 0..4). */
+ * not 0..4 or 6). */
 int moe_set_tuning(const moe_tuning* t);
 
 /* Per-stage device timing.  mask selects the stages to time (bit s = stage

@@ -14,7 +14,7 @@ import os
 __all__ = [
     "MoEError", "MoEProblem", "make_problem", "load_library", "moe_workspace_bytes",
     "moe_router_logits", "moe_route", "moe_permute", "moe_permute_static", "moe_expert_ffn",
-    "moe_unpermute", "moe_latent_down",
+    "moe_unpermute", "moe_latent_down", "moe_router_topk",
     "moe_forward", "moe_get_last_error", "moe_launch_count", "moe_profile_enable",
     "moe_profile_read", "moe_pack_weights", "moe_watchdog_selftest", "moe_describe", "STAGES",
     "W_FP8",
@@ -58,7 +58,7 @@ class MoETuning(ctypes.Structure):
                                              "pair_small", "mx_1cta", "router_tile", "pdl")]
 
 
-ROUTER_TILES = {"auto": 0, "8x8": 1, "8x16": 2, "8x16s4": 3, "12w8x16": 4}
+ROUTER_TILES = {"auto": 0, "8x8": 1, "8x16": 2, "8x16s4": 3, "12w8x16": 4, "tc": 6}
 
 
 def make_problem(T, H, I, E, top_k, I_shared=0, latent=0, wfmt=W_FP8, flags=0) -> MoEProblem:
@@ -71,7 +71,7 @@ _EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_router_logits", "mo
             "moe_permute", "moe_permute_static", "moe_expert_ffn", "moe_unpermute", "moe_forward",
             "moe_get_last_error", "moe_launch_count", "moe_profile_enable", "moe_profile_read",
             "moe_pack_weights", "moe_watchdog_selftest", "moe_describe", "moe_latent_down",
-            "moe_get_tuning", "moe_set_tuning")
+            "moe_get_tuning", "moe_set_tuning", "moe_router_topk")
 
 
 def load_library(path: str = LIB_PATH):
@@ -97,6 +97,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_unpermute.argtypes = [PP, P, P, P, P, P]
     L.moe_latent_down.argtypes = [PP, P, P, P, P, ctypes.c_size_t, P]
+    L.moe_router_topk.argtypes = [PP, P, P, P, P, P, P, ctypes.c_size_t, P]
     L.moe_get_tuning.argtypes = [ctypes.POINTER(MoETuning)]
     L.moe_set_tuning.argtypes = [ctypes.POINTER(MoETuning)]
     L.moe_forward.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P]
@@ -182,6 +183,13 @@ def moe_pack_weights(p, w13, w2, w13_scale, w2_scale, w13_packed, w2_packed,
 def moe_unpermute(p, y_rows, perm, shared, out, stream=None):
     _check(load_library().moe_unpermute(ctypes.byref(p), _ptr(y_rows), _ptr(perm), _ptr(shared),
                                         _ptr(out), _stream(stream)), "moe_unpermute")
+
+
+def moe_router_topk(p, x, router_w, bias, topk_idx, topk_w, ws, stream=None):
+    _check(load_library().moe_router_topk(ctypes.byref(p), _ptr(x), _ptr(router_w), _ptr(bias),
+                                          _ptr(topk_idx), _ptr(topk_w), _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_router_topk")
 
 
 def moe_latent_down(p, x, latent_down, z, ws, stream=None):

@@ -82,7 +82,7 @@ constexpr int P_SMEM =
     1024 + P_STAGES * P_STAGE + P_STG + P_SCL + P_NUM_BARS * 8 + 16 + P_STAGES * 4;
 
 enum { KIND_FP8 = 0, KIND_BF16 = 1 };
-enum { EPI_SWIGLU = 0, EPI_DOWN = 1, EPI_STORE = 2 };
+enum { EPI_SWIGLU = 0, EPI_DOWN = 1, EPI_STORE = 2, EPI_F32 = 3 };
 
 // One launch: the tiles, the K segments and the epilogue's operands.
 struct PairGemm {
@@ -112,6 +112,9 @@ struct PairGemm {
                           // epilogue takes that token's activation scale
   const int32_t* src;     // [R] token of each routed row (gather only)
   int R, T;               // routed rows, tokens (gather only)
+  int a_period;           // dense: A's K stage is kb % a_period (0: kb), so one A
+                          // row block meets several consecutive K blocks of B
+  int n_valid;            // EPI_F32: output columns that exist (ldo >= n_valid)
   int* err;
 };
 
@@ -347,7 +350,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
               load_w(st + P_A_BYTES, tw, wrow, kb, fb_leader);
             }
           } else if (kb < g.kb1) {
-            tma_load_2d_pair(st, &tm_x, kb * EL, it.y + 128 * (int)rank, fb_leader);
+            tma_load_2d_pair(st, &tm_x, (g.a_period ? kb % g.a_period : kb) * EL,
+                             it.y + 128 * (int)rank, fb_leader);
             load_w(st + P_A_BYTES, tw, wrow, kb, fb_leader);
           } else {
             const int k2 = (kb - g.kb1) * EL;
@@ -557,6 +561,17 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           tmem_ld16(tbase + c + 16, v[1]);
         };
         auto emit = [&](const uint32_t (&v)[2][16], int c) {
+          if (EPI == EPI_F32) {  // fp32 out, row by row (a small output)
+            if (valid) {
+              float* orow = static_cast<float*>(g.out) + (size_t)row * g.ldo;
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int col = c0 + co + c + jj;
+                if (col < g.n_valid) orow[col] = __uint_as_float(v[jj >> 4][jj & 15]);
+              }
+            }
+            return;
+          }
           uint32_t packed[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
@@ -745,6 +760,28 @@ cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s) {
   // dense launches have no small tiles: the half-box maps are never read
   if (d.swiglu) return launch_pair_gemm<KIND_BF16, EPI_SWIGLU>(tw, tw, tx, tw2, tx2, tx, tw, tw, g, s);
   return launch_pair_gemm<KIND_BF16, EPI_STORE>(tw, tw, tx, tw2, tx2, tx, tw, tw, g, s);
+}
+
+cudaError_t launch_dense_bf16_f32(const void* x, int Kx, const void* w, int Kw, int rows, int N,
+                                  float* out, int* err, cudaStream_t s) {
+  // out[rows, N] fp32 = sum over Kw of x[:, k mod Kx] w[:, k]; Kx, Kw multiples of 64
+  if (Kx % 64 || Kw % Kx || N <= 0 || rows <= 0) return cudaErrorInvalidValue;
+  CUtensorMap tw, tx;
+  if (!pair_map(&tw, KIND_BF16, 3, w, Kw, N, 1) || !pair_map(&tx, KIND_BF16, 2, x, Kx, rows, 1))
+    return cudaErrorInvalidValue;
+  PairGemm g{};
+  g.items = nullptr;
+  g.dense_rows = rows;
+  g.nb = (N + P_N - 1) / P_N;  // rows of w past N read as zeros; their columns are not stored
+  g.kb1 = Kw / 64;
+  g.kb2 = 0;
+  g.a_period = Kx / 64;
+  g.rows_total = rows;
+  g.out = out;
+  g.ldo = N;
+  g.n_valid = N;
+  g.err = err;
+  return launch_pair_gemm<KIND_BF16, EPI_F32>(tw, tw, tx, tw, tx, tx, tw, tw, g, s);
 }
 
 }  // namespace moe

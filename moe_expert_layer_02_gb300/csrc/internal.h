@@ -78,6 +78,19 @@ cudaError_t launch_router_logits(const void* x, const float* wr, const float* bi
 // sel_bias (nullable), weights the chosen sigmoid scores renormalised
 cudaError_t launch_topk(const float* logits, const float* sel_bias, int sigmoid, int32_t* idx,
                         float* w, int T, int E, int k, cudaStream_t s);
+// S1 + S2 with tensor-core logits (route.cu): launch_router_tc writes the
+// approximate logits approx [T, E] (without bias) from the router weights split
+// into three bf16 pieces wp [E][3H], with the norms xnorm [T] and wnorm [E];
+// launch_topk_tc then makes the same selection as the canonical router logits
+// followed by launch_topk (recomputing canonical logits where the approximate
+// ones leave the order in doubt).  logit_bias: softmax routing's bias (added to
+// the logits); sel_bias: sigmoid routing's selection bias.
+cudaError_t launch_router_tc(const void* x, const float* wr, int T, int H, int E, uint16_t* wp,
+                             float* xnorm, float* wnorm, float* approx, int* err, cudaStream_t s);
+cudaError_t launch_topk_tc(const float* approx, const float* logit_bias, const float* sel_bias,
+                           int sigmoid, const void* x, const float* wr, const float* xnorm,
+                           const float* wnorm, int32_t* idx, float* w, int T, int H, int E, int k,
+                           cudaStream_t s);
 
 // ---------------------------------------------------------------- permute.cu
 // cc[e * nch + c] = #tokens of chunk c that picked expert e.
@@ -189,6 +202,10 @@ struct DenseGemmArgs {
   int* err;
 };
 cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s);
+// out[rows, N] fp32 = sum_{k < Kw} x[:, k mod Kx] * w[:, k] (x [rows, Kx], w [N, Kw]
+// bf16, Kx % 64 == 0, Kw a multiple of Kx): one accumulation in tensor memory.
+cudaError_t launch_dense_bf16_f32(const void* x, int Kx, const void* w, int Kw, int rows, int N,
+                                  float* out, int* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- latent_down.cu
 // z [T, L] = nearest-even bf16 of the exact x Wd^T (x [T, H], Wd [L, H] bf16):

@@ -110,9 +110,10 @@ struct Plan {
   int act;          // FFN1 activation: 0 SwiGLU, 1 SiTU
   bool fused;       // S7 in the FFN2 epilogue (MOE_F_FUSED_COMBINE, where honoured)
   bool gather;      // S4 quantises per token; the FFN1 producer gathers the rows
+  bool tc_router;   // S1 on the tensor cores, S2 made exact (route.cu)
   size_t acc;       // fused combine: fp32 [T, H] sum
   size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
-      hq, hs, y, z, zflag, yn, hsh, total;
+      hq, hs, y, z, zflag, yn, hsh, rwp, rxn, rwn, total;
 };
 
 int choose_bn(const moe_problem* p) {
@@ -141,6 +142,17 @@ int choose_bn(const moe_problem* p) {
 }
 
 bool use_pair_gemm(const Plan& q);
+
+// S1 on the tensor cores when the batch fills at least sixteen SM pairs with
+// 256 x 256 logit tiles (the canonical CUDA-core router below that: at T=512,
+// E=256 its 60 us beat two busy pairs); tuning().router_tile 6 forces it, 1..5
+// pick a CUDA-core tile.
+bool use_tc_router(const moe_problem* p) {
+  const int rt = tuning().router_tile;
+  if (rt == 6) return true;
+  if (rt != 0) return false;
+  return (int64_t)((p->T + 255) / 256) * ((p->E + 255) / 256) >= 16;
+}
 
 Plan make_plan(const moe_problem* p) {
   Plan q{};
@@ -176,6 +188,7 @@ Plan make_plan(const moe_problem* p) {
   // (tile::gather4, 32 per stage and CTA); T=16384: FFN1 12.06 vs 3.70 ms, S4
   // 0.099 vs 0.225 ms; T=8192 skewed: FFN1 5.63 vs 1.55 ms.
   q.gather = !q.mx && !q.blockwise && tuning().ffn1_gather;
+  q.tc_router = use_tc_router(p);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -204,6 +217,11 @@ Plan make_plan(const moe_problem* p) {
   q.acc = take(q.fused ? T * (size_t)q.K * 4 : 0);
   q.z = take(q.L ? T * (size_t)q.L * 2 : 0);
   q.zflag = take(q.L ? latent_down_flag_bytes(q.T, q.L) : 0);
+  // tensor-core router: weight pieces [E][3H] bf16 and the norms (always
+  // planned, so that moe_router_topk can take either path)
+  q.rwp = take(E * 3 * (size_t)q.H * 2);
+  q.rxn = take(T * 4);
+  q.rwn = take(E * 4);
   q.yn = take(q.L ? T * (size_t)q.L * 2 : 0);
   q.hsh = take(q.shared_bf16 ? T * (size_t)q.Is * 2 : 0);
   q.total = o;
@@ -350,6 +368,35 @@ int run_experts(const Plan& q, const GroupedFfnArgs& a, int rows_total, cudaStre
   return MOE_OK;
 }
 
+// S1 + S2 into idx / tw [T, k]: tensor-core logits with the selection made
+// exact, or the canonical CUDA-core router and top-k; the same routing either way.
+int route_tokens(const moe_problem* p, const Plan& q, void* ws, const void* x,
+                 const float* router_w, const float* router_bias, int32_t* idx, float* tw,
+                 int* err, cudaStream_t s) {
+  float* logits = at<float>(ws, q.logits);
+  const int sig = sigmoid_routing(p) ? 1 : 0;
+  if (q.tc_router) {
+    {
+      StageTimer t(MOE_STAGE_ROUTER, s);
+      MOE_TRY(launch_router_tc(x, router_w, q.T, q.H, q.E, at<uint16_t>(ws, q.rwp),
+                               at<float>(ws, q.rxn), at<float>(ws, q.rwn), logits, err, s));
+    }
+    StageTimer t(MOE_STAGE_TOPK, s);
+    MOE_TRY(launch_topk_tc(logits, logit_bias(p, router_bias), selection_bias(p, router_bias), sig,
+                           x, router_w, at<float>(ws, q.rxn), at<float>(ws, q.rwn), idx, tw, q.T,
+                           q.H, q.E, q.k, s));
+    return MOE_OK;
+  }
+  {
+    StageTimer t(MOE_STAGE_ROUTER, s);
+    MOE_TRY(launch_router_logits(x, router_w, logit_bias(p, router_bias), logits, q.T, q.H, q.E,
+                                 err, s));
+  }
+  StageTimer t(MOE_STAGE_TOPK, s);
+  MOE_TRY(launch_topk(logits, selection_bias(p, router_bias), sig, idx, tw, q.T, q.E, q.k, s));
+  return MOE_OK;
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -377,6 +424,7 @@ void tuning_from_env() {
   if (env_is("MOE_ROUTER_TILE", "8x16")) rt = 2;
   if (env_is("MOE_ROUTER_TILE", "8x16s4")) rt = 3;
   if (env_is("MOE_ROUTER_TILE", "12w8x16")) rt = 4;
+  if (env_is("MOE_ROUTER_TILE", "tc")) rt = 6;
   const int32_t v[8] = {tn ? std::atoi(tn) : 0,
                         env_is("MOE_GATHER", "1") ? 1 : 0,
                         env_is("MOE_INDEX", "3pass") ? 1 : 0,
@@ -492,6 +540,23 @@ int moe_route(const moe_problem* p, const float* logits, const float* bias, int3
   StageTimer t(MOE_STAGE_TOPK, s);
   return cuda_status(launch_topk(logits, selection_bias(p, bias), sigmoid_routing(p) ? 1 : 0,
                                  topk_idx, topk_w, p->T, p->E, p->top_k, s));
+}
+
+int moe_router_topk(const moe_problem* p, const void* x, const float* router_w,
+                    const float* bias, int32_t* topk_idx, float* topk_w, void* ws,
+                    size_t ws_bytes, void* stream) {
+  int st = check_problem(p);
+  if (st) return st;
+  if (!x || !router_w || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if ((p->flags & MOE_F_ROUTER_BIAS) && !bias) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(router_w, 16)) return MOE_ERR_INVALID_ARG;
+  const Plan q = make_plan(p);
+  if (!ws || ws_bytes < q.total || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  DeviceInfo* di = device_info();
+  if (!di) return MOE_ERR_CUDA;
+  if (p->T == 0) return MOE_OK;
+  return route_tokens(p, q, ws, x, router_w, bias, topk_idx, topk_w, di->err,
+                      static_cast<cudaStream_t>(stream));
 }
 
 int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, int32_t* counts,
@@ -625,7 +690,6 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   if (!di) return MOE_ERR_CUDA;
   if (p->T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* logits = at<float>(ws, q.logits);
   int32_t* idx = at<int32_t>(ws, q.idx);
   float* tw = at<float>(ws, q.tw);
   int32_t* off = at<int32_t>(ws, q.off);
@@ -634,16 +698,8 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
   float* xscale = at<float>(ws, q.xscale);
   uint8_t* xq = at<uint8_t>(ws, q.xq);
   uint16_t* y = at<uint16_t>(ws, q.y);
-  {
-    StageTimer t(MOE_STAGE_ROUTER, s);
-    MOE_TRY(launch_router_logits(x, router_w, logit_bias(p, router_bias), logits, q.T, q.H, q.E,
-                                 di->err, s));
-  }
-  {
-    StageTimer t(MOE_STAGE_TOPK, s);
-    MOE_TRY(launch_topk(logits, selection_bias(p, router_bias), sigmoid_routing(p) ? 1 : 0, idx, tw,
-                        q.T, q.E, q.k, s));
-  }
+  st = route_tokens(p, q, ws, x, router_w, router_bias, idx, tw, di->err, s);
+  if (st) return st;
   // LatentMoE: the experts run on z = bf16(x Wd^T) ("Kimi K3 ...", s.2.4)
   const void* xin = x;
   if (q.L) {
@@ -766,7 +822,7 @@ int moe_set_tuning(const moe_tuning* t) {
                         t->pair_small, t->mx_1cta, t->router_tile, t->pdl};
   const bool tile_ok = v[0] == 0 || v[0] == 32 || v[0] == 64 || v[0] == 96 || v[0] == 128 ||
                        v[0] == 256;
-  if (!tile_ok || v[6] < 0 || v[6] > 4) return MOE_ERR_INVALID_ARG;
+  if (!tile_ok || v[6] < 0 || v[6] > 6 || v[6] == 5) return MOE_ERR_INVALID_ARG;
   for (int i : {1, 2, 3, 4, 5, 7})
     if (v[i] != 0 && v[i] != 1) return MOE_ERR_INVALID_ARG;
   std::call_once(g_tune_once, tuning_from_env);  // the environment never overrides a set

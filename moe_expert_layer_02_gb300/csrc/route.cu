@@ -298,6 +298,227 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---------------------------------------------------------------- S1 + S2 on tensor cores
+// The router GEMM has T x E x H multiply-adds (69 G at T=16384, H=8192,
+// E=256), which the CUDA cores take 1.4 ms over in the canonical order.  Here
+// the tensor cores compute the logits: x is bf16, and every fp32 router weight
+// splits exactly into three bf16 pieces, w = w_lo + w_mid + w_hi (8 + 8 + 8
+// significant bits), so x . w = x . w_lo + x . w_mid + x . w_hi with products
+// exact in fp32; one tcgen05 accumulation over K = 3H, small pieces first,
+// gives an approximate logit a[t,e] within a few units of 2^-23 |x_t| |w_e|
+// of the canonical one.  The selection is then made exact: per token, the top
+// k + 1 approximate keys are compared with per-element margins
+// m[t,e] = MOE_RFLAG_ULPS * 2^-23 * |x_t| * |w_e| (|.| the Euclidean norm);
+// when every adjacent gap exceeds the two margins, the approximate order is the
+// canonical order.  Otherwise every expert that could still take a place
+// (key + margin >= the k-th key - its margin) gets its canonical logit (32
+// fused multiply-add chains over h = l (mod 32), the halving tree, the bias
+// last: bit for bit the router kernel's value), and the top k among those are
+// chosen exactly.  The routing weights come from the logits the selection used.
+//
+// Margin calibration (GB300; x N(0,1), router N(0, 1/H); tokens whose
+// selection or order came out different from the canonical routing, by margin
+// in units of 2^-23 |x_t| |w_e|): 0 -> 3 of 16384 at T=16384, H=8192, E=256,
+// k=8 and 1 of 8192 on the Zipf-biased T=8192 batch; 1, 4, 16 and 64 -> none
+// on those and on T=4096, H=7168, E=896, k=16.  Eight leaves a factor of
+// eight over the smallest clean margin; the recompute then runs on a few per
+// cent of tokens (S1 + S2: 0.38 ms at T=16384 against 1.49 ms canonical).
+#ifndef MOE_RFLAG_ULPS
+#define MOE_RFLAG_ULPS 8.0f
+#endif
+
+// Blocks [0, E): router row e -> pieces (lo, mid, hi) at wp[e][0..3H) and its
+// norm.  Blocks past E: eight tokens each, one warp per token: |x_t|.
+__global__ void __launch_bounds__(256)
+    router_prep_kernel(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                       uint16_t* __restrict__ wp, float* __restrict__ xnorm,
+                       float* __restrict__ wnorm, int T, int H, int E) {
+  pdl_wait();
+  pdl_release();
+  __shared__ float s_part[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if ((int)blockIdx.x < E) {
+    const int e = blockIdx.x;
+    const float* row = wr + (size_t)e * H;
+    uint16_t* lo = wp + (size_t)e * 3 * H;
+    float ss = 0.0f;
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+      const float v = row[h];
+      const __nv_bfloat16 bh = __float2bfloat16_rn(v);
+      const float r1 = __fsub_rn(v, __bfloat162float(bh));  // exact
+      const __nv_bfloat16 bm = __float2bfloat16_rn(r1);
+      const float r2 = __fsub_rn(r1, __bfloat162float(bm));  // exact, <= 8 significant bits
+      const __nv_bfloat16 bl = __float2bfloat16_rn(r2);      // exact
+      lo[h] = *reinterpret_cast<const uint16_t*>(&bl);
+      lo[H + h] = *reinterpret_cast<const uint16_t*>(&bm);
+      lo[2 * H + h] = *reinterpret_cast<const uint16_t*>(&bh);
+      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) s_part[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.0f;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += s_part[i];
+      wnorm[e] = sqrtf(t);
+    }
+  } else {
+    const int t = ((int)blockIdx.x - E) * 8 + warp;
+    if (t >= T) return;
+    const uint16_t* row = x + (size_t)t * H;
+    float ss = 0.0f;
+    for (int h = lane; h < H; h += 32) {
+      const float v = bf16_bits_to_f32(row[h]);
+      ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) xnorm[t] = sqrtf(ss);
+  }
+}
+
+// The canonical logit of (token row xr, router row wrow), as the router kernel
+// computes it, in every lane of the warp.
+__device__ __forceinline__ float canonical_logit(const uint16_t* __restrict__ xr,
+                                                 const float* __restrict__ wrow, int H, int lane) {
+  float p = 0.0f;
+  for (int h = lane; h < H; h += 32) p = fmaf(bf16_bits_to_f32(xr[h]), wrow[h], p);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) p = p + __shfl_down_sync(0xffffffffu, p, o);
+  return __shfl_sync(0xffffffffu, p, 0);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256)
+    topk_tc_kernel(const float* __restrict__ approx, const float* __restrict__ logit_bias,
+                   const float* __restrict__ sel_bias, int sigmoid,
+                   const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                   const float* __restrict__ xnorm, const float* __restrict__ wnorm,
+                   int32_t* __restrict__ idx, float* __restrict__ w, int T, int H, int E, int k) {
+  pdl_wait();
+  pdl_release();
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = approx + (size_t)t * E;
+  const float xm = MOE_RFLAG_ULPS * 0x1p-23f * xnorm[t];
+  // keys (as the canonical top-k forms them) and their margins
+  float kv[VPL], km[VPL], lv[VPL];
+  uint64_t key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = i * 32 + lane;
+    float l = 0.0f, v = 0.0f, m = 0.0f;
+    if (e < E) {
+      l = row[e];
+      if (logit_bias) l = __fadd_rn(l, logit_bias[e]);
+      const float ml = xm * wnorm[e];
+      if (sigmoid) {
+        v = sigmoid_fixed(l);
+        if (sel_bias) v = __fadd_rn(v, sel_bias[e]);
+        m = 0.25f * ml + 0x1p-20f;  // sigmoid' <= 1/4, plus its own last-bit error
+      } else {
+        v = l;
+        m = ml + 0x1p-22f * fabsf(l);  // plus the bias addition's rounding
+      }
+    }
+    lv[i] = l;
+    kv[i] = v;
+    km[i] = m;
+    key[i] = (e < E) ? ((uint64_t)float_order_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - e) : 0;
+  }
+  // the k + 1 best keys by the approximate values: lane j keeps the j-th
+  const int nsel = k < E ? k + 1 : k;
+  float my_v = 0.0f, my_m = 0.0f, my_l = 0.0f;
+  int my_e = 0;
+  for (int j = 0; j < nsel; ++j) {
+    uint64_t best = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+    float bv = 0.0f, bm = 0.0f, bl = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (key[i] == best) {  // the owner drops the winner and shares its values
+        key[i] = 0;
+        bv = kv[i];
+        bm = km[i];
+        bl = lv[i];
+      }
+    const int owner = e & 31;
+    bv = __shfl_sync(0xffffffffu, bv, owner);
+    bm = __shfl_sync(0xffffffffu, bm, owner);
+    bl = __shfl_sync(0xffffffffu, bl, owner);
+    if (lane == j) {
+      my_v = bv;
+      my_m = bm;
+      my_l = bl;
+      my_e = e;
+    }
+  }
+  // the approximate order is the canonical one when every adjacent gap of the
+  // k + 1 best keys exceeds both margins
+  const float nx_v = __shfl_down_sync(0xffffffffu, my_v, 1);
+  const float nx_m = __shfl_down_sync(0xffffffffu, my_m, 1);
+  const bool close = lane < k && lane + 1 < nsel && !(my_v - nx_v > my_m + nx_m);
+  if (__any_sync(0xffffffffu, close)) {
+    // exact: the canonical keys of every expert that could still place
+    const float kth_v = __shfl_sync(0xffffffffu, my_v, k - 1);
+    const float kth_m = __shfl_sync(0xffffffffu, my_m, k - 1);
+    const float floor_v = kth_v - kth_m;
+    uint64_t top = 0;  // lane j < k: the j-th best canonical key so far
+    float top_l = 0.0f;
+    const uint16_t* xr = x + (size_t)t * H;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e0 = i * 32 + lane;
+      unsigned cand = __ballot_sync(0xffffffffu, e0 < E && kv[i] + km[i] >= floor_v);
+      while (cand) {
+        const int b = __ffs(cand) - 1;
+        cand &= cand - 1u;
+        const int e = i * 32 + b;
+        float l = canonical_logit(xr, wr + (size_t)e * H, H, lane);
+        if (logit_bias) l = __fadd_rn(l, logit_bias[e]);
+        float v = l;
+        if (sigmoid) {
+          v = sigmoid_fixed(l);
+          if (sel_bias) v = __fadd_rn(v, sel_bias[e]);
+        }
+        const uint64_t ck = ((uint64_t)float_order_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - e);
+        // insert into the sorted top-k list held by lanes 0..k-1
+        const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && top > ck));
+        const uint64_t up = __shfl_up_sync(0xffffffffu, top, 1);
+        const float up_l = __shfl_up_sync(0xffffffffu, top_l, 1);
+        if (lane < k && pos < k) {
+          if (lane == pos) {
+            top = ck;
+            top_l = l;
+          } else if (lane > pos) {
+            top = up;
+            top_l = up_l;
+          }
+        }
+      }
+    }
+    my_e = (int)(0xFFFFFFFFu - (uint32_t)(top & 0xFFFFFFFFu));
+    my_l = top_l;
+  }
+  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+  const float ex = lane >= k ? 0.0f : sigmoid ? sigmoid_fixed(my_l) : expf(my_l - l0);
+  float sum = 0.0f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);  // j ascending
+  if (lane < k) {
+    idx[(size_t)t * k + lane] = my_e;
+    w[(size_t)t * k + lane] = ex / sum;
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -373,6 +594,43 @@ cudaError_t launch_router_logits(const void* x, const float* wr, const float* bi
   if (2L * big_blocks >= sms && big_blocks <= sms)
     return launch_router_impl<8, 16, 4>(x, wr, bias, logits, T, H, E, err, s);
   return launch_router_impl<8, 8>(x, wr, bias, logits, T, H, E, err, s);
+}
+
+cudaError_t launch_router_tc(const void* x, const float* wr, int T, int H, int E, uint16_t* wp,
+                             float* xnorm, float* wnorm, float* approx, int* err, cudaStream_t s) {
+  if (T <= 0 || H % 64 || E <= 0 || E > 1024) return cudaErrorInvalidValue;
+  count_launch();
+  cudaError_t e = launch_kernel(router_prep_kernel, dim3(E + (T + 7) / 8), dim3(256), 0, s, 1,
+                                static_cast<const uint16_t*>(x), wr, wp, xnorm, wnorm, T, H, E);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  e = launch_dense_bf16_f32(x, H, wp, 3 * H, T, E, approx, err, s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_tc(const float* approx, const float* logit_bias, const float* sel_bias,
+                           int sigmoid, const void* x, const float* wr, const float* xnorm,
+                           const float* wnorm, int32_t* idx, float* w, int T, int H, int E, int k,
+                           cudaStream_t s) {
+  if (T <= 0 || E <= 0 || E > 1024 || k > 32 || k > E) return cudaErrorInvalidValue;
+  const int blocks = (T * 32 + 255) / 256;
+  const int vpl = (E + 31) / 32;
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  count_launch();
+  cudaError_t e;
+#define MOE_TOPK_TC(V)                                                                      \
+  launch_kernel(topk_tc_kernel<V>, dim3(blocks), dim3(256), 0, s, 1, approx, logit_bias,   \
+                sel_bias, sigmoid, xb, wr, xnorm, wnorm, idx, w, T, H, E, k)
+  if (vpl <= 1) e = MOE_TOPK_TC(1);
+  else if (vpl <= 2) e = MOE_TOPK_TC(2);
+  else if (vpl <= 4) e = MOE_TOPK_TC(4);
+  else if (vpl <= 8) e = MOE_TOPK_TC(8);
+  else if (vpl <= 16) e = MOE_TOPK_TC(16);
+  else e = MOE_TOPK_TC(32);
+#undef MOE_TOPK_TC
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const float* logits, const float* sel_bias, int sigmoid, int32_t* idx,

@@ -210,7 +210,8 @@ def test_tuning_round_trip_and_range_checks(m, tuning):
     tuning(tile_n=64, router_tile="8x16s4", pdl=0)
     t = m.moe_get_tuning()
     assert t["tile_n"] == 64 and t["router_tile"] == 3 and t["pdl"] == 0
-    for bad in (dict(tile_n=48), dict(router_tile=5), dict(ffn1_gather=2), dict(pdl=-1)):
+    for bad in (dict(tile_n=48), dict(router_tile=5), dict(router_tile=7), dict(ffn1_gather=2),
+                dict(pdl=-1)):
         with pytest.raises(m.MoEError) as ei:
             m.moe_set_tuning(**bad)
         assert ei.value.status == 1  # MOE_ERR_INVALID_ARG, nothing changed

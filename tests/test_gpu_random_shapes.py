@@ -72,7 +72,7 @@ def draw(seed: int):
     if r.random() < 0.3:
         knobs["mx_1cta"] = 1
     if r.random() < 0.5:
-        knobs["router_tile"] = str(r.choice(["8x8", "8x16", "8x16s4", "12w8x16"]))
+        knobs["router_tile"] = str(r.choice(["8x8", "8x16", "8x16s4", "12w8x16", "tc"]))
     # the MXFP4 SM-pair kernels need packed weights
     packed = bool(r.random() < (0.8 if cfg.wfmt == "mxfp4" else 0.5))
     return cfg, knobs, packed

@@ -1,0 +1,106 @@
+"""GPU parity of moe_router_topk (S1 + S2 in one call): the tensor-core logits
+with the selection made exact must give the oracle's canonical routing bit for
+bit -- expert indices and their order.  Its weights come from the logits the
+selection used: canonical ones on the tokens whose order the margins could not
+settle, the tensor-core ones elsewhere, so they are held to the error those
+margins bound (below; 1e-5 relative where that is smaller)
+("Optimising Ling-2.6-1T on TPU with SGLang-JAX", s.1 top-8 routing; "Kimi K3
+... feasibility analysis", s.2.4 renormalised top-k and noaux_tc sigmoid
+routing).  Runs the tensor-core path on every shape (forced) and the automatic
+choice on the named workloads, including constructed exact ties."""
+import numpy as np
+import pytest
+import torch
+
+import _gpu as G
+import moe_inputs as mi
+from test_gpu_stages import BIASED, E3, FULL, KE, LATENT, MAXE, RAGGED, SKEW_SMALL, T1
+
+pytestmark = pytest.mark.gpu
+ids = lambda c: c.name
+
+K3 = mi.CONFIGS["latent_k3"]
+SIG_SMALL = mi.MoEConfig("sig_small", T=300, H=512, I=128, E=40, k=6, routing="sigmoid",
+                         sel_bias=True)
+
+
+ULPS = 8.0  # the kernel's margin, in units of 2^-23 |x_t| |w_e|
+
+
+def _oracle_routing(orc, cfg, h):
+    """(idx, weights, logits) of the oracle; logits fp32 [T, E], unbiased
+    for sigmoid routing (the bias steers selection only)."""
+    if cfg.routing == "sigmoid":
+        lg = orc.router_logits(h["x"], h["router_w"])
+        return orc.topk(lg, cfg.k, routing="sigmoid", bias=h["router_bias"]) + (lg,)
+    lg = orc.router_logits(h["x"], h["router_w"], h["router_bias"])
+    return orc.topk(lg, cfg.k) + (lg,)
+
+
+def _weight_rtol(cfg, h, idx, lg):
+    """Per-token, per-slot bound on the relative error of the routing weights
+    when each chosen logit l_j is off by at most m_j = ULPS 2^-23 |x_t| |w_j|.
+    Softmax over the chosen logits: dw_i / w_i <= m_i + max_j m_j.  Sigmoid
+    scores s_j, renormalised: ds_j <= m_j / 4 + 2^-20 (the sigmoid's slope is
+    at most 1/4, plus its own rounding), so dw_i / w_i <= ds_i / s_i +
+    max_j ds_j / s_j.  Doubled for second-order terms and fp32 rounding, and
+    never below 1e-5."""
+    x = G.bf16_values(np.asarray(h["x"]).view(np.uint16)).reshape(cfg.T, cfg.H)
+    xn = np.sqrt((x * x).sum(axis=1))
+    wr = np.asarray(h["router_w"], np.float64)
+    wn = np.sqrt((wr * wr).sum(axis=1))
+    m = ULPS * 2.0 ** -23 * xn[:, None] * wn[idx]
+    if cfg.routing == "sigmoid":
+        s = 1.0 / (1.0 + np.exp(-np.take_along_axis(lg.astype(np.float64), idx, axis=1)))
+        rel = (m / 4 + 2.0 ** -20) / s
+    else:
+        rel = m
+    return np.maximum(2.0 * (rel + rel.max(axis=1, keepdims=True)), 1e-5)
+
+
+def _check(orc, cfg, inp):
+    m = G.lib()
+    h = G.host(inp, keys=("x", "router_w", "router_bias"))
+    idx, w, lg = _oracle_routing(orc, cfg, h)
+    p = G.problem(cfg)
+    ws = G.workspace(p)
+    gi = torch.full((cfg.T, cfg.k), -1, dtype=torch.int32, device="cuda")
+    gw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device="cuda")
+    m.moe_router_topk(p, inp["x"], inp["router_w"], inp["router_bias"], gi, gw, ws)
+    assert m.moe_get_last_error() == 0
+    got = gi.cpu().numpy()
+    bad = np.nonzero((got != idx).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} of {cfg.T} tokens routed differently, first {bad[:5]}"
+    rel = np.abs(gw.cpu().numpy() - w) / np.abs(w)
+    tol = _weight_rtol(cfg, h, idx, lg)
+    worst = np.unravel_index(np.argmax(rel / tol), rel.shape)
+    assert (rel <= tol).all(), (f"weight rel error {rel[worst]:.3g} > bound {tol[worst]:.3g} "
+                                f"at token {worst[0]}, slot {worst[1]}; max rel {rel.max():.3g}")
+
+
+@pytest.mark.parametrize("cfg", [mi.CONFIGS["toy"], RAGGED, MAXE, T1, KE, E3, BIASED, SKEW_SMALL,
+                                 SIG_SMALL], ids=ids)
+def test_router_topk_tensor_cores_small(orc, cfg, tuning):
+    tuning(router_tile="tc")
+    _check(orc, cfg, G.gpu_inputs(cfg))
+
+
+@pytest.mark.parametrize("path", ["auto", "tc"])
+@pytest.mark.parametrize("cfg", FULL + [LATENT, K3], ids=ids)
+def test_router_topk_full_size(orc, cfg, path, tuning):
+    tuning(router_tile=path)
+    _check(orc, cfg, G.gpu_inputs(cfg))
+
+
+def test_router_topk_exact_ties(orc, tuning):
+    # duplicated router rows give exactly equal logits: the lower index must
+    # come first, and the approximate logits cannot decide that on their own
+    tuning(router_tile="tc")
+    cfg = mi.MoEConfig("ties", T=256, H=512, I=128, E=24, k=5)
+    inp = dict(G.gpu_inputs(cfg))
+    wr = inp["router_w"].clone()
+    wr[7] = wr[3]
+    wr[11] = wr[3]
+    wr[20] = wr[15]
+    inp["router_w"] = wr
+    _check(orc, cfg, inp)
