@@ -3,7 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config decode|prefill|skewed|latent|toy|...]
                     [--also prefill,skewed,latent] [--also-steps 30]
-    python bench.py --stage router|route|latent_down --dims A B C [--steps K]
+    python bench.py --stage router|route|router_topk|latent_down --dims ... [--steps K]
 
 A step is one moe_forward over one batch (router logits -> top-k -> permute +
 fp8 quant -> grouped FFN1 -> requant -> grouped FFN2 -> gather + shared),
@@ -61,10 +61,12 @@ def parse():
                          "records of the same line (comma list; 'none' for none; one GPU only)")
     ap.add_argument("--also-steps", type=int, default=30,
                     help="timed steps of each nested workload")
-    ap.add_argument("--stage", choices=["router", "route", "latent_down"], default=None,
+    ap.add_argument("--stage", choices=["router", "route", "router_topk", "latent_down"],
+                    default=None,
                     help="time one entry point alone instead of the layer (see run_stage)")
-    ap.add_argument("--dims", type=int, nargs=3, default=None,
-                    help="with --stage: T H E (router), T E k (route) or T H L (latent_down)")
+    ap.add_argument("--dims", type=int, nargs="+", default=None,
+                    help="with --stage: T H E (router), T E k (route), T H E k (router_topk) "
+                         "or T H L (latent_down)")
     return ap.parse_args()
 
 
@@ -627,7 +629,9 @@ def run_stage(args):
     """Time one entry point alone on seeded inputs (for profiling a stage under
     ncu without a whole layer's weights on the device): ``--stage router
     --dims T H E`` (moe_router_logits), ``--stage route --dims T E k``
-    (moe_route) or ``--stage latent_down --dims T H L`` (moe_latent_down).
+    (moe_route), ``--stage router_topk --dims T H E k`` (moe_router_topk on
+    the tensor-core path) or ``--stage latent_down --dims T H L``
+    (moe_latent_down).
     x ~ N(0,1) bf16, router weights ~ N(0,1/H) fp32, logits ~ N(0,1), Wd ~
     N(0,1/H) bf16, generated on the device from seed 0."""
     import torch
@@ -646,6 +650,17 @@ def run_stage(args):
         out = torch.empty(T, E, device="cuda")
         p = m.make_problem(T, H, 128, E, 1)
         call = lambda: m.moe_router_logits(p, x, w, None, out)  # noqa: E731
+        work, unit = 2.0 * T * H * E, "TFLOP/s"
+    elif args.stage == "router_topk":
+        T, H, E, k = args.dims
+        x = torch.randn(T, H, device="cuda", generator=g).to(torch.bfloat16)
+        w = torch.randn(E, H, device="cuda", generator=g) / H ** 0.5
+        idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+        wt = torch.empty(T, k, device="cuda")
+        m.moe_set_tuning(router_tile="tc")
+        p = m.make_problem(T, H, 128, E, k)
+        wsb = torch.empty(m.moe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+        call = lambda: m.moe_router_topk(p, x, w, None, idx, wt, wsb)  # noqa: E731
         work, unit = 2.0 * T * H * E, "TFLOP/s"
     elif args.stage == "latent_down":
         T, H, L = args.dims
@@ -686,8 +701,9 @@ def run_stage(args):
 def main():
     args = parse()
     if args.stage:
-        if not args.dims:
-            raise SystemExit("--stage needs --dims")
+        want = 4 if args.stage == "router_topk" else 3
+        if not args.dims or len(args.dims) != want:
+            raise SystemExit(f"--stage {args.stage} needs --dims with {want} numbers")
         return run_stage(args)
     import moe_inputs as mi
     cfg = mi.CONFIGS[args.config]

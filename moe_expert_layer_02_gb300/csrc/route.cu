@@ -306,15 +306,20 @@ __global__ void __launch_bounds__(256)
 // significant bits), so x . w = x . w_lo + x . w_mid + x . w_hi with products
 // exact in fp32; one tcgen05 accumulation over K = 3H, small pieces first,
 // gives an approximate logit a[t,e] within a few units of 2^-23 |x_t| |w_e|
-// of the canonical one.  The selection is then made exact: per token, the top
-// k + 1 approximate keys are compared with per-element margins
-// m[t,e] = MOE_RFLAG_ULPS * 2^-23 * |x_t| * |w_e| (|.| the Euclidean norm);
-// when every adjacent gap exceeds the two margins, the approximate order is the
-// canonical order.  Otherwise every expert that could still take a place
-// (key + margin >= the k-th key - its margin) gets its canonical logit (32
-// fused multiply-add chains over h = l (mod 32), the halving tree, the bias
-// last: bit for bit the router kernel's value), and the top k among those are
-// chosen exactly.  The routing weights come from the logits the selection used.
+// of the canonical one.  The selection is then made exact.  Each expert's
+// canonical key lies within m[t,e] = MOE_RFLAG_ULPS * 2^-23 * |x_t| * |w_e|
+// (|.| the Euclidean norm) of its approximate key.  Per token, the experts
+// come out in approximate order, and a cut after position j is proven where
+// every lower bound (key - margin) up to j lies above every upper bound after
+// it, those of the experts not yet taken out included: the true order then
+// keeps positions 0..j, as a set, above all the rest.  Once a cut at or past
+// position k - 1 is proven, only the runs of two or more positions between
+// cuts are uncertain; their experts get canonical logits (32 fused
+// multiply-add chains over h = l (mod 32), the halving tree, the bias last:
+// bit for bit the router kernel's value) and each run is sorted by the
+// canonical keys.  If 32 positions prove no such cut, every expert whose
+// upper bound reaches the least lower bound of the first k is recomputed.
+// The routing weights come from the logits the selection used.
 //
 // Margin calibration (GB300; x N(0,1), router N(0, 1/H); tokens whose
 // selection or order came out different from the canonical routing, by margin
@@ -339,20 +344,32 @@ __global__ void __launch_bounds__(256)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if ((int)blockIdx.x < E) {
     const int e = blockIdx.x;
-    const float* row = wr + (size_t)e * H;
+    const float4* row = reinterpret_cast<const float4*>(wr + (size_t)e * H);
     uint16_t* lo = wp + (size_t)e * 3 * H;
     float ss = 0.0f;
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
-      const float v = row[h];
-      const __nv_bfloat16 bh = __float2bfloat16_rn(v);
-      const float r1 = __fsub_rn(v, __bfloat162float(bh));  // exact
-      const __nv_bfloat16 bm = __float2bfloat16_rn(r1);
-      const float r2 = __fsub_rn(r1, __bfloat162float(bm));  // exact, <= 8 significant bits
-      const __nv_bfloat16 bl = __float2bfloat16_rn(r2);      // exact
-      lo[h] = *reinterpret_cast<const uint16_t*>(&bl);
-      lo[H + h] = *reinterpret_cast<const uint16_t*>(&bm);
-      lo[2 * H + h] = *reinterpret_cast<const uint16_t*>(&bh);
-      ss = fmaf(v, v, ss);
+    for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
+      const float4 v4 = row[c];
+      const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+      uint16_t pl[4], pm[4], ph[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat16 bh = __float2bfloat16_rn(v[j]);
+        const float r1 = __fsub_rn(v[j], __bfloat162float(bh));  // exact
+        const __nv_bfloat16 bm = __float2bfloat16_rn(r1);
+        const float r2 = __fsub_rn(r1, __bfloat162float(bm));  // exact, <= 8 significant bits
+        const __nv_bfloat16 bl = __float2bfloat16_rn(r2);      // exact
+        pl[j] = *reinterpret_cast<const uint16_t*>(&bl);
+        pm[j] = *reinterpret_cast<const uint16_t*>(&bm);
+        ph[j] = *reinterpret_cast<const uint16_t*>(&bh);
+        ss = fmaf(v[j], v[j], ss);
+      }
+      auto pack = [](const uint16_t (&q)[4]) {
+        return make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16),
+                          (uint32_t)q[2] | ((uint32_t)q[3] << 16));
+      };
+      reinterpret_cast<uint2*>(lo)[c] = pack(pl);
+      reinterpret_cast<uint2*>(lo + H)[c] = pack(pm);
+      reinterpret_cast<uint2*>(lo + 2 * H)[c] = pack(ph);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -364,13 +381,20 @@ __global__ void __launch_bounds__(256)
       wnorm[e] = sqrtf(t);
     }
   } else {
-    const int t = ((int)blockIdx.x - E) * 8 + warp;
+    const long t = ((long)blockIdx.x - E) * 8 + warp;
     if (t >= T) return;
-    const uint16_t* row = x + (size_t)t * H;
+    // eight bf16 per 16-byte load (rows start 16-byte aligned: H % 64 == 0)
+    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     float ss = 0.0f;
-    for (int h = lane; h < H; h += 32) {
-      const float v = bf16_bits_to_f32(row[h]);
-      ss = fmaf(v, v, ss);
+    for (int c = lane; c < H / 8; c += 32) {
+      const uint4 q = row[c];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a0 = __uint_as_float(w[j] << 16), a1 = __uint_as_float(w[j] & 0xFFFF0000u);
+        ss = fmaf(a0, a0, ss);
+        ss = fmaf(a1, a1, ss);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -389,8 +413,65 @@ __device__ __forceinline__ float canonical_logit(const uint16_t* __restrict__ xr
   return __shfl_sync(0xffffffffu, p, 0);
 }
 
+// Four canonical logits of one token row against four router rows at once
+// (the x loads shared); each is computed exactly as canonical_logit does.
+__device__ __forceinline__ void canonical_logits4(const uint16_t* __restrict__ xr,
+                                                  const float* __restrict__ w0,
+                                                  const float* __restrict__ w1,
+                                                  const float* __restrict__ w2,
+                                                  const float* __restrict__ w3, int H, int lane,
+                                                  float (&out)[4]) {
+  float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+#pragma unroll 4
+  for (int h = lane; h < H; h += 32) {
+    const float xv = bf16_bits_to_f32(xr[h]);
+    p0 = fmaf(xv, w0[h], p0);
+    p1 = fmaf(xv, w1[h], p1);
+    p2 = fmaf(xv, w2[h], p2);
+    p3 = fmaf(xv, w3[h], p3);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    p0 = p0 + __shfl_down_sync(0xffffffffu, p0, o);
+    p1 = p1 + __shfl_down_sync(0xffffffffu, p1, o);
+    p2 = p2 + __shfl_down_sync(0xffffffffu, p2, o);
+    p3 = p3 + __shfl_down_sync(0xffffffffu, p3, o);
+  }
+  out[0] = __shfl_sync(0xffffffffu, p0, 0);
+  out[1] = __shfl_sync(0xffffffffu, p1, 0);
+  out[2] = __shfl_sync(0xffffffffu, p2, 0);
+  out[3] = __shfl_sync(0xffffffffu, p3, 0);
+}
+
+// Blocks of four warps, one token per warp: a warp that recomputes canonical
+// logits holds back only three others.
+constexpr int TOPK_TC_THREADS = 128;
+
+// The warp's 32 values sorted in descending order (lane 0 the largest) by a
+// bitonic network: blocks of 2, 4, .. 16 lanes are sorted in alternating
+// directions and merged, the last merge descending.
+template <typename K>
+__device__ __forceinline__ K warp_sort_desc(K v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const K o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    }
+  }
+  return v;
+}
+
+// The float a key's upper half was made from (float_order_key inverted).
+__device__ __forceinline__ float key_value(uint64_t key) {
+  const uint32_t k = (uint32_t)(key >> 32);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 template <int VPL>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(TOPK_TC_THREADS, 1)
     topk_tc_kernel(const float* __restrict__ approx, const float* __restrict__ logit_bias,
                    const float* __restrict__ sel_bias, int sigmoid,
                    const uint16_t* __restrict__ x, const float* __restrict__ wr,
@@ -398,91 +479,223 @@ __global__ void __launch_bounds__(256)
                    int32_t* __restrict__ idx, float* __restrict__ w, int T, int H, int E, int k) {
   pdl_wait();
   pdl_release();
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  __shared__ uint64_t s_cand[TOPK_TC_THREADS / 32][32];  // per warp: candidate keys
+  const long t = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* row = approx + (size_t)t * E;
   const float xm = MOE_RFLAG_ULPS * 0x1p-23f * xnorm[t];
-  // keys (as the canonical top-k forms them) and their margins
-  float kv[VPL], km[VPL], lv[VPL];
+  // key of expert e (as the canonical top-k forms it) from its approximate
+  // logit l; its margin follows from the key's value and |w_e|
+  auto logit_of = [&](int e) {
+    float l = row[e];
+    if (logit_bias) l = __fadd_rn(l, logit_bias[e]);
+    return l;
+  };
+  auto value_of = [&](int e, float l) {
+    float v = l;
+    if (sigmoid) {
+      v = sigmoid_fixed(l);
+      if (sel_bias) v = __fadd_rn(v, sel_bias[e]);
+    }
+    return v;
+  };
+  auto margin_of = [&](int e, float v) {
+    const float ml = xm * wnorm[e];
+    // sigmoid' <= 1/4, plus its own last-bit error; either way the bias
+    // addition's rounding (two units of the key's last place)
+    return (sigmoid ? 0.25f * ml + 0x1p-20f : ml) + 0x1p-22f * fabsf(v);
+  };
   uint64_t key[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = i * 32 + lane;
-    float l = 0.0f, v = 0.0f, m = 0.0f;
-    if (e < E) {
-      l = row[e];
-      if (logit_bias) l = __fadd_rn(l, logit_bias[e]);
-      const float ml = xm * wnorm[e];
-      if (sigmoid) {
-        v = sigmoid_fixed(l);
-        if (sel_bias) v = __fadd_rn(v, sel_bias[e]);
-        m = 0.25f * ml + 0x1p-20f;  // sigmoid' <= 1/4, plus its own last-bit error
-      } else {
-        v = l;
-        m = ml + 0x1p-22f * fabsf(l);  // plus the bias addition's rounding
-      }
-    }
-    lv[i] = l;
-    kv[i] = v;
-    km[i] = m;
-    key[i] = (e < E) ? ((uint64_t)float_order_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - e) : 0;
+    key[i] = (e < E) ? ((uint64_t)float_order_key(value_of(e, logit_of(e))) << 32) |
+                           (uint64_t)(0xFFFFFFFFu - e)
+                     : 0;
   }
-  // the k + 1 best keys by the approximate values: lane j keeps the j-th
-  const int nsel = k < E ? k + 1 : k;
+  // Experts in approximate order: lane j holds the j-th (value, margin, logit,
+  // index).  Every expert whose value key reaches the (k + 1)-th largest of
+  // the 32 lanes' best -- at least k + 1 experts, seldom more than 32 -- comes
+  // out at once, compacted one per lane and sorted by a bitonic network.
+  // More follow, one at a time, only while no cut at or past position k - 1
+  // is proven (below); past 32 candidates all of them come out that way.
   float my_v = 0.0f, my_m = 0.0f, my_l = 0.0f;
   int my_e = 0;
-  for (int j = 0; j < nsel; ++j) {
-    uint64_t best = 0;
+  const int n_max = E < 32 ? E : 32;
+  const int nsel = k < n_max ? k + 1 : n_max;
+  int n = 0;
+  {
+    uint32_t lm = 0;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) best = key[i] > best ? key[i] : best;
+    for (int i = 0; i < VPL; ++i) lm = max(lm, (uint32_t)(key[i] >> 32));
+    const uint32_t theta = __shfl_sync(0xffffffffu, warp_sort_desc(lm, lane), nsel - 1);
+    int cnt = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
-    float bv = 0.0f, bm = 0.0f, bl = 0.0f;
+    for (int i = 0; i < VPL; ++i) cnt += (key[i] != 0 && (uint32_t)(key[i] >> 32) >= theta);
+    const int total = __reduce_add_sync(0xffffffffu, cnt);
+    if (total <= 32) {
+      int off = cnt;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i)
-      if (key[i] == best) {  // the owner drops the winner and shares its values
-        key[i] = 0;
-        bv = kv[i];
-        bm = km[i];
-        bl = lv[i];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, off, o);
+        if (lane >= o) off += u;
       }
-    const int owner = e & 31;
-    bv = __shfl_sync(0xffffffffu, bv, owner);
-    bm = __shfl_sync(0xffffffffu, bm, owner);
-    bl = __shfl_sync(0xffffffffu, bl, owner);
-    if (lane == j) {
-      my_v = bv;
-      my_m = bm;
-      my_l = bl;
-      my_e = e;
+      off -= cnt;
+      uint64_t* slot = s_cand[threadIdx.x >> 5];
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (key[i] != 0 && (uint32_t)(key[i] >> 32) >= theta) {
+          slot[off++] = key[i];
+          key[i] = 0;
+        }
+      __syncwarp();
+      const uint64_t c = warp_sort_desc(lane < total ? slot[lane] : (uint64_t)0, lane);
+      n = total;
+      if (lane < n) {
+        my_e = (int)(0xFFFFFFFFu - (uint32_t)(c & 0xFFFFFFFFu));
+        my_l = logit_of(my_e);
+        my_v = value_of(my_e, my_l);
+        my_m = margin_of(my_e, my_v);
+      }
     }
   }
-  // the approximate order is the canonical one when every adjacent gap of the
-  // k + 1 best keys exceeds both margins
-  const float nx_v = __shfl_down_sync(0xffffffffu, my_v, 1);
-  const float nx_m = __shfl_down_sync(0xffffffffu, my_m, 1);
-  const bool close = lane < k && lane + 1 < nsel && !(my_v - nx_v > my_m + nx_m);
-  if (__any_sync(0xffffffffu, close)) {
-    // exact: the canonical keys of every expert that could still place
-    const float kth_v = __shfl_sync(0xffffffffu, my_v, k - 1);
-    const float kth_m = __shfl_sync(0xffffffffu, my_m, k - 1);
-    const float floor_v = kth_v - kth_m;
+  int target = n > nsel ? n : nsel;
+  int b = -1;         // the first proven cut at or past position k - 1
+  unsigned cuts = 0;  // bit j: positions 0..j are, in truth, the j + 1 best
+  float pl = 0.0f;    // min of the lower bounds v - m over positions 0..lane
+  for (;;) {
+    for (; n < target; ++n) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (key[i] == best) key[i] = 0;  // the owner drops the winner
+      if (lane == n) {
+        my_e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+        my_l = logit_of(my_e);
+        my_v = value_of(my_e, my_l);
+        my_m = margin_of(my_e, my_v);
+      }
+    }
+    // the largest upper bound v + m among the experts not taken out
+    float tail_u = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (key[i] != 0) {
+        const float v = key_value(key[i]);
+        tail_u = fmaxf(tail_u, v + margin_of(i * 32 + lane, v));
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tail_u = fmaxf(tail_u, __shfl_xor_sync(0xffffffffu, tail_u, o));
+    // A cut after position j is proven when every lower bound up to j lies
+    // above every upper bound after it (those of the experts not taken out
+    // included): true values then keep positions 0..j above all others.
+    pl = lane < n ? my_v - my_m : INFINITY;
+    float su = lane < n ? my_v + my_m : -INFINITY;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float lo = __shfl_up_sync(0xffffffffu, pl, o);
+      const float hi = __shfl_down_sync(0xffffffffu, su, o);
+      if (lane >= o) pl = fminf(pl, lo);
+      if (lane + o < 32) su = fmaxf(su, hi);
+    }
+    float su_next = __shfl_down_sync(0xffffffffu, su, 1);
+    if (lane == 31) su_next = -INFINITY;
+    su_next = fmaxf(su_next, tail_u);
+    cuts = __ballot_sync(0xffffffffu, lane < n && pl > su_next);
+    const unsigned late = cuts >> (k - 1);
+    if (late) {
+      b = k - 2 + __ffs(late);
+      break;
+    }
+    if (n >= n_max) break;
+    target = n + 1;
+  }
+  const uint16_t* xr = x + (size_t)t * H;
+  if (b >= 0) {
+    // Between two cuts the approximate order proves nothing: every run of two
+    // or more positions up to b gets canonical keys and is sorted by them.
+    const unsigned below = cuts & ((1u << lane) - 1u);
+    const int start = below ? 32 - __clz(below) : 0;
+    const unsigned from = lane == 0 ? cuts : cuts & ~((1u << lane) - 1u);
+    const int end = from ? __ffs(from) - 1 : 31;
+    const unsigned redo = __ballot_sync(0xffffffffu, lane <= b && end > start);
+    if (redo) {
+      uint64_t ck = 0;
+      unsigned todo = redo;
+      while (todo) {  // up to four canonical logits per pass over x
+        int pos[4], ex[4], c = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          pos[q] = todo ? __ffs(todo) - 1 : -1;
+          if (todo) {
+            todo &= todo - 1u;
+            ++c;
+          }
+          ex[q] = __shfl_sync(0xffffffffu, my_e, pos[q] < 0 ? pos[0] : pos[q]);
+        }
+        float cl[4];
+        canonical_logits4(xr, wr + (size_t)ex[0] * H, wr + (size_t)ex[1] * H,
+                          wr + (size_t)ex[2] * H, wr + (size_t)ex[3] * H, H, lane, cl);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q < c && lane == pos[q]) {
+            float l = cl[q];
+            if (logit_bias) l = __fadd_rn(l, logit_bias[ex[q]]);
+            float v = l;
+            if (sigmoid) {
+              v = sigmoid_fixed(l);
+              if (sel_bias) v = __fadd_rn(v, sel_bias[ex[q]]);
+            }
+            my_l = l;
+            ck = ((uint64_t)float_order_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - ex[q]);
+          }
+        }
+      }
+      // rank within the run, then move every lane to its place
+      int rank = 0;
+      for (int i = 0; i <= b; ++i) {
+        const uint64_t ki = __shfl_sync(0xffffffffu, ck, i);
+        const int si = __shfl_sync(0xffffffffu, start, i);
+        if (si == start && ki > ck) ++rank;
+      }
+      const int dest = lane <= b ? start + rank : lane;
+      int src = lane;
+      for (int i = 0; i <= b; ++i)
+        if (__shfl_sync(0xffffffffu, dest, i) == lane) src = i;
+      my_e = __shfl_sync(0xffffffffu, my_e, src);
+      my_l = __shfl_sync(0xffffffffu, my_l, src);
+    }
+  } else {
+    // No cut within 32 positions: the canonical keys of every expert whose
+    // upper bound reaches the least lower bound of the first k, sorted by
+    // insertion into lanes 0..k-1.
+    const float floor_v = __shfl_sync(0xffffffffu, pl, k - 1);
     uint64_t top = 0;  // lane j < k: the j-th best canonical key so far
     float top_l = 0.0f;
-    const uint16_t* xr = x + (size_t)t * H;
+    // the 32 taken out (lane j: position j), then the rest in index order
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e0 = i * 32 + lane;
-      unsigned cand = __ballot_sync(0xffffffffu, e0 < E && kv[i] + km[i] >= floor_v);
+    for (int i = -1; i < VPL; ++i) {
+      bool c;
+      if (i < 0) {
+        c = lane < n && !(my_v + my_m < floor_v);  // a NaN bound keeps the expert
+      } else {
+        const int e0 = i * 32 + lane;
+        const float v = key_value(key[i]);
+        c = key[i] != 0 && !(v + margin_of(e0, v) < floor_v);
+      }
+      unsigned cand = __ballot_sync(0xffffffffu, c);
       while (cand) {
-        const int b = __ffs(cand) - 1;
+        const int bb = __ffs(cand) - 1;
         cand &= cand - 1u;
-        const int e = i * 32 + b;
+        const int e = i < 0 ? __shfl_sync(0xffffffffu, my_e, bb) : i * 32 + bb;
         float l = canonical_logit(xr, wr + (size_t)e * H, H, lane);
         if (logit_bias) l = __fadd_rn(l, logit_bias[e]);
         float v = l;
@@ -491,7 +704,6 @@ __global__ void __launch_bounds__(256)
           if (sel_bias) v = __fadd_rn(v, sel_bias[e]);
         }
         const uint64_t ck = ((uint64_t)float_order_key(v) << 32) | (uint64_t)(0xFFFFFFFFu - e);
-        // insert into the sorted top-k list held by lanes 0..k-1
         const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && top > ck));
         const uint64_t up = __shfl_up_sync(0xffffffffu, top, 1);
         const float up_l = __shfl_up_sync(0xffffffffu, top_l, 1);
@@ -599,6 +811,9 @@ cudaError_t launch_router_logits(const void* x, const float* wr, const float* bi
 cudaError_t launch_router_tc(const void* x, const float* wr, int T, int H, int E, uint16_t* wp,
                              float* xnorm, float* wnorm, float* approx, int* err, cudaStream_t s) {
   if (T <= 0 || H % 64 || E <= 0 || E > 1024) return cudaErrorInvalidValue;
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(wr) % 16 ||
+      reinterpret_cast<uintptr_t>(wp) % 16)
+    return cudaErrorInvalidValue;  // the prep kernel's vector loads and stores
   count_launch();
   cudaError_t e = launch_kernel(router_prep_kernel, dim3(E + (T + 7) / 8), dim3(256), 0, s, 1,
                                 static_cast<const uint16_t*>(x), wr, wp, xnorm, wnorm, T, H, E);
@@ -614,19 +829,22 @@ cudaError_t launch_topk_tc(const float* approx, const float* logit_bias, const f
                            const float* wnorm, int32_t* idx, float* w, int T, int H, int E, int k,
                            cudaStream_t s) {
   if (T <= 0 || E <= 0 || E > 1024 || k > 32 || k > E) return cudaErrorInvalidValue;
-  const int blocks = (T * 32 + 255) / 256;
+  const long blocks = ((long)T * 32 + TOPK_TC_THREADS - 1) / TOPK_TC_THREADS;
+  if (blocks > 0x7FFFFFFFL) return cudaErrorInvalidValue;
   const int vpl = (E + 31) / 32;
   const uint16_t* xb = static_cast<const uint16_t*>(x);
   count_launch();
   cudaError_t e;
 #define MOE_TOPK_TC(V)                                                                      \
-  launch_kernel(topk_tc_kernel<V>, dim3(blocks), dim3(256), 0, s, 1, approx, logit_bias,   \
+  launch_kernel(topk_tc_kernel<V>, dim3((unsigned)blocks), dim3(TOPK_TC_THREADS), 0, s, 1, \
+                approx, logit_bias,                                                         \
                 sel_bias, sigmoid, xb, wr, xnorm, wnorm, idx, w, T, H, E, k)
   if (vpl <= 1) e = MOE_TOPK_TC(1);
   else if (vpl <= 2) e = MOE_TOPK_TC(2);
   else if (vpl <= 4) e = MOE_TOPK_TC(4);
   else if (vpl <= 8) e = MOE_TOPK_TC(8);
   else if (vpl <= 16) e = MOE_TOPK_TC(16);
+  else if (vpl <= 28) e = MOE_TOPK_TC(28);  // E <= 896
   else e = MOE_TOPK_TC(32);
 #undef MOE_TOPK_TC
   if (e != cudaSuccess) return e;

@@ -104,3 +104,44 @@ def test_router_topk_exact_ties(orc, tuning):
     wr[20] = wr[15]
     inp["router_w"] = wr
     _check(orc, cfg, inp)
+
+
+def test_router_topk_run_across_the_boundary(orc, tuning):
+    # eight copies of one router row with a bias that puts them first for
+    # every token: positions 0..7 tie exactly, the k = 5 boundary falls inside
+    # that run, and selection must take more than k + 1 experts out before a
+    # cut is proven
+    tuning(router_tile="tc")
+    cfg = mi.MoEConfig("run8", T=256, H=512, I=128, E=24, k=5, zipf_bias=True)
+    inp = dict(G.gpu_inputs(cfg))
+    wr = inp["router_w"].clone()
+    for e in (2, 5, 6, 9, 13, 17, 20, 23):
+        wr[e] = wr[2]
+    inp["router_w"] = wr
+    bias = torch.zeros(cfg.E, dtype=torch.float32, device="cuda")
+    bias[[2, 5, 6, 9, 13, 17, 20, 23]] = 50.0
+    inp["router_bias"] = bias
+    _check(orc, cfg, inp)
+
+
+def test_router_topk_no_cut_within_32(orc, tuning):
+    # forty identical experts ahead of all others: no cut can be proven among
+    # the first 32 positions, so every expert that could place is recomputed
+    tuning(router_tile="tc")
+    cfg = mi.MoEConfig("run40", T=128, H=512, I=128, E=64, k=8, zipf_bias=True)
+    inp = dict(G.gpu_inputs(cfg))
+    same = [e for e in range(cfg.E) if e % 8 != 0][:40]
+    wr = inp["router_w"].clone()
+    for e in same:
+        wr[e] = wr[same[0]]
+    inp["router_w"] = wr
+    bias = torch.zeros(cfg.E, dtype=torch.float32, device="cuda")
+    bias[same] = 50.0
+    inp["router_bias"] = bias
+    _check(orc, cfg, inp)
+    # sigmoid routing with the selection bias doing the lifting
+    cfg = cfg.with_(name="run40_sig", routing="sigmoid", sel_bias=True, zipf_bias=False)
+    inp2 = dict(G.gpu_inputs(cfg))
+    inp2["router_w"] = wr
+    inp2["router_bias"] = bias
+    _check(orc, cfg, inp2)
