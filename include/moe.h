@@ -188,7 +188,7 @@ int moe_router_topk(const moe_problem* p, const void* x, const float* router_w,
  *   x [T, H] bf16, latent_down [latent, H] bf16 -> z [T, latent] bf16 (output)
  *   ws / ws_bytes: workspace of at least moe_workspace_bytes(p) (per-element
  *   recompute flags live there)
- * Needs latent > 0; H and latent multiples of 256 and 4 H + 2 latent <=
+ * Needs latent > 0; H and latent multiples of 256 and 2 H + 2 latent <=
  * 163840 (else MOE_ERR_UNSUPPORTED); pointers 16-byte aligned. */
 int moe_latent_down(const moe_problem* p, const void* x, const void* latent_down, void* z,
                     void* ws, size_t ws_bytes, void* stream);

@@ -94,14 +94,15 @@ cudaError_t launch_topk_tc(const float* approx, const float* logit_bias, const f
 
 // ---------------------------------------------------------------- permute.cu
 // cc[e * nch + c] = #tokens of chunk c that picked expert e.
-cudaError_t launch_count(const int32_t* idx, int32_t* cc, int T, int E, int k, int* err,
-                         cudaStream_t s);
+// ticket: one int the count kernel zeroes and the scan kernel's blocks count on
+cudaError_t launch_count(const int32_t* idx, int32_t* cc, int32_t* ticket, int T, int E, int k,
+                         int* err, cudaStream_t s);
 // cbase[e * nch + c] = rows of expert e in chunks < c; cnt, off (E+1); then the
 // tile work list: groups 0..E-1 are the routed experts (rows off[g]..off[g+1]),
 // group E (if shared_rows > 0) covers rows shared_row0 .. shared_row0+shared_rows.
-cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t* off, int T, int E,
-                        int k, int4* items, int32_t* n_items, int max_items, int BN,
-                        int shared_row0, int shared_rows, cudaStream_t s);
+cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t* off,
+                        int32_t* ticket, int T, int E, int k, int4* items, int32_t* n_items,
+                        int max_items, int BN, int shared_row0, int shared_rows, cudaStream_t s);
 cudaError_t launch_items_from_offsets(const int32_t* off, int E, int4* items, int32_t* n_items,
                                       int max_items, int BN, cudaStream_t s);
 // count + scan + rank in one single-block launch, for T <= 1024 when the

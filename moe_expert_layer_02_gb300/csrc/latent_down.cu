@@ -402,6 +402,27 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, aa), __fsub_rn(b, bb));
 }
 
+// Packed pairs of fp32 (.x in the low word): two independent IEEE
+// round-to-nearest operations per instruction.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t x, uint32_t y) {
+  return (uint64_t)x | ((uint64_t)y << 32);
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Nearest-even bf16 of the exact value hi + lo, where (hi, lo) = TwoSum output
 // (|lo| <= ulp(hi) / 2).  Every bf16 rounding boundary is an fp32 value, so
 // hi + lo lies on hi's side of it unless hi is the boundary itself; then lo's
@@ -417,19 +438,22 @@ __device__ __forceinline__ uint16_t bf16_of_sum(float hi, float lo) {
 }
 
 constexpr int FX_THREADS = 256;
-constexpr int FX_SMEM_MAX = 160 * 1024;  // x row as fp32 + flagged-column list: 4 H + 2 L bytes
+constexpr int FX_SMEM_MAX = 160 * 1024;  // x row (bf16) + flagged-column list: 2 H + 2 L bytes
+constexpr int FX_AHEAD = 8;              // 16-byte weight loads a lane issues ahead of its sums
 
-// One block per token: x[t] goes to shared memory as fp32, then each warp
+// One block per token: x[t] goes to shared memory (bf16), then each warp
 // takes flagged elements in turn.  Lane j sums the products of columns
-// 8 (j + 32 m) .. 8 (j + 32 m) + 7 (m ascending) with TwoSum, and the warp
-// combines the lanes' (hi, lo) pairs.
+// 8 (j + 32 m) .. 8 (j + 32 m) + 7 (m ascending) with TwoSum in two chains,
+// even and odd columns, run as packed fp32 pairs (six instructions per
+// product instead of ten, though the fp32 pipe does the same work: T=4096,
+// H=7168, L=3584, 0.5% of z flagged: 152 -> 130 us); the lane joins its
+// chains and the warp combines the lanes' (hi, lo) pairs.
 __global__ void __launch_bounds__(FX_THREADS)
     latent_fix_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wd,
                       uint16_t* __restrict__ z, const uint32_t* __restrict__ flags, int T, int H,
                       int L) {
-  extern __shared__ float4 fx_smem[];
-  float* xs = reinterpret_cast<float*>(fx_smem);
-  uint16_t* list = reinterpret_cast<uint16_t*>(xs + H);  // flagged columns of this token
+  extern __shared__ uint4 fx_smem[];
+  uint16_t* list = reinterpret_cast<uint16_t*>(fx_smem + H / 8);  // flagged columns of this token
   __shared__ int n_list;
   pdl_wait();
   const int t = blockIdx.x;
@@ -445,49 +469,65 @@ __global__ void __launch_bounds__(FX_THREADS)
       list[atomicAdd(&n_list, 1)] = (uint16_t)(32 * w + j);
     }
   }
-  const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)t * H);
-  for (int i = threadIdx.x; i < H / 4; i += FX_THREADS) {  // 4 bf16 -> 4 fp32
-    const uint2 v = xr[i];
-    fx_smem[i] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
-                             __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
-  }
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  for (int i = threadIdx.x; i < H / 8; i += FX_THREADS) fx_smem[i] = xr[i];
   __syncthreads();
   const int n = n_list;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C8 = H / 8;  // 16-byte chunks of a row
   for (int i = warp; i < n; i += FX_THREADS / 32) {
     const int l = list[i];
     const uint4* wr = reinterpret_cast<const uint4*>(wd + (size_t)l * H);
-    float hi = 0.0f, lo = 0.0f;
-    for (int c = lane; c < H / 8; c += 32) {
-      const uint4 wv = __ldg(wr + c);
-      const float4 xa = fx_smem[2 * c], xb = fx_smem[2 * c + 1];
-      // products of bf16 values: 16 significant bits, exact in fp32
-      const float p[8] = {
-          __fmul_rn(xa.x, __uint_as_float(wv.x << 16)), __fmul_rn(xa.y, __uint_as_float(wv.x & 0xFFFF0000u)),
-          __fmul_rn(xa.z, __uint_as_float(wv.y << 16)), __fmul_rn(xa.w, __uint_as_float(wv.y & 0xFFFF0000u)),
-          __fmul_rn(xb.x, __uint_as_float(wv.z << 16)), __fmul_rn(xb.y, __uint_as_float(wv.z & 0xFFFF0000u)),
-          __fmul_rn(xb.z, __uint_as_float(wv.w << 16)), __fmul_rn(xb.w, __uint_as_float(wv.w & 0xFFFF0000u))};
+    // Two TwoSum chains per lane in packed pairs: .x takes the even products
+    // (the low bf16 of every word), .y the odd ones; the lane's chunks
+    // c = lane + 32 m in ascending m, FX_AHEAD weight loads in flight before
+    // the sums that need them.
+    uint64_t hi2 = 0, lo2 = 0;
+    for (int c0 = lane; c0 < C8; c0 += 32 * FX_AHEAD) {
+      uint4 wv[FX_AHEAD];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float s, e;
-        two_sum(hi, p[k], s, e);
-        hi = s;
-        lo = __fadd_rn(lo, e);
+      for (int u = 0; u < FX_AHEAD; ++u)
+        wv[u] = c0 + 32 * u < C8 ? __ldg(wr + c0 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < FX_AHEAD; ++u) {
+        if (c0 + 32 * u >= C8) break;
+        const uint4 xv = fx_smem[c0 + 32 * u];
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        const uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // products of bf16 values: 16 significant bits, exact in fp32
+          const uint64_t p = f2_mul(f2_pack(xw[q] << 16, xw[q] & 0xFFFF0000u),
+                                    f2_pack(ww[q] << 16, ww[q] & 0xFFFF0000u));
+          const uint64_t sm = f2_add(hi2, p);  // TwoSum(hi2, p), both halves at once
+          const uint64_t bb = f2_sub(sm, hi2);
+          const uint64_t aa = f2_sub(sm, bb);
+          lo2 = f2_add(lo2, f2_add(f2_sub(hi2, aa), f2_sub(p, bb)));
+          hi2 = sm;
+        }
       }
+    }
+    float hi, lo;
+    {
+      float sm, e;
+      two_sum(__uint_as_float((uint32_t)hi2), __uint_as_float((uint32_t)(hi2 >> 32)), sm, e);
+      hi = sm;
+      lo = __fadd_rn(__fadd_rn(__uint_as_float((uint32_t)lo2), __uint_as_float((uint32_t)(lo2 >> 32))),
+                     e);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
       const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-      float s, e;
-      two_sum(hi, h2, s, e);
-      hi = s;
+      float sm, e;
+      two_sum(hi, h2, sm, e);
+      hi = sm;
       lo = __fadd_rn(__fadd_rn(lo, l2), e);
     }
     if (lane == 0) {
-      float s, e;
-      two_sum(hi, lo, s, e);  // renormalise: |e| <= ulp(s) / 2
-      z[(size_t)t * L + l] = bf16_of_sum(s, e);
+      float sm, e;
+      two_sum(hi, lo, sm, e);  // renormalise: |e| <= ulp(sm) / 2
+      z[(size_t)t * L + l] = bf16_of_sum(sm, e);
     }
   }
   pdl_release();
@@ -552,7 +592,7 @@ cudaError_t launch_latent_down(const void* x, const void* wd, void* z, uint32_t*
   if (L % 256 || !wide_kernel_usable()) return cudaErrorInvalidDeviceFunction;
   cudaError_t e = launch_down_gemm<256>(x, wd, g, s);
   if (e != cudaSuccess) return e;
-  const size_t fx_smem = (size_t)H * 4 + (size_t)L * 2;
+  const size_t fx_smem = (size_t)H * 2 + (size_t)L * 2;
   if (fx_smem > (size_t)FX_SMEM_MAX) return cudaErrorInvalidValue;
   e = ensure_max_smem<latent_fix_kernel>(FX_SMEM_MAX);
   if (e != cudaSuccess) return e;

@@ -112,7 +112,7 @@ struct Plan {
   bool gather;      // S4 quantises per token; the FFN1 producer gathers the rows
   bool tc_router;   // S1 on the tensor cores, S2 made exact (route.cu)
   size_t acc;       // fused combine: fp32 [T, H] sum
-  size_t logits, idx, tw, cc, cbase, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
+  size_t logits, idx, tw, cc, cbase, ticket, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
       hq, hs, y, z, zflag, yn, hsh, rwp, rxn, rwn, total;
 };
 
@@ -201,6 +201,7 @@ Plan make_plan(const moe_problem* p) {
   q.tw = take(T * k * 4);
   q.cc = take(E * q.nch * 4);
   q.cbase = take(E * q.nch * 4);
+  q.ticket = take(4);
   q.cnt = take(E * 4);
   q.off = take((E + 1) * 4);
   q.perm = take(T * k * 4);
@@ -270,8 +271,8 @@ int check_supported(const moe_problem* p) {
   if (p->latent > 0) {
     if (s8) return MOE_ERR_UNSUPPORTED;
     if (p->H % 256 || p->latent % 256) return MOE_ERR_UNSUPPORTED;
-    // the exact down projection keeps an fp32 row of x and a column list in shared memory
-    if (4 * (int64_t)p->H + 2 * (int64_t)p->latent > 160 * 1024) return MOE_ERR_UNSUPPORTED;
+    // the exact down projection keeps a bf16 row of x and a column list in shared memory
+    if (2 * (int64_t)p->H + 2 * (int64_t)p->latent > 160 * 1024) return MOE_ERR_UNSUPPORTED;
   } else {
     if (sb) return MOE_ERR_UNSUPPORTED;
     if (mx && s8) return MOE_ERR_UNSUPPORTED;
@@ -585,9 +586,11 @@ int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, in
       MOE_TRY(launch_index_small(topk_idx, nullptr, counts, offsets, perm, src_row, nullptr, q.T,
                                  q.E, q.k, nullptr, nullptr, 0, q.BN, 0, 0, di->err, s));
     } else {
-      MOE_TRY(launch_count(topk_idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
-      MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), counts, offsets, q.T,
-                          q.E, q.k, nullptr, nullptr, 0, q.BN, 0, 0, s));
+      MOE_TRY(launch_count(topk_idx, at<int32_t>(ws, q.cc), at<int32_t>(ws, q.ticket), q.T, q.E,
+                           q.k, di->err, s));
+      MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), counts, offsets,
+                          at<int32_t>(ws, q.ticket), q.T, q.E, q.k, nullptr, nullptr, 0, q.BN, 0,
+                          0, s));
       MOE_TRY(launch_rank(topk_idx, nullptr, offsets, at<int32_t>(ws, q.cbase), perm, src_row,
                           nullptr, q.T, q.E, q.k, s));
     }
@@ -716,10 +719,12 @@ int moe_forward(const moe_problem* p, const void* x, const float* router_w,
                                  at<int32_t>(ws, q.n_items), q.max_items, q.BN, q.R,
                                  q.shared ? q.T : 0, di->err, s));
     } else {
-      MOE_TRY(launch_count(idx, at<int32_t>(ws, q.cc), q.T, q.E, q.k, di->err, s));
+      MOE_TRY(launch_count(idx, at<int32_t>(ws, q.cc), at<int32_t>(ws, q.ticket), q.T, q.E, q.k,
+                           di->err, s));
       MOE_TRY(launch_scan(at<int32_t>(ws, q.cc), at<int32_t>(ws, q.cbase), at<int32_t>(ws, q.cnt),
-                          off, q.T, q.E, q.k, at<int4>(ws, q.items), at<int32_t>(ws, q.n_items),
-                          q.max_items, q.BN, q.R, q.shared ? q.T : 0, s));
+                          off, at<int32_t>(ws, q.ticket), q.T, q.E, q.k, at<int4>(ws, q.items),
+                          at<int32_t>(ws, q.n_items), q.max_items, q.BN, q.R, q.shared ? q.T : 0,
+                          s));
       MOE_TRY(launch_rank(idx, tw, off, at<int32_t>(ws, q.cbase), perm, at<int32_t>(ws, q.src),
                           row_w, q.T, q.E, q.k, s));
     }

@@ -44,12 +44,13 @@ __device__ __forceinline__ void build_chunk_bits(const int32_t* __restrict__ idx
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
-    count_kernel(const int32_t* __restrict__ idx, int32_t* __restrict__ cc, int T, int E, int k,
-                 int nch, int* err) {
+    count_kernel(const int32_t* __restrict__ idx, int32_t* __restrict__ cc, int32_t* ticket,
+                 int T, int E, int k, int nch, int* err) {
   pdl_wait();  // the previous kernel's outputs are complete and visible
   pdl_release();
   extern __shared__ uint32_t s_bits[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;  // scan_kernel's completion count
   const int c = blockIdx.x * kWarps + warp;
   if (c >= nch) return;  // whole warp leaves together
   uint32_t* bits = s_bits + warp * E;
@@ -151,49 +152,71 @@ __device__ void build_items(const int32_t* off, int E, int BN, int shared_row0, 
   if (threadIdx.x == 0) *n_items = min(carry, max_items);
 }
 
+// One warp per expert (32 per block): the exclusive scan of its per-chunk
+// counts gives the chunk bases, eight chunk counts per lane loaded before the
+// scans that use them.  The block that finishes last (a ticket taken after
+// every block's writes are fenced; no block waits for another) turns the
+// expert totals into offsets and the tile list.
 __global__ void __launch_bounds__(1024)
     scan_kernel(const int32_t* __restrict__ cc, int32_t* __restrict__ cbase, int32_t* cnt,
-                int32_t* off, int E, int nch, int R, int4* items, int32_t* n_items, int max_items,
-                int BN, int shared_row0, int shared_rows) {
+                int32_t* off, int32_t* ticket, int E, int nch, int R, int4* items,
+                int32_t* n_items, int max_items, int BN, int shared_row0, int shared_rows) {
   pdl_wait();  // the previous kernel's outputs are complete and visible
   __shared__ int s_cnt[kMaxExperts + 1];
   __shared__ int s_warp[33];
+  __shared__ bool s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += 32) {
+  const int e = blockIdx.x * 32 + warp;
+  if (e < E) {
+    const int32_t* row = cc + (size_t)e * nch;
+    int32_t* base = cbase + (size_t)e * nch;
     int run = 0;
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = (c < nch) ? cc[(size_t)e * nch + c] : 0;
-      int x = v;
+    for (int c0 = 0; c0 < nch; c0 += 32 * 8) {
+      int v[8];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + 32 * u + lane;
+        v[u] = c < nch ? row[c] : 0;
       }
-      if (c < nch) cbase[(size_t)e * nch + c] = run + x - v;
-      run += __shfl_sync(0xffffffffu, x, 31);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        int x = v[u];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        const int c = c0 + 32 * u + lane;
+        if (c < nch) base[c] = run + x - v[u];
+        run += __shfl_sync(0xffffffffu, x, 31);
+      }
     }
-    if (lane == 0) s_cnt[e] = run;
+    if (lane == 0) cnt[e] = run;
   }
-  __syncthreads();
-  const int v = threadIdx.x < E ? s_cnt[threadIdx.x] : 0;
-  int total;
-  const int ex = block_exclusive_scan(v, s_warp, &total);
-  if (threadIdx.x < E) {
-    cnt[threadIdx.x] = v;
-    off[threadIdx.x] = ex;
-    s_cnt[threadIdx.x] = ex;
-  }
-  if (threadIdx.x == 0) {
-    off[E] = total;  // == R when every index was valid
-    s_cnt[E] = total;
-  }
-  __syncthreads();
-  if (items) build_items(s_cnt, E, BN, shared_row0, shared_rows, items, n_items, max_items, s_warp);
-  // the tile list is final and visible before the next kernels may launch:
-  // the expert GEMMs read it before their pdl_wait
   __threadfence();
   __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    const int v = threadIdx.x < E ? __ldcg(cnt + threadIdx.x) : 0;
+    int total;
+    const int ex = block_exclusive_scan(v, s_warp, &total);
+    if (threadIdx.x < E) {
+      off[threadIdx.x] = ex;
+      s_cnt[threadIdx.x] = ex;
+    }
+    if (threadIdx.x == 0) {
+      off[E] = total;  // == R when every index was valid
+      s_cnt[E] = total;
+    }
+    __syncthreads();
+    if (items) build_items(s_cnt, E, BN, shared_row0, shared_rows, items, n_items, max_items, s_warp);
+    // the tile list is final and visible before the next kernels may launch:
+    // the expert GEMMs read it before their pdl_wait
+    __threadfence();
+    __syncthreads();
+  }
   pdl_release();
 }
 
@@ -644,22 +667,23 @@ cudaError_t launch_combine_rmsnorm(const void* y, const int32_t* perm, const voi
   return go(combine_rmsnorm_kernel<kMaxTopK>);
 }
 
-cudaError_t launch_count(const int32_t* idx, int32_t* cc, int T, int E, int k, int* err,
-                         cudaStream_t s) {
+cudaError_t launch_count(const int32_t* idx, int32_t* cc, int32_t* ticket, int T, int E, int k,
+                         int* err, cudaStream_t s) {
   const int nch = num_chunks(T);
   const int blocks = (nch + kWarps - 1) / kWarps;
   const size_t smem = (size_t)kWarps * E * sizeof(uint32_t);
   count_launch();
-  return launch_kernel(count_kernel, dim3(blocks), dim3(kWarps * 32), smem, s, 1, idx, cc, T, E, k,
-                       nch, err);
+  return launch_kernel(count_kernel, dim3(blocks), dim3(kWarps * 32), smem, s, 1, idx, cc, ticket,
+                       T, E, k, nch, err);
 }
 
-cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t* off, int T, int E,
-                        int k, int4* items, int32_t* n_items, int max_items, int BN,
-                        int shared_row0, int shared_rows, cudaStream_t s) {
+cudaError_t launch_scan(const int32_t* cc, int32_t* cbase, int32_t* cnt, int32_t* off,
+                        int32_t* ticket, int T, int E, int k, int4* items, int32_t* n_items,
+                        int max_items, int BN, int shared_row0, int shared_rows, cudaStream_t s) {
+  if (E <= 0 || E > kMaxExperts) return cudaErrorInvalidValue;
   count_launch();
-  return launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, s, 1, cc, cbase, cnt, off, E,
-                       num_chunks(T), T * k, items, n_items, max_items, BN, shared_row0,
+  return launch_kernel(scan_kernel, dim3((E + 31) / 32), dim3(1024), 0, s, 1, cc, cbase, cnt, off,
+                       ticket, E, num_chunks(T), T * k, items, n_items, max_items, BN, shared_row0,
                        shared_rows);
 }
 

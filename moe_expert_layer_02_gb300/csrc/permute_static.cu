@@ -7,9 +7,9 @@
 // and output buffers, or a latency-critical loop where cudaMalloc is not
 // allowed because it can synchronise the device.  moe_permute_static serves
 // them: the two tables live in a fixed array in this library's own device
-// memory (kStaticTableInts int32 each, 4 MiB in total, held on every GPU that
-// loads the library until the process exits), so the caller passes only inputs
-// and outputs.
+// memory (kStaticTableInts int32 each, 4 MiB in total, plus one word the scan
+// counts its finished blocks on; held on every GPU that loads the library
+// until the process exits), so the caller passes only inputs and outputs.
 //
 // Limits and sharing: a problem needs E * ceil(T / 32) <= kStaticTableInts
 // entries per table; larger problems are rejected with MOE_ERR_WORKSPACE.  All
@@ -31,7 +31,7 @@ constexpr int64_t kStaticTableInts = int64_t(1) << 19;  // 2 MiB per table
 
 // The scratch itself.  In host code this name is only a stand-in for the
 // device symbol; its device address comes from cudaGetSymbolAddress below.
-static __device__ __align__(256) int32_t g_permute_scratch[2 * kStaticTableInts];
+static __device__ __align__(256) int32_t g_permute_scratch[2 * kStaticTableInts + 64];
 
 constexpr int kMaxDev = 64;
 int32_t* g_scratch_addr[kMaxDev] = {};
@@ -83,8 +83,9 @@ extern "C" int moe_permute_static(const moe_problem* p, const int32_t* topk_idx,
   if (!scratch || !err) return MOE_ERR_CUDA;
   int32_t* cc = scratch;                       // per-chunk counts  [E, nch]
   int32_t* cbase = scratch + kStaticTableInts;  // per-chunk bases   [E, nch]
-  if (launch_count(topk_idx, cc, T, E, k, err, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_scan(cc, cbase, counts, offsets, T, E, k, nullptr, nullptr, 0, 32, 0, 0, s) !=
+  int32_t* ticket = scratch + 2 * kStaticTableInts;  // the scan's completion count
+  if (launch_count(topk_idx, cc, ticket, T, E, k, err, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_scan(cc, cbase, counts, offsets, ticket, T, E, k, nullptr, nullptr, 0, 32, 0, 0, s) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_rank(topk_idx, nullptr, offsets, cbase, perm, src_row, nullptr, T, E, k, s) !=
