@@ -247,10 +247,10 @@ int moe_permute_static(const moe_problem* p, const int32_t* topk_idx, const void
  *   MXFP4 (K = H or latent a multiple of 256): a stage reads two 128-row
  *     blocks, W1 and W3 block p (rows p*128 and I + p*128) of w13, or W2 blocks
  *     2p and 2p+1 of w2.  Weights become [E][P][K/128][2][128 rows][64 bytes]
- *     and scales [E][P][K/128][2][32][4] 32-bit words, word (l, c) of block
- *     b holding the four e8m0 bytes of k-stage kb of that block's row 32c + l
- *     (the image tcgen05.cp copies into tensor memory): one 256-row copy and
- *     one 1 KB copy per stage.
+ *     and scales [E][P][K/128][4][2][8][4] 32-bit words, word (j, b, i, c)
+ *     holding the four e8m0 bytes of k-stage kb of row 32c + 8j + i of block
+ *     b (the tensor-memory image of the block-scaled MMAs, lane 8j + i,
+ *     column c): one 256-row copy and one 1 KB copy per stage.
  *   w13 [E, 2I, K] / w2 [E, K, I]: fp8 bytes, or MXFP4 bytes of two e2m1 each
  *     ([E, 2I, K/2] / [E, K, I/2]), 16-byte aligned (K = H, or latent)
  *   w13_scale [E, 2I, K/32], w2_scale [E, K, I/32] e8m0 and their packed

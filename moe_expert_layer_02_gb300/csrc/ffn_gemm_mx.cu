@@ -116,6 +116,22 @@ __device__ __forceinline__ uint64_t sf_desc(uint32_t addr) {
          ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
 }
 
+// The same for one block of a stage's scales in moe_pack_weights' order
+// ([4 j][2 blocks][8 rows][16 B]): its 8-row core matrices are 256 bytes apart.
+__device__ __forceinline__ uint64_t sf_desc_g256(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(256 >> 4) << 16) |
+         ((uint64_t)(256 >> 4) << 32) | (1ull << 46);
+}
+
+// Both blocks' scales of a stage as one 128-row x 32-byte source (the 1 KB
+// of moe_pack_weights' order once per lane quarter): 8-row core matrices 256
+// bytes apart (stride offset), the second block's 16 bytes of each row 128
+// bytes on (leading offset).
+__device__ __forceinline__ uint64_t sf_desc_pair(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) |
+         ((uint64_t)(256 >> 4) << 32) | (1ull << 46);
+}
+
 // Copy a 32-row x 128-bit block from shared memory to tensor memory columns
 // [taddr, taddr + 4) of all four lane quarters (row l -> lane l of each quarter).
 __device__ __forceinline__ void tmem_cp_32x128_x4(uint32_t taddr, uint64_t desc) {
@@ -198,7 +214,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     const int sbytes = Kel / 32;             // scale bytes per weight row
     const bool sf_pf_ok = (reinterpret_cast<uintptr_t>(scales) & 15) == 0;  // bulk prefetch alignment
     // packed (moe_pack_weights): weights [E][NB][KB][2 blocks][128 rows][64 B] and
-    // scales [E][NB][KB][2 blocks][512 B], so a stage is one 256-row box + 1 KB
+    // scales [E][NB][KB][4][2 blocks][8][16 B], so a stage is one 256-row box + 1 KB
     auto sf_packed = [&](int e, int nb, int kb) {
       return scales + (((size_t)e * NB + nb) * KB + kb) * (C::NA * MX_SF_SLOT);
     };
@@ -239,13 +255,14 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         const uint32_t fb = smem_u32(&full[stage]);
         const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT);
         if (!a.packed) {
-          // row-major scales: lane l copies rows 32c + l of each block (4 bytes each)
+          // row-major scales: lane l copies rows 32c + l of each block (4 bytes
+          // each) into moe_pack_weights' order, word (l / 8, blk, l % 8, c)
 #pragma unroll
           for (int blk = 0; blk < C::NA; ++blk) {
             const uint8_t* src = sb + (size_t)(block_row(blk, nb) + lane) * sbytes + kb * 4;
+            const uint32_t dst = sfs + (lane >> 3) * 256 + blk * 128 + (lane & 7) * 16;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              cp_async4(sfs + lane * 16 + blk * MX_SF_SLOT + c * 4, src + (size_t)(32 * c) * sbytes);
+            for (int c = 0; c < 4; ++c) cp_async4(dst + c * 4, src + (size_t)(32 * c) * sbytes);
           }
           cp_async_arrive_noinc(fb);
         }
@@ -310,7 +327,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
           const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT);
 #pragma unroll
           for (int blk = 0; blk < C::NA; ++blk)
-            tmem_cp_32x128_x4(sfa + blk * 4, sf_desc(sfs + blk * MX_SF_SLOT));
+            tmem_cp_32x128_x4(sfa + blk * 4, sf_desc_g256(sfs + blk * 128));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t idesc = idesc_mx(MX_BM, n, kk);
@@ -422,22 +439,26 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 // loads that tile's 256-row weight box and its two scale images, and runs that
 // tile's epilogue on its own tensor memory.  Weights and scales must be in
 // moe_pack_weights' order; every copy is a TMA load counted on the even CTA's
-// full barrier.  The even CTA's warp 1 copies both CTAs' scale images into
-// their tensor memory (tcgen05.cp.cta_group::2: each CTA's image from its own
-// shared memory, same offsets) and issues the pair's MMAs; its commits arrive
-// on both CTAs' barriers; both epilogues release accumulators on the even
-// CTA's barrier.  All waits are bounded as in the single-SM kernel.
+// full barrier.  Each CTA loads a stage's 1 KB of scales once per
+// tensor-memory lane quarter, and the even CTA's warp 1 copies both blocks'
+// scales of both CTAs into their tensor memory with one
+// tcgen05.cp.cta_group::2.128x256b per stage (each CTA's from its own shared
+// memory, same offsets), then issues the pair's MMAs; its commits arrive on
+// both CTAs' barriers; both epilogues release accumulators on the even CTA's
+// barrier.  All waits are bounded as in the single-SM kernel.
 //
 // What bounds it: the tensor pipe's time per instruction.  A block-scaled
 // M = 256, K = 32 MMA holds the pipe ~120 cycles whatever its N (16 and 80
 // token rows measured alike), and e2m1 weights take two such MMAs per 128-row
 // block and 128-K stage where e4m3 takes one per 16 KB of weights: eight per
 // stage, ~960 cycles, against ~860 cycles for the stage's 16 KB per SM at HBM
-// speed; each tcgen05.cp of a block's scales adds ~60 cycles in the same pipe.
-// Timing-only variants on T=4096, L=3584, I=3072, E=896 top-16, FFN1: no MMAs
-// and no scale copies 1.65 ms; copies only 1.66; MMAs only 1.89; both (this
-// kernel) 2.13; one weight block per stage (4 MMAs, 1 copy) 1.70; N = 16 2.04;
-// one copy per stage 2.01.  Changes that did not help: packed weight loads
+// speed; a tcgen05.cp adds ~60 cycles in the same pipe whatever its shape,
+// hence one 128x256b copy per stage rather than one 32x128b.warpx4 copy per
+// block (FFN1 2.13 -> 2.02 ms, FFN2 1.07 -> 1.02 ms).  Timing-only variants on
+// T=4096, L=3584, I=3072, E=896 top-16, FFN1: no MMAs and no scale copies
+// 1.65 ms; copies only 1.66; MMAs only 1.89; MMAs and two copies per stage
+// 2.13; one weight block per stage (4 MMAs, 1 copy) 1.70; N = 16 2.04; one
+// copy per stage 2.01.  Changes that did not help: packed weight loads
 // instead of unpacked ones, or an L2 prefetch 4 or 8 stages ahead (no
 // change); each stage's copies issued one stage ahead, after waiting for that
 // stage's data (2.40: the MMAs wait one load longer); the scales written by
@@ -449,9 +470,9 @@ struct MxPairCfg {
   static constexpr int BH = BN / 2;  // activation rows staged per CTA
   static constexpr int B_BYTES = BH * MX_BK;
   static constexpr int STAGE_SMEM = NA * MX_A_SMEM + B_BYTES;
-  static constexpr int STAGE_TX = NA * MX_A_TX + B_BYTES + NA * MX_SF_SLOT;  // per CTA
-  static constexpr int STAGES =
-      mx_min((MX_SMEM_BUDGET - MX_SF_SLOT) / (STAGE_SMEM + NA * MX_SF_SLOT), 8);
+  static constexpr int SF_STAGE = 4 * NA * MX_SF_SLOT;  // the stage's 1 KB once per lane quarter
+  static constexpr int STAGE_TX = NA * MX_A_TX + B_BYTES + SF_STAGE;  // per CTA
+  static constexpr int STAGES = mx_min((MX_SMEM_BUDGET - MX_SF_SLOT) / (STAGE_SMEM + SF_STAGE), 8);
   static constexpr int ACC_COLS = NA * BN;
   static constexpr int ACC_STAGES = 2;
   static constexpr int SFB_COL = ACC_STAGES * ACC_COLS;
@@ -459,7 +480,7 @@ struct MxPairCfg {
   static constexpr int TMEM_USED = SFA_COL + STAGES * NA * 4;
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_STAGES + 1;
-  static constexpr int SF_BYTES = STAGES * NA * MX_SF_SLOT + MX_SF_SLOT;
+  static constexpr int SF_BYTES = STAGES * SF_STAGE + MX_SF_SLOT;
   static constexpr int SMEM = 1024 + STAGES * STAGE_SMEM + SF_BYTES + NUM_BARS * 8 + 16 + STAGES * 4;
   static_assert(TMEM_USED <= TMEM_COLS, "tensor memory budget");
   static_assert(B_BYTES % 1024 == 0, "operand tiles keep 1024-byte alignment");
@@ -475,6 +496,12 @@ __device__ __forceinline__ void mma_mx_pair(uint32_t d, uint64_t adesc, uint64_t
       "[%5], p;\n\t}" ::"r"(d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
       : "memory");
+}
+
+// Both CTAs: a 128-row x 256-bit block from each CTA's shared memory (same
+// offset) into tensor-memory lanes 0..127, columns [taddr, taddr + 8).
+__device__ __forceinline__ void tmem_cp_128x256_pair(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
 // Both CTAs: a 32-row x 128-bit block from each CTA's shared memory (same
@@ -493,7 +520,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sf = smem + C::STAGES * C::STAGE_SMEM;  // [STAGES][NA][512 B], then the 2^0 block
+  uint8_t* sf = smem + C::STAGES * C::STAGE_SMEM;  // [STAGES][4 quarters][1 KB], then the 2^0 block
   uint64_t* bars = reinterpret_cast<uint64_t*>(sf + C::SF_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
@@ -508,7 +535,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   {
-    uint32_t* one = reinterpret_cast<uint32_t*>(sf + C::STAGES * C::NA * MX_SF_SLOT);
+    uint32_t* one = reinterpret_cast<uint32_t*>(sf + C::STAGES * C::SF_STAGE);
     for (int i = threadIdx.x; i < MX_SF_SLOT / 4; i += blockDim.x) one[i] = 0x7F7F7F7Fu;
     fence_proxy_async_smem();
   }
@@ -563,13 +590,16 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             break;
           }
           const uint32_t st = smem_u32(smem + stage * C::STAGE_SMEM);
-          const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT);
+          const uint32_t sfs = smem_u32(sf + stage * C::SF_STAGE);
           const uint32_t fb_leader = mapa_shared(smem_u32(&full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * C::STAGE_TX);
           tma_load_3d_pair(st, &tm_w, 0, C::NA * MX_BM * (nb * KB + kb), it.x, fb_leader);
           tma_load_2d_pair(st + C::NA * MX_A_SMEM, &tm_x, kb * MX_BK, it.y + (int)rank * half,
                            fb_leader);
-          tma_load_2d_pair(sfs, &tm_s, 0, ((it.x * NB + nb) * KB + kb) * C::NA, fb_leader);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)  // the stage's scales once per tensor-memory lane quarter
+            tma_load_2d_pair(sfs + q * C::NA * MX_SF_SLOT, &tm_s, 0,
+                             ((it.x * NB + nb) * KB + kb) * C::NA, fb_leader);
           s_issued[stage] = phase + 1u;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -591,7 +621,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
       bool issued_any = false;
       const uint32_t sfb = tmem + C::SFB_COL;
       {
-        const uint64_t one = sf_desc(smem_u32(sf + C::STAGES * C::NA * MX_SF_SLOT));
+        const uint64_t one = sf_desc(smem_u32(sf + C::STAGES * C::SF_STAGE));
         tmem_cp_32x128_x4_pair(sfb, one);
         tmem_cp_32x128_x4_pair(sfb + 4, one);
       }
@@ -613,10 +643,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
           const uint32_t a0 = smem_u32(smem + stage * C::STAGE_SMEM);
           const uint32_t b0 = a0 + C::NA * MX_A_SMEM;
           const uint32_t sfa = tmem + C::SFA_COL + stage * C::NA * 4;
-          const uint32_t sfs = smem_u32(sf + stage * C::NA * MX_SF_SLOT);
-#pragma unroll
-          for (int blk = 0; blk < C::NA; ++blk)
-            tmem_cp_32x128_x4_pair(sfa + blk * 4, sf_desc(sfs + blk * MX_SF_SLOT));
+          // both blocks' scales in one copy: lanes 32q + l, columns sfa .. sfa + 7
+          tmem_cp_128x256_pair(sfa, sf_desc_pair(smem_u32(sf + stage * C::SF_STAGE)));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t idesc = idesc_mx(2 * MX_BM, n, kk);

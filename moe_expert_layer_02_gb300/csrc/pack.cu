@@ -38,11 +38,15 @@ __global__ void pack_tiles_kernel(const uint32_t* __restrict__ src, uint32_t* __
 // MXFP4 stages read two 128-row weight blocks at once: W1 and W3 block p of
 // w13 (block rows p*128 and I + p*128), or W2 blocks 2p and 2p + 1 of w2.  The
 // packed order keeps each stage's two tiles adjacent,
-//   weights [G][P][KB][2][128 rows][64 bytes]   (one 256-row TMA box), and
-//   scales  [G][P][KB][2][32 lanes][4] words    (one 1 KB bulk copy),
-// where a scale word (l, c) is the four e8m0 bytes of k-stage kb of row 32c + l:
-// the 512-byte image tcgen05.cp (32x128b, replicated to the four lane
-// quarters) copies into the tensor-memory layout of block-scaled MMAs, M = 128.
+//   weights [G][P][KB][2][128 rows][64 bytes]       (one 256-row TMA box), and
+//   scales  [G][P][KB][4 j][2 blk][8 i][4 c] words  (1 KB per stage),
+// where word (j, blk, i, c) holds the four e8m0 bytes of k-stage kb of row
+// 32c + 8j + i of block blk.  Block-scaled MMAs (M = 128 per CTA) read a
+// block's scales from tensor memory as lane l = 8j + i, column c, in every
+// lane quarter; in this order one stage's 1 KB, repeated once per lane
+// quarter, is the 128-row x 32-byte source of a single tcgen05.cp.128x256b
+// (8-row groups 256 bytes apart, the second block 128 bytes along each row)
+// that fills both blocks' columns.
 // Source row of (p, blk, r): p * 128 * pstep + blk * bstep + r.
 __global__ void pack_mx_weights_kernel(const uint32_t* __restrict__ src,
                                        uint32_t* __restrict__ dst, int64_t words, int R, int KB,
@@ -66,8 +70,9 @@ __global__ void pack_mx_scales_kernel(const uint32_t* __restrict__ src, uint32_t
                                       int64_t words, int R, int KB, int pstep, int bstep) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= words) return;
-  const int c = (int)(i & 3), l = (int)((i >> 2) & 31);
-  const int blk = (int)((i >> 7) & 1);
+  const int c = (int)(i & 3), ii = (int)((i >> 2) & 7);
+  const int blk = (int)((i >> 5) & 1), j = (int)((i >> 6) & 3);
+  const int l = 8 * j + ii;
   const int64_t t = i >> 8;  // (g, p, kb)
   const int kb = (int)(t % KB);
   const int64_t gp = t / KB;

@@ -82,7 +82,7 @@ def _block_rows(key, cfg, p, b):
 
 def test_mxfp4_pack_is_a_permutation():
     # weights: packed[e, p, kb, b, r, :] == w[e, row(p, b) + r, 64kb : 64kb + 64]  (128 e2m1)
-    # scales:  packed[e, p, kb, b, l, c, :] == s[e, row(p, b) + 32c + l, 4kb : 4kb + 4]
+    # scales:  packed[e, p, kb, j, b, i, c, :] == s[e, row(p, b) + 32c + 8j + i, 4kb : 4kb + 4]
     cfg = MX_PLAIN.with_(I=512)
     inp = G.gpu_inputs(cfg)
     pk = G.pack(cfg, inp)
@@ -90,13 +90,14 @@ def test_mxfp4_pack_is_a_permutation():
         w, t = inp[key].view(cfg.E, R, C // 2), pk[key].reshape(cfg.E, R // 256, C // 128, 2, 128, 64)
         sk = key + "_scale"
         s = inp[sk].view(cfg.E, R, C // 32)
-        img = pk[sk].reshape(cfg.E, R // 256, C // 128, 2, 32, 4, 4)  # e, p, kb, b, l, c, byte
+        img = pk[sk].reshape(cfg.E, R // 256, C // 128, 4, 2, 8, 4, 4)  # e, p, kb, j, b, i, c, byte
         for p in range(R // 256):
             for b in range(2):
                 rows = _block_rows(key, cfg, p, b)
                 got_w = t[:, p, :, b].permute(0, 2, 1, 3).reshape(cfg.E, 128, C // 2)
                 assert torch.equal(got_w, w[:, rows]), (key, p, b)
-                got_s = img[:, p, :, b].permute(0, 3, 2, 1, 4).reshape(cfg.E, 128, C // 32)
+                # [e, kb, j, i, c, byte] -> rows 32c + 8j + i
+                got_s = img[:, p, :, :, b].permute(0, 4, 2, 3, 1, 5).reshape(cfg.E, 128, C // 32)
                 assert torch.equal(got_s, s[:, rows]), (sk, p, b)
 
 
