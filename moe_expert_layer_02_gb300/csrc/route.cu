@@ -327,7 +327,8 @@ __global__ void __launch_bounds__(256)
 // k=8 and 1 of 8192 on the Zipf-biased T=8192 batch; 1, 4, 16 and 64 -> none
 // on those and on T=4096, H=7168, E=896, k=16.  Eight leaves a factor of
 // eight over the smallest clean margin; the recompute then runs on a few per
-// cent of tokens (S1 + S2: 0.38 ms at T=16384 against 1.49 ms canonical).
+// cent of tokens (S1 + S2: 0.25 ms at T=16384, E=256 alone, 0.31 ms inside
+// the layer, against 1.49 ms canonical).
 #ifndef MOE_RFLAG_ULPS
 #define MOE_RFLAG_ULPS 8.0f
 #endif
@@ -422,7 +423,7 @@ __device__ __forceinline__ void canonical_logits4(const uint16_t* __restrict__ x
                                                   const float* __restrict__ w3, int H, int lane,
                                                   float (&out)[4]) {
   float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
-#pragma unroll 4
+#pragma unroll 8
   for (int h = lane; h < H; h += 32) {
     const float xv = bf16_bits_to_f32(xr[h]);
     p0 = fmaf(xv, w0[h], p0);
@@ -628,6 +629,10 @@ __global__ void __launch_bounds__(TOPK_TC_THREADS, 1)
     const int end = from ? __ffs(from) - 1 : 31;
     const unsigned redo = __ballot_sync(0xffffffffu, lane <= b && end > start);
     if (redo) {
+      // the rows the recompute streams, into L2 first: x[t] (mostly evicted
+      // since the GEMM read it) and the undecided experts' router rows
+      if (lane == 0) prefetch_l2(xr, (uint32_t)H * 2);
+      if ((redo >> lane) & 1u) prefetch_l2(wr + (size_t)my_e * H, (uint32_t)H * 4);
       uint64_t ck = 0;
       unsigned todo = redo;
       while (todo) {  // up to four canonical logits per pass over x

@@ -145,3 +145,16 @@ def test_router_topk_no_cut_within_32(orc, tuning):
     inp2["router_w"] = wr
     inp2["router_bias"] = bias
     _check(orc, cfg, inp2)
+
+
+@pytest.mark.parametrize("cfg", [
+    mi.MoEConfig("k32_e40", T=200, H=512, I=128, E=40, k=32),
+    mi.MoEConfig("k32_e1024_sig", T=96, H=512, I=128, E=1024, k=32, routing="sigmoid",
+                 sel_bias=True),
+    mi.MoEConfig("k31_e1024", T=96, H=1024, I=128, E=1024, k=31)], ids=ids)
+def test_router_topk_widest_selection(orc, cfg, tuning):
+    # k = 32 fills all 32 lanes with the first candidates, so the only cut that
+    # can be proven is after position 31, against every expert not taken out;
+    # E = 1024 runs the 32-keys-per-lane kernel
+    tuning(router_tile="tc")
+    _check(orc, cfg, G.gpu_inputs(cfg))
