@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--stage", choices=["router", "route", "router_topk", "latent_down"],
                     default=None,
                     help="time one entry point alone instead of the layer (see run_stage)")
+    ap.add_argument("--router-tile", default=None,
+                    help="router kernel choice (auto, tc or a CUDA-core tile; moe_tuning's "
+                         "router_tile); --stage router_topk defaults to tc")
     ap.add_argument("--dims", type=int, nargs="+", default=None,
                     help="with --stage: T H E (router), T E k (route), T H E k (router_topk) "
                          "or T H L (latent_down)")
@@ -657,7 +660,7 @@ def run_stage(args):
         w = torch.randn(E, H, device="cuda", generator=g) / H ** 0.5
         idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
         wt = torch.empty(T, k, device="cuda")
-        m.moe_set_tuning(router_tile="tc")
+        m.moe_set_tuning(router_tile=args.router_tile or "tc")
         p = m.make_problem(T, H, 128, E, k)
         wsb = torch.empty(m.moe_workspace_bytes(p), dtype=torch.uint8, device="cuda")
         call = lambda: m.moe_router_topk(p, x, w, None, idx, wt, wsb)  # noqa: E731

@@ -158,16 +158,17 @@ int moe_route(const moe_problem* p, const float* logits, const float* bias, int3
 /* S1 + S2 in one call: the routing moe_router_logits followed by moe_route
  * gives, bit for bit in topk_idx (Ling write-up, s.1 top-8 routing; "Kimi K3
  * ... feasibility analysis", s.2.4), computed the way moe_forward does it.
- * Large batches (at least sixteen 256 x 256 logit tiles) compute the logits on
- * the tensor cores: every fp32 router weight is split exactly into three bf16
- * pieces, x . w is one tensor-core accumulation of exact products, and a
- * token's selection is accepted only when every adjacent gap among its k + 1
- * best keys exceeds the two keys' error margins (a multiple of 2^-23 |x_t|
- * |w_e|); otherwise the canonical logits of every expert that could still
- * place are computed in moe_router_logits' order and the top k taken among
- * them.  topk_w is the softmax (or sigmoid share) of the logits the selection
- * used, within 1e-5 relative of moe_route's.  Smaller batches run
- * moe_router_logits and moe_route.
+ * The logits are computed on the tensor cores: every fp32 router weight is
+ * split exactly into three bf16 pieces and x . w is a tensor-core
+ * accumulation of exact products (for small batches over several K ranges
+ * whose sums are added), within a bound m = 8 2^-23 |x_t| |w_e| (plus the
+ * additions' rounding) of the canonical logit.  A token's order is kept
+ * wherever those bounds prove it (every lower bound up to a position above
+ * every upper bound after it); the experts between unproven positions get
+ * their canonical logits, computed in moe_router_logits' order, and are
+ * ordered by them.  topk_w is the softmax (or sigmoid share) of the logits
+ * the selection used, within 2 (m_i + max_j m_j) relative of moe_route's.
+ * moe_tuning's router_tile 1..4 selects moe_router_logits + moe_route instead.
  *   x [T, H] bf16, router_w [E, H] fp32, bias as for moe_router_logits (softmax
  *   routing) or moe_route (MOE_F_SIGMOID_ROUTING)
  *   topk_idx [T, top_k] int32, topk_w [T, top_k] fp32 (outputs)
@@ -378,10 +379,11 @@ typedef struct {
   int32_t gemm_1cta;   /* 1: single-SM fp8 grouped GEMMs for 256-row tiles as well    */
   int32_t pair_small;  /* 1 (default): SM-pair items of <= 128 rows as M = 128 tiles  */
   int32_t mx_1cta;     /* 1: single-SM MXFP4 grouped GEMMs                             */
-  int32_t router_tile; /* 0 automatic; CUDA-core router: 1: 8 warps of 8 tokens x 8
-                          experts, 2: 8 x 16, 3: 8 x 16 with four chunks a stage,
-                          4: 12 warps of 8 x 16; 6: tensor-core logits with the
-                          selection made exact (moe_router_topk), at any size    */
+  int32_t router_tile; /* 0 (default) or 6: tensor-core logits with the selection
+                          made exact (moe_router_topk); the CUDA-core router in
+                          the canonical order: 1: 8 warps of 8 tokens x 8 experts,
+                          2: 8 x 16, 3: 8 x 16 with four chunks a stage, 4: 12
+                          warps of 8 x 16                                        */
   int32_t pdl;         /* 1 (default): programmatic dependent launch between kernels */
 } moe_tuning;
 

@@ -115,6 +115,11 @@ struct PairGemm {
   int a_period;           // dense: A's K stage is kb % a_period (0: kb), so one A
                           // row block meets several consecutive K blocks of B
   int n_valid;            // EPI_F32: output columns that exist (ldo >= n_valid)
+  int ksplit;             // dense EPI_F32: K cut into this many stage ranges (0, 1:
+                          // none), range s stored as its own fp32 block at
+                          // out + s * split_stride, so a grid of few tiles still
+                          // fills the GPU; each range is non-empty
+  size_t split_stride;
   int* err;
 };
 
@@ -251,7 +256,10 @@ __global__ void __launch_bounds__(P_THREADS, 1)
   const int KB = g.kb1 + g.kb2;
   const int n_items = g.items ? min(*g.n_items, g.max_items)
                               : (g.dense_rows + 2 * P_ROWS - 1) / (2 * P_ROWS);
-  const int n_tiles = n_items * NB;
+  // dense split-K: tile t is K range t % S of output tile t / S
+  const int S = (!g.items && EPI == EPI_F32 && g.ksplit > 1) ? g.ksplit : 1;
+  const int KBs = (KB + S - 1) / S;
+  const int n_tiles = n_items * NB * S;
   const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
 
   if (warp == 0) {
@@ -266,7 +274,9 @@ __global__ void __launch_bounds__(P_THREADS, 1)
         int stop = lane == 0 ? *s_abort : 0;
         if (gat) stop = __shfl_sync(0xffffffffu, stop, 0);
         if (stop) break;
-        const int2 tc = tile_coords(g, tile, NB, n_items);
+        const int sk = tile % S;
+        const int k0 = sk * KBs, k1 = min(KB, k0 + KBs);
+        const int2 tc = tile_coords(g, tile / S, NB, n_items);
         const int item = tc.x, nb = tc.y;
         const int4 it = tile_item(g, item);
         const bool shared = g.items && it.x >= g.E;
@@ -303,7 +313,7 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           }
         }
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = k0; kb < k1; ++kb) {
           int got = 1;
           if (lane == 0) got = mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, g.err, s_abort);
           if (gat) got = __shfl_sync(0xffffffffu, got, 0);
@@ -380,14 +390,15 @@ __global__ void __launch_bounds__(P_THREADS, 1)
       const uint32_t idesc256 = pair_idesc<KIND>(), idesc128 = pair_idesc<KIND>(128);
       for (int tile = cluster; tile < n_tiles && !*s_abort; tile += n_clusters, ++it_local) {
         const uint32_t idesc =
-            is_small(g, tile_item(g, tile_coords(g, tile, NB, n_items).x)) ? idesc128 : idesc256;
+            is_small(g, tile_item(g, tile_coords(g, tile / S, NB, n_items).x)) ? idesc128 : idesc256;
+        const int k0 = (tile % S) * KBs, k1 = min(KB, k0 + KBs);
         const int acc = it_local % P_ACC_STAGES;
         const uint32_t acc_phase = (uint32_t)(it_local / P_ACC_STAGES) & 1u;
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, g.err, s_abort)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * P_N;
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = k0; kb < k1; ++kb) {
           if (!mbar_wait(smem_u32(&full[stage]), phase, g.err, s_abort)) {
             ok = false;
             break;
@@ -398,7 +409,8 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < P_BK / P_UMMA_B; ++kk)
             pair_mma<KIND>(d, smem_desc_sw128(a0 + kk * P_UMMA_B),
-                           smem_desc_sw128(b0 + kk * P_UMMA_B), idesc, (kb | kk) ? 1u : 0u);
+                           smem_desc_sw128(b0 + kk * P_UMMA_B), idesc,
+                           ((kb - k0) | kk) ? 1u : 0u);
           issued_any = true;
           mma_commit_pair(smem_u32(&empty[stage]), 0x3);
           if (++stage == P_STAGES) {
@@ -424,10 +436,11 @@ __global__ void __launch_bounds__(P_THREADS, 1)
     int grp = 0;  // groups stored by this warp (transpose buffer = grp & 1)
     int it_local = 0;
     for (int tile = cluster; tile < n_tiles; tile += n_clusters, ++it_local) {
-      const int2 tc = tile_coords(g, tile, NB, n_items);
+      const int2 tc = tile_coords(g, tile / S, NB, n_items);
       const int item = tc.x, nb = tc.y;
       const int4 it = tile_item(g, item);
       const bool shared = g.items && it.x >= g.E;
+      const size_t part = (size_t)(tile % S) * g.split_stride;  // split-K: this range's block
       const int acc = it_local % P_ACC_STAGES;
       const uint32_t acc_phase = (uint32_t)(it_local / P_ACC_STAGES) & 1u;
       // this tile's channel scales: two per thread, read before the wait
@@ -483,6 +496,31 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           if (wr0 + rr < it.z && (unsigned)orow_i < (unsigned)g.rows_total)
             *reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.out) + (size_t)orow_i * g.ldo +
                                       col + 8 * ch) = v;
+        }
+      };
+      // fp32 output (EPI_F32): 16 columns of the warp's 32 rows at output
+      // column `col` through the same staging buffer, 16-byte stores of four
+      // columns (row stride and valid columns multiples of four)
+      auto put32 = [&](const uint32_t (&vals)[16], int col) {
+        const uint32_t buf = stg_w + (uint32_t)(grp & 1) * P_STG_BUF;
+        ++grp;
+        const uint32_t ra = buf + lane * P_STG_ROW;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          st_shared_v4(ra + (((uint32_t)i ^ swz) << 4), vals[4 * i], vals[4 * i + 1],
+                       vals[4 * i + 2], vals[4 * i + 3]);
+        __syncwarp();
+        const int ch = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 8 * i + (lane >> 2);
+          const uint4 v = ld_shared_v4(buf + rr * P_STG_ROW +
+                                       (((uint32_t)ch ^ ((uint32_t)(rr >> 1) & 3u)) << 4));
+          const int orow_i = it.y + wr0 + rr;
+          const int colx = col + 4 * ch;
+          if (wr0 + rr < it.z && (unsigned)orow_i < (unsigned)g.rows_total && colx < g.n_valid)
+            *reinterpret_cast<uint4*>(static_cast<float*>(g.out) + part + (size_t)orow_i * g.ldo +
+                                      colx) = v;
         }
       };
       // Columns in groups of 32 (two tcgen05.ld x16 per operand), software
@@ -561,35 +599,40 @@ __global__ void __launch_bounds__(P_THREADS, 1)
           tmem_ld16(tbase + c + 16, v[1]);
         };
         auto emit = [&](const uint32_t (&v)[2][16], int c) {
-          if (EPI == EPI_F32) {  // fp32 out, row by row (a small output)
-            if (valid) {
-              float* orow = static_cast<float*>(g.out) + (size_t)row * g.ldo;
+          if constexpr (EPI == EPI_F32) {
+            if (g.ldo % 4 == 0 && g.n_valid % 4 == 0) {
+              put32(v[0], c0 + co + c);
+              put32(v[1], c0 + co + c + 16);
+              return;
+            }
+            if (valid) {  // fp32 out, row by row
+              float* orow = static_cast<float*>(g.out) + part + (size_t)row * g.ldo;
 #pragma unroll
               for (int jj = 0; jj < 32; ++jj) {
                 const int col = c0 + co + c + jj;
                 if (col < g.n_valid) orow[col] = __uint_as_float(v[jj >> 4][jj & 15]);
               }
             }
-            return;
-          }
-          uint32_t packed[16];
+          } else {
+            uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            float4 s4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-            if (EPI == EPI_DOWN) s4 = *reinterpret_cast<const float4*>(scl + co + c + j);
-            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-            float yv[4];
+            for (int j = 0; j < 32; j += 4) {
+              float4 s4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+              if (EPI == EPI_DOWN) s4 = *reinterpret_cast<const float4*>(scl + co + c + j);
+              const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+              float yv[4];
 #pragma unroll
-            for (int u2 = 0; u2 < 4; ++u2) {
-              const int jj = j + u2;
-              float y0 = __uint_as_float(v[jj >> 4][jj & 15]);
-              if (EPI == EPI_DOWN) y0 = ((y0 * hs) * sv[u2]) * rw;
-              yv[u2] = y0;
+              for (int u2 = 0; u2 < 4; ++u2) {
+                const int jj = j + u2;
+                float y0 = __uint_as_float(v[jj >> 4][jj & 15]);
+                if (EPI == EPI_DOWN) y0 = ((y0 * hs) * sv[u2]) * rw;
+                yv[u2] = y0;
+              }
+              packed[j / 2] = pack_bf16x2(yv[0], yv[1]);
+              packed[j / 2 + 1] = pack_bf16x2(yv[2], yv[3]);
             }
-            packed[j / 2] = pack_bf16x2(yv[0], yv[1]);
-            packed[j / 2 + 1] = pack_bf16x2(yv[2], yv[3]);
+            put(packed, c0 + co + c);
           }
-          put(packed, c0 + co + c);
         };
         load(va, 0);
         tmem_ld_wait();
@@ -762,10 +805,29 @@ cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s) {
   return launch_pair_gemm<KIND_BF16, EPI_STORE>(tw, tw, tx, tw2, tx2, tx, tw, tw, g, s);
 }
 
+int dense_split_k(int rows, int N, int Kw) {
+  // enough K ranges for every SM pair to take one when the output has few
+  // tiles, each range at least eight stages of 64 K; none for larger outputs
+  const long tiles = (long)((rows + 255) / 256) * ((N + P_N - 1) / P_N);
+  const long pairs = device_sm_count() / 2;
+  const int KB = Kw / 64;
+  if (tiles <= 0 || tiles * 2 > pairs || KB < 16) return 1;  // (an empty batch: none)
+  int S = (int)(pairs / tiles);
+  S = S < KB / 8 ? S : KB / 8;
+  const int KBs = (KB + S - 1) / S;
+  return (KB + KBs - 1) / KBs;  // every range non-empty
+}
+
 cudaError_t launch_dense_bf16_f32(const void* x, int Kx, const void* w, int Kw, int rows, int N,
-                                  float* out, int* err, cudaStream_t s) {
-  // out[rows, N] fp32 = sum over Kw of x[:, k mod Kx] w[:, k]; Kx, Kw multiples of 64
-  if (Kx % 64 || Kw % Kx || N <= 0 || rows <= 0) return cudaErrorInvalidValue;
+                                  float* out, int ksplit, int* err, cudaStream_t s) {
+  // out[rows, N] fp32 = sum over Kw of x[:, k mod Kx] w[:, k]; Kx, Kw multiples of 64;
+  // with ksplit > 1 (dense_split_k's value), ksplit partial blocks [rows, N]
+  // back to back whose sum is out
+  if (Kx % 64 || Kw % Kx || N <= 0 || rows <= 0 || ksplit < 1) return cudaErrorInvalidValue;
+  if (ksplit > 1) {
+    const int KB = Kw / 64, KBs = (KB + ksplit - 1) / ksplit;
+    if ((ksplit - 1) * KBs >= KB) return cudaErrorInvalidValue;  // an empty range
+  }
   CUtensorMap tw, tx;
   if (!pair_map(&tw, KIND_BF16, 3, w, Kw, N, 1) || !pair_map(&tx, KIND_BF16, 2, x, Kx, rows, 1))
     return cudaErrorInvalidValue;
@@ -780,6 +842,8 @@ cudaError_t launch_dense_bf16_f32(const void* x, int Kx, const void* w, int Kw, 
   g.out = out;
   g.ldo = N;
   g.n_valid = N;
+  g.ksplit = ksplit;
+  g.split_stride = (size_t)rows * N;
   g.err = err;
   return launch_pair_gemm<KIND_BF16, EPI_F32>(tw, tw, tx, tw, tx, tx, tw, tw, g, s);
 }

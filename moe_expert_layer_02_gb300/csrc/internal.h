@@ -85,12 +85,17 @@ cudaError_t launch_topk(const float* logits, const float* sel_bias, int sigmoid,
 // followed by launch_topk (recomputing canonical logits where the approximate
 // ones leave the order in doubt).  logit_bias: softmax routing's bias (added to
 // the logits); sel_bias: sigmoid routing's selection bias.
+// approx: `splits` blocks [T, E] fp32 (splits = dense_split_k(T, E, 3 H));
+// with splits > 1 launch_router_tc leaves their sum in the first block and a
+// bound on the running sums' magnitudes in the second, which launch_topk_tc
+// reads
 cudaError_t launch_router_tc(const void* x, const float* wr, int T, int H, int E, uint16_t* wp,
-                             float* xnorm, float* wnorm, float* approx, int* err, cudaStream_t s);
-cudaError_t launch_topk_tc(const float* approx, const float* logit_bias, const float* sel_bias,
-                           int sigmoid, const void* x, const float* wr, const float* xnorm,
-                           const float* wnorm, int32_t* idx, float* w, int T, int H, int E, int k,
-                           cudaStream_t s);
+                             float* xnorm, float* wnorm, float* approx, int splits, int* err,
+                             cudaStream_t s);
+cudaError_t launch_topk_tc(const float* approx, int splits, const float* logit_bias,
+                           const float* sel_bias, int sigmoid, const void* x, const float* wr,
+                           const float* xnorm, const float* wnorm, int32_t* idx, float* w, int T,
+                           int H, int E, int k, cudaStream_t s);
 
 // ---------------------------------------------------------------- permute.cu
 // cc[e * nch + c] = #tokens of chunk c that picked expert e.
@@ -205,8 +210,11 @@ struct DenseGemmArgs {
 cudaError_t launch_dense_bf16(const DenseGemmArgs& d, cudaStream_t s);
 // out[rows, N] fp32 = sum_{k < Kw} x[:, k mod Kx] * w[:, k] (x [rows, Kx], w [N, Kw]
 // bf16, Kx % 64 == 0, Kw a multiple of Kx): one accumulation in tensor memory.
+// K ranges for the dense fp32-output GEMM (1 = none): enough for every SM pair
+// when its output has few 256 x 256 tiles, each range non-empty.
+int dense_split_k(int rows, int N, int Kw);
 cudaError_t launch_dense_bf16_f32(const void* x, int Kx, const void* w, int Kw, int rows, int N,
-                                  float* out, int* err, cudaStream_t s);
+                                  float* out, int ksplit, int* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- latent_down.cu
 // z [T, L] = nearest-even bf16 of the exact x Wd^T (x [T, H], Wd [L, H] bf16):

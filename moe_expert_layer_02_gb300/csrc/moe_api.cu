@@ -111,6 +111,7 @@ struct Plan {
   bool fused;       // S7 in the FFN2 epilogue (MOE_F_FUSED_COMBINE, where honoured)
   bool gather;      // S4 quantises per token; the FFN1 producer gathers the rows
   bool tc_router;   // S1 on the tensor cores, S2 made exact (route.cu)
+  int rsplit;       // K ranges of the tensor-core router GEMM (logits blocks)
   size_t acc;       // fused combine: fp32 [T, H] sum
   size_t logits, idx, tw, cc, cbase, ticket, cnt, off, perm, src, row_w, xscale, items, n_items, xq, h,
       hq, hs, y, z, zflag, yn, hsh, rwp, rxn, rwn, total;
@@ -143,15 +144,15 @@ int choose_bn(const moe_problem* p) {
 
 bool use_pair_gemm(const Plan& q);
 
-// S1 on the tensor cores when the batch fills at least sixteen SM pairs with
-// 256 x 256 logit tiles (the canonical CUDA-core router below that: at T=512,
-// E=256 its 60 us beat two busy pairs); tuning().router_tile 6 forces it, 1..5
-// pick a CUDA-core tile.
+// S1 on the tensor cores with S2 made exact unless tuning().router_tile picks
+// a CUDA-core tile (1..4).  With small batches split into K ranges, the
+// tensor-core path is the faster at every size measured (S1 + S2 on GB300,
+// E=256, H=8192: T=1 22 vs 41 us, T=512 35 vs 61, T=2048 55 vs 237; E=896,
+// H=7168, k=16: T=1 31 vs 44, T=512 58 vs 220).
 bool use_tc_router(const moe_problem* p) {
   const int rt = tuning().router_tile;
-  if (rt == 6) return true;
-  if (rt != 0) return false;
-  return (int64_t)((p->T + 255) / 256) * ((p->E + 255) / 256) >= 16;
+  (void)p;
+  return rt == 0 || rt == 6;
 }
 
 Plan make_plan(const moe_problem* p) {
@@ -189,6 +190,7 @@ Plan make_plan(const moe_problem* p) {
   // 0.099 vs 0.225 ms; T=8192 skewed: FFN1 5.63 vs 1.55 ms.
   q.gather = !q.mx && !q.blockwise && tuning().ffn1_gather;
   q.tc_router = use_tc_router(p);
+  q.rsplit = q.H % 64 == 0 ? dense_split_k(q.T, q.E, 3 * q.H) : 1;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -196,7 +198,7 @@ Plan make_plan(const moe_problem* p) {
     return at;
   };
   const size_t T = q.T, E = q.E, k = q.k, R = q.R, RT = q.RT;
-  q.logits = take(T * E * 4);
+  q.logits = take(T * E * 4 * (size_t)q.rsplit);  // the router GEMM's K ranges, when split
   q.idx = take(T * k * 4);
   q.tw = take(T * k * 4);
   q.cc = take(E * q.nch * 4);
@@ -380,12 +382,13 @@ int route_tokens(const moe_problem* p, const Plan& q, void* ws, const void* x,
     {
       StageTimer t(MOE_STAGE_ROUTER, s);
       MOE_TRY(launch_router_tc(x, router_w, q.T, q.H, q.E, at<uint16_t>(ws, q.rwp),
-                               at<float>(ws, q.rxn), at<float>(ws, q.rwn), logits, err, s));
+                               at<float>(ws, q.rxn), at<float>(ws, q.rwn), logits, q.rsplit, err,
+                               s));
     }
     StageTimer t(MOE_STAGE_TOPK, s);
-    MOE_TRY(launch_topk_tc(logits, logit_bias(p, router_bias), selection_bias(p, router_bias), sig,
-                           x, router_w, at<float>(ws, q.rxn), at<float>(ws, q.rwn), idx, tw, q.T,
-                           q.H, q.E, q.k, s));
+    MOE_TRY(launch_topk_tc(logits, q.rsplit, logit_bias(p, router_bias),
+                           selection_bias(p, router_bias), sig, x, router_w, at<float>(ws, q.rxn),
+                           at<float>(ws, q.rwn), idx, tw, q.T, q.H, q.E, q.k, s));
     return MOE_OK;
   }
   {
@@ -498,14 +501,20 @@ int moe_describe(const moe_problem* p, char* buf, size_t len) {
     if (q.mx) return mx_pair_eligible(mxa, ffn1) ? "grouped_mx_pair_kernel" : "grouped_mx_kernel";
     return pair ? "pair_gemm_kernel" : "grouped_ffn_kernel";
   };
+  char router[48];
+  if (q.tc_router)
+    std::snprintf(router, sizeof router, "tensor-cores,k_ranges=%d", q.rsplit);
+  else
+    std::snprintf(router, sizeof router, "cuda-cores");
   const int n = std::snprintf(
       buf, len,
       "ffn1=%s<FFN1,BN=%d> ffn2=%s<FFN2,BN=%d> tile_rows=%d ffn1_rows=%s weights=%s%s%s "
-      "combine=%s max_items=%d workspace=%zu",
-      gemm(true), q.BN, gemm(false), q.BN, q.BN, q.gather ? "gathered" : "permuted", q.mx ? "mxfp4" : q.blockwise ? "fp8-block128" : "fp8",
-      q.packed ? ",packed" : "", q.L > 0 ? " latent=bf16-pair-gemms" : "",
-      q.fused ? "fused-ffn2-fp32-sum" : q.L > 0 ? "gather-rmsnorm" : "gather", q.max_items,
-      q.total);
+      "combine=%s router=%s max_items=%d workspace=%zu",
+      gemm(true), q.BN, gemm(false), q.BN, q.BN, q.gather ? "gathered" : "permuted",
+      q.mx ? "mxfp4" : q.blockwise ? "fp8-block128" : "fp8", q.packed ? ",packed" : "",
+      q.L > 0 ? " latent=bf16-pair-gemms" : "",
+      q.fused ? "fused-ffn2-fp32-sum" : q.L > 0 ? "gather-rmsnorm" : "gather", router,
+      q.max_items, q.total);
   return (n < 0 || (size_t)n >= len) ? MOE_ERR_INVALID_ARG : MOE_OK;
 }
 

@@ -444,6 +444,25 @@ __device__ __forceinline__ void canonical_logits4(const uint16_t* __restrict__ x
   out[3] = __shfl_sync(0xffffffffu, p3, 0);
 }
 
+// Split-K router GEMM: blocks 0..splits-1 of n logits each -> block 0 = their
+// sum (block order), block 1 = the sum of their magnitudes (rounded up), one
+// thread per logit.
+__global__ void __launch_bounds__(256)
+    router_sum_splits_kernel(float* __restrict__ p, size_t n, int splits) {
+  pdl_wait();
+  pdl_release();
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float l = p[i], a = fabsf(l);
+  for (int sp = 1; sp < splits; ++sp) {
+    const float v = p[(size_t)sp * n + i];
+    l = __fadd_rn(l, v);
+    a = __fadd_ru(a, fabsf(v));
+  }
+  p[i] = l;
+  p[n + i] = a;
+}
+
 // Blocks of four warps, one token per warp: a warp that recomputes canonical
 // logits holds back only three others.
 constexpr int TOPK_TC_THREADS = 128;
@@ -473,7 +492,8 @@ __device__ __forceinline__ float key_value(uint64_t key) {
 
 template <int VPL>
 __global__ void __launch_bounds__(TOPK_TC_THREADS, 1)
-    topk_tc_kernel(const float* __restrict__ approx, const float* __restrict__ logit_bias,
+    topk_tc_kernel(const float* __restrict__ approx, int splits, size_t split_stride,
+                   const float* __restrict__ logit_bias,
                    const float* __restrict__ sel_bias, int sigmoid,
                    const uint16_t* __restrict__ x, const float* __restrict__ wr,
                    const float* __restrict__ xnorm, const float* __restrict__ wnorm,
@@ -485,7 +505,13 @@ __global__ void __launch_bounds__(TOPK_TC_THREADS, 1)
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* row = approx + (size_t)t * E;
+  // split-K logits (router_sum_splits_kernel): block 0 holds the sum of the
+  // blocks, block 1 the sum of their magnitudes, which bounds every running
+  // sum, so the splits - 1 additions add at most (splits - 1) 2^-24 of it to
+  // a logit's error
+  const float* row_a = row + split_stride;
   const float xm = MOE_RFLAG_ULPS * 0x1p-23f * xnorm[t];
+  const float am = (float)(splits - 1) * 0x1p-24f;
   // key of expert e (as the canonical top-k forms it) from its approximate
   // logit l; its margin follows from the key's value and |w_e|
   auto logit_of = [&](int e) {
@@ -502,7 +528,7 @@ __global__ void __launch_bounds__(TOPK_TC_THREADS, 1)
     return v;
   };
   auto margin_of = [&](int e, float v) {
-    const float ml = xm * wnorm[e];
+    const float ml = xm * wnorm[e] + (splits > 1 ? am * row_a[e] : 0.0f);
     // sigmoid' <= 1/4, plus its own last-bit error; either way the bias
     // addition's rounding (two units of the key's last place)
     return (sigmoid ? 0.25f * ml + 0x1p-20f : ml) + 0x1p-22f * fabsf(v);
@@ -814,7 +840,8 @@ cudaError_t launch_router_logits(const void* x, const float* wr, const float* bi
 }
 
 cudaError_t launch_router_tc(const void* x, const float* wr, int T, int H, int E, uint16_t* wp,
-                             float* xnorm, float* wnorm, float* approx, int* err, cudaStream_t s) {
+                             float* xnorm, float* wnorm, float* approx, int splits, int* err,
+                             cudaStream_t s) {
   if (T <= 0 || H % 64 || E <= 0 || E > 1024) return cudaErrorInvalidValue;
   if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(wr) % 16 ||
       reinterpret_cast<uintptr_t>(wp) % 16)
@@ -823,17 +850,24 @@ cudaError_t launch_router_tc(const void* x, const float* wr, int T, int H, int E
   cudaError_t e = launch_kernel(router_prep_kernel, dim3(E + (T + 7) / 8), dim3(256), 0, s, 1,
                                 static_cast<const uint16_t*>(x), wr, wp, xnorm, wnorm, T, H, E);
   if (e != cudaSuccess) return e;
-  count_launch();
-  e = launch_dense_bf16_f32(x, H, wp, 3 * H, T, E, approx, err, s);
+  e = launch_dense_bf16_f32(x, H, wp, 3 * H, T, E, approx, splits, err, s);  // counts itself
   if (e != cudaSuccess) return e;
+  if (splits > 1) {
+    const size_t n = (size_t)T * E;
+    count_launch();
+    e = launch_kernel(router_sum_splits_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                      1, approx, n, splits);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk_tc(const float* approx, const float* logit_bias, const float* sel_bias,
-                           int sigmoid, const void* x, const float* wr, const float* xnorm,
-                           const float* wnorm, int32_t* idx, float* w, int T, int H, int E, int k,
-                           cudaStream_t s) {
-  if (T <= 0 || E <= 0 || E > 1024 || k > 32 || k > E) return cudaErrorInvalidValue;
+cudaError_t launch_topk_tc(const float* approx, int splits, const float* logit_bias,
+                           const float* sel_bias, int sigmoid, const void* x, const float* wr,
+                           const float* xnorm, const float* wnorm, int32_t* idx, float* w, int T,
+                           int H, int E, int k, cudaStream_t s) {
+  if (T <= 0 || E <= 0 || E > 1024 || k > 32 || k > E || splits < 1) return cudaErrorInvalidValue;
+  const size_t stride = (size_t)T * E;
   const long blocks = ((long)T * 32 + TOPK_TC_THREADS - 1) / TOPK_TC_THREADS;
   if (blocks > 0x7FFFFFFFL) return cudaErrorInvalidValue;
   const int vpl = (E + 31) / 32;
@@ -842,8 +876,8 @@ cudaError_t launch_topk_tc(const float* approx, const float* logit_bias, const f
   cudaError_t e;
 #define MOE_TOPK_TC(V)                                                                      \
   launch_kernel(topk_tc_kernel<V>, dim3((unsigned)blocks), dim3(TOPK_TC_THREADS), 0, s, 1, \
-                approx, logit_bias,                                                         \
-                sel_bias, sigmoid, xb, wr, xnorm, wnorm, idx, w, T, H, E, k)
+                approx, splits, stride, logit_bias, sel_bias, sigmoid, xb, wr, xnorm, wnorm, idx,  \
+                w, T, H, E, k)
   if (vpl <= 1) e = MOE_TOPK_TC(1);
   else if (vpl <= 2) e = MOE_TOPK_TC(2);
   else if (vpl <= 4) e = MOE_TOPK_TC(4);

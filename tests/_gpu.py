@@ -11,6 +11,8 @@ from __future__ import annotations
 
 import functools
 
+import re
+
 import numpy as np
 import torch
 
@@ -68,6 +70,14 @@ def host(inp: dict, keys=None) -> dict:
             _host_cache[ck] = (v, a)
         out[k] = a
     return out
+
+
+def routing_launches(p) -> int:
+    """Kernel launches of S1 + S2 for problem p, from the plan moe_describe
+    reports: on the tensor cores prep, GEMM, the sum of its K ranges when there
+    are several, top-k; on the CUDA cores router and top-k."""
+    mt = re.search(r"router=tensor-cores,k_ranges=(\d+)", lib().moe_describe(p))
+    return 2 if mt is None else 3 + (int(mt[1]) > 1)
 
 
 def pack(cfg: mi.MoEConfig, inp: dict) -> dict:

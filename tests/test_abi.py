@@ -126,6 +126,15 @@ def test_describe_names_the_kernels(m):
     assert lib.moe_describe(ctypes.byref(m.make_problem(4, 100, 128, 8, 2)), buf, 8) == 1
 
 
+def test_describe_names_the_router(m, tuning):
+    # the tensor-core router with its exact selection by default, at every
+    # size; a CUDA-core tile when one is chosen
+    for T in (1, 512, 16384):
+        assert "router=tensor-cores" in m.moe_describe(m.make_problem(T, 8192, 2048, 256, 8))
+    tuning(router_tile="8x16")
+    assert "router=cuda-cores" in m.moe_describe(m.make_problem(512, 8192, 2048, 256, 8))
+
+
 def test_fused_combine_plan(m):
     # honoured on the single-SM fp8 GEMMs: the fp32 sum [T, H] replaces the
     # bf16 y rows [T*k + T, H] in the workspace; ignored on the SM-pair GEMMs

@@ -37,9 +37,24 @@ def _oracle_routing(orc, cfg, h):
     return orc.topk(lg, cfg.k) + (lg,)
 
 
+def _router_splits(cfg):
+    """K ranges of the tensor-core router GEMM: enough for every SM pair when
+    its output has few 256 x 256 tiles, at least 8 stages of 64 each."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    tiles = -(-cfg.T // 256) * -(-cfg.E // 256)
+    kb = 3 * cfg.H // 64
+    if tiles * 2 > pairs or kb < 16:
+        return 1
+    s = min(pairs // tiles, kb // 8)
+    kbs = -(-kb // s)
+    return -(-kb // kbs)
+
+
 def _weight_rtol(cfg, h, idx, lg):
     """Per-token, per-slot bound on the relative error of the routing weights
-    when each chosen logit l_j is off by at most m_j = ULPS 2^-23 |x_t| |w_j|.
+    when each chosen logit l_j is off by at most m_j = ULPS 2^-23 |x_t| |w_j|
+    (plus (S - 1) 2^-24 |x_t| |w_j| when the GEMM's K runs in S ranges whose
+    sums are added: each running sum is at most |x_t| |w_j|).
     Softmax over the chosen logits: dw_i / w_i <= m_i + max_j m_j.  Sigmoid
     scores s_j, renormalised: ds_j <= m_j / 4 + 2^-20 (the sigmoid's slope is
     at most 1/4, plus its own rounding), so dw_i / w_i <= ds_i / s_i +
@@ -49,7 +64,7 @@ def _weight_rtol(cfg, h, idx, lg):
     xn = np.sqrt((x * x).sum(axis=1))
     wr = np.asarray(h["router_w"], np.float64)
     wn = np.sqrt((wr * wr).sum(axis=1))
-    m = ULPS * 2.0 ** -23 * xn[:, None] * wn[idx]
+    m = (ULPS * 2.0 ** -23 + (_router_splits(cfg) - 1) * 2.0 ** -24) * xn[:, None] * wn[idx]
     if cfg.routing == "sigmoid":
         s = 1.0 / (1.0 + np.exp(-np.take_along_axis(lg.astype(np.float64), idx, axis=1)))
         rel = (m / 4 + 2.0 ** -20) / s
