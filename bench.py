@@ -163,8 +163,9 @@ def kernel_traffic(kernel: str, cfg_name: str):
 
 
 def source_sha() -> str:
-    """Hash of the expert-GEMM sources the traffic figure depends on: code only
-    (comments and whitespace do not change the kernel)."""
+    """Hash of the expert-GEMM sources the traffic figure depends on: the
+    single-SM grouped GEMM, the device helpers and the argument struct it
+    reads, code only (comments and whitespace do not change the kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_layer_02_gb300", "csrc")
     for n in ("ffn_gemm.cu", "device.cuh", "internal.h"):
@@ -172,6 +173,9 @@ def source_sha() -> str:
             code = f.read()
         code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
         code = re.sub(r"//[^\n]*", " ", code)
+        if n == "internal.h":  # only the kernel's argument struct
+            m = re.search(r"struct GroupedFfnArgs \{.*?\};", code, flags=re.S)
+            code = m.group(0) if m else code
         h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
