@@ -116,15 +116,18 @@ enum {
 const char* moe_status_string(int status);
 
 /* Host-only: a one-line description of how moe_forward runs problem `p` (the
- * grouped-GEMM kernels, token-tile rows, weight format, workspace bytes),
+ * grouped-GEMM kernels, token-tile rows, weight format, router, workspace
+ * bytes),
  * written NUL-terminated into buf[len].  MOE_ERR_INVALID_ARG if `p` is invalid
  * or buf too short, MOE_ERR_UNSUPPORTED for a combination this build does not
  * run.  For logs and benchmarks; the text format may change. */
 int moe_describe(const moe_problem* p, char* buf, size_t len);
 
 /* Bytes of device workspace that moe_forward, moe_permute, moe_expert_ffn,
- * moe_router_topk and moe_latent_down
- * need for problem `p` (0 if `p` is invalid).  Pure host computation. */
+ * moe_router_topk and moe_latent_down need for problem `p` (0 if `p` is
+ * invalid).  Host computation; it reads the current device's SM count (small
+ * batches split the router GEMM into more K ranges on more SMs), so size the
+ * workspace on the device that will run the calls. */
 size_t moe_workspace_bytes(const moe_problem* p);
 
 /* S1 -- router logits.  logits[t,e] = sum_h float(x[t,h]) * router_w[e,h]
