@@ -824,6 +824,7 @@ cudaError_t launch_dense_bf16_f32(const void* x, int Kx, const void* w, int Kw, 
   // with ksplit > 1 (dense_split_k's value), ksplit partial blocks [rows, N]
   // back to back whose sum is out
   if (Kx % 64 || Kw % Kx || N <= 0 || rows <= 0 || ksplit < 1) return cudaErrorInvalidValue;
+  if (reinterpret_cast<uintptr_t>(out) % 16) return cudaErrorInvalidValue;  // 16-byte stores
   if (ksplit > 1) {
     const int KB = Kw / 64, KBs = (KB + ksplit - 1) / ksplit;
     if ((ksplit - 1) * KBs >= KB) return cudaErrorInvalidValue;  // an empty range
