@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, top_k > E, misaligned pointer */
-  MOE_ERR_UNSUPPORTED = 2, /* valid problem this build does not implement        */
+  MOE_ERR_UNSUPPORTED = 2, /* valid problem this library does not implement      */
   MOE_ERR_WORKSPACE = 3,   /* ws NULL or ws_bytes < moe_workspace_bytes           */
   MOE_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed         */
   MOE_ERR_TIMEOUT = 5      /* a device-side pipeline wait exceeded its limit      */
@@ -119,7 +119,7 @@ const char* moe_status_string(int status);
  * grouped-GEMM kernels, token-tile rows, weight format, router, workspace
  * bytes),
  * written NUL-terminated into buf[len].  MOE_ERR_INVALID_ARG if `p` is invalid
- * or buf too short, MOE_ERR_UNSUPPORTED for a combination this build does not
+ * or buf too short, MOE_ERR_UNSUPPORTED for a combination this library does not
  * run.  For logs and benchmarks; the text format may change. */
 int moe_describe(const moe_problem* p, char* buf, size_t len);
 
@@ -330,7 +330,7 @@ int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
  * and repeats bit for bit.  The flag is a request: it is honoured for fp8
  * per-channel experts on the single-SM grouped GEMMs without latent (moe_describe
  * names the combine that runs) and ignored elsewhere.
- * Combinations this build runs (others return MOE_ERR_UNSUPPORTED): without
+ * Combinations this library runs (others return MOE_ERR_UNSUPPORTED): without
  * latent, an fp8 shared expert with I_shared = I or none; with latent, a bf16
  * shared expert or none and H, L multiples of 256; MXFP4 experts with K (H or
  * L) a multiple of 256 and no fp8 shared expert. */

@@ -258,7 +258,7 @@ int check_problem(const moe_problem* p) {
 
 namespace {
 
-// Shapes this build runs on the GPU: fp8 experts with an optional fp8 shared
+// Shapes this library runs on the GPU: fp8 experts with an optional fp8 shared
 // expert (I_shared == I, fused into the grouped GEMMs), or the LatentMoE block
 // (latent > 0, optional bf16 shared expert) with fp8 or MXFP4 experts, or
 // MXFP4 experts on their own; block-wise fp8 wherever fp8 runs, with K and I at
