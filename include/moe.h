@@ -158,23 +158,24 @@ int moe_router_logits(const moe_problem* p, const void* x, const float* router_w
 int moe_route(const moe_problem* p, const float* logits, const float* bias, int32_t* topk_idx,
               float* topk_w, void* stream);
 
-/* S1 + S2 in one call: the routing moe_router_logits followed by moe_route
- * gives, bit for bit in topk_idx (Ling write-up, s.1 top-8 routing; "Kimi K3
- * ... feasibility analysis", s.2.4), computed the way moe_forward does it.
- * The logits are computed on the tensor cores: every fp32 router weight is
- * split exactly into three bf16 pieces and x . w is a tensor-core
- * accumulation of exact products (for small batches over several K ranges
- * whose sums are added), taken to lie within m = 8 2^-23 |x_t| |w_e| (plus
- * the additions' rounding) of the canonical logit.  A token's order is kept
- * wherever those margins separate the keys (every lower bound up to a
- * position above every upper bound after it); the experts between
- * undecided positions get their canonical logits, computed in
- * moe_router_logits' order, and are ordered by them.  The margin is a
- * calibrated bound (measured errors ~40 times smaller on normally distributed
- * inputs), not a worst-case one: inputs built so that large partial sums
- * cancel could exceed it.  moe_router_logits + moe_route, or moe_tuning's
- * router_tile 1..4, give the canonical routing for any input.  topk_w is the softmax (or sigmoid share) of the logits
- * the selection used, within 2 (m_i + max_j m_j) relative of moe_route's.
+/* S1 + S2 in one call, as moe_forward runs them: the routing that
+ * moe_router_logits followed by moe_route gives (Ling write-up, s.1 top-8
+ * routing; "Kimi K3 ... feasibility analysis", s.2.4), bit for bit in
+ * topk_idx wherever the margins below hold.  The logits are computed on the
+ * tensor cores: every fp32 router weight is split exactly into three bf16
+ * pieces and x . w is a tensor-core accumulation of exact products (for
+ * small batches over several K ranges whose sums are added), taken to lie
+ * within m = 8 2^-23 |x_t| |w_e| (plus the additions' rounding) of the
+ * canonical logit.  A token's order is kept wherever those margins separate
+ * the keys (every lower bound up to a position above every upper bound after
+ * it); the experts between undecided positions get their canonical logits,
+ * computed in moe_router_logits' order, and are ordered by them.  The margin
+ * is a calibrated bound (measured errors ~40 times smaller on normally
+ * distributed inputs), not a worst-case one: inputs built so that large
+ * partial sums cancel could exceed it.  moe_router_logits + moe_route, or
+ * moe_tuning's router_tile 1..4, give the canonical routing for any input.
+ * topk_w is the softmax (or sigmoid share) of the logits the selection used,
+ * within 2 (m_i + max_j m_j) relative of moe_route's.
  *   x [T, H] bf16, router_w [E, H] fp32, bias as for moe_router_logits (softmax
  *   routing) or moe_route (MOE_F_SIGMOID_ROUTING)
  *   topk_idx [T, top_k] int32, topk_w [T, top_k] fp32 (outputs)
