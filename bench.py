@@ -620,9 +620,16 @@ def run_ours(args, cfg):
     if extra:
         line["workloads"] = {}
         for name in extra:
-            Wx = load_workload(m, mi.CONFIGS[name], dev, pack, base=W)
-            line["workloads"][name] = workload_record(m, Wx, args, ws_n, local, args.also_steps)
-            del Wx
+            # a nested workload that fails is recorded as such; the headline
+            # record above was measured already and is still printed
+            try:
+                Wx = load_workload(m, mi.CONFIGS[name], dev, pack, base=W)
+                line["workloads"][name] = workload_record(m, Wx, args, ws_n, local,
+                                                          args.also_steps)
+                del Wx
+            except (Exception, SystemExit) as exc:  # noqa: BLE001
+                print(f"bench.py: workload {name} failed: {exc!r}", file=sys.stderr, flush=True)
+                line["workloads"][name] = {"error": repr(exc)[:300]}
             torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(line), flush=True)
