@@ -55,3 +55,14 @@ def test_kernel_traffic_only_for_the_current_source(tree):
 def test_replica_value_single_rank():
     value, ms = bench.replica_value(12.5, 2.0, 1)
     assert ms == 2.0 and value == pytest.approx(12.5 / 2.0e-3)
+
+
+def test_source_sha_reads_only_the_argument_struct_of_internal_h(tree):
+    # declarations of other kernels do not change the expert GEMM; a field of
+    # the struct it reads does
+    base = bench.source_sha()
+    _edit(tree, "internal.h", lambda s: s + "\nnamespace moe { int some_other_launcher(int); }\n")
+    assert bench.source_sha() == base
+    _edit(tree, "internal.h", lambda s: s.replace("struct GroupedFfnArgs {",
+                                                  "struct GroupedFfnArgs {\n  int probe_field;", 1))
+    assert bench.source_sha() != base
