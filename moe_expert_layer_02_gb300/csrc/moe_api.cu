@@ -342,9 +342,12 @@ GroupedFfnArgs ffn_args(const Plan& q, void* ws, const void* xq, const float* xs
 
 // Small batches build the permutation in one single-block launch
 // (index_small_kernel); tuning().index_3pass forces the three-kernel path.
+// One single-block index launch for small batches; from 512 tokens the count,
+// multi-block scan and rank kernels are faster (T=512, E=256: index stage 17
+// vs 20 us on GB300).
 bool use_index_small(const Plan& q) {
   if (tuning().index_3pass) return false;
-  return index_small_fits(q.T, q.E);
+  return q.T < 512 && index_small_fits(q.T, q.E);
 }
 
 // Large batches (256-row tiles) run the grouped GEMMs on SM pairs;

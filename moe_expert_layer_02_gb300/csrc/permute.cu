@@ -220,11 +220,11 @@ __global__ void __launch_bounds__(1024)
   pdl_release();
 }
 
-// S3 for small batches (T <= 1024) in one block of 1024 threads: the
-// per-chunk expert masks, the per-expert chunk scans, the expert offsets, the
-// tile list and the stable ranks of count_kernel, scan_kernel and rank_kernel,
-// with the masks and chunk bases in shared memory ([nch][E] words each) and one
-// launch instead of three.  Warp c owns chunk c and lane l its token, whose
+// S3 for small batches in one block of 1024 threads (up to 1024 tokens fit;
+// the layer uses it below 512): the per-chunk expert masks, the per-expert
+// chunk scans, the expert offsets, the tile list and the stable ranks of
+// count_kernel, scan_kernel and rank_kernel, with the masks and chunk bases in
+// shared memory ([nch][E] words each) and one launch instead of three.  Warp c owns chunk c and lane l its token, whose
 // top-k indices and weights are loaded once, up front, into registers.  Same
 // results bit for bit.  KMAX >= k bounds the per-lane register arrays.
 template <int KMAX>
