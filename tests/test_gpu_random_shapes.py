@@ -20,7 +20,7 @@ from test_gpu_forward import run_forward
 pytestmark = pytest.mark.gpu
 
 KINDS = ("fp8", "fp8_shared", "fp8_block", "mxfp4", "latent", "fp8_pair")
-N_CASES = 60
+N_CASES = 150
 
 
 def draw(seed: int):
