@@ -310,6 +310,9 @@ int moe_unpermute(const moe_problem* p, const void* y_rows, const int32_t* perm,
                   const void* shared, void* out, void* stream);
 
 /* The whole layer, S1..S8, queued on `stream` with no host round trip.
+ * S1 + S2 run as moe_router_topk does (tensor-core logits, selection made
+ * exact against the canonical order within its calibrated margins; the
+ * CUDA-core router when moe_tuning's router_tile picks one of its tiles).
  *   x [T, H] bf16; router_w [E, H] fp32; router_bias [E] fp32 (MOE_F_ROUTER_BIAS:
  *   added to the logits, or with MOE_F_SIGMOID_ROUTING to the scores for
  *   selection only); MOE_F_SITU switches every expert (routed and shared) to
