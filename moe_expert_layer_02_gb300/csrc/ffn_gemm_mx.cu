@@ -447,23 +447,26 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 // both CTAs' barriers; both epilogues release accumulators on the even CTA's
 // barrier.  All waits are bounded as in the single-SM kernel.
 //
-// What bounds it: the tensor pipe's time per instruction.  A block-scaled
-// M = 256, K = 32 MMA holds the pipe ~120 cycles whatever its N (16 and 80
-// token rows measured alike), and e2m1 weights take two such MMAs per 128-row
-// block and 128-K stage where e4m3 takes one per 16 KB of weights: eight per
-// stage, ~960 cycles, against ~860 cycles for the stage's 16 KB per SM at HBM
-// speed; a tcgen05.cp adds ~60 cycles in the same pipe whatever its shape,
-// hence one 128x256b copy per stage rather than one 32x128b.warpx4 copy per
-// block (FFN1 2.13 -> 2.02 ms, FFN2 1.07 -> 1.02 ms).  Timing-only variants on
-// T=4096, L=3584, I=3072, E=896 top-16, FFN1: no MMAs and no scale copies
-// 1.65 ms; copies only 1.66; MMAs only 1.89; MMAs and two copies per stage
-// 2.13; one weight block per stage (4 MMAs, 1 copy) 1.70; N = 16 2.04; one
-// copy per stage 2.01.  Changes that did not help: packed weight loads
-// instead of unpacked ones, or an L2 prefetch 4 or 8 stages ahead (no
-// change); each stage's copies issued one stage ahead, after waiting for that
-// stage's data (2.40: the MMAs wait one load longer); the scales written by
-// four more warps with tcgen05.st instead of tcgen05.cp (3.98: the stores
-// wait for the MMAs in flight, so every stage drains the pipe).
+// What bounds it: the weight loads and the MMAs together, neither alone.  A
+// block-scaled K = 32 MMA holds the tensor pipe a fixed time whatever its N
+// (155 cycles for 128 rows per SM and N = 16 to 256 in a timing probe), a
+// tcgen05.cp ~60-90 cycles whatever its shape, hence one 128x256b copy per
+// stage rather than one 32x128b.warpx4 copy per block (FFN1 2.13 -> 2.02 ms,
+// FFN2 1.07 -> 1.02 ms).  Timing-only variants on T=4096, L=3584, I=3072,
+// E=896 top-16, FFN1: no MMAs and no scale copies 1.65 ms; copies only 1.66;
+// MMAs only 1.89; MMAs and two copies per stage 2.13; one weight block per
+// stage (4 MMAs, 1 copy) 1.70; N = 16 2.04; one copy per stage 2.01.  With
+// the operands swapped on single SMs (128 token rows as A, the stage's 256
+// weight rows as N: four MMAs per stage instead of eight, parity-green) FFN1
+// took 2.01-2.05 ms and FFN2 1.10: halving the instructions changes nothing,
+// since either way a stage moves 85-100 KB through shared memory (the e2m1
+// operand lands unpacked, 32 KB per 16 KB from HBM, and the MMAs read it all
+// back).  Changes that did not help: packed weight loads instead of unpacked
+// ones, or an L2 prefetch 4 or 8 stages ahead (no change); each stage's
+// copies issued one stage ahead, after waiting for that stage's data (2.40:
+// the MMAs wait one load longer); the scales written by four more warps with
+// tcgen05.st instead of tcgen05.cp (3.98: the stores wait for the MMAs in
+// flight, so every stage drains the pipe).
 template <bool FFN1, int BN>
 struct MxPairCfg {
   static constexpr int NA = 2;
