@@ -148,6 +148,12 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- helpers
+# The sources a committed traffic figure depends on (code only), by the file
+# that holds the kernel: the single-SM grouped GEMM by default, the SM-pair
+# GEMMs and the MXFP4 GEMMs for the summaries that name them.
+DEFAULT_TRAFFIC_SOURCES = ("ffn_gemm.cu", "device.cuh", "internal.h")
+
+
 def kernel_traffic(kernel: str, cfg_name: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
     current kernel source (else None)."""
@@ -157,23 +163,27 @@ def kernel_traffic(kernel: str, cfg_name: str):
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_sha") != source_sha():
+    files = tuple(d.get("source_files", DEFAULT_TRAFFIC_SOURCES))
+    try:
+        if d.get("source_sha") != source_sha(files):
+            return None
+    except OSError:
         return None
     return d.get("dram_bytes_per_launch")
 
 
-def source_sha() -> str:
-    """Hash of the expert-GEMM sources the traffic figure depends on: the
-    single-SM grouped GEMM, the device helpers and the argument struct it
-    reads, code only (comments and whitespace do not change the kernel)."""
+def source_sha(files=DEFAULT_TRAFFIC_SOURCES) -> str:
+    """Hash of the expert-GEMM sources a traffic figure depends on (by default
+    the single-SM grouped GEMM, the device helpers and the argument struct it
+    reads), code only (comments and whitespace do not change the kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "moe_expert_layer_02_gb300", "csrc")
-    for n in ("ffn_gemm.cu", "device.cuh", "internal.h"):
+    for n in files:
         with open(os.path.join(csrc, n)) as f:
             code = f.read()
         code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
         code = re.sub(r"//[^\n]*", " ", code)
-        if n == "internal.h":  # only the kernel's argument struct
+        if n == "internal.h":  # only the kernels' argument struct
             m = re.search(r"struct GroupedFfnArgs \{.*?\};", code, flags=re.S)
             code = m.group(0) if m else code
         h.update(" ".join(code.split()).encode())

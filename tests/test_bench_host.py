@@ -9,7 +9,7 @@ import pytest
 
 import bench
 
-FILES = ("ffn_gemm.cu", "device.cuh", "internal.h")
+FILES = ("ffn_gemm.cu", "ffn_gemm_2cta.cu", "ffn_gemm_mx.cu", "device.cuh", "internal.h")
 
 
 @pytest.fixture()
@@ -66,3 +66,20 @@ def test_source_sha_reads_only_the_argument_struct_of_internal_h(tree):
     _edit(tree, "internal.h", lambda s: s.replace("struct GroupedFfnArgs {",
                                                   "struct GroupedFfnArgs {\n  int probe_field;", 1))
     assert bench.source_sha() != base
+
+
+def test_kernel_traffic_follows_the_files_a_summary_names(tree):
+    # a summary of the SM-pair GEMM names its own source; editing another
+    # kernel's file leaves it valid, editing its own does not
+    pair = ("ffn_gemm_2cta.cu", "device.cuh", "internal.h")
+    (tree / "profiles" / "ffn1_prefill.json").write_text(json.dumps(
+        {"source_files": list(pair), "source_sha": bench.source_sha(pair),
+         "dram_bytes_per_launch": 7.0}))
+    (tree / "profiles" / "ffn1_decode.json").write_text(json.dumps(
+        {"source_sha": bench.source_sha(), "dram_bytes_per_launch": 5.0}))
+    _edit(tree, "ffn_gemm.cu", lambda s: s + "\nnamespace moe { constexpr int kProbe = 3; }\n")
+    assert bench.kernel_traffic("ffn1", "prefill") == 7.0
+    assert bench.kernel_traffic("ffn1", "decode") is None
+    _edit(tree, "ffn_gemm_2cta.cu", lambda s: s + "\nnamespace moe { constexpr int kProbe = 4; }\n")
+    assert bench.kernel_traffic("ffn1", "prefill") is None
+
