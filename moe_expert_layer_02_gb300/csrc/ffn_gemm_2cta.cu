@@ -667,25 +667,12 @@ __global__ void __launch_bounds__(P_THREADS, 1)
 // Grouped items of <= 128 rows as M = 128 tiles unless tuning().pair_small is 0.
 bool pair_small_tiles() { return tuning().pair_small != 0; }
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // Map over a row-major [groups][rows][inner] tensor of 1-byte (fp8) or
 // 2-byte (bf16) elements; box = 128 bytes x box_rows rows (128, or 64 for the
 // halves of M = 128 tiles), 128-byte swizzle.
 bool pair_map(CUtensorMap* m, int kind, int rank, const void* base, uint64_t inner,
               uint64_t rows, uint64_t groups, uint32_t box_rows = P_ROWS) {
-  auto enc = encoder();
+  auto enc = tensor_map_encoder();
   if (!enc || !base) return false;
   const int es = kind == KIND_FP8 ? 1 : 2;
   cuuint64_t dims[3] = {inner, rows, groups};

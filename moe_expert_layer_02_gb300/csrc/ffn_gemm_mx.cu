@@ -752,23 +752,10 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 mx_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 template <bool FFN1, int BN>
 cudaError_t launch_mx_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   using C = MxCfg<FFN1, BN>;
-  auto enc = mx_encoder();
+  auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorInvalidValue;
   const int Kel = FFN1 ? a.K : a.I;
   const int Wrows = FFN1 ? 2 * a.I : a.K;
@@ -816,7 +803,7 @@ cudaError_t launch_mx_impl(const GroupedFfnArgs& a, cudaStream_t s) {
 template <bool FFN1, int BN>
 cudaError_t launch_mx_pair_impl(const GroupedFfnArgs& a, cudaStream_t s) {
   using C = MxPairCfg<FFN1, BN>;
-  auto enc = mx_encoder();
+  auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorInvalidValue;
   const int Kel = FFN1 ? a.K : a.I;
   const int Wrows = FFN1 ? 2 * a.I : a.K;

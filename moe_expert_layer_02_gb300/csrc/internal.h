@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <atomic>
 
 #include <cuda_runtime.h>
@@ -29,6 +30,10 @@ inline cudaError_t ensure_max_smem(int bytes) {
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
   return e;
 }
+
+// The driver's cuTensorMapEncodeTiled, looked up once per process (thread-safe);
+// nullptr if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // The launch choices of moe_tuning (include/moe.h): read once from the MOE_*
 // environment variables, replaced by moe_set_tuning; a snapshot per call.

@@ -534,16 +534,8 @@ __global__ void __launch_bounds__(FX_THREADS)
 }
 
 bool ld_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-  if (!enc) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return false;
-    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+  const auto enc = tensor_map_encoder();
+  if (!enc) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {(cuuint32_t)LD_EL, box_rows};

@@ -768,16 +768,8 @@ namespace {
 
 bool router_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int H,
                 int rows, int box_rows) {  // [box_rows][128] boxes
-  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-  if (!enc) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return false;
-    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+  const auto enc = tensor_map_encoder();
+  if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)H * esize};
   cuuint32_t box[2] = {(cuuint32_t)RT_CH, (cuuint32_t)box_rows};
