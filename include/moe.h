@@ -388,7 +388,9 @@ typedef struct {
   int32_t index_3pass; /* 1: count / scan / rank kernels even where one block would do */
   int32_t gemm_1cta;   /* 1: single-SM fp8 grouped GEMMs for 256-row tiles as well    */
   int32_t pair_small;  /* 1 (default): SM-pair items of <= 128 rows as M = 128 tiles  */
-  int32_t mx_1cta;     /* 1: single-SM MXFP4 grouped GEMMs                             */
+  int32_t mx_1cta;     /* 1: single-SM MXFP4 grouped GEMMs; 0 (default): SM pairs where
+                          the weights are packed (moe_pack_weights) and the
+                          128-row weight blocks pair up                              */
   int32_t router_tile; /* 0 (default) or 6: tensor-core logits with the selection
                           made exact (moe_router_topk); the CUDA-core router in
                           the canonical order: 1: 8 warps of 8 tokens x 8 experts,
